@@ -1,0 +1,242 @@
+"""Pure-Python oracle for the connector-agnostic KV-cache block checksum.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may call it.  It shares no code with
+the CUDA library (no headers, helpers or tables).
+
+It is written straight from the definition on the page
+"vllm.distributed.kv_transfer.kv_checksum.checksum" (vLLM API docs), module
+docstring items 1 and 2, the attributes ``MAX_KV_HEADS_PER_LAYER`` and
+``BLOCK_CHECKSUM_BYTES``, the dataclass ``KVChecksumBlocks`` and the function
+``num_valid_tokens`` described there.  Every integer is an exact Python int,
+reduced mod 2**64 only where the definition says "mod 2**64", so this form is
+the slow, obviously-correct ground truth for small inputs.
+
+Definition restated (same page, module docstring):
+
+* A *slice* is the KV of one layer and one KV head inside one block: the K and
+  the V of the block's tokens for that head, laid out token by token (per
+  token: the K bytes of the head, then its V bytes) and cut into little-endian
+  8-byte pieces.  Piece ``p`` of the token at request position ``t`` has index
+  ``j = t*P + p`` where ``P`` is the number of pieces per token.
+* ``s = sum_j x_j * (2*j + 1) mod 2**64``  (item 1).
+* ``c = sum_{layer, head} m * s mod 2**64`` with
+  ``m = 2*(layer*H + head) + 1`` and ``H = MAX_KV_HEADS_PER_LAYER = 1 << 16``
+  (item 2; the attribute list of the same page).
+* Slots of the last block at or past ``num_tokens`` are not checksummed
+  (dataclass ``KVChecksumBlocks``, field ``num_tokens``).
+
+Readings where the page is silent:
+
+* Latent (MLA) caches hold one row per token and count as a single KV head
+  (global head ``head_offset``) whose token slice is the whole row: there is
+  no K/V split, so ``P = row_bytes / 8``.
+* A block id outside ``[0, num_blocks)`` of any cache makes that position's
+  checksum 0 and sets bit ``STATUS_BAD_BLOCK_ID`` in the returned status.
+* Per-token bytes that are not a multiple of 8, and layers with more than
+  ``H`` KV heads, are rejected (the page: such groups "are not checksummed").
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Sequence
+
+import numpy as np
+
+MASK64 = (1 << 64) - 1
+
+# H in the slice factor (attribute MAX_KV_HEADS_PER_LAYER = 1 << 16).
+MAX_KV_HEADS_PER_LAYER = 1 << 16
+
+# Bytes of one block's checksum (attribute BLOCK_CHECKSUM_BYTES = 8).
+BLOCK_CHECKSUM_BYTES = 8
+
+LAYOUT_NHD = 0     # pool [2, num_blocks, block_size, num_heads, head_bytes]
+LAYOUT_HND = 1     # pool [2, num_blocks, num_heads, block_size, head_bytes]
+LAYOUT_LATENT = 2  # pool [num_blocks, block_size, row_bytes]
+
+STATUS_BAD_BLOCK_ID = 1
+
+
+@dataclass(frozen=True)
+class OracleCache:
+    """One layer's paged KV pool on the host, as raw bytes.
+
+    ``data`` is a C-contiguous uint8 array holding the whole pool in the order
+    given by ``layout``.  ``head_bytes`` is the bytes of one head's K (equal to
+    its V) for one token; for ``LAYOUT_LATENT`` it is the bytes of one token's
+    latent row and ``num_heads`` must be 1.
+    """
+
+    data: np.ndarray
+    num_blocks: int
+    layout: int
+    layer: int
+    head_offset: int
+    num_heads: int
+    head_bytes: int
+
+
+@dataclass(frozen=True)
+class OracleRequests:
+    """Requests in CSR form.
+
+    Request ``r`` owns global position indices
+    ``pos_offsets[r] <= i < pos_offsets[r+1]``; index ``i`` is block position
+    ``first_position[r] + (i - pos_offsets[r])`` of the request and holds block
+    ``block_ids[i]``.  This is the page's dataclass ``KVChecksumBlocks`` for
+    one KV cache group, flattened over requests.
+    """
+
+    pos_offsets: Sequence[int]
+    first_position: Sequence[int]
+    num_tokens: Sequence[int]
+    block_ids: Sequence[int]
+
+
+def num_valid_tokens(position: int, block_size: int, num_tokens: int) -> int:
+    """How many of the request's first ``num_tokens`` tokens block
+    ``position`` holds (function ``num_valid_tokens``): the block's slots are
+    tokens ``position*block_size + slot``; count those below ``num_tokens``."""
+    return sum(1 for slot in range(block_size)
+               if token_position(position, block_size, slot) < num_tokens)
+
+
+def pieces_per_token(cache: OracleCache) -> int:
+    """``P``: a token's slice is its K bytes then its V bytes for one head
+    (module docstring, item 1), or its latent row."""
+    if cache.layout == LAYOUT_LATENT:
+        return cache.head_bytes // 8
+    return 2 * cache.head_bytes // 8
+
+
+def piece_byte_offset(cache: OracleCache, block_size: int, block: int,
+                      slot: int, head: int, p: int) -> int:
+    """Byte offset in ``cache.data`` of piece ``p`` of slot ``slot``'s slice
+    for local head ``head`` in physical block ``block``.
+
+    The logical order (K bytes then V bytes of the head, token by token) is
+    fixed by the definition; the memory order comes from the declared layout.
+    """
+    hb = cache.head_bytes
+    byte = 8 * p
+    if cache.layout == LAYOUT_LATENT:
+        return (block * block_size + slot) * hb + byte
+    kv = 0
+    if byte >= hb:
+        kv, byte = 1, byte - hb
+    page = kv * cache.num_blocks + block
+    if cache.layout == LAYOUT_NHD:
+        return ((page * block_size + slot) * cache.num_heads + head) * hb + byte
+    if cache.layout == LAYOUT_HND:
+        return ((page * cache.num_heads + head) * block_size + slot) * hb + byte
+    raise ValueError(f"unknown layout {cache.layout}")
+
+
+def read_piece(cache: OracleCache, offset: int) -> int:
+    """Little-endian unsigned 8-byte piece at ``offset``."""
+    return int.from_bytes(bytes(cache.data[offset:offset + 8]), "little")
+
+
+def token_position(position: int, block_size: int, slot: int) -> int:
+    """``t``: the token's position in the request; block ``position`` holds
+    tokens ``position*block_size`` onwards (function ``num_valid_tokens``)."""
+    return position * block_size + slot
+
+
+def piece_index(t: int, P: int, p: int) -> int:
+    """``j = t*P + p`` (module docstring, item 1)."""
+    return t * P + p
+
+
+def piece_weight(j: int) -> int:
+    """The odd weight ``2*j + 1`` of piece ``j`` (item 1)."""
+    return 2 * j + 1
+
+
+def slice_checksum(cache: OracleCache, block_size: int, block: int,
+                   position: int, nv: int, head: int) -> int:
+    """``s = sum_j x_j*(2j+1) mod 2**64`` over the first ``nv`` slots of the
+    block for one (layer, local head) slice (item 1)."""
+    P = pieces_per_token(cache)
+    s = 0
+    for slot in range(nv):
+        t = token_position(position, block_size, slot)
+        for p in range(P):
+            x = read_piece(cache, piece_byte_offset(cache, block_size, block,
+                                                    slot, head, p))
+            s += x * piece_weight(piece_index(t, P, p))
+    return s & MASK64
+
+
+def slice_factor(layer: int, global_head: int) -> int:
+    """``m = 2*(layer*H + head) + 1`` (item 2)."""
+    return 2 * (layer * MAX_KV_HEADS_PER_LAYER + global_head) + 1
+
+
+def check_cache(cache: OracleCache, block_size: int) -> None:
+    """Reject what the definition does not cover (see module docstring)."""
+    if cache.head_bytes <= 0 or cache.head_bytes % 8:
+        raise ValueError("per-token bytes must be a positive multiple of 8")
+    if cache.layout == LAYOUT_LATENT and cache.num_heads != 1:
+        raise ValueError("a latent cache has exactly one head")
+    if cache.head_offset < 0 or cache.num_heads < 1:
+        raise ValueError("bad head range")
+    if cache.head_offset + cache.num_heads > MAX_KV_HEADS_PER_LAYER:
+        raise ValueError("more KV heads per layer than H are not checksummed")
+    halves = 1 if cache.layout == LAYOUT_LATENT else 2
+    need = halves * cache.num_blocks * block_size * cache.num_heads * cache.head_bytes
+    if cache.data.size < need:
+        raise ValueError("pool smaller than its declared geometry")
+
+
+def block_checksum(caches: Sequence[OracleCache], block_size: int, block: int,
+                   position: int, num_tokens: int) -> int:
+    """``c = sum_{layer, head} m*s mod 2**64`` for block ``block`` at block
+    position ``position`` of a request with ``num_tokens`` tokens (item 2)."""
+    nv = num_valid_tokens(position, block_size, num_tokens)
+    c = 0
+    for cache in caches:
+        for h in range(cache.num_heads):
+            s = slice_checksum(cache, block_size, block, position, nv, h)
+            c += slice_factor(cache.layer, cache.head_offset + h) * s
+    return c & MASK64
+
+
+def block_checksums(caches: Sequence[OracleCache], block_size: int,
+                    requests: OracleRequests) -> tuple[list[int], int]:
+    """One uint64 per global position index, plus a status word.
+
+    Positions whose block id is outside ``[0, num_blocks)`` of some cache give
+    0 and set ``STATUS_BAD_BLOCK_ID``.
+    """
+    if block_size <= 0:
+        raise ValueError("block_size must be positive")
+    for cache in caches:
+        check_cache(cache, block_size)
+    po = list(requests.pos_offsets)
+    total = po[-1] if po else 0
+    if not po or po[0] != 0 or any(b < a for a, b in zip(po, po[1:])):
+        raise ValueError("pos_offsets must start at 0 and not decrease")
+    if len(requests.block_ids) < total:
+        raise ValueError("fewer block ids than positions")
+    out = [0] * total
+    status = 0
+    for r in range(len(po) - 1):
+        for i in range(po[r], po[r + 1]):
+            position = requests.first_position[r] + (i - po[r])
+            block = int(requests.block_ids[i])
+            if any(block < 0 or block >= c.num_blocks for c in caches):
+                status |= STATUS_BAD_BLOCK_ID
+                continue
+            out[i] = block_checksum(caches, block_size, block, position,
+                                    requests.num_tokens[r])
+    return out, status
+
+
+def combine_partials(parts: Sequence[Sequence[int]]) -> list[int]:
+    """Partials from TP ranks and PP stages sum to ``c`` (module docstring,
+    the paragraph on TP ranks and PP stages): element-wise sum mod 2**64."""
+    return [sum(col) & MASK64 for col in zip(*parts)]
