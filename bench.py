@@ -1,0 +1,502 @@
+"""Benchmark: KV-cache block checksums on one GB300 (or N replicas).
+
+One *step* is one ``kvcs_block_checksums`` call over the whole workload: every
+block position of every request, over every layer's paged K/V.  The default
+workload is the Llama-3-8B-shaped one (32 layers, 8 KV heads, head_size 128,
+bf16, block_size 16, 64 requests of 512..4096 tokens, ~19 GB of KV).
+
+Printed (rank 0, one JSON line):
+  value      KV GB/s read, device-timed with CUDA events over K steps, KV
+             already resident in HBM.  The KV (tens of GB) is far larger than
+             the 129 MB L2, so no flush is needed between steps.
+  e2e        the same metric through the public API with host buffers: each
+             step copies the KV pools and block tables from pinned host
+             memory into the device pools (a load of offloaded KV), runs the
+             call and reads the checksums back.
+  roofline   the bulk-copy kernel against measured HBM bandwidth.
+  cpu_baseline  the CPU oracle (scalar C, all host cores) on a sample.
+
+``--impl reference`` times the CPU oracle instead (the reference arm).
+With ``torchrun --nproc-per-node N`` every rank checksums its own replica of
+the workload (weak scaling); the checksum needs no exchange between ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import torch  # noqa: E402
+
+METRIC = ("KV checksum GB/s read + blocks/s (device-timed, 1×GB300) and "
+          "% of HBM peak")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def make_workload(name: str, seed: int, device):
+    from paged_kv_cache_kvcs_gb300 import workloads as W
+    if name == "llama3_8b":
+        return W.llama3_8b(seed, device)
+    if name == "llama3_8b_small":      # ~1 GB: for ncu captures
+        return W.llama3_8b(seed, device, num_requests=8, min_len=1024, max_len=1024)
+    if name == "mla":
+        return W.mla(seed, device)
+    if name == "llama3_70b":
+        return W.llama3_70b(seed, device)
+    if name.startswith("llama3_70b_r"):  # request-count sweep point
+        return W.llama3_70b(seed, device, num_requests=int(name[len("llama3_70b_r"):]))
+    if name == "tiny":
+        return W.tiny(seed, device)
+    raise SystemExit(f"unknown config {name}")
+
+
+def kv_bytes(wl) -> int:
+    """Algorithmic KV bytes one step reads: valid tokens of every position
+    times the bytes a token occupies across all caches."""
+    per_token = sum((1 if c.layout == 2 else 2) * c.num_heads * c.head_bytes
+                    for c in wl.caches)
+    po = wl.pos_offsets.cpu().tolist()
+    fp = wl.first_position.cpu().tolist()
+    nt = wl.num_tokens.cpu().tolist()
+    bs = wl.block_size
+    tokens = 0
+    for r in range(len(fp)):
+        lo = fp[r] * bs
+        hi = (fp[r] + po[r + 1] - po[r]) * bs
+        tokens += max(0, min(hi, nt[r]) - lo)
+    return tokens * per_token
+
+
+def describe(wl, name) -> dict:
+    i = wl.info
+    return {"workload": f"{name}_paged_kv_checksum", "layers": i.get("layers"),
+            "kv_heads": i.get("heads"), "head_bytes": i.get("head_bytes"),
+            "block_size": wl.block_size, "layout": ["NHD", "HND", "LATENT"][i.get("layout", 0)],
+            "kv_recipe": i.get("kind"), "requests": wl.num_requests,
+            "positions": wl.num_positions, "kv_bytes": kv_bytes(wl),
+            "seed": i.get("seed"),
+            "l2": "KV working set far above the 129 MB L2; no flush between steps"}
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = Path(os.environ.get("TMPDIR", "/tmp")) / f"kvcs_clocks_{os.getpid()}.csv"
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in self.path.read_text().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, parts))
+            except (ValueError, IndexError):
+                continue
+        try:
+            self.path.unlink()
+        except OSError:
+            pass
+        inside = [p for ts, p in rows if t0 - 0.15 <= ts <= t1 + 0.15]
+        if not inside and rows:  # too short a region: nearest samples
+            inside = [p for ts, p in sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:2]]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[2]) for p in inside if num(p[2]) is not None]
+        mx = [num(p[3]) for p in inside if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for p in inside for k in range(4)
+                          if p[6 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((num(p[4]) or 0.0) for p in inside) if inside else None}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peak():
+    f = ROOT / "MEASURED_PEAKS.json"
+    try:
+        d = json.loads(f.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = ROOT / "paged_kv_cache_kvcs_gb300" / "csrc"
+    for p in sorted(csrc.glob("*")):
+        h.update(p.name.encode())
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, units_per_launch: int):
+    """DRAM bytes per launch from the committed ncu summary of this workload's
+    kernel, scaled to this launch by units processed; None when the summary
+    is missing or was taken on different kernel sources."""
+    f = ROOT / "profiles" / f"kvcs_bulk_kernel_{workload}.md"
+    if not f.exists():
+        return None
+    text = f.read_text()
+    m_src = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_unit:\s*([0-9.eE+]+)", text)
+    if not (m_src and m_b) or m_src.group(1) != kernel_source_hash():
+        return None
+    return float(m_b.group(1)) * units_per_launch
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def all_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def all_sum(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _oracle_inputs(wl, n: int, seed: int):
+    """Host inputs of the oracle for ``n`` random block positions of the
+    workload (only the pages they read), and the KV bytes they hold."""
+    import numpy as np
+    from oracle.kvcs_oracle import OracleCache, OracleRequests
+
+    rng = np.random.default_rng(seed)
+    P = wl.num_positions
+    po = wl.pos_offsets.cpu()
+    pos = torch.as_tensor(np.sort(rng.choice(P, size=min(n, P), replace=False)))
+    req = torch.searchsorted(po, pos, right=True) - 1
+    q = wl.first_position.cpu()[req] + (pos - po[req])
+    nt = wl.num_tokens.cpu()[req]
+    ids = wl.block_ids.cpu()[pos].to(torch.int64).to(wl.block_ids.device)
+    caches = []
+    for c in wl.caches:
+        halves = 1 if c.layout == 2 else 2
+        page = wl.block_size * c.num_heads * c.head_bytes
+        pages = c.pool.view(halves, c.num_blocks, page)[:, ids].cpu().numpy()
+        caches.append(OracleCache(pages.reshape(-1), len(pos), c.layout, c.layer,
+                                  c.head_offset, c.num_heads, c.head_bytes))
+    reqs = OracleRequests(list(range(len(pos) + 1)), q.tolist(), nt.tolist(),
+                          list(range(len(pos))))
+    per_token = sum((1 if c.layout == 2 else 2) * c.num_heads * c.head_bytes
+                    for c in wl.caches)
+    bs = wl.block_size
+    valid = sum(max(0, min(bs, int(t) - int(qq) * bs)) for qq, t in zip(q, nt))
+    return caches, reqs, valid * per_token, len(pos)
+
+
+def oracle_run(wl, n: int, threads: int, seed: int):
+    """One timed oracle run over ``n`` random positions: (seconds, KV bytes,
+    positions)."""
+    from oracle import c_oracle
+    caches, reqs, nbytes, npos = _oracle_inputs(wl, n, seed)
+    t0 = time.perf_counter()
+    c_oracle.block_checksums(caches, wl.block_size, reqs, num_threads=threads)
+    return time.perf_counter() - t0, nbytes, npos
+
+
+def oracle_calibrate(wl, seconds: float, threads: int, seed: int) -> int:
+    """Positions whose oracle run takes about ``seconds``."""
+    n = 8
+    while True:
+        dt, _, npos = oracle_run(wl, n, threads, seed)
+        if dt >= 0.5 * seconds or npos >= wl.num_positions:
+            return max(1, min(wl.num_positions, int(round(n * seconds / max(dt, 1e-4)))))
+        n = min(wl.num_positions, max(2 * n, int(n * 0.6 * seconds / max(dt, 1e-4))))
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, ws, rank):
+    """The CPU oracle, as it stands, on the machine's host cores."""
+    if rank != 0:
+        return
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    wl = make_workload(args.config, args.seed, dev)
+    cores = host_cores()
+    n = oracle_calibrate(wl, 1.5, cores, args.seed)
+    times = []
+    for k in range(args.warmup + args.steps):
+        dt, nbytes, npos = oracle_run(wl, n, cores, args.seed + 1 + k)
+        if k >= args.warmup:
+            times.append((nbytes / dt / 1e9, npos / dt))
+    sample = (f"each step: {n} random block positions of the workload "
+              f"(~{nbytes / 1e9:.2f} GB of KV), scalar C oracle on {cores} threads")
+    value = statistics.mean(t[0] for t in times)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3),
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "u64", "data": "synthetic",
+            "blocks_per_s": round(statistics.mean(t[1] for t in times), 3),
+            "config": describe(wl, args.config),
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import paged_kv_cache_kvcs_gb300 as kvcs
+
+    kvcs.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = make_workload(args.config, args.seed + rank, dev)
+    stream = torch.cuda.Stream(dev)
+    out = torch.empty(wl.num_positions, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions)
+    nbytes = kv_bytes(wl)
+
+    def step():
+        kvcs.workload_checksums(wl, out=out, status=status, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise SystemExit(f"status {int(status.item())} during warm-up")
+
+    # ---- device-timed region: K steps, events on the launching stream ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device() if ws == 1 else local) \
+        if rank == 0 else None
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    launches0 = kvcs.launch_count()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(ws)
+    launches = kvcs.launch_count() - launches0
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+    per = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+    total_s = starts[0].elapsed_time(ends[-1]) / 1e3
+    total_s = all_max(total_s, ws)
+    job_bytes = all_sum(nbytes * args.steps, ws)
+    job_blocks = all_sum(wl.num_positions * args.steps, ws)
+    value = job_bytes / total_s / 1e9
+    launch_s = statistics.mean(per)
+
+    # ---- end to end: host buffers through the public API ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, dev, stream, ws)
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    achieved = nbytes / launch_s / 1e9
+    traffic = profiled_traffic(args.config, plan["units"])
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u64", "data": "synthetic",
+        "blocks_per_s": round(job_blocks / total_s, 1),
+        "hbm_frac_of_nominal_8tbs": round(value / ws / NOMINAL_HBM_GBS, 4),
+        "config": {**describe(wl, args.config), "parallelism": f"replicas{ws}"},
+        "plan": {k: plan[k] for k in ("kernel", "split", "launches", "memsets", "grid",
+                                      "threads", "smem_bytes", "stage_bytes", "units")},
+        "gpu_launches": int(launches),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "kernel": "kvcs_bulk_kernel" if plan["kernel"] == 0
+                     else "kvcs_generic_kernel",
+                     "launch_ms": round(launch_s * 1e3, 4)},
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        cores = host_cores()
+        n = oracle_calibrate(wl, args.cpu_seconds, cores, args.seed)
+        dt, nb, npos = oracle_run(wl, n, cores, args.seed + 7)
+        line["cpu_baseline"] = {
+            "value": round(nb / dt / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "blocks_per_s": round(npos / dt, 2),
+            "sample": f"{npos} random block positions of the workload "
+                      f"({nb / 1e9:.2f} GB of KV), one run of {dt:.1f} s on "
+                      f"{cores} threads"}
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, wl, dev, stream, ws):
+    """Each step: pinned host -> device copies of every KV pool and of the
+    request tables, the checksum call, and a device -> host read of the
+    checksums and the status word."""
+    import paged_kv_cache_kvcs_gb300 as kvcs
+
+    host_pools = [torch.empty(c.pool.numel(), dtype=torch.uint8, pin_memory=True)
+                  for c in wl.caches]
+    for h, c in zip(host_pools, wl.caches):
+        h.copy_(c.pool)
+    tabs = [wl.pos_offsets, wl.first_position, wl.num_tokens, wl.block_ids]
+    host_tabs = [t.cpu().pin_memory() for t in tabs]
+    out = torch.empty(wl.num_positions, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    host_out = torch.empty(wl.num_positions, dtype=torch.int64, pin_memory=True)
+    host_status = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    h2d = sum(h.numel() for h in host_pools) + sum(t.numel() * t.element_size() for t in host_tabs)
+    d2h = host_out.numel() * 8 + 4
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def one():
+        for h, c in zip(host_pools, wl.caches):
+            c.pool.copy_(h, non_blocking=True)
+        for h, t in zip(host_tabs, tabs):
+            t.copy_(h, non_blocking=True)
+        status.zero_()
+        kvcs.workload_checksums(wl, out=out, status=status, stream=stream)
+        host_out.copy_(out, non_blocking=True)
+        host_status.copy_(status, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            one()
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(host_status.item()) != 0:
+        raise SystemExit("status set during the end-to-end run")
+    secs = all_max(t0.elapsed_time(t1) / 1e3, ws)
+    total = all_sum(kv_bytes(wl) * steps, ws)
+    del host_pools
+    return {"value": round(total / secs / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps, "ms_per_step": round(secs / steps * 1e3, 3),
+            "what": "pinned-host KV pools + block tables -> device, checksum, "
+                    "checksums -> pinned host, every step"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="llama3_8b")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    ws, rank, local = dist_setup() if torch.cuda.is_available() else (1, 0, 0)
+    if ws != args.gpus and rank == 0:
+        print(f"note: --gpus {args.gpus} but WORLD_SIZE {ws}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank)
+        else:
+            run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

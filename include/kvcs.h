@@ -1,0 +1,191 @@
+/*
+ * kvcs.h -- C ABI of the GB300 (sm_103a) KV-cache block checksum library.
+ *
+ * What it computes (page "vllm.distributed.kv_transfer.kv_checksum.checksum",
+ * vLLM API docs, module docstring items 1 and 2):
+ *
+ *   A slice is the KV of one layer and one KV head inside one block: per
+ *   token, that head's K bytes then its V bytes, token by token, cut into
+ *   little-endian 8-byte pieces x_j with j = t*P + p (t = the token's
+ *   position in the request, P = pieces per token, p = the piece within the
+ *   token).  Its checksum is
+ *       s = sum_j x_j * (2j + 1)                      mod 2^64
+ *   and the block's checksum is
+ *       c = sum_{layer, head} m * s                   mod 2^64,
+ *       m = 2 * (layer * 65536 + global_head) + 1.
+ *   Slots at or past the request's num_tokens are skipped (dataclass
+ *   KVChecksumBlocks; function num_valid_tokens): the block at position q
+ *   holds request tokens q*block_size .. q*block_size + block_size - 1, and
+ *   only those below num_tokens count.
+ *
+ * Because every slice is weighted by its global layer and head, partial
+ * results from several calls (tensor-parallel head shards, pipeline stages,
+ * several caches of one layer) combine by wrapping uint64 addition
+ * (module docstring, paragraph on TP ranks and PP stages).
+ *
+ * Memory: the caller owns every buffer.  The library allocates nothing and
+ * enqueues all work on the caller's stream; calls are asynchronous.
+ * Thread safety: calls may be issued concurrently from several host threads
+ * and streams; they share no mutable state apart from a launch counter.
+ */
+#ifndef KVCS_H_
+#define KVCS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* H in the slice factor: the page's MAX_KV_HEADS_PER_LAYER = 1 << 16.
+ * A cache whose global heads reach past it is rejected (the page: groups
+ * with more KV heads per layer are not checksummed). */
+#define KVCS_MAX_KV_HEADS_PER_LAYER 65536
+
+/* Bytes per block checksum (the page's BLOCK_CHECKSUM_BYTES: one 64-bit
+ * word; values are unsigned). */
+#define KVCS_BLOCK_CHECKSUM_BYTES 8
+
+/* Cache layouts (page "【vLLM 源码解析】KV Cache", section "reshape kv_cache":
+ * a raw byte pool reshaped to [2, num_blocks, block_size, heads, head_size]).
+ *   NHD:    pool [2 (K, V)][num_blocks][block_size][num_heads][head_bytes]
+ *   HND:    pool [2 (K, V)][num_blocks][num_heads][block_size][head_bytes]
+ *   LATENT: pool [num_blocks][block_size][row_bytes]  (MLA: one latent row
+ *           per token, no K/V split; counted as one head whose token slice
+ *           is the whole row, P = row_bytes / 8) */
+typedef enum kvcs_layout {
+  KVCS_LAYOUT_NHD = 0,
+  KVCS_LAYOUT_HND = 1,
+  KVCS_LAYOUT_LATENT = 2
+} kvcs_layout;
+
+/* One layer's paged pool (one attention layer, or one of several caches of
+ * a layer such as an indexer's, numbered by consecutive head offsets).
+ * Read-only to the library. */
+typedef struct kvcs_cache {
+  const void *base;    /* DEVICE pointer to the pool; 8-byte aligned
+                          (16-byte alignment enables the bulk-copy kernel) */
+  int64_t num_blocks;  /* pages in the pool; valid block ids are [0, num_blocks) */
+  int32_t layout;      /* a kvcs_layout */
+  int32_t layer;       /* layer number taken from the layer's name, >= 0 */
+  int32_t head_offset; /* global index of this cache's local head 0 (TP shard
+                          offset, or the head count of earlier caches of the
+                          same layer); LATENT: the one head's global index */
+  int32_t num_heads;   /* local KV heads; 1 for LATENT */
+  int32_t head_bytes;  /* NHD/HND: bytes of one head's K (= its V) for one
+                          token; LATENT: bytes of one token row.  A positive
+                          multiple of 8. */
+  int32_t reserved;    /* must be 0 */
+} kvcs_cache;
+
+/* The requests to checksum, in CSR form over requests.  All pointers are
+ * DEVICE pointers, read-only to the library.  This is the page's dataclass
+ * KVChecksumBlocks (num_tokens; per group the first block position and the
+ * block ids at consecutive positions) for one KV-cache group, flattened. */
+typedef struct kvcs_requests {
+  int64_t num_requests;          /* R >= 0 */
+  const int64_t *pos_offsets;    /* [R + 1]: request r owns global position
+                                    indices [pos_offsets[r], pos_offsets[r+1]);
+                                    pos_offsets[0] = 0, non-decreasing,
+                                    pos_offsets[R] = total_positions */
+  const int64_t *first_position; /* [R]: block position (>= 0) of the request's
+                                    first listed block */
+  const int64_t *num_tokens;     /* [R]: tokens whose KV the blocks hold */
+  const int32_t *block_ids;      /* [total_positions]: index i holds block
+                                    position first_position[r] + i - pos_offsets[r]
+                                    of request r */
+} kvcs_requests;
+
+/* Return codes (negative: nothing was enqueued unless stated). */
+#define KVCS_OK 0
+#define KVCS_EINVAL (-1)      /* null pointer, non-positive block_size,
+                                 head_bytes not a positive multiple of 8,
+                                 unknown layout, latent cache with heads != 1,
+                                 negative layer or head offset, reserved != 0,
+                                 misaligned base, two caches covering the same
+                                 (layer, global head) */
+#define KVCS_EUNSUPPORTED (-2) /* head_offset + num_heads > 65536 */
+#define KVCS_ECUDA (-3)       /* a CUDA call failed (launch, attribute query);
+                                 work may have been partly enqueued */
+
+/* Bits set in the caller's device status word by the kernels (OR-ed in; the
+ * caller zeroes the word when it wants a fresh reading).  None of them traps
+ * or aborts the context. */
+#define KVCS_STATUS_BAD_BLOCK_ID 1u /* some block id was outside [0, num_blocks)
+                                       of some cache: that position's output
+                                       is 0 */
+#define KVCS_STATUS_BAD_REQUESTS 2u /* pos_offsets not starting at 0, decreasing,
+                                       or not ending at total_positions, or a
+                                       negative first_position: the affected
+                                       positions' outputs are 0 */
+#define KVCS_STATUS_TIMEOUT 4u      /* an internal pipeline wait ran past its
+                                       time limit (about 2 s) and gave up: the
+                                       outputs of that call are not valid */
+
+/*
+ * kvcs_block_checksums -- one uint64 block checksum per global position index.
+ *
+ *   caches           HOST array of num_caches descriptors (copied into the
+ *                    launch; may be freed when the call returns).
+ *   num_caches       >= 1.  Any number; above an internal per-launch limit
+ *                    the work is split over several launches.
+ *   block_size       tokens per block (> 0), the same for every cache.
+ *   reqs             HOST pointer to the request table (whose arrays are on
+ *                    the device).
+ *   total_positions  pos_offsets[R] as known to the host (>= 0).
+ *   out              DEVICE uint64[total_positions], written entirely:
+ *                    out[i] = c of global position index i, or 0 where the
+ *                    position holds no valid token or is flagged bad.
+ *   status           DEVICE uint32 word or NULL; see KVCS_STATUS_*.
+ *   stream           a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Returns KVCS_OK once the work is enqueued.  Validation of the host
+ * arguments happens before any CUDA call, so a negative return other than
+ * KVCS_ECUDA means nothing was enqueued.  Data-dependent problems in the
+ * device arrays are reported through *status, never by a fault.
+ */
+int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
+                         int32_t block_size, const kvcs_requests *reqs,
+                         int64_t total_positions, uint64_t *out,
+                         uint32_t *status, void *stream);
+
+/* Which kernel and launch shape kvcs_block_checksums would use.  Filled by
+ * kvcs_plan; no CUDA work is enqueued. */
+typedef struct kvcs_plan_info {
+  int32_t kernel;        /* 0 = bulk-copy pipeline, 1 = generic 8-byte loads */
+  int32_t split;         /* 1 if positions are split across CTAs (output is
+                            zeroed first and partial sums are added with
+                            64-bit atomics) */
+  int32_t launches;      /* kernel launches per call (one per cache group) */
+  int32_t memsets;       /* cudaMemsetAsync calls per call (0 or 1) */
+  int32_t grid;          /* CTAs per kernel launch */
+  int32_t threads;       /* threads per CTA */
+  int32_t smem_bytes;    /* dynamic shared memory per CTA */
+  int32_t stage_bytes;   /* bytes per pipeline stage (bulk kernel) */
+  int64_t units;         /* work units (page pieces) per launch */
+  int64_t kv_bytes_max;  /* KV bytes if every position held block_size tokens */
+} kvcs_plan_info;
+
+/*
+ * kvcs_plan -- the plan for a call with these caches and sizes.
+ *   num_sms  SM count to plan for; 0 = query the current device (a CUDA call).
+ * Returns the same error codes as kvcs_block_checksums for bad arguments.
+ */
+int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+              int64_t total_positions, int32_t num_sms, kvcs_plan_info *info);
+
+/* Short text for a return code; never NULL. */
+const char *kvcs_strerror(int code);
+
+/* Kernels this library has launched in this process (all devices, all
+ * threads).  Memsets are not counted. */
+uint64_t kvcs_launch_count(void);
+
+/* ABI version: (major << 16) | minor. */
+int32_t kvcs_version(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* KVCS_H_ */

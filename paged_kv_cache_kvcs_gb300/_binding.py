@@ -1,0 +1,213 @@
+"""ctypes binding to ``libkvcs.so``: argument marshalling only.
+
+Every step of the checksum runs in the library's CUDA kernels.  There is no
+fallback: if the library has not been built, loading raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+from typing import Sequence
+
+LIB_PATH = Path(__file__).resolve().parent / "_build" / "libkvcs.so"
+
+KVCS_LAYOUT_NHD = 0
+KVCS_LAYOUT_HND = 1
+KVCS_LAYOUT_LATENT = 2
+KVCS_MAX_KV_HEADS_PER_LAYER = 65536
+KVCS_BLOCK_CHECKSUM_BYTES = 8
+
+KVCS_OK = 0
+KVCS_EINVAL = -1
+KVCS_EUNSUPPORTED = -2
+KVCS_ECUDA = -3
+
+KVCS_STATUS_BAD_BLOCK_ID = 1
+KVCS_STATUS_BAD_REQUESTS = 2
+KVCS_STATUS_TIMEOUT = 4
+
+
+class kvcs_cache(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
+                ("layout", ctypes.c_int32), ("layer", ctypes.c_int32),
+                ("head_offset", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("head_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class kvcs_requests(ctypes.Structure):
+    _fields_ = [("num_requests", ctypes.c_int64),
+                ("pos_offsets", ctypes.c_void_p),
+                ("first_position", ctypes.c_void_p),
+                ("num_tokens", ctypes.c_void_p),
+                ("block_ids", ctypes.c_void_p)]
+
+
+class kvcs_plan_info(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("split", ctypes.c_int32),
+                ("launches", ctypes.c_int32), ("memsets", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("units", ctypes.c_int64), ("kv_bytes_max", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+# Every symbol kvcs.h declares, with its ctypes signature.
+SIGNATURES = {
+    "kvcs_block_checksums": (ctypes.c_int, [
+        ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
+        ctypes.POINTER(kvcs_requests), ctypes.c_int64, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p]),
+    "kvcs_plan": (ctypes.c_int, [
+        ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(kvcs_plan_info)]),
+    "kvcs_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "kvcs_launch_count": (ctypes.c_uint64, []),
+    "kvcs_version": (ctypes.c_int32, []),
+}
+
+_lib = None
+
+
+class KvcsError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+        self.code = code
+
+
+def load_library() -> ctypes.CDLL:
+    """Load ``_build/libkvcs.so``; raise if it was not built."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(str(LIB_PATH))
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return load_library().kvcs_strerror(code).decode()
+
+
+def launch_count() -> int:
+    return int(load_library().kvcs_launch_count())
+
+
+def version() -> int:
+    return int(load_library().kvcs_version())
+
+
+def cache_array(caches: Sequence) -> ctypes.Array:
+    """Pack cache descriptors.  Each item has ``pool`` (a tensor, or an int
+    device address), ``num_blocks``, ``layout``, ``layer``, ``head_offset``,
+    ``num_heads`` and ``head_bytes``."""
+    arr = (kvcs_cache * max(1, len(caches)))()
+    for i, c in enumerate(caches):
+        pool = c.pool
+        base = pool if isinstance(pool, int) else pool.data_ptr()
+        arr[i] = kvcs_cache(base, c.num_blocks, c.layout, c.layer, c.head_offset,
+                            c.num_heads, c.head_bytes, 0)
+    return arr
+
+
+def kvcs_block_checksums(caches: ctypes.Array, num_caches: int, block_size: int,
+                         reqs: kvcs_requests, total_positions: int, out: int,
+                         status: int | None, stream: int | None) -> int:
+    """The C entry point, one-to-one; raises ``KvcsError`` on a negative
+    return."""
+    rc = load_library().kvcs_block_checksums(
+        caches, num_caches, block_size, ctypes.byref(reqs), total_positions,
+        out, status or None, stream or None)
+    if rc != KVCS_OK:
+        raise KvcsError(rc, "kvcs_block_checksums")
+    return rc
+
+
+def kvcs_plan(caches: ctypes.Array, num_caches: int, block_size: int,
+              total_positions: int, num_sms: int = 0) -> dict:
+    info = kvcs_plan_info()
+    rc = load_library().kvcs_plan(caches, num_caches, block_size,
+                                  total_positions, num_sms, ctypes.byref(info))
+    if rc != KVCS_OK:
+        raise KvcsError(rc, "kvcs_plan")
+    return info.as_dict()
+
+
+def _check_pool(c, block_size: int) -> None:
+    import torch
+    t = c.pool
+    if isinstance(t, int):
+        return
+    if not t.is_cuda:
+        raise ValueError("cache pools must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("cache pools must be contiguous")
+    halves = 1 if c.layout == KVCS_LAYOUT_LATENT else 2
+    need = halves * c.num_blocks * block_size * c.num_heads * c.head_bytes
+    if t.numel() * t.element_size() < need:
+        raise ValueError("cache pool is smaller than its declared geometry")
+    del torch
+
+
+def block_checksums(caches: Sequence, block_size: int, pos_offsets, first_position,
+                    num_tokens, block_ids, out=None, status=None, stream=None,
+                    total_positions: int | None = None):
+    """Torch front end of ``kvcs_block_checksums``.
+
+    ``pos_offsets``/``first_position``/``num_tokens`` are int64 CUDA tensors,
+    ``block_ids`` an int32 CUDA tensor.  Returns ``out``: an int64 CUDA tensor
+    whose elements hold the uint64 checksums' bits (view it as uint64 on the
+    host).  ``status``, if given, is an int32 CUDA tensor of one element into
+    which ``KVCS_STATUS_*`` bits are OR-ed.
+    """
+    import torch
+    for c in caches:
+        _check_pool(c, block_size)
+    for name, t, dt in (("pos_offsets", pos_offsets, torch.int64),
+                        ("first_position", first_position, torch.int64),
+                        ("num_tokens", num_tokens, torch.int64),
+                        ("block_ids", block_ids, torch.int32)):
+        if not (t.is_cuda and t.dtype == dt and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if total_positions is None:
+        total_positions = int(pos_offsets[-1].item())
+    dev = pos_offsets.device
+    if out is None:
+        out = torch.empty(max(total_positions, 0), dtype=torch.int64, device=dev)
+    elif out.numel() < total_positions or out.dtype not in (torch.int64, torch.uint64):
+        raise ValueError("out must hold total_positions 64-bit words")
+    reqs = kvcs_requests(pos_offsets.numel() - 1, pos_offsets.data_ptr(),
+                         first_position.data_ptr(), num_tokens.data_ptr(),
+                         block_ids.data_ptr())
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    arr = cache_array(caches)
+    kvcs_block_checksums(arr, len(caches), block_size, reqs, total_positions,
+                         out.data_ptr() if total_positions > 0 else None,
+                         status.data_ptr() if status is not None else None, stream)
+    return out
+
+
+def workload_checksums(wl, out=None, status=None, stream=None):
+    """``block_checksums`` over a ``workloads.Workload``."""
+    return block_checksums(wl.caches, wl.block_size, wl.pos_offsets,
+                           wl.first_position, wl.num_tokens, wl.block_ids,
+                           out=out, status=status, stream=stream,
+                           total_positions=wl.num_positions)
+
+
+def plan_for(caches: Sequence, block_size: int, total_positions: int,
+             num_sms: int = 0) -> dict:
+    return kvcs_plan(cache_array(caches), len(caches), block_size,
+                     total_positions, num_sms)

@@ -1,0 +1,306 @@
+// kvcs.cu -- host side of the KV-cache block checksum library: argument
+// validation, launch planning and the exported C ABI declared in kvcs.h.
+//
+// The library allocates no memory.  Every call validates its host arguments
+// before touching CUDA, plans one or more launches of one kernel and enqueues
+// them (plus, when CTAs share positions, one cudaMemsetAsync of the output)
+// on the caller's stream.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kvcs.h"
+#include "kvcs_kernels.cuh"
+
+namespace kvcs {
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+
+constexpr u64 kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int sms = 0;
+  cudaError_t err = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+// SM count of the current device; sets the bulk kernel's shared-memory
+// attribute once per device.
+cudaError_t device_setup(int *sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  DeviceState &d = g_dev[dev];
+  std::call_once(d.once, [&d, dev]() {
+    int n = 0;
+    d.err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaFuncSetAttribute(kvcs_bulk_kernel,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kBulkSmemBytes);
+    d.sms = n;
+  });
+  *sms = d.sms;
+  return d.err;
+}
+
+struct Plan {
+  int kernel = 0;  // 0 bulk, 1 generic
+  int split = 0;
+  int groups = 1;
+  int grid = 0;
+  long long units = 0;       // units of the largest launch
+  long long kv_bytes_max = 0;
+};
+
+bool bulk_eligible(const kvcs_cache &c, int block_size) {
+  if (reinterpret_cast<uintptr_t>(c.base) % 16) return false;
+  if (c.head_bytes % 16) return false;
+  const long long hb = c.head_bytes;
+  switch (c.layout) {
+    case KVCS_LAYOUT_NHD: return hb * c.num_heads <= kStageBytes;
+    case KVCS_LAYOUT_HND: return hb * block_size <= kStageBytes;
+    default: return hb <= kStageBytes;
+  }
+}
+
+// Host-argument checks shared by kvcs_plan and kvcs_block_checksums.
+int validate_caches(const kvcs_cache *caches, int32_t num_caches,
+                    int32_t block_size) {
+  if (!caches || num_caches < 1 || block_size <= 0) return KVCS_EINVAL;
+  struct Span {
+    int32_t layer;
+    int64_t lo, hi;
+  };
+  std::vector<Span> spans;
+  spans.reserve(num_caches);
+  for (int32_t i = 0; i < num_caches; ++i) {
+    const kvcs_cache &c = caches[i];
+    if (!c.base || c.num_blocks < 0 || c.reserved != 0) return KVCS_EINVAL;
+    if (c.layout < KVCS_LAYOUT_NHD || c.layout > KVCS_LAYOUT_LATENT) return KVCS_EINVAL;
+    if (c.layer < 0 || c.head_offset < 0 || c.num_heads < 1) return KVCS_EINVAL;
+    if (c.head_bytes <= 0 || c.head_bytes % 8) return KVCS_EINVAL;
+    if (c.layout == KVCS_LAYOUT_LATENT && c.num_heads != 1) return KVCS_EINVAL;
+    if (reinterpret_cast<uintptr_t>(c.base) % 8) return KVCS_EINVAL;
+    if (static_cast<int64_t>(c.head_offset) + c.num_heads > KVCS_MAX_KV_HEADS_PER_LAYER)
+      return KVCS_EUNSUPPORTED;
+    // Bytes per page must stay addressable in 64 bits (always true for real
+    // pools; guards absurd descriptors).
+    const double page = static_cast<double>(block_size) * c.num_heads * c.head_bytes;
+    if (page * 2.0 * static_cast<double>(c.num_blocks) > 9.0e18) return KVCS_EINVAL;
+    spans.push_back({c.layer, c.head_offset,
+                     static_cast<int64_t>(c.head_offset) + c.num_heads});
+  }
+  std::sort(spans.begin(), spans.end(), [](const Span &a, const Span &b) {
+    return a.layer != b.layer ? a.layer < b.layer : a.lo < b.lo;
+  });
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].layer == spans[i - 1].layer && spans[i].lo < spans[i - 1].hi)
+      return KVCS_EINVAL;  // two caches weigh the same (layer, global head)
+  return KVCS_OK;
+}
+
+DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
+  DevCache d;
+  std::memset(&d, 0, sizeof(d));
+  d.base = static_cast<const unsigned char *>(c.base);
+  d.m0 = 2ull * (static_cast<u64>(c.layer) * KVCS_MAX_KV_HEADS_PER_LAYER +
+                 static_cast<u64>(c.head_offset)) + 1ull;
+  d.layout = c.layout;
+  d.heads = c.num_heads;
+  d.hb = c.head_bytes;
+  d.page_bytes = static_cast<u64>(block_size) * c.num_heads * c.head_bytes;
+  d.half_stride = static_cast<u64>(c.num_blocks) * d.page_bytes;
+  d.halves = c.layout == KVCS_LAYOUT_LATENT ? 1 : 2;
+  d.P = (c.layout == KVCS_LAYOUT_LATENT ? c.head_bytes : 2 * c.head_bytes) / 8;
+  // Units: split a page into runs that fit a stage, as evenly as possible.
+  if (c.layout == KVCS_LAYOUT_HND) {
+    d.rowb = c.head_bytes;
+    const int fit = std::max(1, static_cast<int>(kStageBytes / (static_cast<long long>(block_size) * c.head_bytes)));
+    d.upp = (c.num_heads + fit - 1) / fit;
+    d.rpu = (c.num_heads + d.upp - 1) / d.upp;
+  } else {
+    d.rowb = c.layout == KVCS_LAYOUT_NHD ? c.num_heads * c.head_bytes : c.head_bytes;
+    const int fit = std::max(1, kStageBytes / std::max(1, d.rowb));
+    d.upp = (block_size + fit - 1) / fit;
+    d.rpu = (block_size + d.upp - 1) / d.upp;
+  }
+  return d;
+}
+
+int make_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+              int64_t total_positions, int sms, Plan *plan) {
+  Plan pl;
+  bool bulk = true;
+  long long bytes_per_pos = 0;
+  for (int32_t i = 0; i < num_caches; ++i) {
+    bulk = bulk && bulk_eligible(caches[i], block_size);
+    const long long halves = caches[i].layout == KVCS_LAYOUT_LATENT ? 1 : 2;
+    bytes_per_pos += halves * block_size * static_cast<long long>(caches[i].num_heads) *
+                     caches[i].head_bytes;
+  }
+  pl.kernel = bulk ? 0 : 1;
+  pl.groups = (num_caches + kMaxCachesPerLaunch - 1) / kMaxCachesPerLaunch;
+  pl.kv_bytes_max = bytes_per_pos * total_positions;
+  if (sms < 1) sms = 1;
+  if (bulk) {
+    long long upp_max = 0;
+    for (int g = 0; g < pl.groups; ++g) {
+      long long U = 0;
+      for (int32_t i = g * kMaxCachesPerLaunch;
+           i < std::min(num_caches, (g + 1) * kMaxCachesPerLaunch); ++i) {
+        const DevCache d = make_dev_cache(caches[i], block_size);
+        U += static_cast<long long>(d.halves) * d.upp;
+      }
+      upp_max = std::max(upp_max, U);
+    }
+    pl.units = upp_max * total_positions;
+    // Whole positions per CTA when that balances well (>= 95% of the even
+    // split); otherwise split at unit granularity.
+    const double per = static_cast<double>(total_positions) / sms;
+    const double eff = per / std::ceil(per > 0 ? per : 1.0);
+    if (total_positions >= sms && eff >= 0.95) {
+      pl.split = 0;
+      pl.grid = sms;
+    } else {
+      pl.split = 1;
+      pl.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, pl.units)));
+    }
+  } else {
+    pl.units = total_positions;
+    pl.split = 0;
+    pl.grid = static_cast<int>(std::max<long long>(
+        1, std::min<long long>(static_cast<long long>(sms) * 8, total_positions)));
+  }
+  *plan = pl;
+  return KVCS_OK;
+}
+
+}  // namespace
+}  // namespace kvcs
+
+using namespace kvcs;
+
+extern "C" {
+
+int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+              int64_t total_positions, int32_t num_sms, kvcs_plan_info *info) {
+  if (!info || total_positions < 0) return KVCS_EINVAL;
+  int rc = validate_caches(caches, num_caches, block_size);
+  if (rc != KVCS_OK) return rc;
+  int sms = num_sms;
+  if (sms <= 0) {
+    if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
+  }
+  Plan pl;
+  make_plan(caches, num_caches, block_size, total_positions, sms, &pl);
+  std::memset(info, 0, sizeof(*info));
+  info->kernel = pl.kernel;
+  info->split = pl.kernel == 0 ? pl.split : 0;
+  info->launches = total_positions > 0 ? pl.groups : 0;
+  info->memsets = (total_positions > 0 && (pl.groups > 1 || (pl.kernel == 0 && pl.split))) ? 1 : 0;
+  info->grid = pl.grid;
+  info->threads = pl.kernel == 0 ? kBulkThreads : kGenericThreads;
+  info->smem_bytes = pl.kernel == 0 ? kBulkSmemBytes : 0;
+  info->stage_bytes = pl.kernel == 0 ? kStageBytes : 0;
+  info->units = pl.units;
+  info->kv_bytes_max = pl.kv_bytes_max;
+  return KVCS_OK;
+}
+
+int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
+                         int32_t block_size, const kvcs_requests *reqs,
+                         int64_t total_positions, uint64_t *out,
+                         uint32_t *status, void *stream) {
+  int rc = validate_caches(caches, num_caches, block_size);
+  if (rc != KVCS_OK) return rc;
+  if (!reqs || total_positions < 0 || reqs->num_requests < 0) return KVCS_EINVAL;
+  if (total_positions == 0) return KVCS_OK;
+  if (!out || !reqs->pos_offsets || !reqs->first_position || !reqs->num_tokens ||
+      !reqs->block_ids)
+    return KVCS_EINVAL;
+  if (reinterpret_cast<uintptr_t>(out) % 8) return KVCS_EINVAL;
+
+  int sms = 0;
+  if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
+  Plan pl;
+  make_plan(caches, num_caches, block_size, total_positions, sms, &pl);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const bool all_atomic = pl.groups > 1;
+  if (all_atomic || (pl.kernel == 0 && pl.split)) {
+    if (cudaMemsetAsync(out, 0, static_cast<size_t>(total_positions) * sizeof(uint64_t),
+                        st) != cudaSuccess)
+      return KVCS_ECUDA;
+  }
+
+  long long min_nb = caches[0].num_blocks;
+  for (int32_t i = 1; i < num_caches; ++i) min_nb = std::min<long long>(min_nb, caches[i].num_blocks);
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.pos_offsets = reinterpret_cast<const long long *>(reqs->pos_offsets);
+  p.first_position = reinterpret_cast<const long long *>(reqs->first_position);
+  p.num_tokens = reinterpret_cast<const long long *>(reqs->num_tokens);
+  p.block_ids = reinterpret_cast<const int *>(reqs->block_ids);
+  p.out = reinterpret_cast<u64 *>(out);
+  p.status = status;
+  p.num_requests = reqs->num_requests;
+  p.total_positions = total_positions;
+  p.min_num_blocks = min_nb;
+  p.timeout_ns = kTimeoutNs;
+  p.block_size = block_size;
+  p.all_atomic = all_atomic ? 1 : 0;
+
+  for (int g = 0; g < pl.groups; ++g) {
+    const int lo = g * kMaxCachesPerLaunch;
+    const int hi = std::min(num_caches, lo + kMaxCachesPerLaunch);
+    p.num_caches = hi - lo;
+    long long U = 0;
+    for (int i = lo; i < hi; ++i) {
+      p.caches[i - lo] = make_dev_cache(caches[i], block_size);
+      U += static_cast<long long>(p.caches[i - lo].halves) * p.caches[i - lo].upp;
+    }
+    p.units_per_pos = U;
+    p.total_units = U * total_positions;
+    if (pl.kernel == 0) {
+      p.split = pl.split;
+      long long grid = pl.grid;
+      if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
+      kvcs_bulk_kernel<<<static_cast<unsigned>(grid), kBulkThreads, kBulkSmemBytes, st>>>(p);
+    } else {
+      p.split = 0;
+      kvcs_generic_kernel<<<static_cast<unsigned>(pl.grid), kGenericThreads, 0, st>>>(p);
+    }
+    if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return KVCS_OK;
+}
+
+const char *kvcs_strerror(int code) {
+  switch (code) {
+    case KVCS_OK: return "success";
+    case KVCS_EINVAL: return "invalid argument";
+    case KVCS_EUNSUPPORTED: return "unsupported: more than 65536 KV heads per layer";
+    case KVCS_ECUDA: return "CUDA error";
+    default: return "unknown error";
+  }
+}
+
+uint64_t kvcs_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int32_t kvcs_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

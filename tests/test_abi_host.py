@@ -1,0 +1,117 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and its host-side validation and planning behave."""
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import paged_kv_cache_kvcs_gb300 as K
+from paged_kv_cache_kvcs_gb300 import _binding as B
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "kvcs.h"
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(kvcs_[a-z_]+)\s*\(",
+                                 text, re.M)))
+
+
+def test_header_declares_the_bound_symbols():
+    names = declared_functions()
+    assert names == sorted(B.SIGNATURES), names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = K.load_library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_strerror():
+    assert K.version() >> 16 == 1
+    for code in (K.KVCS_OK, K.KVCS_EINVAL, K.KVCS_EUNSUPPORTED, K.KVCS_ECUDA, 99):
+        assert isinstance(K.strerror(code), str) and K.strerror(code)
+
+
+class FakeCache:
+    def __init__(self, base=1 << 20, num_blocks=100, layout=0, layer=0,
+                 head_offset=0, num_heads=8, head_bytes=256):
+        self.pool = base
+        self.num_blocks = num_blocks
+        self.layout = layout
+        self.layer = layer
+        self.head_offset = head_offset
+        self.num_heads = num_heads
+        self.head_bytes = head_bytes
+
+
+def plan(caches, bs=16, positions=1000, sms=152):
+    return K.plan_for(caches, bs, positions, num_sms=sms)
+
+
+def code_of(caches, bs=16, positions=10):
+    try:
+        plan(caches, bs, positions)
+        return 0
+    except K.KvcsError as e:
+        return e.code
+
+
+def test_validation_codes():
+    ok = FakeCache()
+    assert code_of([ok]) == 0
+    assert code_of([FakeCache(head_bytes=12)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(head_bytes=0)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layout=3)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layout=2, num_heads=2)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layer=-1)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(base=0)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(base=(1 << 20) + 4)]) == K.KVCS_EINVAL
+    assert code_of([ok], bs=0) == K.KVCS_EINVAL
+    assert code_of([FakeCache(head_offset=65530, num_heads=7)]) == K.KVCS_EUNSUPPORTED
+    assert code_of([FakeCache(head_offset=65528, num_heads=8)]) == 0
+    # overlapping (layer, global head) between two caches
+    assert code_of([FakeCache(head_offset=0, num_heads=4),
+                    FakeCache(head_offset=3, num_heads=4)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(head_offset=0, num_heads=4),
+                    FakeCache(head_offset=4, num_heads=4)]) == 0
+    assert code_of([FakeCache(layer=0), FakeCache(layer=1)]) == 0
+
+
+def test_block_checksums_rejects_before_any_cuda_call():
+    arr = K.cache_array([FakeCache(head_bytes=12)])
+    reqs = B.kvcs_requests(1, 16, 32, 48, 64)
+    rc = K.load_library().kvcs_block_checksums(arr, 1, 16, ctypes.byref(reqs), 4,
+                                               128, None, None)
+    assert rc == K.KVCS_EINVAL
+    arr = K.cache_array([FakeCache()])
+    rc = K.load_library().kvcs_block_checksums(arr, 1, 16, ctypes.byref(reqs), 4,
+                                               None, None, None)
+    assert rc == K.KVCS_EINVAL          # null output
+    rc = K.load_library().kvcs_block_checksums(arr, 1, 16, ctypes.byref(reqs), 0,
+                                               None, None, None)
+    assert rc == K.KVCS_OK              # nothing to do, nothing enqueued
+
+
+def test_plan_shapes():
+    llama8b = [FakeCache(layer=i, num_blocks=9300) for i in range(32)]
+    p = plan(llama8b, positions=9220)
+    assert p["kernel"] == 0 and p["split"] == 0 and p["memsets"] == 0
+    assert p["launches"] == 1 and p["grid"] == 152
+    assert p["units"] == 9220 * 64 and p["stage_bytes"] == 32768
+    assert p["kv_bytes_max"] == 9220 * 32 * 2 * 32768
+    # one 70B-shaped request: too few positions for whole-position CTAs
+    p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=128)
+    assert p["split"] == 1 and p["memsets"] == 1 and p["grid"] == 152
+    # latent rows of 1152 B: 3 units per 64-slot page
+    p = plan([FakeCache(layout=2, num_heads=1, head_bytes=1152, layer=i)
+              for i in range(61)], bs=64, positions=4096)
+    assert p["units"] == 4096 * 61 * 3 and p["split"] == 0
+    # odd per-head bytes: generic kernel
+    assert plan([FakeCache(head_bytes=24)])["kernel"] == 1
+    # more caches than one launch takes
+    p = plan([FakeCache(layer=i, num_heads=1, head_bytes=16) for i in range(300)])
+    assert p["launches"] == 3 and p["memsets"] == 1
