@@ -162,6 +162,8 @@ typedef struct kvcs_plan_info {
   int32_t threads;       /* threads per CTA */
   int32_t smem_bytes;    /* dynamic shared memory per CTA */
   int32_t stage_bytes;   /* bytes per pipeline stage (bulk kernel) */
+  int32_t stages;        /* pipeline stages per CTA (bulk kernel) */
+  int32_t reserved;
   int64_t units;         /* work units (page pieces) per launch */
   int64_t kv_bytes_max;  /* KV bytes if every position held block_size tokens */
 } kvcs_plan_info;

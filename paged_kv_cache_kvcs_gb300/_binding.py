@@ -48,6 +48,7 @@ class kvcs_plan_info(ctypes.Structure):
                 ("launches", ctypes.c_int32), ("memsets", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("units", ctypes.c_int64), ("kv_bytes_max", ctypes.c_int64)]
 
     def as_dict(self) -> dict:

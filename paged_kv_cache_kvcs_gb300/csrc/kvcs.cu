@@ -48,7 +48,7 @@ cudaError_t device_setup(int *sms) {
     if (d.err == cudaSuccess)
       d.err = cudaFuncSetAttribute(kvcs_bulk_kernel,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kBulkSmemBytes);
+                                   kSmemLimit);
     d.sms = n;
   });
   *sms = d.sms;
@@ -60,18 +60,22 @@ struct Plan {
   int split = 0;
   int groups = 1;
   int grid = 0;
+  int stage_bytes = 0;       // of the first launch
+  int stages = 0;
   long long units = 0;       // units of the largest launch
   long long kv_bytes_max = 0;
 };
 
+// The bulk kernel stages whole rows (NHD, latent) or whole heads (HND) with
+// 16-byte-aligned bulk copies and reads 16-byte columns.
 bool bulk_eligible(const kvcs_cache &c, int block_size) {
   if (reinterpret_cast<uintptr_t>(c.base) % 16) return false;
   if (c.head_bytes % 16) return false;
   const long long hb = c.head_bytes;
   switch (c.layout) {
-    case KVCS_LAYOUT_NHD: return hb * c.num_heads <= kStageBytes;
-    case KVCS_LAYOUT_HND: return hb * block_size <= kStageBytes;
-    default: return hb <= kStageBytes;
+    case KVCS_LAYOUT_NHD: return hb * c.num_heads <= kMaxUnitBytes;
+    case KVCS_LAYOUT_HND: return hb * block_size <= kMaxUnitBytes;
+    default: return hb <= kMaxUnitBytes;
   }
 }
 
@@ -124,19 +128,80 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
   d.half_stride = static_cast<u64>(c.num_blocks) * d.page_bytes;
   d.halves = c.layout == KVCS_LAYOUT_LATENT ? 1 : 2;
   d.P = (c.layout == KVCS_LAYOUT_LATENT ? c.head_bytes : 2 * c.head_bytes) / 8;
-  // Units: split a page into runs that fit a stage, as evenly as possible.
+  d.hb_shift = -1;
+  for (int k = 0; k < 31; ++k)
+    if (c.head_bytes == (1 << k)) d.hb_shift = k;
+  // Units: cut a page into runs of about kUnitTargetBytes, as evenly as
+  // possible, of whole rows (NHD, latent) or whole heads (HND).
   if (c.layout == KVCS_LAYOUT_HND) {
     d.rowb = c.head_bytes;
-    const int fit = std::max(1, static_cast<int>(kStageBytes / (static_cast<long long>(block_size) * c.head_bytes)));
+    const long long head = static_cast<long long>(block_size) * c.head_bytes;
+    const int fit = static_cast<int>(std::max<long long>(1, kUnitTargetBytes / head));
     d.upp = (c.num_heads + fit - 1) / fit;
     d.rpu = (c.num_heads + d.upp - 1) / d.upp;
   } else {
     d.rowb = c.layout == KVCS_LAYOUT_NHD ? c.num_heads * c.head_bytes : c.head_bytes;
-    const int fit = std::max(1, kStageBytes / std::max(1, d.rowb));
+    const int fit = std::max(1, kUnitTargetBytes / std::max(1, d.rowb));
     d.upp = (block_size + fit - 1) / fit;
     d.rpu = (block_size + d.upp - 1) / d.upp;
   }
   return d;
+}
+
+// Largest unit of one cache, in bytes.
+long long unit_bytes(const DevCache &d, int block_size) {
+  if (d.layout == KVCS_LAYOUT_HND)
+    return static_cast<long long>(d.rpu) * block_size * d.hb;
+  return static_cast<long long>(d.rpu) * d.rowb;
+}
+
+// Shape of one bulk launch over caches [lo, hi): units per position, pages
+// per unit, stage size and count.
+struct LaunchShape {
+  long long units_per_pos = 0;
+  int ppu = 1;
+  int pages_per_pos = 0;
+  int stage_bytes = 0;
+  int stages = 0;
+};
+
+LaunchShape launch_shape(const kvcs_cache *caches, int lo, int hi, int block_size) {
+  LaunchShape ls;
+  bool uniform = true;
+  long long biggest = 16;
+  for (int i = lo; i < hi; ++i) {
+    const DevCache d = make_dev_cache(caches[i], block_size);
+    ls.units_per_pos += static_cast<long long>(d.halves) * d.upp;
+    ls.pages_per_pos += d.halves;
+    biggest = std::max(biggest, unit_bytes(d, block_size));
+    uniform = uniform && d.upp == 1 && caches[i].layout == caches[lo].layout &&
+              caches[i].num_heads == caches[lo].num_heads &&
+              caches[i].head_bytes == caches[lo].head_bytes;
+  }
+  if (uniform) {
+    // Every page fits a unit and all pages look alike: pack consecutive
+    // pages of a position (e.g. a layer's K and V) into one unit.
+    const DevCache d = make_dev_cache(caches[lo], block_size);
+    const long long page = static_cast<long long>(d.page_bytes);
+    const long long ppu = std::max<long long>(
+        1, std::min<long long>(ls.pages_per_pos, kUnitTargetBytes / page));
+    if (ppu > 1) {
+      ls.ppu = static_cast<int>(ppu);
+      ls.units_per_pos = (ls.pages_per_pos + ls.ppu - 1) / ls.ppu;
+      biggest = ppu * page;
+    }
+  }
+  ls.stage_bytes = static_cast<int>((biggest + 127) / 128 * 128);
+  ls.stages = std::min(kMaxStages, (kSmemLimit - kHeaderBytes) / ls.stage_bytes);
+  return ls;
+}
+
+// Consumer warps per group: the smallest of 1, 2, 4, 8 (at least
+// kMinGroupWarps) that leaves no more groups than stages.
+int group_warps_for(int stages) {
+  int gw = kMinGroupWarps;
+  while (gw < kConsumerWarps && kConsumerWarps / gw > stages) gw *= 2;
+  return gw;
 }
 
 int make_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
@@ -157,13 +222,14 @@ int make_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
   if (bulk) {
     long long upp_max = 0;
     for (int g = 0; g < pl.groups; ++g) {
-      long long U = 0;
-      for (int32_t i = g * kMaxCachesPerLaunch;
-           i < std::min(num_caches, (g + 1) * kMaxCachesPerLaunch); ++i) {
-        const DevCache d = make_dev_cache(caches[i], block_size);
-        U += static_cast<long long>(d.halves) * d.upp;
+      const LaunchShape ls = launch_shape(
+          caches, g * kMaxCachesPerLaunch,
+          std::min(num_caches, (g + 1) * kMaxCachesPerLaunch), block_size);
+      upp_max = std::max(upp_max, ls.units_per_pos);
+      if (g == 0) {
+        pl.stage_bytes = ls.stage_bytes;
+        pl.stages = ls.stages;
       }
-      upp_max = std::max(upp_max, U);
     }
     pl.units = upp_max * total_positions;
     // Whole positions per CTA when that balances well (>= 95% of the even
@@ -212,8 +278,9 @@ int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
   info->memsets = (total_positions > 0 && (pl.groups > 1 || (pl.kernel == 0 && pl.split))) ? 1 : 0;
   info->grid = pl.grid;
   info->threads = pl.kernel == 0 ? kBulkThreads : kGenericThreads;
-  info->smem_bytes = pl.kernel == 0 ? kBulkSmemBytes : 0;
-  info->stage_bytes = pl.kernel == 0 ? kStageBytes : 0;
+  info->smem_bytes = pl.kernel == 0 ? bulk_smem_bytes(pl.stages, pl.stage_bytes) : 0;
+  info->stage_bytes = pl.kernel == 0 ? pl.stage_bytes : 0;
+  info->stages = pl.kernel == 0 ? pl.stages : 0;
   info->units = pl.units;
   info->kv_bytes_max = pl.kv_bytes_max;
   return KVCS_OK;
@@ -272,13 +339,26 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
       p.caches[i - lo] = make_dev_cache(caches[i], block_size);
       U += static_cast<long long>(p.caches[i - lo].halves) * p.caches[i - lo].upp;
     }
+    p.ppu = 1;
+    p.pages_per_pos = 0;
+    if (pl.kernel == 0) {
+      const LaunchShape ls = launch_shape(caches, lo, hi, block_size);
+      U = ls.units_per_pos;
+      p.ppu = ls.ppu;
+      p.pages_per_pos = ls.pages_per_pos;
+      p.stage_bytes = ls.stage_bytes;
+      p.stages = ls.stages;
+    }
     p.units_per_pos = U;
     p.total_units = U * total_positions;
     if (pl.kernel == 0) {
       p.split = pl.split;
+      p.group_warps = group_warps_for(p.stages);
+      p.groups = kConsumerWarps / p.group_warps;
       long long grid = pl.grid;
       if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
-      kvcs_bulk_kernel<<<static_cast<unsigned>(grid), kBulkThreads, kBulkSmemBytes, st>>>(p);
+      kvcs_bulk_kernel<<<static_cast<unsigned>(grid), kBulkThreads,
+                         bulk_smem_bytes(p.stages, p.stage_bytes), st>>>(p);
     } else {
       p.split = 0;
       kvcs_generic_kernel<<<static_cast<unsigned>(pl.grid), kGenericThreads, 0, st>>>(p);

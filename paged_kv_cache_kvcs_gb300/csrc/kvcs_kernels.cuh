@@ -29,12 +29,21 @@ namespace kvcs {
 typedef unsigned long long u64;
 typedef unsigned int u32;
 
-constexpr int kStageBytes = 32768;    // one pipeline stage (max unit size)
-constexpr int kStages = 6;            // stages in the shared-memory ring
-constexpr int kConsumerWarps = 8;     // warps reducing staged data
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kBulkThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kRing = kStages + 2;    // flush slots (see consumer_flush)
+#ifndef KVCS_MIN_GROUP_WARPS
+#define KVCS_MIN_GROUP_WARPS 1
+#endif
+#ifndef KVCS_UNIT_TARGET_BYTES
+#define KVCS_UNIT_TARGET_BYTES 49152
+#endif
+
+constexpr int kConsumerWarps = 8;                  // warps reducing staged data
+constexpr int kMinGroupWarps = KVCS_MIN_GROUP_WARPS;  // warps sharing one unit, at least
+constexpr int kBulkThreads = kConsumerWarps * 32 + 32;  // + one producer warp
+constexpr int kMaxStages = 32;                     // pipeline stages, at most
+constexpr int kRingSlots = kMaxStages + 2;         // per-position accumulators
+constexpr int kUnitTargetBytes = KVCS_UNIT_TARGET_BYTES;
+constexpr int kMaxUnitBytes = 65536;               // keeps >= 3 stages
+constexpr int kSmemLimit = 232448;                 // dynamic smem per CTA
 constexpr int kMaxCachesPerLaunch = 128;
 constexpr int kGenericThreads = 256;
 
@@ -58,11 +67,13 @@ struct DevCache {
   int layout;
   int heads;        // local heads (1 for latent)
   int hb;           // bytes per head per token per half (latent: row bytes)
+  int hb_shift;     // log2(hb) when hb is a power of two, else -1
   int rowb;         // bytes of one staged row: NHD heads*hb, HND hb, latent row
   int P;            // pieces per token: NHD/HND 2 hb / 8, latent row / 8
   int halves;       // 2 (K, V) or 1 (latent)
   int upp;          // units per page
   int rpu;          // rows (NHD, latent) or heads (HND) per unit
+  int pad;
 };
 
 struct Params {
@@ -82,12 +93,19 @@ struct Params {
   int num_caches;
   int all_atomic;            // outputs were zeroed; every result is added
   int split;                 // CTA ranges are in units, not whole positions
+  int stages;                // pipeline stages in shared memory
+  int stage_bytes;           // bytes per stage (multiple of 128)
+  int group_warps;           // consumer warps per group: 1, 2, 4 or 8
+  int groups;                // kConsumerWarps / group_warps, <= stages
+  int ppu;                   // pages per unit: > 1 only when every cache has
+                             // the same geometry and a page fits a unit
+  int pages_per_pos;         // sum of halves over the caches
   DevCache caches[kMaxCachesPerLaunch];
 };
 
 // What the producer tells the consumers about one staged unit.
 struct UnitMeta {
-  long long pos;   // global position index; -1 ends the stream
+  long long pos;   // global position index; -1 ends the group's stream
   long long q;     // block position inside the request
   int cache;
   int half;        // 0: K or latent row, 1: V
@@ -95,7 +113,20 @@ struct UnitMeta {
   int count;       // NHD/latent: slots in the unit; HND: heads in the unit
   int nv;          // valid slots of the block
   int mode;        // kFlushStore or kFlushAtomic
+  int slot;        // accumulator slot of the position
+  int npages;      // consecutive pages in the unit (each packed after the
+                   // previous one's valid bytes)
 };
+
+// Fixed part of the dynamic shared memory; the stages follow it.
+struct SmemHeader {
+  UnitMeta meta[kMaxStages];
+  u64 full[kMaxStages];
+  u64 empty[kMaxStages];
+  u64 ring_acc[kRingSlots];
+  u32 ring_cnt[kRingSlots];
+};
+constexpr int kHeaderBytes = (static_cast<int>(sizeof(SmemHeader)) + 127) / 128 * 128;
 
 __device__ __forceinline__ void set_status(const Params &p, u32 bit) {
   if (p.status) atomicOr(p.status, bit);
@@ -148,10 +179,11 @@ __device__ PosInfo position_info(const Params &p, long long pos, long long r,
     set_status(p, kStatusBadRequests);
     return pi;
   }
-  const long long q = p.first_position[r] + (pos - p.pos_offsets[r]);
+  const long long fp = p.first_position[r];
+  const long long q = fp + (pos - p.pos_offsets[r]);
   const long long nt = p.num_tokens[r];
   const long long b = p.block_ids[pos];
-  if (p.first_position[r] < 0) {
+  if (fp < 0) {
     set_status(p, kStatusBadRequests);
     return pi;
   }
@@ -177,50 +209,64 @@ __device__ PosInfo position_info(const Params &p, long long pos, long long r,
 // Consumer side: reduction of one staged unit
 // ---------------------------------------------------------------------------
 
-// Sum over one staged unit of this thread's share of the block checksum.
-// Staged rows are `rowb` bytes; the thread always reads the same 16-byte
-// column of every row it visits, so the head and piece pair are fixed for it
-// (NHD, latent) or change only at head boundaries (HND).
-__device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
-                                        const unsigned char *stage, int ctid,
-                                        u64 bsz) {
-  const int rowb = C.rowb;
-  const int cols = rowb >> 4;
-  int col0, cstep, rl, rstep;
-  if (cols <= kConsumerThreads) {
-    rstep = kConsumerThreads / cols;
-    rl = ctid / cols;
-    if (rl >= rstep) return 0;
-    col0 = ctid - rl * cols;
-    cstep = cols;
+// How a consumer thread walks staged rows of `rowb` bytes: it always reads
+// the same 16-byte column(s), so for NHD and latent units its head and piece
+// pair are fixed and for HND units they change only at head boundaries.
+struct ThreadMap {
+  int rowb;    // geometry this map was made for (-1: none yet)
+  int cols;    // 16-byte columns per row
+  int col0;    // first column (== cols: this thread is idle)
+  int cstep;   // column stride
+  int rl;      // first row
+  int rstep;   // row stride
+};
+
+__device__ __forceinline__ void make_map(ThreadMap &t, int rowb, int gtid,
+                                         int group_threads) {
+  t.rowb = rowb;
+  t.cols = rowb >> 4;
+  if (t.cols <= group_threads) {
+    t.rstep = group_threads / t.cols;
+    t.rl = gtid / t.cols;
+    t.col0 = gtid - t.rl * t.cols;
+    t.cstep = t.cols;
+    if (t.rl >= t.rstep) t.col0 = t.cols;
   } else {
-    rstep = 1;
-    rl = 0;
-    col0 = ctid;
-    cstep = kConsumerThreads;
+    t.rstep = 1;
+    t.rl = 0;
+    t.col0 = gtid;
+    t.cstep = group_threads;
   }
+}
+
+// This thread's share of one staged unit's contribution to the block
+// checksum (see the reformulation at the top of this file).
+__device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
+                                        int half, const unsigned char *stage,
+                                        const ThreadMap &t, u64 bsz) {
   const u64 P = static_cast<u64>(C.P);
   const u64 t0P = static_cast<u64>(m.q) * bsz * P;
-  const int half_pieces = m.half * (C.hb >> 3);
+  const int half_pieces = half * (C.hb >> 3);
+  const int rowb = t.rowb;
   u64 acc = 0;
   if (C.layout != kLayoutHND) {
     const int nrows = m.count;
     const u32 r0 = static_cast<u32>(m.first);
-    for (int col = col0; col < cols; col += cstep) {
+    for (int col = t.col0; col < t.cols; col += t.cstep) {
       int h_col, p_col;
       if (C.layout == kLayoutNHD) {
         const int cb = col << 4;
-        h_col = cb / C.hb;
+        h_col = C.hb_shift >= 0 ? (cb >> C.hb_shift) : cb / C.hb;
         p_col = ((cb - h_col * C.hb) >> 3) + half_pieces;
       } else {
         h_col = 0;
         p_col = col << 1;
       }
       u64 S = 0, T = 0, U = 0;
-      const unsigned char *sp = stage + static_cast<size_t>(rl) * rowb + (col << 4);
-      const size_t step = static_cast<size_t>(rstep) * rowb;
+      const unsigned char *sp = stage + static_cast<size_t>(t.rl) * rowb + (col << 4);
+      const size_t step = static_cast<size_t>(t.rstep) * rowb;
 #pragma unroll 4
-      for (int r = rl; r < nrows; r += rstep, sp += step) {
+      for (int r = t.rl; r < nrows; r += t.rstep, sp += step) {
         const uint4 v = *reinterpret_cast<const uint4 *>(sp);
         const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
         const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
@@ -238,15 +284,15 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
     // (slots 0 .. nv-1) of hb bytes, packed head after head.
     const int nv = m.nv;
     const int nrows = m.count * nv;
-    for (int col = col0; col < cols; col += cstep) {
-      int r = rl;
+    for (int col = t.col0; col < t.cols; col += t.cstep) {
+      int r = t.rl;
       if (r >= nrows) continue;
       const u64 B = 2ull * (t0P + static_cast<u64>((col << 1) + half_pieces)) + 1ull;
       int hh = r / nv;
       int slot = r - hh * nv;
       u64 S = 0, T = 0, U = 0;
       const unsigned char *sp = stage + static_cast<size_t>(r) * rowb + (col << 4);
-      const size_t step = static_cast<size_t>(rstep) * rowb;
+      const size_t step = static_cast<size_t>(t.rstep) * rowb;
       while (true) {
         const uint4 v = *reinterpret_cast<const uint4 *>(sp);
         const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
@@ -255,9 +301,9 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
         S += X;
         U += x1;
         T += static_cast<u64>(static_cast<u32>(slot)) * X;
-        r += rstep;
+        r += t.rstep;
         sp += step;
-        slot += rstep;
+        slot += t.rstep;
         if (slot >= nv || r >= nrows) {
           const u64 mh = C.m0 + 2ull * static_cast<u64>(m.first + hh);
           acc += mh * (B * S + 2ull * P * T + 2ull * U);
@@ -279,33 +325,14 @@ __device__ __forceinline__ u64 warp_sum(u64 v) {
   return v;
 }
 
-// Combine the consumer warps' sums for one position without a CTA barrier:
-// each warp adds its sum into ring slot `seq % kRing` and bumps the slot's
-// count; the warp that completes the count writes the result and clears the
-// slot.  A warp can run at most kStages units ahead of the slowest one (the
-// producer refills a stage only after every warp released it), hence at most
-// kStages flushes ahead, so kRing = kStages + 2 slots are never reused early.
-// Without a barrier a warp that gave up on a timed-out wait cannot leave the
-// others blocked.
-__device__ __forceinline__ void consumer_flush(const Params &p, u64 *ring_acc,
-                                               u32 *ring_cnt, u32 seq,
-                                               long long pos, int mode, u64 acc,
-                                               int lane) {
-  const u64 v = warp_sum(acc);
-  if (lane == 0) {
-    const u32 slot = seq % kRing;
-    atomicAdd(&ring_acc[slot], v);
-    __threadfence_block();
-    const u32 prev = atomicAdd(&ring_cnt[slot], 1u);
-    if (prev == kConsumerWarps - 1) {
-      __threadfence_block();
-      const u64 total = atomicAdd(&ring_acc[slot], 0ull);
-      ring_acc[slot] = 0;
-      ring_cnt[slot] = 0;
-      if (mode == kFlushStore) p.out[pos] = total;
-      else atomicAdd(p.out + pos, total);
-    }
-  }
+// Write a finished position's checksum: a plain store when this CTA holds
+// every unit of it, else a 64-bit atomic add into the pre-zeroed output.
+__device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
+                                              int slot, long long pos, int mode) {
+  __threadfence_block();
+  const u64 total = atomicAdd(&hdr->ring_acc[slot], 0ull);
+  if (mode == kFlushStore) p.out[pos] = total;
+  else atomicAdd(p.out + pos, total);
 }
 
 // ---------------------------------------------------------------------------
@@ -313,41 +340,56 @@ __device__ __forceinline__ void consumer_flush(const Params &p, u64 *ring_acc,
 // ---------------------------------------------------------------------------
 //
 // Persistent: CTA g owns a contiguous range of work units.  A unit is a run
-// of whole rows of one page (one block's K, its V, or its latent rows) that
-// fits a 32 KiB stage; for HND a unit is a run of whole heads.  When the
-// positions outnumber the CTAs the ranges are whole positions and every
-// result is stored once (no atomics); otherwise they are cut at unit
-// granularity and positions shared by two CTAs are combined with 64-bit
-// atomics into the pre-zeroed output.
+// of whole rows of one page (one block's K, its V, or its latent rows), or
+// of whole heads for HND, of about 16 KiB; the stage size is the launch's
+// largest unit, and as many stages as fit in shared memory form a ring.
+// When the positions outnumber the CTAs the ranges are whole positions and
+// every result is stored once, without atomics; otherwise the ranges are cut
+// at unit granularity and positions shared by two CTAs are combined with
+// 64-bit atomics into the pre-zeroed output.
 //
 // Warp 0, lane 0 is the producer: it walks the range, turns (position,
 // cache, half) into page addresses through the block table and issues one
 // bulk copy per unit (one per head for a partial HND block) into the next
-// free stage, signalling the stage's "full" mbarrier by transaction bytes.
-// Warps 1..8 consume stages in order and release them on the "empty"
-// mbarrier.  Every wait is bounded; a wait that runs out sets
-// KVCS_STATUS_TIMEOUT and the kernel returns without hanging.
+// stage, signalling the stage's "full" mbarrier by transaction bytes.  The
+// consumer warps form `groups` groups of `group_warps` warps; emitted unit i
+// goes to group i % groups, which reduces it, adds its share into the
+// position's accumulator slot and releases the stage on its "empty" mbarrier.
+//
+// Parity waits only tell a phase from the one before it, so a waiter must
+// never be two phases ahead.  Stage s holds units s, s + NS, s + 2 NS, ...
+// consumed by different groups; before waiting for fill f of stage s a group
+// therefore first waits for the release of fill f - 1.  That wait is itself
+// safe because groups <= stages: the group has consumed its own previous
+// unit, so every unit up to f - 1's was emitted, and the producer emitted
+// fill f - 1 only after fill f - 2 was released.
+//
+// A position's slot counts the contributions: each consumer warp adds 1 per
+// unit, and the producer subtracts (warps per group) x (units it emitted)
+// once the position is done.  Whoever brings the count back to zero writes
+// the result, so no CTA-wide barrier is needed and a warp that gave up on a
+// timed-out wait can never block another.  Slots are reused kRingSlots
+// positions later; since a stage is refilled only after it was released, and
+// a contribution is made before its stage is released, a slot's last user
+// has finished long before the producer re-initialises it.
+//
+// Every wait is bounded; a wait that runs out sets KVCS_STATUS_TIMEOUT and
+// the kernel returns without hanging.
 __global__ void __launch_bounds__(kBulkThreads, 1)
     kvcs_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char *stages = smem;
-  UnitMeta *meta = reinterpret_cast<UnitMeta *>(smem + kStages * kStageBytes);
-  u64 *full = reinterpret_cast<u64 *>(meta + kStages);
-  u64 *empty = full + kStages;
-  u64 *ring_acc = empty + kStages;
-  u32 *ring_cnt = reinterpret_cast<u32 *>(ring_acc + kRing);
+  SmemHeader *hdr = reinterpret_cast<SmemHeader *>(smem);
+  unsigned char *stages = smem + kHeaderBytes;
+  const int NS = p.stages;
+  const int SB = p.stage_bytes;
 
   const int tid = threadIdx.x;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(ptx::smem_addr(full + s), 1);
-      ptx::mbar_init(ptx::smem_addr(empty + s), kConsumerWarps);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&hdr->full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&hdr->empty[s]), p.group_warps);
     }
     ptx::fence_barrier_init();
-  }
-  if (tid < kRing) {
-    ring_acc[tid] = 0;
-    ring_cnt[tid] = 0;
   }
   __syncthreads();
 
@@ -372,44 +414,63 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     const u64 policy = ptx::policy_evict_first();
     const long long U = p.units_per_pos;
     const long long bs = p.block_size;
-    u32 it = 0;
+    int s = 0;          // stage of the next unit
+    u32 f = 0;          // fill number of that stage
+    u32 it = 0;         // units emitted
+    u32 seq = 0;        // positions that got an accumulator slot
     bool aborted = false;
     if (u_begin < u_end) {
       long long pos = u_begin / U;
-      int k = static_cast<int>(u_begin - pos * U);
-      int ci = 0;
-      while (k >= p.caches[ci].halves * p.caches[ci].upp) {
-        k -= p.caches[ci].halves * p.caches[ci].upp;
-        ++ci;
+      const int k = static_cast<int>(u_begin - pos * U);
+      int ci = 0, half = 0, sub = 0;
+      if (p.ppu > 1) {
+        const int page = k * p.ppu;
+        ci = page / p.caches[0].halves;
+        half = page - ci * p.caches[0].halves;
+      } else {
+        int kk = k;
+        while (kk >= p.caches[ci].halves * p.caches[ci].upp) {
+          kk -= p.caches[ci].halves * p.caches[ci].upp;
+          ++ci;
+        }
+        half = kk / p.caches[ci].upp;
+        sub = kk - half * p.caches[ci].upp;
       }
-      int half = k / p.caches[ci].upp;
-      int sub = k - half * p.caches[ci].upp;
       long long r = find_request(p, pos);
       PosInfo cur = position_info(p, pos, r, u_begin, u_end);
-      bool emitted = false;
-      for (long long u = u_begin; u < u_end && !aborted; ++u) {
+      int mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
+      int slot = 0;
+      u32 n_emit = 0;
+      for (long long u = u_begin; u < u_end; ++u) {
         const DevCache &C = p.caches[ci];
+        int npg = 1;
+        if (p.ppu > 1) npg = min(p.ppu, p.pages_per_pos - (ci * C.halves + half));
         if (!cur.skip) {
-          int first = sub * C.rpu, count;
-          u32 bytes;
+          const int first = sub * C.rpu;
+          int count;
+          u32 pbytes;   // valid bytes of one page of the unit
           if (C.layout == kLayoutHND) {
             count = max(0, min(C.rpu, C.heads - first));
-            bytes = static_cast<u32>(count) * static_cast<u32>(cur.nv) *
-                    static_cast<u32>(C.hb);
+            pbytes = static_cast<u32>(count) * static_cast<u32>(cur.nv) *
+                     static_cast<u32>(C.hb);
           } else {
             count = max(0, min(C.rpu, cur.nv - first));
-            bytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
+            pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
           }
-          if (bytes > 0) {
-            const int s = static_cast<int>(it % kStages);
-            const u32 f = it / kStages;
-            if (!ptx::mbar_wait_bounded(ptx::smem_addr(empty + s), (f & 1u) ^ 1u,
+          if (pbytes > 0) {
+            if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
                                         p.timeout_ns)) {
               set_status(p, kStatusTimeout);
               aborted = true;
               break;
             }
-            UnitMeta &mm = meta[s];
+            if (n_emit == 0) {
+              slot = static_cast<int>(seq % kRingSlots);
+              ++seq;
+              hdr->ring_acc[slot] = 0ull;
+              hdr->ring_cnt[slot] = 0u;
+            }
+            UnitMeta &mm = hdr->meta[s];
             mm.pos = pos;
             mm.q = cur.q;
             mm.cache = ci;
@@ -417,114 +478,171 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             mm.first = first;
             mm.count = count;
             mm.nv = cur.nv;
-            mm.mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
-            const u32 fb = ptx::smem_addr(full + s);
-            ptx::mbar_arrive_expect_tx(fb, bytes);
-            const unsigned char *page = C.base +
-                static_cast<u64>(half) * C.half_stride +
-                static_cast<u64>(cur.block) * C.page_bytes;
-            const u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * kStageBytes);
-            if (C.layout == kLayoutHND) {
-              const u64 head_stride = static_cast<u64>(bs) * C.hb;
-              if (cur.nv == bs) {
-                ptx::bulk_g2s(dst, page + static_cast<u64>(first) * head_stride,
-                              bytes, fb, policy);
+            mm.mode = mode;
+            mm.slot = slot;
+            mm.npages = npg;
+            const u32 fb = ptx::smem_addr(&hdr->full[s]);
+            ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
+            u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
+            int pci = ci, phalf = half;
+            for (int k2 = 0; k2 < npg; ++k2) {
+              const DevCache &D = p.caches[pci];
+              const unsigned char *page = D.base +
+                  static_cast<u64>(phalf) * D.half_stride +
+                  static_cast<u64>(cur.block) * D.page_bytes;
+              if (D.layout == kLayoutHND) {
+                const u64 head_stride = static_cast<u64>(bs) * D.hb;
+                if (cur.nv == bs) {
+                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * head_stride,
+                                pbytes, fb, policy);
+                } else {
+                  const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(D.hb);
+                  for (int h = 0; h < count; ++h)
+                    ptx::bulk_g2s(dst + static_cast<u32>(h) * run,
+                                  page + static_cast<u64>(first + h) * head_stride,
+                                  run, fb, policy);
+                }
               } else {
-                const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(C.hb);
-                for (int h = 0; h < count; ++h)
-                  ptx::bulk_g2s(dst + static_cast<u32>(h) * run,
-                                page + static_cast<u64>(first + h) * head_stride,
-                                run, fb, policy);
+                ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes,
+                              fb, policy);
               }
-            } else {
-              ptx::bulk_g2s(dst, page + static_cast<u64>(first) * C.rowb, bytes,
-                            fb, policy);
+              dst += pbytes;
+              if (++phalf == D.halves) {
+                phalf = 0;
+                ++pci;
+              }
             }
             ++it;
-            emitted = true;
+            ++n_emit;
+            if (++s == NS) {
+              s = 0;
+              ++f;
+            }
           }
         }
-        // advance to the next unit
-        if (++sub == C.upp) {
+        // advance the cursor past this unit
+        bool pos_done = false;
+        if (p.ppu > 1) {
+          // every cache has C.halves halves when pages are packed
+          const int flat = ci * C.halves + half + npg;
+          ci = flat / C.halves;
+          half = flat - ci * C.halves;
+          pos_done = ci >= p.num_caches;
+        } else if (++sub == C.upp) {
           sub = 0;
           if (++half == C.halves) {
             half = 0;
-            if (++ci == p.num_caches) {
-              ci = 0;
-              // position finished in this CTA
-              if (cur.whole && !emitted && !p.all_atomic) p.out[pos] = 0ull;
-              ++pos;
-              emitted = false;
-              if (u + 1 < u_end) {
-                r = advance_request(p, r, pos);
-                cur = position_info(p, pos, r, u_begin, u_end);
-              }
-            }
+            pos_done = ++ci == p.num_caches;
+          }
+        }
+        if (pos_done) ci = 0;
+        if (pos_done || u + 1 == u_end) {
+          // close the position: this thread's share of the slot count
+          if (n_emit > 0) {
+            const u32 delta = 0u - static_cast<u32>(p.group_warps) * n_emit;
+            const u32 prev = atomicAdd(&hdr->ring_cnt[slot], delta);
+            if (prev + delta == 0u) finalize_slot(p, hdr, slot, pos, mode);
+          } else if (cur.whole && !p.all_atomic) {
+            p.out[pos] = 0ull;
+          }
+          n_emit = 0;
+          if (pos_done && u + 1 < u_end) {
+            ++pos;
+            r = advance_request(p, r, pos);
+            cur = position_info(p, pos, r, u_begin, u_end);
+            mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
           }
         }
       }
     }
     if (!aborted) {
-      // end-of-stream marker
-      const int s = static_cast<int>(it % kStages);
-      const u32 f = it / kStages;
-      if (ptx::mbar_wait_bounded(ptx::smem_addr(empty + s), (f & 1u) ^ 1u,
-                                 p.timeout_ns)) {
-        meta[s].pos = -1;
-        ptx::mbar_arrive(ptx::smem_addr(full + s));
+      // one end-of-stream marker per consumer group
+      for (int k = 0; k < p.groups; ++k) {
+        if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
+                                    p.timeout_ns)) {
+          set_status(p, kStatusTimeout);
+          break;
+        }
+        hdr->meta[s].pos = -1;
+        ptx::mbar_arrive(ptx::smem_addr(&hdr->full[s]));
         ++it;
-      } else {
-        set_status(p, kStatusTimeout);
+        if (++s == NS) {
+          s = 0;
+          ++f;
+        }
       }
     }
     // Wait (bounded) until every copy this thread issued has landed, so no
     // bulk copy is still writing into shared memory when the CTA exits.
-    for (int s = 0; s < kStages; ++s) {
-      if (it > static_cast<u32>(s)) {
-        const u32 last = (it - 1 - s) / kStages;
-        ptx::mbar_wait_bounded(ptx::smem_addr(full + s), last & 1u, p.timeout_ns);
+    for (int st = 0; st < NS; ++st) {
+      if (it > static_cast<u32>(st)) {
+        const u32 last = (it - 1 - st) / static_cast<u32>(NS);
+        ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->full[st]), last & 1u, p.timeout_ns);
       }
     }
     return;
   }
 
   // ------------------------------ consumers -------------------------------
-  const int ctid = tid - 32;
+  const int cw = (tid >> 5) - 1;              // consumer warp 0..7
+  const int gw = p.group_warps;
+  const int group = cw / gw;
+  const int gtid = (cw - group * gw) * 32 + (tid & 31);
   const int lane = tid & 31;
   const u64 bsz = static_cast<u64>(p.block_size);
-  u64 acc = 0;
-  long long cur_pos = -1;
-  int cur_mode = kFlushStore;
-  u32 seq = 0;
-  for (u32 it = 0;; ++it) {
-    const int s = static_cast<int>(it % kStages);
-    const u32 f = it / kStages;
-    if (!ptx::mbar_wait_bounded(ptx::smem_addr(full + s), f & 1u, p.timeout_ns)) {
+  ThreadMap map;
+  map.rowb = -1;
+  int s = group;       // stage of this group's next unit (groups <= stages)
+  u32 f = 0;           // its fill number
+  while (true) {
+    // fill f - 1 of this stage (another group's unit) must be released
+    // before fill f can be told apart from fill f - 2
+    if (f > 0 && !ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]),
+                                         (f - 1u) & 1u, p.timeout_ns)) {
       set_status(p, kStatusTimeout);
       return;
     }
-    const UnitMeta m = meta[s];
-    if (m.pos < 0) break;
-    if (m.pos != cur_pos) {
-      if (cur_pos >= 0) {
-        consumer_flush(p, ring_acc, ring_cnt, seq, cur_pos, cur_mode, acc, lane);
-        ++seq;
-      }
-      cur_pos = m.pos;
-      cur_mode = m.mode;
-      acc = 0;
+    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->full[s]), f & 1u, p.timeout_ns)) {
+      set_status(p, kStatusTimeout);
+      return;
     }
-    acc += unit_sum(p.caches[m.cache], m,
-                    stages + static_cast<size_t>(s) * kStageBytes, ctid, bsz);
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(empty + s));
+    const UnitMeta m = hdr->meta[s];
+    if (m.pos < 0) break;
+    const unsigned char *sp = stages + static_cast<size_t>(s) * SB;
+    int ci = m.cache, half = m.half;
+    u64 v = 0;
+    for (int k = 0; k < m.npages; ++k) {
+      const DevCache &C = p.caches[ci];
+      if (C.rowb != map.rowb) make_map(map, C.rowb, gtid, gw * 32);
+      v += unit_sum(C, m, half, sp, map, bsz);
+      sp += C.layout == kLayoutHND
+                ? static_cast<size_t>(m.count) * m.nv * C.hb
+                : static_cast<size_t>(m.count) * C.rowb;
+      if (++half == C.halves) {
+        half = 0;
+        ++ci;
+      }
+    }
+    v = warp_sum(v);
+    if (lane == 0) {
+      atomicAdd(&hdr->ring_acc[m.slot], v);
+      __threadfence_block();
+      const u32 prev = atomicAdd(&hdr->ring_cnt[m.slot], 1u);
+      if (prev + 1u == 0u) finalize_slot(p, hdr, m.slot, m.pos, m.mode);
+      ptx::mbar_arrive(ptx::smem_addr(&hdr->empty[s]));
+    }
+    s += p.groups;
+    if (s >= NS) {
+      s -= NS;
+      ++f;
+    }
   }
-  if (cur_pos >= 0) consumer_flush(p, ring_acc, ring_cnt, seq, cur_pos, cur_mode, acc, lane);
 }
 
-constexpr int kBulkSmemBytes =
-    kStages * kStageBytes + kStages * static_cast<int>(sizeof(UnitMeta)) +
-    2 * kStages * 8 + kRing * 8 + kRing * 4;
+// Dynamic shared memory of a launch with `stages` stages of `stage_bytes`.
+constexpr int bulk_smem_bytes(int stages, int stage_bytes) {
+  return kHeaderBytes + stages * stage_bytes;
+}
 
 // ---------------------------------------------------------------------------
 // Generic kernel: direct 8-byte loads, any geometry the ABI accepts

@@ -101,17 +101,35 @@ def test_plan_shapes():
     p = plan(llama8b, positions=9220)
     assert p["kernel"] == 0 and p["split"] == 0 and p["memsets"] == 0
     assert p["launches"] == 1 and p["grid"] == 152
-    assert p["units"] == 9220 * 64 and p["stage_bytes"] == 32768
+    # one 32 KiB page (K or V of a layer) per unit
+    assert p["units"] == 9220 * 32 * 2 and p["stage_bytes"] == 32768
+    assert p["stages"] == 7 and p["smem_bytes"] <= 232448
     assert p["kv_bytes_max"] == 9220 * 32 * 2 * 32768
+    # 70B-shaped fp8: 16 KiB pages, a layer's K and V packed into one unit
+    p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=16384)
+    assert p["units"] == 16384 * 80 and p["stage_bytes"] == 32768
     # one 70B-shaped request: too few positions for whole-position CTAs
     p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=128)
     assert p["split"] == 1 and p["memsets"] == 1 and p["grid"] == 152
-    # latent rows of 1152 B: 3 units per 64-slot page
+    # latent rows of 1152 B: three units of at most 22 rows per 64-slot page
     p = plan([FakeCache(layout=2, num_heads=1, head_bytes=1152, layer=i)
               for i in range(61)], bs=64, positions=4096)
     assert p["units"] == 4096 * 61 * 3 and p["split"] == 0
-    # odd per-head bytes: generic kernel
+    assert p["stage_bytes"] == 22 * 1152 and p["stages"] == 9
+    # HND with 16 KiB per head (block_size 64): two heads per unit
+    p = plan([FakeCache(layout=1, layer=i) for i in range(4)], bs=64, positions=500)
+    assert p["units"] == 500 * 4 * 2 * 4 and p["stage_bytes"] == 32768
+    # tiny pages (4 KiB): all four pages of a position in one unit
+    p = plan([FakeCache(layer=i, num_heads=2, head_bytes=128) for i in range(2)],
+             positions=7)
+    assert p["units"] == 7 and p["stage_bytes"] == 16384 and p["split"] == 1
+    # mixed geometry: no packing
+    p = plan([FakeCache(layer=0, head_bytes=128), FakeCache(layer=1, head_bytes=64)],
+             positions=10)
+    assert p["units"] == 10 * 4
+    # odd per-head bytes, or rows too wide to stage: generic kernel
     assert plan([FakeCache(head_bytes=24)])["kernel"] == 1
+    assert plan([FakeCache(num_heads=512, head_bytes=256)])["kernel"] == 1
     # more caches than one launch takes
     p = plan([FakeCache(layer=i, num_heads=1, head_bytes=16) for i in range(300)])
     assert p["launches"] == 3 and p["memsets"] == 1

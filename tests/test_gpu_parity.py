@@ -72,6 +72,16 @@ BULK = [
          lengths=[8] * 152),                          # whole-position mode
     dict(layout=W.LAYOUT_HND, layers=2, heads=2, head_bytes=16, block_size=4,
          lengths=(4,), layer_numbers=(32767, 9), head_offset=65534),
+    dict(layout=W.LAYOUT_HND, layers=2, heads=2, head_bytes=256, block_size=256,
+         lengths=(300, 256)),                         # 64 KiB units, 3 stages
+    dict(layout=W.LAYOUT_NHD, layers=3, heads=8, head_bytes=128, block_size=16,
+         lengths=[37] * 40, first_positions=[1] * 40),  # fp8-shaped, 16 KiB pages
+    dict(layout=W.LAYOUT_HND, layers=5, heads=2, head_bytes=64, block_size=16,
+         lengths=(70, 9, 16)),                        # 2 KiB pages, 10 per unit
+    dict(layout=W.LAYOUT_LATENT, layers=7, heads=1, head_bytes=64, block_size=16,
+         lengths=(33, 100), extra_positions=(1, 0)),  # 1 KiB pages, 7 per unit
+    dict(layout=W.LAYOUT_NHD, layers=6, heads=4, head_bytes=1024, block_size=2,
+         lengths=(11, 4)),                            # 8 KiB pages, 4 per unit
 ]
 
 
@@ -89,6 +99,7 @@ def test_bulk_kernel_matches_oracle(case, seed):
 
 def test_whole_position_mode_is_used():
     wl = W.random_case(0, DEV, **BULK[10])
+    assert wl.num_positions == 304
     plan = K.plan_for(wl.caches, wl.block_size, wl.num_positions)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if wl.num_positions >= sms and (wl.num_positions % sms == 0):
@@ -104,8 +115,8 @@ GENERIC = [
          lengths=(10,), first_positions=(1,)),
     dict(layout=W.LAYOUT_LATENT, layers=2, heads=1, head_bytes=72, block_size=16,
          lengths=(40,), extra_positions=(1,)),
-    dict(layout=W.LAYOUT_HND, layers=1, heads=2, head_bytes=256, block_size=256,
-         lengths=(300,)),                             # head run > one stage
+    dict(layout=W.LAYOUT_HND, layers=1, heads=2, head_bytes=256, block_size=512,
+         lengths=(600,)),                             # head run > 64 KiB
 ]
 
 
@@ -226,3 +237,29 @@ def test_invariance_small():
             assert pb[k] == pa[4 * k:4 * k + 4].sum(dtype=np.uint64)
     exp, _ = oracle(cons)
     assert_equal(b, exp)
+
+
+def test_mixed_geometry_caches():
+    """Caches of different shapes in one call: an attention cache and an
+    indexer cache of layer 0 (consecutive head numbers), an HND layer and a
+    latent layer, all addressed by one block table."""
+    g = torch.Generator(device=DEV).manual_seed(11)
+    base = W.random_case(11, DEV, layers=1, heads=4, head_bytes=128, block_size=16,
+                         lengths=(70, 33, 5))
+    nb = base.caches[0].num_blocks
+    specs = [(W.LAYOUT_NHD, 0, 0, 4, 128), (W.LAYOUT_NHD, 0, 4, 1, 64),
+             (W.LAYOUT_HND, 1, 0, 2, 256), (W.LAYOUT_LATENT, 2, 0, 1, 576),
+             (W.LAYOUT_NHD, 3, 2, 3, 32)]
+    caches = []
+    for layout, layer, off, heads, hb in specs:
+        nbytes = W.pool_bytes(layout, nb, 16, heads, hb)
+        caches.append(W.CacheSpec(W.fill_bytes(nbytes, W.BYTES, g, torch.device(DEV)),
+                                  nb, layout, layer, off, heads, hb))
+    wl = W.Workload("mixed", 16, caches, base.pos_offsets, base.first_position,
+                    base.num_tokens, base.block_ids)
+    plan = K.plan_for(wl.caches, wl.block_size, wl.num_positions)
+    assert plan["kernel"] == 0
+    got, st = gpu(wl)
+    exp, est = oracle(wl)
+    assert st == est == 0
+    assert_equal(got, exp)
