@@ -105,20 +105,20 @@ def test_plan_shapes():
     assert p["units"] == 9220 * 32 * 2 and p["stage_bytes"] == 32768
     assert p["stages"] == 7 and p["smem_bytes"] <= 232448
     assert p["kv_bytes_max"] == 9220 * 32 * 2 * 32768
-    # 70B-shaped fp8: 16 KiB pages, a layer's K and V packed into one unit
+    # 70B-shaped fp8: 16 KiB pages, three consecutive pages packed per unit
     p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=16384)
-    assert p["units"] == 16384 * 80 and p["stage_bytes"] == 32768
+    assert p["units"] == 16384 * 54 and p["stage_bytes"] == 49152 and p["stages"] == 4
     # one 70B-shaped request: too few positions for whole-position CTAs
     p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=128)
     assert p["split"] == 1 and p["memsets"] == 1 and p["grid"] == 152
-    # latent rows of 1152 B: three units of at most 22 rows per 64-slot page
+    # latent rows of 1152 B: two units of 32 rows per 64-slot page
     p = plan([FakeCache(layout=2, num_heads=1, head_bytes=1152, layer=i)
               for i in range(61)], bs=64, positions=4096)
-    assert p["units"] == 4096 * 61 * 3 and p["split"] == 0
-    assert p["stage_bytes"] == 22 * 1152 and p["stages"] == 9
-    # HND with 16 KiB per head (block_size 64): two heads per unit
+    assert p["units"] == 4096 * 61 * 2 and p["split"] == 0
+    assert p["stage_bytes"] == 32 * 1152 and p["stages"] == 6
+    # HND with 16 KiB per head (block_size 64): three heads per unit
     p = plan([FakeCache(layout=1, layer=i) for i in range(4)], bs=64, positions=500)
-    assert p["units"] == 500 * 4 * 2 * 4 and p["stage_bytes"] == 32768
+    assert p["units"] == 500 * 4 * 2 * 3 and p["stage_bytes"] == 49152
     # tiny pages (4 KiB): all four pages of a position in one unit
     p = plan([FakeCache(layer=i, num_heads=2, head_bytes=128) for i in range(2)],
              positions=7)
