@@ -53,8 +53,8 @@ def make_workload(name: str, seed: int, device):
     from paged_kv_cache_kvcs_gb300 import workloads as W
     if name == "llama3_8b":
         return W.llama3_8b(seed, device)
-    if name == "llama3_8b_small":      # ~1 GB: for ncu captures
-        return W.llama3_8b(seed, device, num_requests=8, min_len=1024, max_len=1024)
+    if name == "llama3_8b_small":      # 2.5 GB, 8 x 152 positions: ncu captures
+        return W.llama3_8b(seed, device, num_requests=19, min_len=1024, max_len=1024)
     if name == "mla":
         return W.mla(seed, device)
     if name == "llama3_70b":
@@ -208,22 +208,29 @@ def dist_setup():
     return ws, rank, local
 
 
-def all_max(x: float, ws: int) -> float:
+def _reduce(x: float, ws: int, op: str) -> float:
+    """Reduce one number over the ranks (NCCL on GPUs, gloo on CPUs)."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def all_max(x: float, ws: int) -> float:
+    return _reduce(x, ws, "max")
 
 
 def all_sum(x: float, ws: int) -> float:
-    if ws == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(x, ws, "sum")
+
+
+def job_throughput(local_bytes: float, local_seconds: float, ws: int) -> float:
+    """Whole-job GB/s of replicas: every rank's bytes over the slowest rank's
+    time."""
+    return all_sum(local_bytes, ws) / all_max(local_seconds, ws) / 1e9
 
 
 def barrier(ws: int):
@@ -277,6 +284,24 @@ def oracle_run(wl, n: int, threads: int, seed: int):
     t0 = time.perf_counter()
     c_oracle.block_checksums(caches, wl.block_size, reqs, num_threads=threads)
     return time.perf_counter() - t0, nbytes, npos
+
+
+def oracle_timed(wl, seconds: float, threads: int, seed: int):
+    """About ``seconds`` of oracle work on one sample of the workload (the
+    sample is repeated when the whole workload takes less): (GB/s,
+    blocks/s, description)."""
+    from oracle import c_oracle
+    n = oracle_calibrate(wl, seconds, threads, seed)
+    caches, reqs, nbytes, npos = _oracle_inputs(wl, n, seed + 7)
+    spent, runs = 0.0, 0
+    while runs == 0 or (spent < 0.8 * seconds and runs < 100):
+        t0 = time.perf_counter()
+        c_oracle.block_checksums(caches, wl.block_size, reqs, num_threads=threads)
+        spent += time.perf_counter() - t0
+        runs += 1
+    desc = (f"{npos} random block positions of the workload ({nbytes / 1e9:.2f} GB "
+            f"of KV), {runs} oracle run(s) totalling {spent:.1f} s on {threads} threads")
+    return nbytes * runs / spent / 1e9, npos * runs / spent, desc
 
 
 def oracle_calibrate(wl, seconds: float, threads: int, seed: int) -> int:
@@ -404,14 +429,10 @@ def run_ours(args, ws, rank, local):
     }
     if ws == 1 and not args.no_cpu_baseline:
         cores = host_cores()
-        n = oracle_calibrate(wl, args.cpu_seconds, cores, args.seed)
-        dt, nb, npos = oracle_run(wl, n, cores, args.seed + 7)
-        line["cpu_baseline"] = {
-            "value": round(nb / dt / 1e9, 3), "unit": "GB/s", "cores": cores,
-            "kind": "oracle", "blocks_per_s": round(npos / dt, 2),
-            "sample": f"{npos} random block positions of the workload "
-                      f"({nb / 1e9:.2f} GB of KV), one run of {dt:.1f} s on "
-                      f"{cores} threads"}
+        gbs, bps, desc = oracle_timed(wl, args.cpu_seconds, cores, args.seed)
+        line["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": cores,
+                                "kind": "oracle", "blocks_per_s": round(bps, 2),
+                                "sample": desc}
     print(json.dumps(line), flush=True)
 
 

@@ -176,6 +176,20 @@ typedef struct kvcs_plan_info {
 int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
               int64_t total_positions, int32_t num_sms, kvcs_plan_info *info);
 
+/*
+ * kvcs_selftest_wait_timeout -- check, on the caller's GPU, that a pipeline
+ * wait that can never finish ends with an error status instead of hanging.
+ *
+ * Launches one thread that waits, with the same bounded wait the checksum
+ * kernels use, on a shared-memory mbarrier phase that nothing completes.
+ * After about limit_ns the wait gives up and KVCS_STATUS_TIMEOUT is OR-ed
+ * into *status (a DEVICE word); the context stays usable.
+ *   limit_ns  in (0, 2e9]; else KVCS_EINVAL.
+ * Not part of the checksum; it exists so failure handling can be tested
+ * without faulting or hanging a GPU.
+ */
+int kvcs_selftest_wait_timeout(uint32_t *status, int64_t limit_ns, void *stream);
+
 /* Short text for a return code; never NULL. */
 const char *kvcs_strerror(int code);
 

@@ -64,6 +64,8 @@ SIGNATURES = {
     "kvcs_plan": (ctypes.c_int, [
         ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(kvcs_plan_info)]),
+    "kvcs_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64,
+                                                   ctypes.c_void_p]),
     "kvcs_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "kvcs_launch_count": (ctypes.c_uint64, []),
     "kvcs_version": (ctypes.c_int32, []),
@@ -212,3 +214,13 @@ def plan_for(caches: Sequence, block_size: int, total_positions: int,
              num_sms: int = 0) -> dict:
     return kvcs_plan(cache_array(caches), len(caches), block_size,
                      total_positions, num_sms)
+
+
+def selftest_wait_timeout(status, limit_ns: int, stream=None) -> None:
+    """Run ``kvcs_selftest_wait_timeout`` on an int32 CUDA status tensor."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(status.device).cuda_stream
+    rc = load_library().kvcs_selftest_wait_timeout(status.data_ptr(), limit_ns, stream)
+    if rc != KVCS_OK:
+        raise KvcsError(rc, "kvcs_selftest_wait_timeout")

@@ -369,6 +369,15 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
   return KVCS_OK;
 }
 
+int kvcs_selftest_wait_timeout(uint32_t *status, int64_t limit_ns, void *stream) {
+  if (!status || limit_ns <= 0 || limit_ns > 2000000000LL) return KVCS_EINVAL;
+  kvcs_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      status, static_cast<u64>(limit_ns));
+  if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return KVCS_OK;
+}
+
 const char *kvcs_strerror(int code) {
   switch (code) {
     case KVCS_OK: return "success";

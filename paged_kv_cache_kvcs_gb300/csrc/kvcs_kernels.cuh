@@ -104,7 +104,7 @@ struct Params {
 };
 
 // What the producer tells the consumers about one staged unit.
-struct UnitMeta {
+struct __align__(16) UnitMeta {
   long long pos;   // global position index; -1 ends the group's stream
   long long q;     // block position inside the request
   int cache;
@@ -157,17 +157,40 @@ __device__ long long find_request(const Params &p, long long pos) {
   return lo;
 }
 
-// Step the request cursor to the one holding `pos` (positions only grow).
-__device__ __forceinline__ long long advance_request(const Params &p,
-                                                     long long r, long long pos) {
-  if (r < 0) return find_request(p, pos);
-  while (r < p.num_requests && p.pos_offsets[r + 1] <= pos) ++r;
-  if (r >= p.num_requests || p.pos_offsets[r] > pos) return find_request(p, pos);
-  return r;
+// The producer's view of the request holding the current position; its
+// fields are reloaded only when the position leaves the request.
+struct ReqCursor {
+  long long r;        // request index, -1: none holds the position
+  long long po0, po1; // pos_offsets[r], pos_offsets[r + 1]
+  long long fp, nt;   // first_position[r], num_tokens[r]
+};
+
+__device__ __forceinline__ void req_load(const Params &p, ReqCursor &c, long long r) {
+  c.r = r;
+  if (r < 0) {
+    c.po0 = c.po1 = c.fp = c.nt = 0;
+    return;
+  }
+  c.po0 = p.pos_offsets[r];
+  c.po1 = p.pos_offsets[r + 1];
+  c.fp = p.first_position[r];
+  c.nt = p.num_tokens[r];
 }
 
-__device__ PosInfo position_info(const Params &p, long long pos, long long r,
-                                 long long u_begin, long long u_end) {
+// Move the cursor to the request holding `pos` (positions only grow): the
+// next request is tried with one load before a binary search.
+__device__ __forceinline__ void req_seek(const Params &p, ReqCursor &c, long long pos) {
+  if (c.r >= 0 && pos >= c.po0 && pos < c.po1) return;
+  long long r = -1;
+  if (c.r >= 0 && c.r + 1 < p.num_requests && pos >= c.po1 &&
+      pos < p.pos_offsets[c.r + 2])
+    r = c.r + 1;
+  if (r < 0) r = find_request(p, pos);
+  req_load(p, c, r);
+}
+
+__device__ PosInfo position_info(const Params &p, long long pos, const ReqCursor &c,
+                                 long long b, long long u_begin, long long u_end) {
   PosInfo pi;
   pi.whole = (pos * p.units_per_pos >= u_begin) &&
              ((pos + 1) * p.units_per_pos <= u_end);
@@ -175,15 +198,7 @@ __device__ PosInfo position_info(const Params &p, long long pos, long long r,
   pi.block = 0;
   pi.nv = 0;
   pi.skip = true;
-  if (r < 0) {
-    set_status(p, kStatusBadRequests);
-    return pi;
-  }
-  const long long fp = p.first_position[r];
-  const long long q = fp + (pos - p.pos_offsets[r]);
-  const long long nt = p.num_tokens[r];
-  const long long b = p.block_ids[pos];
-  if (fp < 0) {
+  if (c.r < 0 || c.fp < 0) {
     set_status(p, kStatusBadRequests);
     return pi;
   }
@@ -191,11 +206,12 @@ __device__ PosInfo position_info(const Params &p, long long pos, long long r,
     set_status(p, kStatusBadBlockId);
     return pi;
   }
+  const long long q = c.fp + (pos - c.po0);
   // Tokens of this block below num_tokens: slots [0, nv).
   const long long bs = p.block_size;
   long long nv = 0;
-  if (q <= nt / bs) {  // q * bs <= nt without overflow
-    nv = nt - q * bs;
+  if (q <= c.nt / bs) {  // q * bs <= nt without overflow
+    nv = c.nt - q * bs;
     if (nv > bs) nv = bs;
   }
   pi.q = q;
@@ -203,6 +219,19 @@ __device__ PosInfo position_info(const Params &p, long long pos, long long r,
   pi.nv = static_cast<int>(nv);
   pi.skip = nv <= 0;
   return pi;
+}
+
+// Three 16-byte shared-memory stores of one unit's metadata.
+__device__ __forceinline__ void store_meta(UnitMeta *dst, long long pos, long long q,
+                                           int cache, int half, int first, int count,
+                                           int nv, int mode, int slot, int npages) {
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+  d[0] = make_uint4(static_cast<u32>(pos), static_cast<u32>(static_cast<u64>(pos) >> 32),
+                    static_cast<u32>(q), static_cast<u32>(static_cast<u64>(q) >> 32));
+  d[1] = make_uint4(static_cast<u32>(cache), static_cast<u32>(half),
+                    static_cast<u32>(first), static_cast<u32>(count));
+  d[2] = make_uint4(static_cast<u32>(nv), static_cast<u32>(mode),
+                    static_cast<u32>(slot), static_cast<u32>(npages));
 }
 
 // ---------------------------------------------------------------------------
@@ -436,8 +465,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         half = kk / p.caches[ci].upp;
         sub = kk - half * p.caches[ci].upp;
       }
-      long long r = find_request(p, pos);
-      PosInfo cur = position_info(p, pos, r, u_begin, u_end);
+      ReqCursor rc;
+      rc.r = -1;
+      req_seek(p, rc, pos);
+      long long b_cur = p.block_ids[pos];
+      long long b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
+      PosInfo cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
       int mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
       int slot = 0;
       u32 n_emit = 0;
@@ -470,17 +503,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               hdr->ring_acc[slot] = 0ull;
               hdr->ring_cnt[slot] = 0u;
             }
-            UnitMeta &mm = hdr->meta[s];
-            mm.pos = pos;
-            mm.q = cur.q;
-            mm.cache = ci;
-            mm.half = half;
-            mm.first = first;
-            mm.count = count;
-            mm.nv = cur.nv;
-            mm.mode = mode;
-            mm.slot = slot;
-            mm.npages = npg;
+            store_meta(&hdr->meta[s], pos, cur.q, ci, half, first, count, cur.nv,
+                       mode, slot, npg);
             const u32 fb = ptx::smem_addr(&hdr->full[s]);
             ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
             u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
@@ -548,8 +572,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           n_emit = 0;
           if (pos_done && u + 1 < u_end) {
             ++pos;
-            r = advance_request(p, r, pos);
-            cur = position_info(p, pos, r, u_begin, u_end);
+            b_cur = b_next;
+            b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
+            req_seek(p, rc, pos);
+            cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
             mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
           }
         }
@@ -724,6 +750,21 @@ __global__ void __launch_bounds__(kGenericThreads)
     }
     __syncthreads();
   }
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded wait
+// ---------------------------------------------------------------------------
+
+// One thread waits on a phase of a fresh mbarrier that nothing will ever
+// complete (count 1, no arrival); the bounded wait must give up and report.
+__global__ void kvcs_wait_selftest_kernel(u32 *status, u64 limit_ns) {
+  __shared__ __align__(8) u64 bar;
+  if (threadIdx.x != 0) return;
+  const u32 b = ptx::smem_addr(&bar);
+  ptx::mbar_init(b, 1);
+  ptx::fence_barrier_init();
+  if (!ptx::mbar_wait_bounded(b, 0u, limit_ns)) atomicOr(status, kStatusTimeout);
 }
 
 }  // namespace kvcs
