@@ -38,8 +38,8 @@ extern "C" {
 #endif
 
 /* H in the slice factor: the page's MAX_KV_HEADS_PER_LAYER = 1 << 16.
- * A cache whose global heads reach past it is rejected (the page: groups
- * with more KV heads per layer are not checksummed). */
+ * A cache whose global heads reach past it is rejected: the page leaves
+ * layers with more KV heads than H out of checksumming. */
 #define KVCS_MAX_KV_HEADS_PER_LAYER 65536
 
 /* Bytes per block checksum (the page's BLOCK_CHECKSUM_BYTES: one 64-bit

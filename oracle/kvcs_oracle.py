@@ -16,7 +16,7 @@ the slow, obviously-correct ground truth for small inputs.
 Definition restated (same page, module docstring):
 
 * A *slice* is the KV of one layer and one KV head inside one block: the K and
-  the V of the block's tokens for that head, laid out token by token (per
+  the V of the block's tokens for that head, one token after another (per
   token: the K bytes of the head, then its V bytes) and cut into little-endian
   8-byte pieces.  Piece ``p`` of the token at request position ``t`` has index
   ``j = t*P + p`` where ``P`` is the number of pieces per token.
@@ -24,7 +24,7 @@ Definition restated (same page, module docstring):
 * ``c = sum_{layer, head} m * s mod 2**64`` with
   ``m = 2*(layer*H + head) + 1`` and ``H = MAX_KV_HEADS_PER_LAYER = 1 << 16``
   (item 2; the attribute list of the same page).
-* Slots of the last block at or past ``num_tokens`` are not checksummed
+* Slots of the last block at or past ``num_tokens`` are left out of the sum
   (dataclass ``KVChecksumBlocks``, field ``num_tokens``).
 
 Readings where the page is silent:
@@ -35,7 +35,8 @@ Readings where the page is silent:
 * A block id outside ``[0, num_blocks)`` of any cache makes that position's
   checksum 0 and sets bit ``STATUS_BAD_BLOCK_ID`` in the returned status.
 * Per-token bytes that are not a multiple of 8, and layers with more than
-  ``H`` KV heads, are rejected (the page: such groups "are not checksummed").
+  ``H`` KV heads, are rejected (the page excludes such groups from
+  checksumming).
 """
 
 from __future__ import annotations
@@ -185,7 +186,7 @@ def check_cache(cache: OracleCache, block_size: int) -> None:
     if cache.head_offset < 0 or cache.num_heads < 1:
         raise ValueError("bad head range")
     if cache.head_offset + cache.num_heads > MAX_KV_HEADS_PER_LAYER:
-        raise ValueError("more KV heads per layer than H are not checksummed")
+        raise ValueError("a layer with more than H KV heads is excluded")
     halves = 1 if cache.layout == LAYOUT_LATENT else 2
     need = halves * cache.num_blocks * block_size * cache.num_heads * cache.head_bytes
     if cache.data.size < need:

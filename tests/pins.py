@@ -13,8 +13,8 @@ fix:
   per-piece indexing the oracle uses;
 * the invariants the page states (additivity over block sizes, layout
   independence, TP/PP partials summing to c, sensitivity to a changed piece
-  and to misplaced data), plus the readings for truncation, first positions
-  and bad block ids.
+  and to data moved to another token, block, head or layer), plus the
+  readings for truncation, first positions and bad block ids.
 
 Nothing here calls the oracle's helpers; the expected values are computed
 with independent code so a bug shared by a form and a pin is unlikely.
@@ -369,8 +369,9 @@ def pin_bad_block_id(form):
 
 
 def pin_sensitivity(form):
-    """Any change to a single piece changes c (odd factors); swapped tokens,
-    blocks, heads and layers of unequal data change it (distinct factors)."""
+    """Changing one piece by any nonzero amount changes c (the weights are
+    odd); swapped tokens, blocks, heads and layers of unequal data change it
+    (the factors are distinct)."""
     bs, hb, heads = 2, 16, 2
     _, caches, r = random_pool_case(47, W.LAYOUT_NHD, layers=2, heads=heads,
                                     hb=hb, bs=bs, lengths=[3], spare=0,
