@@ -359,9 +359,11 @@ def run_ours(args, ws, rank, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions)
     nbytes = kv_bytes(wl)
+    ck = kvcs.workload_checksummer(wl)
+    raw_stream = stream.cuda_stream
 
     def step():
-        kvcs.workload_checksums(wl, out=out, status=status, stream=stream)
+        ck(out, status, raw_stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -397,10 +399,38 @@ def run_ours(args, ws, rank, local):
     value = job_bytes / total_s / 1e9
     launch_s = statistics.mean(per)
 
+    # ---- request-count sweep: the first n requests of the workload ----
+    sweep = None
+    if args.sweep:
+        sweep = []
+        n = 1
+        while n <= wl.num_requests:
+            sub = type(wl)(wl.name, wl.block_size, wl.caches, wl.pos_offsets[:n + 1],
+                           wl.first_position[:n], wl.num_tokens[:n],
+                           wl.block_ids[:int(wl.pos_offsets[n])], wl.info)
+            sck = kvcs.workload_checksummer(sub)
+            sb = kv_bytes(sub)
+            k = max(10, min(500, int(2e10 / max(sb, 1))))
+            with torch.cuda.stream(stream):
+                for _ in range(5):
+                    sck(out, status, raw_stream)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(k):
+                    sck(out, status, raw_stream)
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            t = e0.elapsed_time(e1) / 1e3 / k
+            sp = kvcs.plan_for(sub.caches, sub.block_size, sub.num_positions)
+            sweep.append({"requests": n, "kv_bytes": sb, "ms": round(t * 1e3, 4),
+                          "gbs": round(sb / t / 1e9, 1), "split": sp["split"]})
+            n *= 2
+
     # ---- end to end: host buffers through the public API ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, wl, dev, stream, ws)
+        e2e = run_e2e(args, wl, dev, stream, ws, ck)
 
     if rank != 0:
         return
@@ -427,6 +457,8 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
         "e2e": e2e,
     }
+    if sweep is not None:
+        line["sweep"] = sweep
     if ws == 1 and not args.no_cpu_baseline:
         cores = host_cores()
         gbs, bps, desc = oracle_timed(wl, args.cpu_seconds, cores, args.seed)
@@ -436,12 +468,11 @@ def run_ours(args, ws, rank, local):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, wl, dev, stream, ws):
-    """Each step: pinned host -> device copies of every KV pool and of the
+def run_e2e(args, wl, dev, stream, ws, ck):
+    """Each step: pinned host -> device copies of every KV pool (spread over
+    several copy streams, so several copy engines work at once) and of the
     request tables, the checksum call, and a device -> host read of the
     checksums and the status word."""
-    import paged_kv_cache_kvcs_gb300 as kvcs
-
     host_pools = [torch.empty(c.pool.numel(), dtype=torch.uint8, pin_memory=True)
                   for c in wl.caches]
     for h, c in zip(host_pools, wl.caches):
@@ -455,14 +486,25 @@ def run_e2e(args, wl, dev, stream, ws):
     h2d = sum(h.numel() for h in host_pools) + sum(t.numel() * t.element_size() for t in host_tabs)
     d2h = host_out.numel() * 8 + 4
     steps = max(1, min(args.steps, args.e2e_steps))
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(max(1, args.copy_streams))]
+    raw = stream.cuda_stream
 
     def one():
-        for h, c in zip(host_pools, wl.caches):
-            c.pool.copy_(h, non_blocking=True)
+        go = torch.cuda.Event()
+        go.record(stream)                 # the previous step's reads are done
+        for i, (h, c) in enumerate(zip(host_pools, wl.caches)):
+            cs = copy_streams[i % len(copy_streams)]
+            cs.wait_event(go)
+            with torch.cuda.stream(cs):
+                c.pool.copy_(h, non_blocking=True)
         for h, t in zip(host_tabs, tabs):
             t.copy_(h, non_blocking=True)
+        for cs in copy_streams:
+            done = torch.cuda.Event()
+            done.record(cs)
+            stream.wait_event(done)
         status.zero_()
-        kvcs.workload_checksums(wl, out=out, status=status, stream=stream)
+        ck(out, status, raw)
         host_out.copy_(out, non_blocking=True)
         host_status.copy_(status, non_blocking=True)
 
@@ -486,6 +528,7 @@ def run_e2e(args, wl, dev, stream, ws):
     return {"value": round(total / secs / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps, "ms_per_step": round(secs / steps * 1e3, 3),
+            "copy_streams": len(copy_streams),
             "what": "pinned-host KV pools + block tables -> device, checksum, "
                     "checksums -> pinned host, every step"}
 
@@ -500,6 +543,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--copy-streams", type=int, default=4)
+    ap.add_argument("--sweep", action="store_true",
+                    help="also time the first 1, 2, 4, ... requests alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

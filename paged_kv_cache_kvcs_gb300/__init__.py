@@ -16,4 +16,4 @@ from ._binding import (  # noqa: F401
     cache_array, kvcs_block_checksums, kvcs_cache, kvcs_plan, kvcs_plan_info,
     kvcs_requests, launch_count, load_library, plan_for, selftest_wait_timeout,
     strerror, version,
-    workload_checksums)
+    workload_checksums, Checksummer, workload_checksummer)

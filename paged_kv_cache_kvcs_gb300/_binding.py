@@ -202,12 +202,62 @@ def block_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
     return out
 
 
+class Checksummer:
+    """A checksum call prepared once for a fixed set of caches and request
+    arrays: the descriptors are checked and marshalled here, so each call
+    is a single ctypes call into ``kvcs_block_checksums``.
+
+    The request tensors may be refilled in place between calls (for
+    example by host-to-device copies); their addresses must not change.
+    """
+
+    def __init__(self, caches: Sequence, block_size: int, pos_offsets,
+                 first_position, num_tokens, block_ids, total_positions: int):
+        import torch
+        for c in caches:
+            _check_pool(c, block_size)
+        for name, t, dt in (("pos_offsets", pos_offsets, torch.int64),
+                            ("first_position", first_position, torch.int64),
+                            ("num_tokens", num_tokens, torch.int64),
+                            ("block_ids", block_ids, torch.int32)):
+            if not (t.is_cuda and t.dtype == dt and t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+        self._keep = (list(caches), pos_offsets, first_position, num_tokens, block_ids)
+        self.num_caches = len(caches)
+        self.block_size = block_size
+        self.total_positions = total_positions
+        self.caches = cache_array(caches)
+        self.reqs = kvcs_requests(pos_offsets.numel() - 1, pos_offsets.data_ptr(),
+                                  first_position.data_ptr(), num_tokens.data_ptr(),
+                                  block_ids.data_ptr())
+        self._fn = load_library().kvcs_block_checksums
+        self._reqs_ref = ctypes.byref(self.reqs)
+
+    def __call__(self, out, status=None, stream: int | None = None):
+        """Enqueue one call writing ``out`` (int64/uint64 CUDA tensor of at
+        least ``total_positions`` words) on ``stream`` (a raw handle)."""
+        rc = self._fn(self.caches, self.num_caches, self.block_size, self._reqs_ref,
+                      self.total_positions,
+                      out.data_ptr() if self.total_positions > 0 else None,
+                      status.data_ptr() if status is not None else None,
+                      stream or None)
+        if rc != KVCS_OK:
+            raise KvcsError(rc, "kvcs_block_checksums")
+        return out
+
+
 def workload_checksums(wl, out=None, status=None, stream=None):
     """``block_checksums`` over a ``workloads.Workload``."""
     return block_checksums(wl.caches, wl.block_size, wl.pos_offsets,
                            wl.first_position, wl.num_tokens, wl.block_ids,
                            out=out, status=status, stream=stream,
                            total_positions=wl.num_positions)
+
+
+def workload_checksummer(wl) -> Checksummer:
+    """A prepared call over a ``workloads.Workload``."""
+    return Checksummer(wl.caches, wl.block_size, wl.pos_offsets, wl.first_position,
+                       wl.num_tokens, wl.block_ids, wl.num_positions)
 
 
 def plan_for(caches: Sequence, block_size: int, total_positions: int,

@@ -263,3 +263,24 @@ def test_mixed_geometry_caches():
     exp, est = oracle(wl)
     assert st == est == 0
     assert_equal(got, exp)
+
+
+def test_prepared_call_matches_and_follows_refilled_tables():
+    wl = W.random_case(12, DEV, layers=3, heads=2, head_bytes=64, block_size=8,
+                       lengths=(50, 17), spare_blocks=4)
+    ck = K.workload_checksummer(wl)
+    out = torch.empty(wl.num_positions, dtype=torch.int64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ck(out, st, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    exp, _ = oracle(wl)
+    assert_equal(out.cpu().numpy().view(np.uint64), exp)
+    # refill the block table in place (same addresses): the prepared call
+    # reads the new ids
+    perm = torch.randperm(wl.caches[0].num_blocks, generator=torch.Generator().manual_seed(3))
+    wl.block_ids.copy_(perm[:wl.num_positions].to(torch.int32).to(DEV))
+    ck(out, st, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    exp2, _ = oracle(wl)
+    assert int(st.item()) == 0
+    assert_equal(out.cpu().numpy().view(np.uint64), exp2)
