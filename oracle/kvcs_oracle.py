@@ -241,3 +241,53 @@ def combine_partials(parts: Sequence[Sequence[int]]) -> list[int]:
     """Partials from TP ranks and PP stages sum to ``c`` (module docstring,
     the paragraph on TP ranks and PP stages): element-wise sum mod 2**64."""
     return [sum(col) & MASK64 for col in zip(*parts)]
+
+
+# ---------------------------------------------------------------------------
+# Replica-key columns, offload row sums and block tags
+# ---------------------------------------------------------------------------
+
+def column_checksums(caches: Sequence[OracleCache], columns: Sequence[int],
+                     num_columns: int, block_size: int,
+                     requests: OracleRequests) -> tuple[list[list[int]], int]:
+    """``values[i][k]``: the partial checksum of position ``i`` over the
+    caches whose replica-key column is ``k`` (paragraph on replicated KV:
+    one partial per key of the layers it covers; dataclass
+    ``KVChecksumGroup``, field ``values``)."""
+    total = requests.pos_offsets[-1] if requests.pos_offsets else 0
+    values = [[0] * num_columns for _ in range(total)]
+    status = 0
+    for k in range(num_columns):
+        sub = [c for c, col in zip(caches, columns) if col == k]
+        vals, st = block_checksums(sub, block_size, requests)
+        status |= st
+        for i, v in enumerate(vals):
+            values[i][k] = v
+    return values, status
+
+
+def row_sums(values: Sequence[Sequence[int]], tags: Sequence[int] | None = None) -> list[int]:
+    """A row's partial checksums summed mod 2**64 (dataclass
+    ``KVChecksumGroup``, field ``stored``), XORed with the block's tag when
+    one is given (function ``block_checksum_tags``)."""
+    out = []
+    for i, row in enumerate(values):
+        r = sum(row) & MASK64
+        if tags is not None:
+            r ^= tags[i]
+        out.append(r)
+    return out
+
+
+def block_checksum_tags(block_hashes: Sequence[bytes], fingerprint: int) -> list[int]:
+    """Per block, the 64-bit word an offloaded checksum is XORed with
+    (function ``block_checksum_tags``): the first eight bytes of the block's
+    hash read as a little-endian unsigned integer, XOR the group's
+    fingerprint."""
+    tags = []
+    for h in block_hashes:
+        word = 0
+        for k in range(8):
+            word += h[k] * (256 ** k)
+        tags.append(word ^ (fingerprint & MASK64))
+    return tags

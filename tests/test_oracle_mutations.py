@@ -101,3 +101,19 @@ def test_missing_mod_reduction_is_caught(monkeypatch):
     monkeypatch.setattr(O, "block_checksum", no_mask)
     assert _fails_some_pin() is not None
     monkeypatch.setattr(O, "block_checksum", orig)
+
+
+TAG_MUTANTS = {
+    "tag_big_endian": lambda hs, fp: [int.from_bytes(h[:8], "big") ^ fp for h in hs],
+    "tag_last_bytes": lambda hs, fp: [int.from_bytes(h[-8:], "little") ^ fp for h in hs],
+    "tag_no_fingerprint": lambda hs, fp: [int.from_bytes(h[:8], "little") for h in hs],
+    "tag_four_bytes": lambda hs, fp: [int.from_bytes(h[:4], "little") ^ fp for h in hs],
+}
+
+
+@pytest.mark.parametrize("name", sorted(TAG_MUTANTS))
+def test_tag_mutant_is_caught(name, monkeypatch):
+    import test_oracle_next1 as T
+    monkeypatch.setattr(O, "block_checksum_tags", TAG_MUTANTS[name])
+    with pytest.raises(AssertionError):
+        T.test_tags_hand_worked()
