@@ -75,7 +75,8 @@ typedef struct kvcs_cache {
   int32_t head_bytes;  /* NHD/HND: bytes of one head's K (= its V) for one
                           token; LATENT: bytes of one token row.  A positive
                           multiple of 8. */
-  int32_t reserved;    /* must be 0 */
+  int32_t column;      /* replica-key column this cache's layer adds into
+                          (kvcs_group_checksums); 0 for kvcs_block_checksums */
 } kvcs_cache;
 
 /* The requests to checksum, in CSR form over requests.  All pointers are
@@ -101,9 +102,10 @@ typedef struct kvcs_requests {
 #define KVCS_EINVAL (-1)      /* null pointer, non-positive block_size,
                                  head_bytes not a positive multiple of 8,
                                  unknown layout, latent cache with heads != 1,
-                                 negative layer or head offset, reserved != 0,
-                                 misaligned base, two caches covering the same
-                                 (layer, global head) */
+                                 negative layer or head offset, a column
+                                 outside [0, num_columns) or a column with no
+                                 cache, misaligned base, two caches covering
+                                 the same (layer, global head) */
 #define KVCS_EUNSUPPORTED (-2) /* head_offset + num_heads > 65536 */
 #define KVCS_ECUDA (-3)       /* a CUDA call failed (launch, attribute query);
                                  work may have been partly enqueued */
@@ -148,6 +150,68 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
                          int32_t block_size, const kvcs_requests *reqs,
                          int64_t total_positions, uint64_t *out,
                          uint32_t *status, void *stream);
+
+/*
+ * Per-position outputs of kvcs_group_checksums.  All pointers are DEVICE
+ * pointers owned by the caller.
+ *
+ * Replicated KV (MLA, or GQA with more TP ranks than KV heads) is tracked per
+ * replica: a worker keeps one partial checksum per replica key
+ * (replicas, replica_index) of the layers it covers (the checksum page,
+ * paragraph on replicated KV; dataclass KVChecksumGroup, field values).  Each
+ * cache names its column; values[i * num_columns + k] is position i's partial
+ * over the caches of column k.
+ *
+ * A load of offloaded KV is checked against the checksums offloaded with it:
+ * each row's partials summed (KVChecksumGroup, field stored), XORed with the
+ * block's tag (function block_checksum_tags) so that it matches only the
+ * block it was stored for.
+ */
+typedef struct kvcs_outputs {
+  int32_t num_columns;       /* >= 1 and <= 64 */
+  int32_t reserved;          /* must be 0 */
+  uint64_t *values;          /* required: [total_positions][num_columns] */
+  uint64_t *row_sums;        /* or NULL: [total_positions], sum of the row's
+                                values XOR tags[i] (when tags is given) */
+  const uint64_t *tags;      /* or NULL: [total_positions] */
+  const uint64_t *expected;  /* or NULL: [total_positions], the stored values
+                                to verify against */
+  uint8_t *mismatch;         /* or NULL (needs expected): [total_positions],
+                                1 where the tagged row sum != expected, else 0 */
+  uint32_t *mismatch_count;  /* or NULL (needs expected): mismatching
+                                positions are added to this word */
+} kvcs_outputs;
+
+/*
+ * kvcs_group_checksums -- partial checksums per replica-key column, and
+ * optionally the tagged row sums and their comparison with stored values.
+ *
+ * Arguments as kvcs_block_checksums, with the outputs in *outs (a HOST
+ * pointer).  Every column in [0, num_columns) must be named by at least one
+ * cache.  With one column, values equals kvcs_block_checksums' output.
+ * Row sums, tags and the comparison cost one small extra kernel launch that
+ * reads values (8 * num_columns bytes per position).
+ */
+int kvcs_group_checksums(const kvcs_cache *caches, int32_t num_caches,
+                         int32_t block_size, const kvcs_requests *reqs,
+                         int64_t total_positions, const kvcs_outputs *outs,
+                         uint32_t *status, void *stream);
+
+/*
+ * kvcs_block_checksum_tags -- the 64-bit tag of each block (the checksum
+ * page, function block_checksum_tags): the first eight bytes of the block's
+ * hash read as a little-endian integer, XOR the group's fingerprint.
+ *
+ *   block_hashes  DEVICE bytes; hash i starts at block_hashes + i*hash_stride
+ *   hash_stride   bytes between consecutive hashes, >= 8
+ *   n             number of blocks (>= 0)
+ *   fingerprint   the group's fingerprint (sum over PP stages of its layers'
+ *                 hashes; computed by the caller)
+ *   tags          DEVICE uint64[n]
+ */
+int kvcs_block_checksum_tags(const void *block_hashes, int64_t hash_stride,
+                             int64_t n, uint64_t fingerprint, uint64_t *tags,
+                             void *stream);
 
 /* Which kernel and launch shape kvcs_block_checksums would use.  Filled by
  * kvcs_plan; no CUDA work is enqueued. */

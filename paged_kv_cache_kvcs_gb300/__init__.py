@@ -16,4 +16,5 @@ from ._binding import (  # noqa: F401
     cache_array, kvcs_block_checksums, kvcs_cache, kvcs_plan, kvcs_plan_info,
     kvcs_requests, launch_count, load_library, plan_for, selftest_wait_timeout,
     strerror, version,
-    workload_checksums, Checksummer, workload_checksummer)
+    workload_checksums, Checksummer, workload_checksummer, kvcs_outputs,
+    group_checksums, block_checksum_tags)

@@ -32,7 +32,14 @@ class kvcs_cache(ctypes.Structure):
     _fields_ = [("base", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
                 ("layout", ctypes.c_int32), ("layer", ctypes.c_int32),
                 ("head_offset", ctypes.c_int32), ("num_heads", ctypes.c_int32),
-                ("head_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("head_bytes", ctypes.c_int32), ("column", ctypes.c_int32)]
+
+
+class kvcs_outputs(ctypes.Structure):
+    _fields_ = [("num_columns", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("values", ctypes.c_void_p), ("row_sums", ctypes.c_void_p),
+                ("tags", ctypes.c_void_p), ("expected", ctypes.c_void_p),
+                ("mismatch", ctypes.c_void_p), ("mismatch_count", ctypes.c_void_p)]
 
 
 class kvcs_requests(ctypes.Structure):
@@ -60,6 +67,13 @@ SIGNATURES = {
     "kvcs_block_checksums": (ctypes.c_int, [
         ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
         ctypes.POINTER(kvcs_requests), ctypes.c_int64, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p]),
+    "kvcs_group_checksums": (ctypes.c_int, [
+        ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
+        ctypes.POINTER(kvcs_requests), ctypes.c_int64, ctypes.POINTER(kvcs_outputs),
+        ctypes.c_void_p, ctypes.c_void_p]),
+    "kvcs_block_checksum_tags": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
         ctypes.c_void_p, ctypes.c_void_p]),
     "kvcs_plan": (ctypes.c_int, [
         ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
@@ -118,7 +132,7 @@ def cache_array(caches: Sequence) -> ctypes.Array:
         pool = c.pool
         base = pool if isinstance(pool, int) else pool.data_ptr()
         arr[i] = kvcs_cache(base, c.num_blocks, c.layout, c.layer, c.head_offset,
-                            c.num_heads, c.head_bytes, 0)
+                            c.num_heads, c.head_bytes, getattr(c, "column", 0))
     return arr
 
 
@@ -274,3 +288,66 @@ def selftest_wait_timeout(status, limit_ns: int, stream=None) -> None:
     rc = load_library().kvcs_selftest_wait_timeout(status.data_ptr(), limit_ns, stream)
     if rc != KVCS_OK:
         raise KvcsError(rc, "kvcs_selftest_wait_timeout")
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def group_checksums(caches: Sequence, block_size: int, pos_offsets, first_position,
+                    num_tokens, block_ids, num_columns: int, values=None,
+                    row_sums=None, tags=None, expected=None, mismatch=None,
+                    mismatch_count=None, status=None, stream=None,
+                    total_positions: int | None = None):
+    """Torch front end of ``kvcs_group_checksums``.  Each cache names its
+    replica-key ``column``; returns ``values`` (int64 CUDA tensor
+    ``[total_positions, num_columns]`` holding uint64 bits).  ``row_sums``,
+    ``tags``, ``expected`` are int64 CUDA tensors of ``total_positions``;
+    ``mismatch`` a uint8 one; ``mismatch_count`` an int32 one-element one."""
+    import torch
+    for c in caches:
+        _check_pool(c, block_size)
+    if total_positions is None:
+        total_positions = int(pos_offsets[-1].item())
+    dev = pos_offsets.device
+    if values is None:
+        values = torch.empty((max(total_positions, 0), num_columns), dtype=torch.int64,
+                             device=dev)
+    outs = kvcs_outputs(num_columns, 0, values.data_ptr() if total_positions > 0 else None,
+                        _ptr(row_sums), _ptr(tags), _ptr(expected), _ptr(mismatch),
+                        _ptr(mismatch_count))
+    reqs = kvcs_requests(pos_offsets.numel() - 1, pos_offsets.data_ptr(),
+                         first_position.data_ptr(), num_tokens.data_ptr(),
+                         block_ids.data_ptr())
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    arr = cache_array(caches)
+    rc = load_library().kvcs_group_checksums(arr, len(caches), block_size,
+                                             ctypes.byref(reqs), total_positions,
+                                             ctypes.byref(outs), _ptr(status), stream)
+    if rc != KVCS_OK:
+        raise KvcsError(rc, "kvcs_group_checksums")
+    return values
+
+
+def block_checksum_tags(block_hashes, fingerprint: int, tags=None, stream=None):
+    """Torch front end of ``kvcs_block_checksum_tags``: ``block_hashes`` is a
+    uint8 CUDA tensor ``[n, hash_bytes]`` (hash_bytes >= 8); returns an int64
+    tensor of ``n`` tags (uint64 bits)."""
+    import torch
+    if not (block_hashes.is_cuda and block_hashes.dtype == torch.uint8
+            and block_hashes.dim() == 2 and block_hashes.stride(1) == 1):
+        raise ValueError("block_hashes must be a CUDA uint8 [n, hash_bytes] tensor")
+    n = block_hashes.shape[0]
+    if tags is None:
+        tags = torch.empty(n, dtype=torch.int64, device=block_hashes.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(block_hashes.device).cuda_stream
+    rc = load_library().kvcs_block_checksum_tags(
+        block_hashes.data_ptr() if n else None, block_hashes.stride(0), n,
+        fingerprint & ((1 << 64) - 1), tags.data_ptr() if n else None, stream)
+    if rc != KVCS_OK:
+        raise KvcsError(rc, "kvcs_block_checksum_tags")
+    return tags

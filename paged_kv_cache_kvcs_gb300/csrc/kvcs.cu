@@ -79,10 +79,15 @@ bool bulk_eligible(const kvcs_cache &c, int block_size) {
   }
 }
 
-// Host-argument checks shared by kvcs_plan and kvcs_block_checksums.
+constexpr int kMaxColumns = 64;
+
+// Host-argument checks shared by every entry point.  Every column in
+// [0, num_columns) must be named by at least one cache.
 int validate_caches(const kvcs_cache *caches, int32_t num_caches,
-                    int32_t block_size) {
+                    int32_t block_size, int32_t num_columns) {
   if (!caches || num_caches < 1 || block_size <= 0) return KVCS_EINVAL;
+  if (num_columns < 1 || num_columns > kMaxColumns) return KVCS_EINVAL;
+  bool used[kMaxColumns] = {false};
   struct Span {
     int32_t layer;
     int64_t lo, hi;
@@ -91,7 +96,9 @@ int validate_caches(const kvcs_cache *caches, int32_t num_caches,
   spans.reserve(num_caches);
   for (int32_t i = 0; i < num_caches; ++i) {
     const kvcs_cache &c = caches[i];
-    if (!c.base || c.num_blocks < 0 || c.reserved != 0) return KVCS_EINVAL;
+    if (!c.base || c.num_blocks < 0) return KVCS_EINVAL;
+    if (c.column < 0 || c.column >= num_columns) return KVCS_EINVAL;
+    used[c.column] = true;
     if (c.layout < KVCS_LAYOUT_NHD || c.layout > KVCS_LAYOUT_LATENT) return KVCS_EINVAL;
     if (c.layer < 0 || c.head_offset < 0 || c.num_heads < 1) return KVCS_EINVAL;
     if (c.head_bytes <= 0 || c.head_bytes % 8) return KVCS_EINVAL;
@@ -112,7 +119,19 @@ int validate_caches(const kvcs_cache *caches, int32_t num_caches,
   for (size_t i = 1; i < spans.size(); ++i)
     if (spans[i].layer == spans[i - 1].layer && spans[i].lo < spans[i - 1].hi)
       return KVCS_EINVAL;  // two caches weigh the same (layer, global head)
+  for (int k = 0; k < num_columns; ++k)
+    if (!used[k]) return KVCS_EINVAL;  // a column no cache adds into
   return KVCS_OK;
+}
+
+// The caches in column order (stable): a column's units are then
+// consecutive within every position, which the kernels rely on.
+std::vector<kvcs_cache> by_column(const kvcs_cache *caches, int32_t num_caches) {
+  std::vector<kvcs_cache> v(caches, caches + num_caches);
+  std::stable_sort(v.begin(), v.end(), [](const kvcs_cache &a, const kvcs_cache &b) {
+    return a.column < b.column;
+  });
+  return v;
 }
 
 DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
@@ -128,6 +147,7 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
   d.half_stride = static_cast<u64>(c.num_blocks) * d.page_bytes;
   d.halves = c.layout == KVCS_LAYOUT_LATENT ? 1 : 2;
   d.P = (c.layout == KVCS_LAYOUT_LATENT ? c.head_bytes : 2 * c.head_bytes) / 8;
+  d.column = c.column;
   d.hb_shift = -1;
   for (int k = 0; k < 31; ++k)
     if (c.head_bytes == (1 << k)) d.hb_shift = k;
@@ -175,6 +195,7 @@ LaunchShape launch_shape(const kvcs_cache *caches, int lo, int hi, int block_siz
     ls.pages_per_pos += d.halves;
     biggest = std::max(biggest, unit_bytes(d, block_size));
     uniform = uniform && d.upp == 1 && caches[i].layout == caches[lo].layout &&
+              caches[i].column == caches[lo].column &&
               caches[i].num_heads == caches[lo].num_heads &&
               caches[i].head_bytes == caches[lo].head_bytes;
   }
@@ -258,56 +279,35 @@ int make_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
 
 using namespace kvcs;
 
-extern "C" {
+namespace {
 
-int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
-              int64_t total_positions, int32_t num_sms, kvcs_plan_info *info) {
-  if (!info || total_positions < 0) return KVCS_EINVAL;
-  int rc = validate_caches(caches, num_caches, block_size);
-  if (rc != KVCS_OK) return rc;
-  int sms = num_sms;
-  if (sms <= 0) {
-    if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
-  }
-  Plan pl;
-  make_plan(caches, num_caches, block_size, total_positions, sms, &pl);
-  std::memset(info, 0, sizeof(*info));
-  info->kernel = pl.kernel;
-  info->split = pl.kernel == 0 ? pl.split : 0;
-  info->launches = total_positions > 0 ? pl.groups : 0;
-  info->memsets = (total_positions > 0 && (pl.groups > 1 || (pl.kernel == 0 && pl.split))) ? 1 : 0;
-  info->grid = pl.grid;
-  info->threads = pl.kernel == 0 ? kBulkThreads : kGenericThreads;
-  info->smem_bytes = pl.kernel == 0 ? bulk_smem_bytes(pl.stages, pl.stage_bytes) : 0;
-  info->stage_bytes = pl.kernel == 0 ? pl.stage_bytes : 0;
-  info->stages = pl.kernel == 0 ? pl.stages : 0;
-  info->units = pl.units;
-  info->kv_bytes_max = pl.kv_bytes_max;
-  return KVCS_OK;
-}
-
-int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
-                         int32_t block_size, const kvcs_requests *reqs,
-                         int64_t total_positions, uint64_t *out,
-                         uint32_t *status, void *stream) {
-  int rc = validate_caches(caches, num_caches, block_size);
+// Shared body of kvcs_block_checksums and kvcs_group_checksums.
+int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block_size,
+                  const kvcs_requests *reqs, int64_t total_positions,
+                  const kvcs_outputs *outs, uint32_t *status, cudaStream_t st) {
+  if (!outs || outs->reserved != 0) return KVCS_EINVAL;
+  const int ncols = outs->num_columns;
+  int rc = validate_caches(caches_in, num_caches, block_size, ncols);
   if (rc != KVCS_OK) return rc;
   if (!reqs || total_positions < 0 || reqs->num_requests < 0) return KVCS_EINVAL;
+  if ((outs->mismatch || outs->mismatch_count) && !outs->expected) return KVCS_EINVAL;
   if (total_positions == 0) return KVCS_OK;
-  if (!out || !reqs->pos_offsets || !reqs->first_position || !reqs->num_tokens ||
-      !reqs->block_ids)
+  if (!outs->values || !reqs->pos_offsets || !reqs->first_position ||
+      !reqs->num_tokens || !reqs->block_ids)
     return KVCS_EINVAL;
-  if (reinterpret_cast<uintptr_t>(out) % 8) return KVCS_EINVAL;
+  if (reinterpret_cast<uintptr_t>(outs->values) % 8) return KVCS_EINVAL;
 
   int sms = 0;
   if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
+  const std::vector<kvcs_cache> sorted = by_column(caches_in, num_caches);
+  const kvcs_cache *caches = sorted.data();
   Plan pl;
   make_plan(caches, num_caches, block_size, total_positions, sms, &pl);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   const bool all_atomic = pl.groups > 1;
   if (all_atomic || (pl.kernel == 0 && pl.split)) {
-    if (cudaMemsetAsync(out, 0, static_cast<size_t>(total_positions) * sizeof(uint64_t),
+    if (cudaMemsetAsync(outs->values, 0,
+                        static_cast<size_t>(total_positions) * ncols * sizeof(uint64_t),
                         st) != cudaSuccess)
       return KVCS_ECUDA;
   }
@@ -321,7 +321,7 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
   p.first_position = reinterpret_cast<const long long *>(reqs->first_position);
   p.num_tokens = reinterpret_cast<const long long *>(reqs->num_tokens);
   p.block_ids = reinterpret_cast<const int *>(reqs->block_ids);
-  p.out = reinterpret_cast<u64 *>(out);
+  p.out = reinterpret_cast<u64 *>(outs->values);
   p.status = status;
   p.num_requests = reqs->num_requests;
   p.total_positions = total_positions;
@@ -329,6 +329,7 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
   p.timeout_ns = kTimeoutNs;
   p.block_size = block_size;
   p.all_atomic = all_atomic ? 1 : 0;
+  p.num_columns = ncols;
 
   for (int g = 0; g < pl.groups; ++g) {
     const int lo = g * kMaxCachesPerLaunch;
@@ -366,6 +367,97 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
     if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }
+
+  if (outs->row_sums || outs->expected) {
+    RowParams rp;
+    rp.values = reinterpret_cast<const u64 *>(outs->values);
+    rp.n = total_positions;
+    rp.num_columns = ncols;
+    rp.row_sums = reinterpret_cast<u64 *>(outs->row_sums);
+    rp.tags = reinterpret_cast<const u64 *>(outs->tags);
+    rp.expected = reinterpret_cast<const u64 *>(outs->expected);
+    rp.mismatch = outs->mismatch;
+    rp.mismatch_count = outs->mismatch_count;
+    const long long blocks = std::min<long long>((total_positions + 255) / 256, 4LL * sms);
+    kvcs_rows_kernel<<<static_cast<unsigned>(std::max<long long>(1, blocks)), 256, 0, st>>>(rp);
+    if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return KVCS_OK;
+}
+
+int columns_of(const kvcs_cache *caches, int32_t num_caches) {
+  int m = 0;
+  for (int32_t i = 0; caches && i < num_caches; ++i) m = std::max(m, caches[i].column + 1);
+  return std::max(1, m);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+              int64_t total_positions, int32_t num_sms, kvcs_plan_info *info) {
+  if (!info || total_positions < 0) return KVCS_EINVAL;
+  int rc = validate_caches(caches, num_caches, block_size, columns_of(caches, num_caches));
+  if (rc != KVCS_OK) return rc;
+  int sms = num_sms;
+  if (sms <= 0) {
+    if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
+  }
+  const std::vector<kvcs_cache> sorted = by_column(caches, num_caches);
+  Plan pl;
+  make_plan(sorted.data(), num_caches, block_size, total_positions, sms, &pl);
+  std::memset(info, 0, sizeof(*info));
+  info->kernel = pl.kernel;
+  info->split = pl.kernel == 0 ? pl.split : 0;
+  info->launches = total_positions > 0 ? pl.groups : 0;
+  info->memsets = (total_positions > 0 && (pl.groups > 1 || (pl.kernel == 0 && pl.split))) ? 1 : 0;
+  info->grid = pl.grid;
+  info->threads = pl.kernel == 0 ? kBulkThreads : kGenericThreads;
+  info->smem_bytes = pl.kernel == 0 ? bulk_smem_bytes(pl.stages, pl.stage_bytes) : 0;
+  info->stage_bytes = pl.kernel == 0 ? pl.stage_bytes : 0;
+  info->stages = pl.kernel == 0 ? pl.stages : 0;
+  info->units = pl.units;
+  info->kv_bytes_max = pl.kv_bytes_max;
+  return KVCS_OK;
+}
+
+int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
+                         int32_t block_size, const kvcs_requests *reqs,
+                         int64_t total_positions, uint64_t *out,
+                         uint32_t *status, void *stream) {
+  kvcs_outputs o;
+  std::memset(&o, 0, sizeof(o));
+  o.num_columns = 1;
+  o.values = out;
+  return run_checksums(caches, num_caches, block_size, reqs, total_positions, &o,
+                       status, static_cast<cudaStream_t>(stream));
+}
+
+int kvcs_group_checksums(const kvcs_cache *caches, int32_t num_caches,
+                         int32_t block_size, const kvcs_requests *reqs,
+                         int64_t total_positions, const kvcs_outputs *outs,
+                         uint32_t *status, void *stream) {
+  return run_checksums(caches, num_caches, block_size, reqs, total_positions, outs,
+                       status, static_cast<cudaStream_t>(stream));
+}
+
+int kvcs_block_checksum_tags(const void *block_hashes, int64_t hash_stride,
+                             int64_t n, uint64_t fingerprint, uint64_t *tags,
+                             void *stream) {
+  if (n < 0 || hash_stride < 8) return KVCS_EINVAL;
+  if (n == 0) return KVCS_OK;
+  if (!block_hashes || !tags || reinterpret_cast<uintptr_t>(tags) % 8) return KVCS_EINVAL;
+  int sms = 0;
+  if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
+  const long long blocks = std::min<long long>((n + 255) / 256, 4LL * sms);
+  kvcs_tags_kernel<<<static_cast<unsigned>(std::max<long long>(1, blocks)), 256, 0,
+                     static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const unsigned char *>(block_hashes), hash_stride, n, fingerprint,
+      reinterpret_cast<u64 *>(tags));
+  if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   return KVCS_OK;
 }
 
@@ -390,6 +482,6 @@ const char *kvcs_strerror(int code) {
 
 uint64_t kvcs_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int32_t kvcs_version(void) { return (1 << 16) | 0; }
+int32_t kvcs_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"

@@ -73,7 +73,7 @@ struct DevCache {
   int halves;       // 2 (K, V) or 1 (latent)
   int upp;          // units per page
   int rpu;          // rows (NHD, latent) or heads (HND) per unit
-  int pad;
+  int column;       // replica-key column the cache adds into
 };
 
 struct Params {
@@ -81,7 +81,7 @@ struct Params {
   const long long *first_position;
   const long long *num_tokens;
   const int *block_ids;
-  u64 *out;
+  u64 *out;                  // [total_positions][num_columns]
   u32 *status;
   long long num_requests;
   long long total_positions;
@@ -100,12 +100,14 @@ struct Params {
   int ppu;                   // pages per unit: > 1 only when every cache has
                              // the same geometry and a page fits a unit
   int pages_per_pos;         // sum of halves over the caches
+  int num_columns;           // replica-key columns of the output
   DevCache caches[kMaxCachesPerLaunch];
 };
 
 // What the producer tells the consumers about one staged unit.
 struct __align__(16) UnitMeta {
-  long long pos;   // global position index; -1 ends the group's stream
+  long long dst;   // output word: position * num_columns + column; -1 ends
+                   // the group's stream
   long long q;     // block position inside the request
   int cache;
   int half;        // 0: K or latent row, 1: V
@@ -222,11 +224,12 @@ __device__ PosInfo position_info(const Params &p, long long pos, const ReqCursor
 }
 
 // Three 16-byte shared-memory stores of one unit's metadata.
-__device__ __forceinline__ void store_meta(UnitMeta *dst, long long pos, long long q,
+__device__ __forceinline__ void store_meta(UnitMeta *dst, long long out_index, long long q,
                                            int cache, int half, int first, int count,
                                            int nv, int mode, int slot, int npages) {
   uint4 *d = reinterpret_cast<uint4 *>(dst);
-  d[0] = make_uint4(static_cast<u32>(pos), static_cast<u32>(static_cast<u64>(pos) >> 32),
+  d[0] = make_uint4(static_cast<u32>(out_index),
+                    static_cast<u32>(static_cast<u64>(out_index) >> 32),
                     static_cast<u32>(q), static_cast<u32>(static_cast<u64>(q) >> 32));
   d[1] = make_uint4(static_cast<u32>(cache), static_cast<u32>(half),
                     static_cast<u32>(first), static_cast<u32>(count));
@@ -354,14 +357,15 @@ __device__ __forceinline__ u64 warp_sum(u64 v) {
   return v;
 }
 
-// Write a finished position's checksum: a plain store when this CTA holds
-// every unit of it, else a 64-bit atomic add into the pre-zeroed output.
+// Write a finished (position, column) checksum: a plain store when this CTA
+// holds every unit of the position, else a 64-bit atomic add into the
+// pre-zeroed output.
 __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
-                                              int slot, long long pos, int mode) {
+                                              int slot, long long dst, int mode) {
   __threadfence_block();
   const u64 total = atomicAdd(&hdr->ring_acc[slot], 0ull);
-  if (mode == kFlushStore) p.out[pos] = total;
-  else atomicAdd(p.out + pos, total);
+  if (mode == kFlushStore) p.out[dst] = total;
+  else atomicAdd(p.out + dst, total);
 }
 
 // ---------------------------------------------------------------------------
@@ -393,9 +397,9 @@ __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
 // unit, so every unit up to f - 1's was emitted, and the producer emitted
 // fill f - 1 only after fill f - 2 was released.
 //
-// A position's slot counts the contributions: each consumer warp adds 1 per
-// unit, and the producer subtracts (warps per group) x (units it emitted)
-// once the position is done.  Whoever brings the count back to zero writes
+// A (position, column) slot counts the contributions: each consumer warp
+// adds 1 per unit, and the producer subtracts (warps per group) x (units it
+// emitted) once the column of the position is done.  Whoever brings the count back to zero writes
 // the result, so no CTA-wide barrier is needed and a warp that gave up on a
 // timed-out wait can never block another.  Slots are reused kRingSlots
 // positions later; since a stage is refilled only after it was released, and
@@ -474,8 +478,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       int mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
       int slot = 0;
       u32 n_emit = 0;
+      int col = p.caches[ci].column;
       for (long long u = u_begin; u < u_end; ++u) {
         const DevCache &C = p.caches[ci];
+        // One accumulator slot per (position, column); the caches arrive
+        // sorted by column, so a column's units are consecutive.
+        const long long dst = pos * p.num_columns + col;
         int npg = 1;
         if (p.ppu > 1) npg = min(p.ppu, p.pages_per_pos - (ci * C.halves + half));
         if (!cur.skip) {
@@ -503,7 +511,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               hdr->ring_acc[slot] = 0ull;
               hdr->ring_cnt[slot] = 0u;
             }
-            store_meta(&hdr->meta[s], pos, cur.q, ci, half, first, count, cur.nv,
+            store_meta(&hdr->meta[s], dst, cur.q, ci, half, first, count, cur.nv,
                        mode, slot, npg);
             const u32 fb = ptx::smem_addr(&hdr->full[s]);
             ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
@@ -560,24 +568,25 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           }
         }
         if (pos_done) ci = 0;
-        if (pos_done || u + 1 == u_end) {
-          // close the position: this thread's share of the slot count
+        if (pos_done || u + 1 == u_end || p.caches[ci].column != col) {
+          // close the (position, column): this thread's share of the count
           if (n_emit > 0) {
             const u32 delta = 0u - static_cast<u32>(p.group_warps) * n_emit;
             const u32 prev = atomicAdd(&hdr->ring_cnt[slot], delta);
-            if (prev + delta == 0u) finalize_slot(p, hdr, slot, pos, mode);
+            if (prev + delta == 0u) finalize_slot(p, hdr, slot, dst, mode);
           } else if (cur.whole && !p.all_atomic) {
-            p.out[pos] = 0ull;
+            p.out[dst] = 0ull;
           }
           n_emit = 0;
-          if (pos_done && u + 1 < u_end) {
-            ++pos;
-            b_cur = b_next;
-            b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
-            req_seek(p, rc, pos);
-            cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
-            mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
-          }
+        }
+        col = p.caches[ci].column;
+        if (pos_done && u + 1 < u_end) {
+          ++pos;
+          b_cur = b_next;
+          b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
+          req_seek(p, rc, pos);
+          cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
+          mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
         }
       }
     }
@@ -589,7 +598,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           set_status(p, kStatusTimeout);
           break;
         }
-        hdr->meta[s].pos = -1;
+        hdr->meta[s].dst = -1;
         ptx::mbar_arrive(ptx::smem_addr(&hdr->full[s]));
         ++it;
         if (++s == NS) {
@@ -633,7 +642,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       return;
     }
     const UnitMeta m = hdr->meta[s];
-    if (m.pos < 0) break;
+    if (m.dst < 0) break;
     const unsigned char *sp = stages + static_cast<size_t>(s) * SB;
     int ci = m.cache, half = m.half;
     u64 v = 0;
@@ -654,7 +663,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       atomicAdd(&hdr->ring_acc[m.slot], v);
       __threadfence_block();
       const u32 prev = atomicAdd(&hdr->ring_cnt[m.slot], 1u);
-      if (prev + 1u == 0u) finalize_slot(p, hdr, m.slot, m.pos, m.mode);
+      if (prev + 1u == 0u) finalize_slot(p, hdr, m.slot, m.dst, m.mode);
       ptx::mbar_arrive(ptx::smem_addr(&hdr->empty[s]));
     }
     s += p.groups;
@@ -704,51 +713,109 @@ __global__ void __launch_bounds__(kGenericThreads)
       else if (b < 0 || b >= p.min_num_blocks) set_status(p, kStatusBadBlockId);
     }
     if (ok && (b < 0 || b >= p.min_num_blocks)) ok = false;
-    u64 acc = 0;
-    if (ok && nv > 0) {
-      const u64 t0 = static_cast<u64>(q) * static_cast<u64>(bs);
-      for (int ci = 0; ci < p.num_caches; ++ci) {
-        const DevCache &C = p.caches[ci];
-        const long long P = C.P;
-        const long long per_slot = static_cast<long long>(C.heads) * P;
-        const long long n = nv * per_slot;
-        const int hp = C.hb >> 3;  // pieces per half
-        for (long long idx = tid; idx < n; idx += kGenericThreads) {
-          const long long slot = idx / per_slot;
-          const long long rem = idx - slot * per_slot;
-          const long long h = rem / P;
-          const long long pc = rem - h * P;
-          u64 off;
-          if (C.layout == kLayoutLatent) {
-            off = (static_cast<u64>(b) * bs + slot) * C.hb + 8 * pc;
-          } else {
-            const long long half = pc >= hp ? 1 : 0;
-            const long long e = (pc - half * hp) * 8;
-            const u64 page = static_cast<u64>(half) * C.half_stride +
-                             static_cast<u64>(b) * C.page_bytes;
-            if (C.layout == kLayoutNHD)
-              off = page + (static_cast<u64>(slot) * C.heads + h) * C.hb + e;
-            else
-              off = page + (static_cast<u64>(h) * bs + slot) * C.hb + e;
+    for (int col = 0; col < p.num_columns; ++col) {
+      u64 acc = 0;
+      if (ok && nv > 0) {
+        const u64 t0 = static_cast<u64>(q) * static_cast<u64>(bs);
+        for (int ci = 0; ci < p.num_caches; ++ci) {
+          const DevCache &C = p.caches[ci];
+          if (C.column != col) continue;
+          const long long P = C.P;
+          const long long per_slot = static_cast<long long>(C.heads) * P;
+          const long long n = nv * per_slot;
+          const int hp = C.hb >> 3;  // pieces per half
+          for (long long idx = tid; idx < n; idx += kGenericThreads) {
+            const long long slot = idx / per_slot;
+            const long long rem = idx - slot * per_slot;
+            const long long h = rem / P;
+            const long long pc = rem - h * P;
+            u64 off;
+            if (C.layout == kLayoutLatent) {
+              off = (static_cast<u64>(b) * bs + slot) * C.hb + 8 * pc;
+            } else {
+              const long long half = pc >= hp ? 1 : 0;
+              const long long e = (pc - half * hp) * 8;
+              const u64 page = static_cast<u64>(half) * C.half_stride +
+                               static_cast<u64>(b) * C.page_bytes;
+              if (C.layout == kLayoutNHD)
+                off = page + (static_cast<u64>(slot) * C.heads + h) * C.hb + e;
+              else
+                off = page + (static_cast<u64>(h) * bs + slot) * C.hb + e;
+            }
+            const u64 x = __ldg(reinterpret_cast<const u64 *>(C.base + off));
+            const u64 j = (t0 + static_cast<u64>(slot)) * static_cast<u64>(P) +
+                          static_cast<u64>(pc);
+            const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
+            acc += x * ((2ull * j + 1ull) * mh);
           }
-          const u64 x = __ldg(reinterpret_cast<const u64 *>(C.base + off));
-          const u64 j = (t0 + static_cast<u64>(slot)) * static_cast<u64>(P) +
-                        static_cast<u64>(pc);
-          const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
-          acc += x * ((2ull * j + 1ull) * mh);
         }
       }
+      acc = warp_sum(acc);
+      if ((tid & 31) == 0) red[tid >> 5] = acc;
+      __syncthreads();
+      if (tid == 0) {
+        u64 total = 0;
+        for (int w = 0; w < kGenericThreads / 32; ++w) total += red[w];
+        const long long dst = pos * p.num_columns + col;
+        if (p.all_atomic) atomicAdd(p.out + dst, total);
+        else p.out[dst] = total;
+      }
+      __syncthreads();
     }
-    acc = warp_sum(acc);
-    if ((tid & 31) == 0) red[tid >> 5] = acc;
-    __syncthreads();
-    if (tid == 0) {
-      u64 total = 0;
-      for (int w = 0; w < kGenericThreads / 32; ++w) total += red[w];
-      if (p.all_atomic) atomicAdd(p.out + pos, total);
-      else p.out[pos] = total;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Row sums, tags and verification (offloaded-KV checks)
+// ---------------------------------------------------------------------------
+
+struct RowParams {
+  const u64 *values;        // [n][num_columns]
+  long long n;
+  int num_columns;
+  u64 *row_sums;            // or null
+  const u64 *tags;          // or null
+  const u64 *expected;      // or null
+  unsigned char *mismatch;  // or null
+  u32 *mismatch_count;      // or null
+};
+
+// Per position: the row's partials summed mod 2^64, XOR its tag; compared
+// with the stored value when one is given.
+__global__ void __launch_bounds__(256) kvcs_rows_kernel(const RowParams rp) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+       i - threadIdx.x < rp.n; i += stride) {
+    bool bad = false;
+    if (i < rp.n) {
+      u64 r = 0;
+      for (int k = 0; k < rp.num_columns; ++k) r += rp.values[i * rp.num_columns + k];
+      if (rp.tags) r ^= rp.tags[i];
+      if (rp.row_sums) rp.row_sums[i] = r;
+      if (rp.expected) {
+        bad = r != rp.expected[i];
+        if (rp.mismatch) rp.mismatch[i] = bad ? 1 : 0;
+      }
     }
-    __syncthreads();
+    if (rp.mismatch_count) {
+      const unsigned votes = __ballot_sync(0xffffffffu, bad);
+      if ((threadIdx.x & 31) == 0 && votes) atomicAdd(rp.mismatch_count, __popc(votes));
+    }
+  }
+}
+
+// tags[i] = (first eight bytes of hash i, little-endian) XOR fingerprint.
+__global__ void __launch_bounds__(256)
+    kvcs_tags_kernel(const unsigned char *hashes, long long stride, long long n,
+                     u64 fingerprint, u64 *tags) {
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+       i < n; i += step) {
+    const unsigned char *h = hashes + i * stride;
+    u64 w = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w |= static_cast<u64>(h[k]) << (8 * k);
+    tags[i] = w ^ fingerprint;
   }
 }
 

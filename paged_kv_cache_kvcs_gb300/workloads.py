@@ -47,6 +47,7 @@ class CacheSpec:
     head_offset: int
     num_heads: int
     head_bytes: int         # K (= V) bytes per head per token; latent: row bytes
+    column: int = 0         # replica-key column (several-key outputs only)
 
 
 @dataclass

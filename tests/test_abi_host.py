@@ -38,7 +38,8 @@ def test_version_and_strerror():
 
 class FakeCache:
     def __init__(self, base=1 << 20, num_blocks=100, layout=0, layer=0,
-                 head_offset=0, num_heads=8, head_bytes=256):
+                 head_offset=0, num_heads=8, head_bytes=256, column=0):
+        self.column = column
         self.pool = base
         self.num_blocks = num_blocks
         self.layout = layout
@@ -79,6 +80,10 @@ def test_validation_codes():
     assert code_of([FakeCache(head_offset=0, num_heads=4),
                     FakeCache(head_offset=4, num_heads=4)]) == 0
     assert code_of([FakeCache(layer=0), FakeCache(layer=1)]) == 0
+    # columns: in range and each used (planning sees max(column) + 1)
+    assert code_of([FakeCache(layer=0), FakeCache(layer=1, column=1)]) == 0
+    assert code_of([FakeCache(layer=0), FakeCache(layer=1, column=2)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layer=0, column=-1)]) == K.KVCS_EINVAL
 
 
 def test_block_checksums_rejects_before_any_cuda_call():
@@ -133,3 +138,22 @@ def test_plan_shapes():
     # more caches than one launch takes
     p = plan([FakeCache(layer=i, num_heads=1, head_bytes=16) for i in range(300)])
     assert p["launches"] == 3 and p["memsets"] == 1
+
+
+def test_group_and_tags_reject_bad_arguments_without_cuda():
+    lib = K.load_library()
+    arr = K.cache_array([FakeCache(layer=0), FakeCache(layer=1, column=1)])
+    reqs = B.kvcs_requests(1, 16, 32, 48, 64)
+    outs = B.kvcs_outputs(1, 0, 128, None, None, None, None, None)
+    # column 1 with num_columns 1
+    assert lib.kvcs_group_checksums(arr, 2, 16, ctypes.byref(reqs), 4,
+                                    ctypes.byref(outs), None, None) == K.KVCS_EINVAL
+    outs = B.kvcs_outputs(2, 0, 128, None, None, None, 256, None)
+    # a mismatch output without expected values
+    assert lib.kvcs_group_checksums(arr, 2, 16, ctypes.byref(reqs), 4,
+                                    ctypes.byref(outs), None, None) == K.KVCS_EINVAL
+    outs = B.kvcs_outputs(65, 0, 128, None, None, None, None, None)
+    assert lib.kvcs_group_checksums(arr, 2, 16, ctypes.byref(reqs), 4,
+                                    ctypes.byref(outs), None, None) == K.KVCS_EINVAL
+    assert lib.kvcs_block_checksum_tags(64, 4, 3, 0, 128, None) == K.KVCS_EINVAL
+    assert lib.kvcs_block_checksum_tags(None, 32, 0, 0, None, None) == K.KVCS_OK
