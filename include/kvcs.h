@@ -61,7 +61,10 @@ typedef enum kvcs_layout {
 
 /* One layer's paged pool (one attention layer, or one of several caches of
  * a layer such as an indexer's, numbered by consecutive head offsets).
- * Read-only to the library. */
+ * Read-only to the library.  A page is one block's K, its V, or its latent
+ * rows: page_bytes = block_size * num_heads * head_bytes contiguous bytes in
+ * the layout's order; the page of (half, block) starts at
+ * base + half * half_stride + block * block_stride. */
 typedef struct kvcs_cache {
   const void *base;    /* DEVICE pointer to the pool; 8-byte aligned
                           (16-byte alignment enables the bulk-copy kernel) */
@@ -77,6 +80,23 @@ typedef struct kvcs_cache {
                           multiple of 8. */
   int32_t column;      /* replica-key column this cache's layer adds into
                           (kvcs_group_checksums); 0 for kvcs_block_checksums */
+  int64_t half_stride; /* NHD/HND: bytes from a block's K page to its V page
+                          (may be negative, e.g. separate K and V tensors);
+                          0 = num_blocks * page_bytes, the [2][num_blocks]...
+                          pool above.  Ignored for LATENT. */
+  int64_t block_stride;/* bytes between consecutive blocks' pages;
+                          0 = page_bytes.  [num_blocks][2][...] pools
+                          (K and V interleaved per block) use half_stride =
+                          page_bytes and block_stride = 2 * page_bytes. */
+  int32_t kernel_block_size; /* HND only: tokens per kernel sub-block when the
+                          attention kernel splits each block into
+                          block_size / kernel_block_size sub-blocks (the KV-cache
+                          page, section "reshape kv_cache"); a block is then
+                          [sub-block][heads][kernel_block_size][head_bytes].
+                          0 = block_size.  Must divide block_size.  For NHD and
+                          LATENT, consecutive sub-blocks are already the
+                          block's rows in order, so the field is ignored. */
+  int32_t reserved;    /* must be 0 */
 } kvcs_cache;
 
 /* The requests to checksum, in CSR form over requests.  All pointers are
@@ -100,6 +120,9 @@ typedef struct kvcs_requests {
 /* Return codes (negative: nothing was enqueued unless stated). */
 #define KVCS_OK 0
 #define KVCS_EINVAL (-1)      /* null pointer, non-positive block_size,
+                                 strides not multiples of 8 or smaller than a
+                                 page, kernel_block_size not dividing
+                                 block_size, reserved != 0,
                                  head_bytes not a positive multiple of 8,
                                  unknown layout, latent cache with heads != 1,
                                  negative layer or head offset, a column

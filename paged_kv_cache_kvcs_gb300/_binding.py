@@ -32,7 +32,9 @@ class kvcs_cache(ctypes.Structure):
     _fields_ = [("base", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
                 ("layout", ctypes.c_int32), ("layer", ctypes.c_int32),
                 ("head_offset", ctypes.c_int32), ("num_heads", ctypes.c_int32),
-                ("head_bytes", ctypes.c_int32), ("column", ctypes.c_int32)]
+                ("head_bytes", ctypes.c_int32), ("column", ctypes.c_int32),
+                ("half_stride", ctypes.c_int64), ("block_stride", ctypes.c_int64),
+                ("kernel_block_size", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class kvcs_outputs(ctypes.Structure):
@@ -123,16 +125,28 @@ def version() -> int:
     return int(load_library().kvcs_version())
 
 
+def _addr(t) -> int:
+    return t if isinstance(t, int) else t.data_ptr()
+
+
 def cache_array(caches: Sequence) -> ctypes.Array:
     """Pack cache descriptors.  Each item has ``pool`` (a tensor, or an int
     device address), ``num_blocks``, ``layout``, ``layer``, ``head_offset``,
-    ``num_heads`` and ``head_bytes``."""
+    ``num_heads`` and ``head_bytes``; optionally ``column``,
+    ``half_stride``, ``block_stride``, ``kernel_block_size`` and ``v_pool``
+    (a separate tensor holding the V pages: the half stride is then the
+    distance from ``pool`` to it)."""
     arr = (kvcs_cache * max(1, len(caches)))()
     for i, c in enumerate(caches):
-        pool = c.pool
-        base = pool if isinstance(pool, int) else pool.data_ptr()
+        base = _addr(c.pool)
+        v_pool = getattr(c, "v_pool", None)
+        half_stride = getattr(c, "half_stride", 0)
+        if v_pool is not None:
+            half_stride = _addr(v_pool) - base
         arr[i] = kvcs_cache(base, c.num_blocks, c.layout, c.layer, c.head_offset,
-                            c.num_heads, c.head_bytes, getattr(c, "column", 0))
+                            c.num_heads, c.head_bytes, getattr(c, "column", 0),
+                            half_stride, getattr(c, "block_stride", 0),
+                            getattr(c, "kernel_block_size", 0), 0)
     return arr
 
 
@@ -160,19 +174,29 @@ def kvcs_plan(caches: ctypes.Array, num_caches: int, block_size: int,
 
 
 def _check_pool(c, block_size: int) -> None:
-    import torch
+    """Every page the descriptor can address lies inside its tensor."""
     t = c.pool
     if isinstance(t, int):
         return
-    if not t.is_cuda:
-        raise ValueError("cache pools must be CUDA tensors")
-    if not t.is_contiguous():
-        raise ValueError("cache pools must be contiguous")
-    halves = 1 if c.layout == KVCS_LAYOUT_LATENT else 2
-    need = halves * c.num_blocks * block_size * c.num_heads * c.head_bytes
-    if t.numel() * t.element_size() < need:
-        raise ValueError("cache pool is smaller than its declared geometry")
-    del torch
+    v_pool = getattr(c, "v_pool", None)
+    for x in (t, v_pool):
+        if x is not None and not (x.is_cuda and x.is_contiguous()):
+            raise ValueError("cache pools must be contiguous CUDA tensors")
+    page = block_size * c.num_heads * c.head_bytes
+    bstride = getattr(c, "block_stride", 0) or page
+    span = (c.num_blocks - 1) * bstride + page if c.num_blocks > 0 else 0
+    if c.layout == KVCS_LAYOUT_LATENT:
+        halves = [(t, 0)]
+    elif v_pool is not None:
+        halves = [(t, 0), (v_pool, 0)]
+    else:
+        hs = getattr(c, "half_stride", 0) or c.num_blocks * page
+        if hs < 0:
+            raise ValueError("a negative half stride needs a separate v_pool tensor")
+        halves = [(t, 0), (t, hs)]
+    for x, off in halves:
+        if off + span > x.numel() * x.element_size():
+            raise ValueError("cache pool is smaller than its declared geometry")
 
 
 def block_checksums(caches: Sequence, block_size: int, pos_offsets, first_position,

@@ -70,7 +70,7 @@ struct Plan {
 // 16-byte-aligned bulk copies and reads 16-byte columns.
 bool bulk_eligible(const kvcs_cache &c, int block_size) {
   if (reinterpret_cast<uintptr_t>(c.base) % 16) return false;
-  if (c.head_bytes % 16) return false;
+  if (c.head_bytes % 16 || c.half_stride % 16 || c.block_stride % 16) return false;
   const long long hb = c.head_bytes;
   switch (c.layout) {
     case KVCS_LAYOUT_NHD: return hb * c.num_heads <= kMaxUnitBytes;
@@ -96,7 +96,7 @@ int validate_caches(const kvcs_cache *caches, int32_t num_caches,
   spans.reserve(num_caches);
   for (int32_t i = 0; i < num_caches; ++i) {
     const kvcs_cache &c = caches[i];
-    if (!c.base || c.num_blocks < 0) return KVCS_EINVAL;
+    if (!c.base || c.num_blocks < 0 || c.reserved != 0) return KVCS_EINVAL;
     if (c.column < 0 || c.column >= num_columns) return KVCS_EINVAL;
     used[c.column] = true;
     if (c.layout < KVCS_LAYOUT_NHD || c.layout > KVCS_LAYOUT_LATENT) return KVCS_EINVAL;
@@ -110,6 +110,19 @@ int validate_caches(const kvcs_cache *caches, int32_t num_caches,
     // pools; guards absurd descriptors).
     const double page = static_cast<double>(block_size) * c.num_heads * c.head_bytes;
     if (page * 2.0 * static_cast<double>(c.num_blocks) > 9.0e18) return KVCS_EINVAL;
+    // Strides: 8-byte multiples; pages of different blocks, and a block's K
+    // and V pages, must not overlap.
+    if (c.half_stride % 8 || c.block_stride % 8) return KVCS_EINVAL;
+    if (c.block_stride != 0 && static_cast<double>(c.block_stride) < page) return KVCS_EINVAL;
+    if (c.layout != KVCS_LAYOUT_LATENT && c.half_stride != 0 &&
+        std::fabs(static_cast<double>(c.half_stride)) < page)
+      return KVCS_EINVAL;
+    if (std::fabs(static_cast<double>(c.half_stride)) > 9.0e18 ||
+        std::fabs(static_cast<double>(c.block_stride)) * static_cast<double>(c.num_blocks) > 9.0e18)
+      return KVCS_EINVAL;
+    if (c.kernel_block_size < 0 ||
+        (c.kernel_block_size > 0 && block_size % c.kernel_block_size != 0))
+      return KVCS_EINVAL;
     spans.push_back({c.layer, c.head_offset,
                      static_cast<int64_t>(c.head_offset) + c.num_heads});
   }
@@ -144,7 +157,13 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
   d.heads = c.num_heads;
   d.hb = c.head_bytes;
   d.page_bytes = static_cast<u64>(block_size) * c.num_heads * c.head_bytes;
-  d.half_stride = static_cast<u64>(c.num_blocks) * d.page_bytes;
+  d.half_stride = c.half_stride != 0
+                      ? c.half_stride
+                      : static_cast<long long>(c.num_blocks) * static_cast<long long>(d.page_bytes);
+  d.block_stride = c.block_stride != 0 ? c.block_stride
+                                       : static_cast<long long>(d.page_bytes);
+  d.kbs = (c.layout == KVCS_LAYOUT_HND && c.kernel_block_size > 0) ? c.kernel_block_size
+                                                                  : block_size;
   d.halves = c.layout == KVCS_LAYOUT_LATENT ? 1 : 2;
   d.P = (c.layout == KVCS_LAYOUT_LATENT ? c.head_bytes : 2 * c.head_bytes) / 8;
   d.column = c.column;
@@ -196,6 +215,8 @@ LaunchShape launch_shape(const kvcs_cache *caches, int lo, int hi, int block_siz
     biggest = std::max(biggest, unit_bytes(d, block_size));
     uniform = uniform && d.upp == 1 && caches[i].layout == caches[lo].layout &&
               caches[i].column == caches[lo].column &&
+              make_dev_cache(caches[i], block_size).kbs ==
+                  make_dev_cache(caches[lo], block_size).kbs &&
               caches[i].num_heads == caches[lo].num_heads &&
               caches[i].head_bytes == caches[lo].head_bytes;
   }

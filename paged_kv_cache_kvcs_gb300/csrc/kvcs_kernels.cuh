@@ -63,7 +63,8 @@ struct DevCache {
   const unsigned char *base;
   u64 m0;           // m of the cache's local head 0: 2 (layer H + head_offset) + 1
   u64 page_bytes;   // bytes of one page (one block of K, of V, or of rows)
-  u64 half_stride;  // num_blocks * page_bytes: offset of the V half
+  long long half_stride;   // bytes from a block's K page to its V page
+  long long block_stride;  // bytes between consecutive blocks' pages
   int layout;
   int heads;        // local heads (1 for latent)
   int hb;           // bytes per head per token per half (latent: row bytes)
@@ -74,6 +75,8 @@ struct DevCache {
   int upp;          // units per page
   int rpu;          // rows (NHD, latent) or heads (HND) per unit
   int column;       // replica-key column the cache adds into
+  int kbs;          // HND: slots per kernel sub-block (block_size if none)
+  int pad;
 };
 
 struct Params {
@@ -297,8 +300,23 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
       u64 S = 0, T = 0, U = 0;
       const unsigned char *sp = stage + static_cast<size_t>(t.rl) * rowb + (col << 4);
       const size_t step = static_cast<size_t>(t.rstep) * rowb;
-#pragma unroll 4
-      for (int r = t.rl; r < nrows; r += t.rstep, sp += step) {
+      int r = t.rl;
+      // four rows per iteration: four independent shared loads in flight
+      for (; r + 3 * t.rstep < nrows; r += 4 * t.rstep, sp += 4 * step) {
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const uint4 *>(sp + k * step);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
+          const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
+          const u64 X = x0 + x1;
+          S += X;
+          U += x1;
+          T += static_cast<u64>(r0 + static_cast<u32>(r + k * t.rstep)) * X;
+        }
+      }
+      for (; r < nrows; r += t.rstep, sp += step) {
         const uint4 v = *reinterpret_cast<const uint4 *>(sp);
         const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
         const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
@@ -520,19 +538,28 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             for (int k2 = 0; k2 < npg; ++k2) {
               const DevCache &D = p.caches[pci];
               const unsigned char *page = D.base +
-                  static_cast<u64>(phalf) * D.half_stride +
-                  static_cast<u64>(cur.block) * D.page_bytes;
+                  static_cast<long long>(phalf) * D.half_stride +
+                  cur.block * D.block_stride;
               if (D.layout == kLayoutHND) {
-                const u64 head_stride = static_cast<u64>(bs) * D.hb;
-                if (cur.nv == bs) {
-                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * head_stride,
+                // A page is [sub-block][heads][kbs][hb] (one sub-block of
+                // block_size slots unless the attention kernel splits
+                // blocks); stage each head's valid slots as one packed run.
+                const u64 head_run = static_cast<u64>(D.kbs) * D.hb;
+                if (cur.nv == bs && D.kbs == bs) {
+                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * head_run,
                                 pbytes, fb, policy);
                 } else {
-                  const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(D.hb);
-                  for (int h = 0; h < count; ++h)
-                    ptx::bulk_g2s(dst + static_cast<u32>(h) * run,
-                                  page + static_cast<u64>(first + h) * head_stride,
-                                  run, fb, policy);
+                  const u64 sub_bytes = static_cast<u64>(D.heads) * head_run;
+                  for (int h = 0; h < count; ++h) {
+                    const unsigned char *src = page + static_cast<u64>(first + h) * head_run;
+                    u32 d = dst + static_cast<u32>(h * cur.nv) * D.hb;
+                    for (int s0 = 0; s0 < cur.nv; s0 += D.kbs) {
+                      const u32 n = static_cast<u32>(min(D.kbs, cur.nv - s0)) * D.hb;
+                      ptx::bulk_g2s(d, src, n, fb, policy);
+                      d += n;
+                      src += sub_bytes;
+                    }
+                  }
                 }
               } else {
                 ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes,
@@ -729,18 +756,19 @@ __global__ void __launch_bounds__(kGenericThreads)
             const long long rem = idx - slot * per_slot;
             const long long h = rem / P;
             const long long pc = rem - h * P;
-            u64 off;
+            long long off;
             if (C.layout == kLayoutLatent) {
-              off = (static_cast<u64>(b) * bs + slot) * C.hb + 8 * pc;
+              off = b * C.block_stride + slot * C.hb + 8 * pc;
             } else {
               const long long half = pc >= hp ? 1 : 0;
               const long long e = (pc - half * hp) * 8;
-              const u64 page = static_cast<u64>(half) * C.half_stride +
-                               static_cast<u64>(b) * C.page_bytes;
-              if (C.layout == kLayoutNHD)
-                off = page + (static_cast<u64>(slot) * C.heads + h) * C.hb + e;
-              else
-                off = page + (static_cast<u64>(h) * bs + slot) * C.hb + e;
+              const long long page = half * C.half_stride + b * C.block_stride;
+              if (C.layout == kLayoutNHD) {
+                off = page + (slot * C.heads + h) * C.hb + e;
+              } else {
+                const long long sb = slot / C.kbs;
+                off = page + ((sb * C.heads + h) * C.kbs + (slot - sb * C.kbs)) * C.hb + e;
+              }
             }
             const u64 x = __ldg(reinterpret_cast<const u64 *>(C.base + off));
             const u64 j = (t0 + static_cast<u64>(slot)) * static_cast<u64>(P) +

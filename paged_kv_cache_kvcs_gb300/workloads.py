@@ -48,6 +48,10 @@ class CacheSpec:
     num_heads: int
     head_bytes: int         # K (= V) bytes per head per token; latent: row bytes
     column: int = 0         # replica-key column (several-key outputs only)
+    half_stride: int = 0    # bytes from a block's K page to its V page (0: packed)
+    block_stride: int = 0   # bytes between blocks' pages (0: packed)
+    kernel_block_size: int = 0  # HND sub-block slots (0: none)
+    v_pool: torch.Tensor | None = None  # separate V tensor, if any
 
 
 @dataclass

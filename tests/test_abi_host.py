@@ -38,8 +38,12 @@ def test_version_and_strerror():
 
 class FakeCache:
     def __init__(self, base=1 << 20, num_blocks=100, layout=0, layer=0,
-                 head_offset=0, num_heads=8, head_bytes=256, column=0):
+                 head_offset=0, num_heads=8, head_bytes=256, column=0,
+                 half_stride=0, block_stride=0, kernel_block_size=0):
         self.column = column
+        self.half_stride = half_stride
+        self.block_stride = block_stride
+        self.kernel_block_size = kernel_block_size
         self.pool = base
         self.num_blocks = num_blocks
         self.layout = layout
@@ -84,6 +88,18 @@ def test_validation_codes():
     assert code_of([FakeCache(layer=0), FakeCache(layer=1, column=1)]) == 0
     assert code_of([FakeCache(layer=0), FakeCache(layer=1, column=2)]) == K.KVCS_EINVAL
     assert code_of([FakeCache(layer=0, column=-1)]) == K.KVCS_EINVAL
+    # strides and sub-blocks (page = 16 * 8 * 256 = 32 KiB)
+    page = 16 * 8 * 256
+    assert code_of([FakeCache(half_stride=page, block_stride=2 * page)]) == 0
+    assert code_of([FakeCache(half_stride=-page)]) == 0
+    assert code_of([FakeCache(half_stride=page // 2)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(block_stride=page - 8)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(block_stride=page + 4)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layout=1, kernel_block_size=4)]) == 0
+    assert code_of([FakeCache(layout=1, kernel_block_size=5)]) == K.KVCS_EINVAL
+    # strides that are 8- but not 16-byte multiples fall back to the generic kernel
+    assert plan([FakeCache(block_stride=page + 8)])["kernel"] == 1
+    assert plan([FakeCache(block_stride=page + 16)])["kernel"] == 0
 
 
 def test_block_checksums_rejects_before_any_cuda_call():

@@ -1,0 +1,120 @@
+"""More cache layouts through the C ABI: explicit half/block strides
+([num_blocks, 2, ...] pools, separate K and V tensors, padded blocks) and
+HND kernel sub-blocks.  Each layout is built from a canonical pool with
+torch views (data movement only) and must give the canonical checksums,
+which are checked against the oracle."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import W
+import paged_kv_cache_kvcs_gb300 as K
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run(wl):
+    from gpu_helpers import gpu_checksums
+    return gpu_checksums(wl)
+
+
+def canonical(seed, layout, hb=64, bs=16, heads=4, layers=3, lengths=(70, 33, 5)):
+    wl = W.random_case(seed, DEV, layout=layout, layers=layers, heads=heads,
+                       head_bytes=hb, block_size=bs, lengths=lengths)
+    from gpu_helpers import full_oracle
+    exp, _ = full_oracle(wl)
+    got, st = run(wl)
+    assert st == 0 and np.array_equal(got, exp)
+    return wl, exp
+
+
+def with_caches(wl, caches):
+    return W.Workload(wl.name, wl.block_size, caches, wl.pos_offsets, wl.first_position,
+                      wl.num_tokens, wl.block_ids)
+
+
+def page_bytes(wl, c):
+    return wl.block_size * c.num_heads * c.head_bytes
+
+
+@pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND])
+@pytest.mark.parametrize("hb", [64, 24])      # bulk kernel, generic kernel
+def test_kv_interleaved_per_block(layout, hb):
+    """[num_blocks, 2, page]: half_stride = page, block_stride = 2 page."""
+    wl, exp = canonical(1, layout, hb=hb)
+    caches = []
+    for c in wl.caches:
+        pb = page_bytes(wl, c)
+        inter = c.pool.view(2, c.num_blocks, pb).transpose(0, 1).contiguous().view(-1)
+        caches.append(dataclasses.replace(c, pool=inter, half_stride=pb, block_stride=2 * pb))
+    got, st = run(with_caches(wl, caches))
+    assert st == 0 and np.array_equal(got, exp)
+
+
+@pytest.mark.parametrize("v_first", [False, True])
+def test_separate_k_and_v_tensors(v_first):
+    wl, exp = canonical(2, W.LAYOUT_NHD)
+    caches = []
+    keep = []
+    for c in wl.caches:
+        pb = page_bytes(wl, c)
+        halves = c.pool.view(2, c.num_blocks * pb)
+        if v_first:                 # V allocated before K: often a negative stride
+            v = halves[1].clone()
+            k = halves[0].clone()
+        else:
+            k = halves[0].clone()
+            v = halves[1].clone()
+        keep.append((k, v))
+        caches.append(dataclasses.replace(c, pool=k, v_pool=v))
+    got, st = run(with_caches(wl, caches))
+    assert st == 0 and np.array_equal(got, exp)
+
+
+@pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND, W.LAYOUT_LATENT])
+@pytest.mark.parametrize("pad", [256, 8])     # bulk kernel, generic kernel
+def test_padded_blocks(layout, pad):
+    hb = 1152 if layout == W.LAYOUT_LATENT else 64
+    heads = 1 if layout == W.LAYOUT_LATENT else 4
+    wl, exp = canonical(3, layout, hb=hb, heads=heads)
+    caches = []
+    for c in wl.caches:
+        pb = page_bytes(wl, c)
+        halves = 1 if layout == W.LAYOUT_LATENT else 2
+        stride = pb + pad
+        buf = torch.zeros(halves * c.num_blocks * stride, dtype=torch.uint8, device=DEV)
+        buf.view(halves * c.num_blocks, stride)[:, :pb] = c.pool.view(halves * c.num_blocks, pb)
+        caches.append(dataclasses.replace(c, pool=buf, block_stride=stride,
+                                          half_stride=c.num_blocks * stride))
+    plan = K.plan_for(caches, wl.block_size, wl.num_positions)
+    assert plan["kernel"] == (0 if pad % 16 == 0 else 1)
+    got, st = run(with_caches(wl, caches))
+    assert st == 0 and np.array_equal(got, exp)
+
+
+@pytest.mark.parametrize("kbs", [1, 4, 8, 16])
+@pytest.mark.parametrize("hb", [64, 24])
+def test_hnd_kernel_sub_blocks(kbs, hb):
+    """HND blocks split into block_size / kbs sub-blocks:
+    [2, num_blocks, sub, heads, kbs, hb]."""
+    bs, heads = 16, 4
+    wl, exp = canonical(4, W.LAYOUT_HND, hb=hb, bs=bs, heads=heads)
+    r = bs // kbs
+    caches = []
+    for c in wl.caches:
+        v = c.pool.view(2, c.num_blocks, heads, r, kbs, hb).permute(0, 1, 3, 2, 4, 5)
+        caches.append(dataclasses.replace(c, pool=v.contiguous().view(-1),
+                                          kernel_block_size=kbs))
+    got, st = run(with_caches(wl, caches))
+    assert st == 0 and np.array_equal(got, exp)
+
+
+def test_nhd_kernel_block_size_is_the_same_memory():
+    wl, exp = canonical(5, W.LAYOUT_NHD)
+    caches = [dataclasses.replace(c, kernel_block_size=4) for c in wl.caches]
+    got, st = run(with_caches(wl, caches))
+    assert st == 0 and np.array_equal(got, exp)
