@@ -52,11 +52,17 @@ extern "C" {
  *   HND:    pool [2 (K, V)][num_blocks][num_heads][block_size][head_bytes]
  *   LATENT: pool [num_blocks][block_size][row_bytes]  (MLA: one latent row
  *           per token, no K/V split; counted as one head whose token slice
- *           is the whole row, P = row_bytes / 8) */
+ *           is the whole row, P = row_bytes / 8)
+ *   XSPLIT: pool [2][num_blocks][num_heads][head_bytes/16][block_size][16]:
+ *           the x-split layout of the KV-cache page's reshape_and_cache
+ *           section ([num_blocks, heads, head_size/x, block_size, x] with x
+ *           elements = 16 bytes), used here for both K and V pages;
+ *           head_bytes must be a multiple of 16 */
 typedef enum kvcs_layout {
   KVCS_LAYOUT_NHD = 0,
   KVCS_LAYOUT_HND = 1,
-  KVCS_LAYOUT_LATENT = 2
+  KVCS_LAYOUT_LATENT = 2,
+  KVCS_LAYOUT_XSPLIT = 3
 } kvcs_layout;
 
 /* One layer's paged pool (one attention layer, or one of several caches of

@@ -15,6 +15,7 @@ LIB_PATH = Path(__file__).resolve().parent / "_build" / "libkvcs.so"
 KVCS_LAYOUT_NHD = 0
 KVCS_LAYOUT_HND = 1
 KVCS_LAYOUT_LATENT = 2
+KVCS_LAYOUT_XSPLIT = 3
 KVCS_MAX_KV_HEADS_PER_LAYER = 65536
 KVCS_BLOCK_CHECKSUM_BYTES = 8
 

@@ -46,7 +46,11 @@ cudaError_t device_setup(int *sms) {
     int n = 0;
     d.err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (d.err == cudaSuccess)
-      d.err = cudaFuncSetAttribute(kvcs_bulk_kernel,
+      d.err = cudaFuncSetAttribute(kvcs_bulk_kernel<false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kSmemLimit);
+    if (d.err == cudaSuccess)
+      d.err = cudaFuncSetAttribute(kvcs_bulk_kernel<true>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kSmemLimit);
     d.sms = n;
@@ -74,7 +78,8 @@ bool bulk_eligible(const kvcs_cache &c, int block_size) {
   const long long hb = c.head_bytes;
   switch (c.layout) {
     case KVCS_LAYOUT_NHD: return hb * c.num_heads <= kMaxUnitBytes;
-    case KVCS_LAYOUT_HND: return hb * block_size <= kMaxUnitBytes;
+    case KVCS_LAYOUT_HND:
+    case KVCS_LAYOUT_XSPLIT: return hb * block_size <= kMaxUnitBytes;
     default: return hb <= kMaxUnitBytes;
   }
 }
@@ -99,7 +104,8 @@ int validate_caches(const kvcs_cache *caches, int32_t num_caches,
     if (!c.base || c.num_blocks < 0 || c.reserved != 0) return KVCS_EINVAL;
     if (c.column < 0 || c.column >= num_columns) return KVCS_EINVAL;
     used[c.column] = true;
-    if (c.layout < KVCS_LAYOUT_NHD || c.layout > KVCS_LAYOUT_LATENT) return KVCS_EINVAL;
+    if (c.layout < KVCS_LAYOUT_NHD || c.layout > KVCS_LAYOUT_XSPLIT) return KVCS_EINVAL;
+    if (c.layout == KVCS_LAYOUT_XSPLIT && c.head_bytes % 16) return KVCS_EINVAL;
     if (c.layer < 0 || c.head_offset < 0 || c.num_heads < 1) return KVCS_EINVAL;
     if (c.head_bytes <= 0 || c.head_bytes % 8) return KVCS_EINVAL;
     if (c.layout == KVCS_LAYOUT_LATENT && c.num_heads != 1) return KVCS_EINVAL;
@@ -164,6 +170,7 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
                                        : static_cast<long long>(d.page_bytes);
   d.kbs = (c.layout == KVCS_LAYOUT_HND && c.kernel_block_size > 0) ? c.kernel_block_size
                                                                   : block_size;
+  d.chunks = c.layout == KVCS_LAYOUT_XSPLIT ? c.head_bytes / 16 : 1;
   d.halves = c.layout == KVCS_LAYOUT_LATENT ? 1 : 2;
   d.P = (c.layout == KVCS_LAYOUT_LATENT ? c.head_bytes : 2 * c.head_bytes) / 8;
   d.column = c.column;
@@ -172,8 +179,8 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
     if (c.head_bytes == (1 << k)) d.hb_shift = k;
   // Units: cut a page into runs of about kUnitTargetBytes, as evenly as
   // possible, of whole rows (NHD, latent) or whole heads (HND).
-  if (c.layout == KVCS_LAYOUT_HND) {
-    d.rowb = c.head_bytes;
+  if (c.layout == KVCS_LAYOUT_HND || c.layout == KVCS_LAYOUT_XSPLIT) {
+    d.rowb = c.layout == KVCS_LAYOUT_HND ? c.head_bytes : 16;
     const long long head = static_cast<long long>(block_size) * c.head_bytes;
     const int fit = static_cast<int>(std::max<long long>(1, kUnitTargetBytes / head));
     d.upp = (c.num_heads + fit - 1) / fit;
@@ -189,7 +196,7 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
 
 // Largest unit of one cache, in bytes.
 long long unit_bytes(const DevCache &d, int block_size) {
-  if (d.layout == KVCS_LAYOUT_HND)
+  if (d.layout == KVCS_LAYOUT_HND || d.layout == KVCS_LAYOUT_XSPLIT)
     return static_cast<long long>(d.rpu) * block_size * d.hb;
   return static_cast<long long>(d.rpu) * d.rowb;
 }
@@ -379,8 +386,15 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       p.groups = kConsumerWarps / p.group_warps;
       long long grid = pl.grid;
       if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
-      kvcs_bulk_kernel<<<static_cast<unsigned>(grid), kBulkThreads,
-                         bulk_smem_bytes(p.stages, p.stage_bytes), st>>>(p);
+      bool general = false;
+      for (int i = lo; i < hi; ++i)
+        general = general || caches[i].layout == KVCS_LAYOUT_HND ||
+                  caches[i].layout == KVCS_LAYOUT_XSPLIT;
+      const size_t smem = bulk_smem_bytes(p.stages, p.stage_bytes);
+      if (general)
+        kvcs_bulk_kernel<true><<<static_cast<unsigned>(grid), kBulkThreads, smem, st>>>(p);
+      else
+        kvcs_bulk_kernel<false><<<static_cast<unsigned>(grid), kBulkThreads, smem, st>>>(p);
     } else {
       p.split = 0;
       kvcs_generic_kernel<<<static_cast<unsigned>(pl.grid), kGenericThreads, 0, st>>>(p);

@@ -50,6 +50,7 @@ constexpr int kGenericThreads = 256;
 constexpr int kLayoutNHD = 0;
 constexpr int kLayoutHND = 1;
 constexpr int kLayoutLatent = 2;
+constexpr int kLayoutXSplit = 3;
 
 constexpr u32 kStatusBadBlockId = 1u;
 constexpr u32 kStatusBadRequests = 2u;
@@ -76,7 +77,7 @@ struct DevCache {
   int rpu;          // rows (NHD, latent) or heads (HND) per unit
   int column;       // replica-key column the cache adds into
   int kbs;          // HND: slots per kernel sub-block (block_size if none)
-  int pad;
+  int chunks;       // HND: 1; x-split: 16-byte chunks per head (hb / 16)
 };
 
 struct Params {
@@ -276,6 +277,7 @@ __device__ __forceinline__ void make_map(ThreadMap &t, int rowb, int gtid,
 
 // This thread's share of one staged unit's contribution to the block
 // checksum (see the reformulation at the top of this file).
+template <bool kGeneral>
 __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
                                         int half, const unsigned char *stage,
                                         const ThreadMap &t, u64 bsz) {
@@ -284,7 +286,7 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
   const int half_pieces = half * (C.hb >> 3);
   const int rowb = t.rowb;
   u64 acc = 0;
-  if (C.layout != kLayoutHND) {
+  if (!kGeneral || (C.layout != kLayoutHND && C.layout != kLayoutXSplit)) {
     const int nrows = m.count;
     const u32 r0 = static_cast<u32>(m.first);
     for (int col = t.col0; col < t.cols; col += t.cstep) {
@@ -331,13 +333,16 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
     }
   } else {
     // HND unit: heads [first, first + count), each with nv staged rows
-    // (slots 0 .. nv-1) of hb bytes, packed head after head.
+    // (slots 0 .. nv-1) of hb bytes, packed head after head.  An x-split
+    // unit is the same with every head cut into `chunks` 16-byte columns:
+    // staged [head][chunk][nv][16], one row per (head, chunk, slot).  Rows
+    // are grouped per (head, chunk); a group's head and piece pair are
+    // fixed, so it keeps the running sums and is weighted once.
     const int nv = m.nv;
-    const int nrows = m.count * nv;
+    const int nrows = m.count * C.chunks * nv;
     for (int col = t.col0; col < t.cols; col += t.cstep) {
       int r = t.rl;
       if (r >= nrows) continue;
-      const u64 B = 2ull * (t0P + static_cast<u64>((col << 1) + half_pieces)) + 1ull;
       int hh = r / nv;
       int slot = r - hh * nv;
       u64 S = 0, T = 0, U = 0;
@@ -355,7 +360,11 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
         sp += step;
         slot += t.rstep;
         if (slot >= nv || r >= nrows) {
-          const u64 mh = C.m0 + 2ull * static_cast<u64>(m.first + hh);
+          const int head = hh / C.chunks;
+          const int chunk = hh - head * C.chunks;
+          const u64 mh = C.m0 + 2ull * static_cast<u64>(m.first + head);
+          const u64 B =
+              2ull * (t0P + static_cast<u64>(((col + chunk) << 1) + half_pieces)) + 1ull;
           acc += mh * (B * S + 2ull * P * T + 2ull * U);
           S = T = U = 0;
           if (r >= nrows) break;
@@ -426,6 +435,11 @@ __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
 //
 // Every wait is bounded; a wait that runs out sets KVCS_STATUS_TIMEOUT and
 // the kernel returns without hanging.
+//
+// kGeneral = false is the instance for launches whose caches are all NHD or
+// latent: it carries no HND or x-split code, which keeps the common path's
+// register allocation and scheduling independent of the rarer layouts.
+template <bool kGeneral>
 __global__ void __launch_bounds__(kBulkThreads, 1)
     kvcs_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -508,7 +522,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           const int first = sub * C.rpu;
           int count;
           u32 pbytes;   // valid bytes of one page of the unit
-          if (C.layout == kLayoutHND) {
+          if (kGeneral && (C.layout == kLayoutHND || C.layout == kLayoutXSplit)) {
             count = max(0, min(C.rpu, C.heads - first));
             pbytes = static_cast<u32>(count) * static_cast<u32>(cur.nv) *
                      static_cast<u32>(C.hb);
@@ -540,7 +554,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               const unsigned char *page = D.base +
                   static_cast<long long>(phalf) * D.half_stride +
                   cur.block * D.block_stride;
-              if (D.layout == kLayoutHND) {
+              if (kGeneral && D.layout == kLayoutHND) {
                 // A page is [sub-block][heads][kbs][hb] (one sub-block of
                 // block_size slots unless the attention kernel splits
                 // blocks); stage each head's valid slots as one packed run.
@@ -560,6 +574,23 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                       src += sub_bytes;
                     }
                   }
+                }
+              } else if (kGeneral && D.layout == kLayoutXSplit) {
+                // A page is [heads][chunks][block_size][16]: stage each
+                // (head, chunk) run of valid slots packed, [h][c][nv][16].
+                const u64 head_bytes_page = static_cast<u64>(bs) * D.hb;
+                if (cur.nv == bs) {
+                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * head_bytes_page,
+                                pbytes, fb, policy);
+                } else {
+                  const u32 run = static_cast<u32>(cur.nv) * 16u;
+                  const unsigned char *src = page + static_cast<u64>(first) * head_bytes_page;
+                  for (int hc = 0; hc < count * D.chunks; ++hc) {
+                    ptx::bulk_g2s(dst, src, run, fb, policy);
+                    dst += run;
+                    src += static_cast<u64>(bs) * 16u;
+                  }
+                  dst -= static_cast<u32>(count * D.chunks) * run;
                 }
               } else {
                 ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes,
@@ -676,8 +707,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     for (int k = 0; k < m.npages; ++k) {
       const DevCache &C = p.caches[ci];
       if (C.rowb != map.rowb) make_map(map, C.rowb, gtid, gw * 32);
-      v += unit_sum(C, m, half, sp, map, bsz);
-      sp += C.layout == kLayoutHND
+      v += unit_sum<kGeneral>(C, m, half, sp, map, bsz);
+      sp += (kGeneral && (C.layout == kLayoutHND || C.layout == kLayoutXSplit))
                 ? static_cast<size_t>(m.count) * m.nv * C.hb
                 : static_cast<size_t>(m.count) * C.rowb;
       if (++half == C.halves) {
@@ -765,6 +796,8 @@ __global__ void __launch_bounds__(kGenericThreads)
               const long long page = half * C.half_stride + b * C.block_stride;
               if (C.layout == kLayoutNHD) {
                 off = page + (slot * C.heads + h) * C.hb + e;
+              } else if (C.layout == kLayoutXSplit) {
+                off = page + ((h * (C.hb >> 4) + (e >> 4)) * bs + slot) * 16 + (e & 15);
               } else {
                 const long long sb = slot / C.kbs;
                 off = page + ((sb * C.heads + h) * C.kbs + (slot - sb * C.kbs)) * C.hb + e;

@@ -28,6 +28,7 @@ import torch
 LAYOUT_NHD = 0
 LAYOUT_HND = 1
 LAYOUT_LATENT = 2
+LAYOUT_XSPLIT = 3   # [2, num_blocks, heads, head_bytes / 16, block_size, 16]
 
 # Value recipes for pool bytes.  Every one produces raw bits that are only
 # ever read back as bytes.

@@ -70,7 +70,7 @@ def test_validation_codes():
     assert code_of([ok]) == 0
     assert code_of([FakeCache(head_bytes=12)]) == K.KVCS_EINVAL
     assert code_of([FakeCache(head_bytes=0)]) == K.KVCS_EINVAL
-    assert code_of([FakeCache(layout=3)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layout=5)]) == K.KVCS_EINVAL
     assert code_of([FakeCache(layout=2, num_heads=2)]) == K.KVCS_EINVAL
     assert code_of([FakeCache(layer=-1)]) == K.KVCS_EINVAL
     assert code_of([FakeCache(base=0)]) == K.KVCS_EINVAL
@@ -97,6 +97,10 @@ def test_validation_codes():
     assert code_of([FakeCache(block_stride=page + 4)]) == K.KVCS_EINVAL
     assert code_of([FakeCache(layout=1, kernel_block_size=4)]) == 0
     assert code_of([FakeCache(layout=1, kernel_block_size=5)]) == K.KVCS_EINVAL
+    # x-split: 16-byte chunks
+    assert code_of([FakeCache(layout=3)]) == 0
+    assert code_of([FakeCache(layout=3, head_bytes=24)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layout=4)]) == K.KVCS_EINVAL
     # strides that are 8- but not 16-byte multiples fall back to the generic kernel
     assert plan([FakeCache(block_stride=page + 8)])["kernel"] == 1
     assert plan([FakeCache(block_stride=page + 16)])["kernel"] == 0

@@ -118,3 +118,32 @@ def test_nhd_kernel_block_size_is_the_same_memory():
     caches = [dataclasses.replace(c, kernel_block_size=4) for c in wl.caches]
     got, st = run(with_caches(wl, caches))
     assert st == 0 and np.array_equal(got, exp)
+
+
+@pytest.mark.parametrize("hb,bs", [(64, 16), (256, 16), (32, 5), (16, 1)])
+@pytest.mark.parametrize("pad", [0, 8])       # bulk kernel, generic kernel
+def test_xsplit_layout(hb, bs, pad):
+    """[2, num_blocks, heads, head_bytes / 16, block_size, 16]: the x-split
+    layout (16-byte x chunks) for K and V pages."""
+    heads = 4
+    wl, exp = canonical(6, W.LAYOUT_NHD, hb=hb, bs=bs, heads=heads,
+                        lengths=(70, 33, 5))
+    C = hb // 16
+    caches = []
+    for c in wl.caches:
+        v = c.pool.view(2, c.num_blocks, bs, heads, C, 16).permute(0, 1, 3, 4, 2, 5)
+        x = v.contiguous().view(2 * c.num_blocks, -1)
+        pb = x.shape[1]
+        if pad:
+            buf = torch.zeros(2 * c.num_blocks, pb + pad, dtype=torch.uint8, device=DEV)
+            buf[:, :pb] = x
+            spec = dataclasses.replace(c, pool=buf.view(-1), layout=W.LAYOUT_XSPLIT,
+                                       block_stride=pb + pad,
+                                       half_stride=c.num_blocks * (pb + pad))
+        else:
+            spec = dataclasses.replace(c, pool=x.view(-1), layout=W.LAYOUT_XSPLIT)
+        caches.append(spec)
+    plan = K.plan_for(caches, wl.block_size, wl.num_positions)
+    assert plan["kernel"] == (1 if pad else 0)
+    got, st = run(with_caches(wl, caches))
+    assert st == 0 and np.array_equal(got, exp)
