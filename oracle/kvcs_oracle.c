@@ -27,6 +27,7 @@
 #define ORACLE_LAYOUT_NHD 0    /* pool [2][num_blocks][block_size][heads][head_bytes] */
 #define ORACLE_LAYOUT_HND 1    /* pool [2][num_blocks][heads][block_size][head_bytes] */
 #define ORACLE_LAYOUT_LATENT 2 /* pool [num_blocks][block_size][row_bytes] */
+#define ORACLE_LAYOUT_STATE 4  /* pool [num_blocks][rows][row_bytes]: Mamba state */
 
 #define ORACLE_H 65536u /* MAX_KV_HEADS_PER_LAYER */
 #define ORACLE_STATUS_BAD_BLOCK_ID 1u
@@ -38,8 +39,8 @@ typedef struct oracle_cache {
   int32_t layer;
   int32_t head_offset;
   int32_t num_heads;
-  int32_t head_bytes; /* K (= V) bytes per head per token; latent: row bytes */
-  int32_t reserved;
+  int32_t head_bytes; /* K (= V) bytes per head per token; latent/state: row bytes */
+  int32_t piece_bytes; /* state: element bytes (2 or 4); else ignored (8) */
 } oracle_cache;
 
 /* Tokens of the request's first num_tokens that block `position` holds. */
@@ -98,6 +99,26 @@ static uint64_t slice_checksum(const oracle_cache *c, int64_t block_size,
   return s;
 }
 
+/* Element p (little-endian, unsigned) of local row `row` of a state block. */
+static uint64_t state_piece(const oracle_cache *c, int64_t block, int64_t row,
+                            int64_t p) {
+  int64_t off = (block * c->num_heads + row) * c->head_bytes + p * c->piece_bytes;
+  uint64_t x = 0;
+  for (int k = 0; k < c->piece_bytes; ++k) x |= (uint64_t)c->data[off + k] << (8 * k);
+  return x;
+}
+
+/* s of one global row of a Mamba state (paragraph on Mamba state): its
+ * elements are the pieces and the piece index is the element index. */
+static uint64_t state_slice_checksum(const oracle_cache *c, int64_t block,
+                                     int64_t row) {
+  uint64_t s = 0;
+  int64_t n = c->head_bytes / c->piece_bytes;
+  for (int64_t p = 0; p < n; ++p)
+    s += state_piece(c, block, row, p) * (2 * (uint64_t)p + 1);
+  return s;
+}
+
 /* m = 2 * (layer * H + head) + 1 (item 2). */
 static uint64_t slice_factor(int64_t layer, int64_t global_head) {
   return 2 * ((uint64_t)layer * ORACLE_H + (uint64_t)global_head) + 1;
@@ -111,6 +132,14 @@ static uint64_t block_checksum(const oracle_cache *caches, int32_t num_caches,
   uint64_t c = 0;
   for (int32_t k = 0; k < num_caches; ++k) {
     const oracle_cache *ca = &caches[k];
+    if (ca->layout == ORACLE_LAYOUT_STATE) {
+      /* a state block lives at position 0 only; its rows are its slices */
+      if (position != 0) continue;
+      for (int64_t r = 0; r < ca->num_heads; ++r)
+        c += slice_factor(ca->layer, (int64_t)ca->head_offset + r) *
+             state_slice_checksum(ca, block, r);
+      continue;
+    }
     for (int64_t h = 0; h < ca->num_heads; ++h) {
       uint64_t s = slice_checksum(ca, block_size, block, position, nv, h);
       c += slice_factor(ca->layer, (int64_t)ca->head_offset + h) * s;
@@ -174,12 +203,19 @@ int oracle_block_checksums(const oracle_cache *caches, int32_t num_caches,
     return -1;
   for (int32_t k = 0; k < num_caches; ++k) {
     const oracle_cache *c = &caches[k];
+    if (c->layout == ORACLE_LAYOUT_STATE) {
+      if ((c->piece_bytes != 2 && c->piece_bytes != 4) || c->head_bytes <= 0 ||
+          c->head_bytes % c->piece_bytes || c->num_heads < 1 || c->head_offset < 0 ||
+          (int64_t)c->head_offset + c->num_heads > (int64_t)ORACLE_H)
+        return -1;
+      continue;
+    }
     if (c->head_bytes <= 0 || c->head_bytes % 8 || c->num_heads < 1 ||
         c->head_offset < 0 ||
         (int64_t)c->head_offset + c->num_heads > (int64_t)ORACLE_H)
       return -1;
     if (c->layout == ORACLE_LAYOUT_LATENT && c->num_heads != 1) return -1;
-    if (c->layout < 0 || c->layout > 2) return -1;
+    if (c->layout < 0 || c->layout > 2) return -1; /* 3 (x-split) is a GPU-side layout */
   }
   if (pos_offsets[0] != 0) return -1;
   for (int64_t r = 0; r < num_requests; ++r)

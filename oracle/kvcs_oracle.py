@@ -57,6 +57,7 @@ BLOCK_CHECKSUM_BYTES = 8
 LAYOUT_NHD = 0     # pool [2, num_blocks, block_size, num_heads, head_bytes]
 LAYOUT_HND = 1     # pool [2, num_blocks, num_heads, block_size, head_bytes]
 LAYOUT_LATENT = 2  # pool [num_blocks, block_size, row_bytes]
+LAYOUT_STATE = 4   # pool [num_blocks, rows, row_bytes]: Mamba running state
 
 STATUS_BAD_BLOCK_ID = 1
 
@@ -69,6 +70,13 @@ class OracleCache:
     given by ``layout``.  ``head_bytes`` is the bytes of one head's K (equal to
     its V) for one token; for ``LAYOUT_LATENT`` it is the bytes of one token's
     latent row and ``num_heads`` must be 1.
+
+    ``LAYOUT_STATE`` holds a Mamba layer's running state, one block per
+    request: ``num_heads`` local rows (the TP-split dimension) of
+    ``head_bytes`` bytes, whose pieces are ``piece_bytes``-byte elements
+    (2 or 4); ``head_offset`` is the global index of local row 0.  A state
+    whose split is unknown is one row per TP shard (``head_offset`` = the
+    shard index).
     """
 
     data: np.ndarray
@@ -78,6 +86,7 @@ class OracleCache:
     head_offset: int
     num_heads: int
     head_bytes: int
+    piece_bytes: int = 8
 
 
 @dataclass(frozen=True)
@@ -179,6 +188,16 @@ def slice_factor(layer: int, global_head: int) -> int:
 
 def check_cache(cache: OracleCache, block_size: int) -> None:
     """Reject what the definition does not cover (see module docstring)."""
+    if cache.layout == LAYOUT_STATE:
+        if cache.piece_bytes not in (2, 4) or cache.head_bytes <= 0 or \
+                cache.head_bytes % cache.piece_bytes:
+            raise ValueError("state rows are whole 2- or 4-byte elements")
+        if cache.head_offset < 0 or cache.num_heads < 1 or \
+                cache.head_offset + cache.num_heads > MAX_KV_HEADS_PER_LAYER:
+            raise ValueError("bad row range")
+        if cache.data.size < cache.num_blocks * cache.num_heads * cache.head_bytes:
+            raise ValueError("pool smaller than its declared geometry")
+        return
     if cache.head_bytes <= 0 or cache.head_bytes % 8:
         raise ValueError("per-token bytes must be a positive multiple of 8")
     if cache.layout == LAYOUT_LATENT and cache.num_heads != 1:
@@ -193,13 +212,39 @@ def check_cache(cache: OracleCache, block_size: int) -> None:
         raise ValueError("pool smaller than its declared geometry")
 
 
+def state_piece(cache: OracleCache, block: int, row: int, p: int) -> int:
+    """Element ``p`` of local row ``row`` of a state block, read unsigned."""
+    w = cache.piece_bytes
+    off = (block * cache.num_heads + row) * cache.head_bytes + w * p
+    return int.from_bytes(bytes(cache.data[off:off + w]), "little")
+
+
+def state_slice_checksum(cache: OracleCache, block: int, row: int) -> int:
+    """``s`` of one global row of a Mamba state (paragraph on Mamba state):
+    the row's elements are its pieces; the state is not per token, so the
+    piece index is the element index."""
+    s = 0
+    for p in range(cache.head_bytes // cache.piece_bytes):
+        s += state_piece(cache, block, row, p) * piece_weight(p)
+    return s & MASK64
+
+
 def block_checksum(caches: Sequence[OracleCache], block_size: int, block: int,
                    position: int, num_tokens: int) -> int:
     """``c = sum_{layer, head} m*s mod 2**64`` for block ``block`` at block
-    position ``position`` of a request with ``num_tokens`` tokens (item 2)."""
+    position ``position`` of a request with ``num_tokens`` tokens (item 2).
+    A Mamba state block lives at position 0 only (paragraph on Mamba state);
+    its rows are its slices."""
     nv = num_valid_tokens(position, block_size, num_tokens)
     c = 0
     for cache in caches:
+        if cache.layout == LAYOUT_STATE:
+            if position != 0:
+                continue
+            for r in range(cache.num_heads):
+                s = state_slice_checksum(cache, block, r)
+                c += slice_factor(cache.layer, cache.head_offset + r) * s
+            continue
         for h in range(cache.num_heads):
             s = slice_checksum(cache, block_size, block, position, nv, h)
             c += slice_factor(cache.layer, cache.head_offset + h) * s
