@@ -63,12 +63,20 @@ def make_workload(name: str, seed: int, device):
         return W.llama3_70b(seed, device, num_requests=int(name[len("llama3_70b_r"):]))
     if name == "tiny":
         return W.tiny(seed, device)
+    if name == "mamba2":                # Mamba2-shaped running states, 10.9 GB
+        return W.mamba2(seed, device)
     raise SystemExit(f"unknown config {name}")
 
 
 def kv_bytes(wl) -> int:
     """Algorithmic KV bytes one step reads: valid tokens of every position
-    times the bytes a token occupies across all caches."""
+    times the bytes a token occupies across all caches (for Mamba states:
+    the state pages of the requests' block position 0)."""
+    if wl.caches and wl.caches[0].layout == 4:
+        state = sum(c.num_heads * c.head_bytes for c in wl.caches)
+        po = wl.pos_offsets.cpu().tolist()
+        fp = wl.first_position.cpu().tolist()
+        return state * sum(1 for r in range(len(fp)) if fp[r] == 0 and po[r + 1] > po[r])
     per_token = sum((1 if c.layout == 2 else 2) * c.num_heads * c.head_bytes
                     for c in wl.caches)
     po = wl.pos_offsets.cpu().tolist()
@@ -87,7 +95,8 @@ def describe(wl, name) -> dict:
     i = wl.info
     return {"workload": f"{name}_paged_kv_checksum", "layers": i.get("layers"),
             "kv_heads": i.get("heads"), "head_bytes": i.get("head_bytes"),
-            "block_size": wl.block_size, "layout": ["NHD", "HND", "LATENT"][i.get("layout", 0)],
+            "block_size": wl.block_size,
+            "layout": ["NHD", "HND", "LATENT", "XSPLIT", "STATE"][i.get("layout", 0)],
             "kv_recipe": i.get("kind"), "requests": wl.num_requests,
             "positions": wl.num_positions, "kv_bytes": kv_bytes(wl),
             "seed": i.get("seed"),
@@ -261,14 +270,19 @@ def _oracle_inputs(wl, n: int, seed: int):
     nt = wl.num_tokens.cpu()[req]
     ids = wl.block_ids.cpu()[pos].to(torch.int64).to(wl.block_ids.device)
     caches = []
+    state = bool(wl.caches) and wl.caches[0].layout == 4
     for c in wl.caches:
-        halves = 1 if c.layout == 2 else 2
-        page = wl.block_size * c.num_heads * c.head_bytes
+        halves = 1 if c.layout in (2, 4) else 2
+        page = (1 if state else wl.block_size) * c.num_heads * c.head_bytes
         pages = c.pool.view(halves, c.num_blocks, page)[:, ids].cpu().numpy()
         caches.append(OracleCache(pages.reshape(-1), len(pos), c.layout, c.layer,
-                                  c.head_offset, c.num_heads, c.head_bytes))
+                                  c.head_offset, c.num_heads, c.head_bytes,
+                                  c.piece_bytes or 8))
     reqs = OracleRequests(list(range(len(pos) + 1)), q.tolist(), nt.tolist(),
                           list(range(len(pos))))
+    if state:
+        per_state = sum(c.num_heads * c.head_bytes for c in wl.caches)
+        return caches, reqs, per_state * int((q == 0).sum()), len(pos)
     per_token = sum((1 if c.layout == 2 else 2) * c.num_heads * c.head_bytes
                     for c in wl.caches)
     bs = wl.block_size

@@ -57,20 +57,31 @@ extern "C" {
  *           the x-split layout of the KV-cache page's reshape_and_cache
  *           section ([num_blocks, heads, head_size/x, block_size, x] with x
  *           elements = 16 bytes), used here for both K and V pages;
- *           head_bytes must be a multiple of 16 */
+ *           head_bytes must be a multiple of 16
+ *   STATE:  pool [num_blocks][num_heads rows][head_bytes]: a Mamba layer's
+ *           running state, one block per request at block position 0 (the
+ *           checksum page, paragraph on Mamba state).  Each row is one
+ *           global row along the TP-split dimension (head_offset = global
+ *           index of local row 0) and is a slice whose pieces are its
+ *           piece_bytes-wide elements (2 or 4) read unsigned, weighted by
+ *           element index.  A state whose split is unknown is passed as one
+ *           row per TP shard (head_offset = the shard index).  Other block
+ *           positions hold no state (0); num_tokens does not apply.  A call
+ *           holds either only STATE caches or none. */
 typedef enum kvcs_layout {
   KVCS_LAYOUT_NHD = 0,
   KVCS_LAYOUT_HND = 1,
   KVCS_LAYOUT_LATENT = 2,
-  KVCS_LAYOUT_XSPLIT = 3
+  KVCS_LAYOUT_XSPLIT = 3,
+  KVCS_LAYOUT_STATE = 4
 } kvcs_layout;
 
 /* One layer's paged pool (one attention layer, or one of several caches of
  * a layer such as an indexer's, numbered by consecutive head offsets).
  * Read-only to the library.  A page is one block's K, its V, or its latent
  * rows: page_bytes = block_size * num_heads * head_bytes contiguous bytes in
- * the layout's order; the page of (half, block) starts at
- * base + half * half_stride + block * block_stride. */
+ * the layout's order (STATE: num_heads * head_bytes); the page of
+ * (half, block) starts at base + half * half_stride + block * block_stride. */
 typedef struct kvcs_cache {
   const void *base;    /* DEVICE pointer to the pool; 8-byte aligned
                           (16-byte alignment enables the bulk-copy kernel) */
@@ -81,9 +92,10 @@ typedef struct kvcs_cache {
                           offset, or the head count of earlier caches of the
                           same layer); LATENT: the one head's global index */
   int32_t num_heads;   /* local KV heads; 1 for LATENT */
-  int32_t head_bytes;  /* NHD/HND: bytes of one head's K (= its V) for one
-                          token; LATENT: bytes of one token row.  A positive
-                          multiple of 8. */
+  int32_t head_bytes;  /* NHD/HND/XSPLIT: bytes of one head's K (= its V)
+                          for one token; LATENT: bytes of one token row; a
+                          positive multiple of 8.  STATE: bytes of one state
+                          row, a positive multiple of piece_bytes. */
   int32_t column;      /* replica-key column this cache's layer adds into
                           (kvcs_group_checksums); 0 for kvcs_block_checksums */
   int64_t half_stride; /* NHD/HND: bytes from a block's K page to its V page
@@ -102,7 +114,7 @@ typedef struct kvcs_cache {
                           0 = block_size.  Must divide block_size.  For NHD and
                           LATENT, consecutive sub-blocks are already the
                           block's rows in order, so the field is ignored. */
-  int32_t reserved;    /* must be 0 */
+  int32_t piece_bytes; /* STATE: element bytes, 2 or 4; other layouts: 0 */
 } kvcs_cache;
 
 /* The requests to checksum, in CSR form over requests.  All pointers are
@@ -128,7 +140,8 @@ typedef struct kvcs_requests {
 #define KVCS_EINVAL (-1)      /* null pointer, non-positive block_size,
                                  strides not multiples of 8 or smaller than a
                                  page, kernel_block_size not dividing
-                                 block_size, reserved != 0,
+                                 block_size, bad piece_bytes, STATE caches
+                                 mixed with KV caches,
                                  head_bytes not a positive multiple of 8,
                                  unknown layout, latent cache with heads != 1,
                                  negative layer or head offset, a column
@@ -245,10 +258,12 @@ int kvcs_block_checksum_tags(const void *block_hashes, int64_t hash_stride,
 /* Which kernel and launch shape kvcs_block_checksums would use.  Filled by
  * kvcs_plan; no CUDA work is enqueued. */
 typedef struct kvcs_plan_info {
-  int32_t kernel;        /* 0 = bulk-copy pipeline, 1 = generic 8-byte loads */
-  int32_t split;         /* 1 if positions are split across CTAs (output is
-                            zeroed first and partial sums are added with
-                            64-bit atomics) */
+  int32_t kernel;        /* 0 = bulk-copy pipeline, 1 = generic direct
+                            loads, 2 = both (caches the bulk kernel cannot
+                            stage go to the generic one) */
+  int32_t split;         /* 1 if the bulk kernel splits positions across CTAs
+                            (output zeroed first, partial sums added with
+                            64-bit atomics; the generic kernel always adds) */
   int32_t launches;      /* kernel launches per call (one per cache group) */
   int32_t memsets;       /* cudaMemsetAsync calls per call (0 or 1) */
   int32_t grid;          /* CTAs per kernel launch */

@@ -16,6 +16,7 @@ KVCS_LAYOUT_NHD = 0
 KVCS_LAYOUT_HND = 1
 KVCS_LAYOUT_LATENT = 2
 KVCS_LAYOUT_XSPLIT = 3
+KVCS_LAYOUT_STATE = 4
 KVCS_MAX_KV_HEADS_PER_LAYER = 65536
 KVCS_BLOCK_CHECKSUM_BYTES = 8
 
@@ -35,7 +36,7 @@ class kvcs_cache(ctypes.Structure):
                 ("head_offset", ctypes.c_int32), ("num_heads", ctypes.c_int32),
                 ("head_bytes", ctypes.c_int32), ("column", ctypes.c_int32),
                 ("half_stride", ctypes.c_int64), ("block_stride", ctypes.c_int64),
-                ("kernel_block_size", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("kernel_block_size", ctypes.c_int32), ("piece_bytes", ctypes.c_int32)]
 
 
 class kvcs_outputs(ctypes.Structure):
@@ -147,7 +148,8 @@ def cache_array(caches: Sequence) -> ctypes.Array:
         arr[i] = kvcs_cache(base, c.num_blocks, c.layout, c.layer, c.head_offset,
                             c.num_heads, c.head_bytes, getattr(c, "column", 0),
                             half_stride, getattr(c, "block_stride", 0),
-                            getattr(c, "kernel_block_size", 0), 0)
+                            getattr(c, "kernel_block_size", 0),
+                            getattr(c, "piece_bytes", 0))
     return arr
 
 
@@ -183,10 +185,10 @@ def _check_pool(c, block_size: int) -> None:
     for x in (t, v_pool):
         if x is not None and not (x.is_cuda and x.is_contiguous()):
             raise ValueError("cache pools must be contiguous CUDA tensors")
-    page = block_size * c.num_heads * c.head_bytes
+    page = (1 if c.layout == KVCS_LAYOUT_STATE else block_size) * c.num_heads * c.head_bytes
     bstride = getattr(c, "block_stride", 0) or page
     span = (c.num_blocks - 1) * bstride + page if c.num_blocks > 0 else 0
-    if c.layout == KVCS_LAYOUT_LATENT:
+    if c.layout in (KVCS_LAYOUT_LATENT, KVCS_LAYOUT_STATE):
         halves = [(t, 0)]
     elif v_pool is not None:
         halves = [(t, 0), (v_pool, 0)]

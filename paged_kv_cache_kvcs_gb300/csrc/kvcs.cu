@@ -59,19 +59,17 @@ cudaError_t device_setup(int *sms) {
   return d.err;
 }
 
-struct Plan {
-  int kernel = 0;  // 0 bulk, 1 generic
-  int split = 0;
-  int groups = 1;
-  int grid = 0;
-  int stage_bytes = 0;       // of the first launch
-  int stages = 0;
-  long long units = 0;       // units of the largest launch
-  long long kv_bytes_max = 0;
-};
+constexpr int kMaxColumns = 64;
 
-// The bulk kernel stages whole rows (NHD, latent) or whole heads (HND) with
-// 16-byte-aligned bulk copies and reads 16-byte columns.
+// Bytes of one page: one block of K, of V, of latent rows, or of state rows.
+long long page_bytes_of(const kvcs_cache &c, int block_size) {
+  if (c.layout == KVCS_LAYOUT_STATE)
+    return static_cast<long long>(c.num_heads) * c.head_bytes;
+  return static_cast<long long>(block_size) * c.num_heads * c.head_bytes;
+}
+
+// The bulk kernel stages whole rows (NHD, latent, state) or whole heads
+// (HND, x-split) with 16-byte-aligned bulk copies and reads 16-byte columns.
 bool bulk_eligible(const kvcs_cache &c, int block_size) {
   if (reinterpret_cast<uintptr_t>(c.base) % 16) return false;
   if (c.head_bytes % 16 || c.half_stride % 16 || c.block_stride % 16) return false;
@@ -80,14 +78,13 @@ bool bulk_eligible(const kvcs_cache &c, int block_size) {
     case KVCS_LAYOUT_NHD: return hb * c.num_heads <= kMaxUnitBytes;
     case KVCS_LAYOUT_HND:
     case KVCS_LAYOUT_XSPLIT: return hb * block_size <= kMaxUnitBytes;
-    default: return hb <= kMaxUnitBytes;
+    default: return hb <= kMaxUnitBytes;  // latent and state rows
   }
 }
 
-constexpr int kMaxColumns = 64;
-
 // Host-argument checks shared by every entry point.  Every column in
-// [0, num_columns) must be named by at least one cache.
+// [0, num_columns) must be named by at least one cache.  State caches (Mamba
+// running states) cannot be mixed with KV caches in one call.
 int validate_caches(const kvcs_cache *caches, int32_t num_caches,
                     int32_t block_size, int32_t num_columns) {
   if (!caches || num_caches < 1 || block_size <= 0) return KVCS_EINVAL;
@@ -99,29 +96,37 @@ int validate_caches(const kvcs_cache *caches, int32_t num_caches,
   };
   std::vector<Span> spans;
   spans.reserve(num_caches);
+  int states = 0;
   for (int32_t i = 0; i < num_caches; ++i) {
     const kvcs_cache &c = caches[i];
-    if (!c.base || c.num_blocks < 0 || c.reserved != 0) return KVCS_EINVAL;
+    if (!c.base || c.num_blocks < 0) return KVCS_EINVAL;
+    if (c.layout < KVCS_LAYOUT_NHD || c.layout > KVCS_LAYOUT_STATE) return KVCS_EINVAL;
     if (c.column < 0 || c.column >= num_columns) return KVCS_EINVAL;
     used[c.column] = true;
-    if (c.layout < KVCS_LAYOUT_NHD || c.layout > KVCS_LAYOUT_XSPLIT) return KVCS_EINVAL;
-    if (c.layout == KVCS_LAYOUT_XSPLIT && c.head_bytes % 16) return KVCS_EINVAL;
     if (c.layer < 0 || c.head_offset < 0 || c.num_heads < 1) return KVCS_EINVAL;
-    if (c.head_bytes <= 0 || c.head_bytes % 8) return KVCS_EINVAL;
+    if (c.layout == KVCS_LAYOUT_STATE) {
+      ++states;
+      if (c.piece_bytes != 2 && c.piece_bytes != 4) return KVCS_EINVAL;
+      if (c.head_bytes <= 0 || c.head_bytes % c.piece_bytes) return KVCS_EINVAL;
+    } else {
+      if (c.piece_bytes != 0) return KVCS_EINVAL;
+      if (c.head_bytes <= 0 || c.head_bytes % 8) return KVCS_EINVAL;
+    }
     if (c.layout == KVCS_LAYOUT_LATENT && c.num_heads != 1) return KVCS_EINVAL;
+    if (c.layout == KVCS_LAYOUT_XSPLIT && c.head_bytes % 16) return KVCS_EINVAL;
     if (reinterpret_cast<uintptr_t>(c.base) % 8) return KVCS_EINVAL;
     if (static_cast<int64_t>(c.head_offset) + c.num_heads > KVCS_MAX_KV_HEADS_PER_LAYER)
       return KVCS_EUNSUPPORTED;
-    // Bytes per page must stay addressable in 64 bits (always true for real
-    // pools; guards absurd descriptors).
-    const double page = static_cast<double>(block_size) * c.num_heads * c.head_bytes;
+    // Bytes must stay addressable in 64 bits (always true for real pools;
+    // guards absurd descriptors).
+    const double page = static_cast<double>(page_bytes_of(c, block_size));
     if (page * 2.0 * static_cast<double>(c.num_blocks) > 9.0e18) return KVCS_EINVAL;
     // Strides: 8-byte multiples; pages of different blocks, and a block's K
     // and V pages, must not overlap.
     if (c.half_stride % 8 || c.block_stride % 8) return KVCS_EINVAL;
     if (c.block_stride != 0 && static_cast<double>(c.block_stride) < page) return KVCS_EINVAL;
-    if (c.layout != KVCS_LAYOUT_LATENT && c.half_stride != 0 &&
-        std::fabs(static_cast<double>(c.half_stride)) < page)
+    const bool two_halves = c.layout != KVCS_LAYOUT_LATENT && c.layout != KVCS_LAYOUT_STATE;
+    if (two_halves && c.half_stride != 0 && std::fabs(static_cast<double>(c.half_stride)) < page)
       return KVCS_EINVAL;
     if (std::fabs(static_cast<double>(c.half_stride)) > 9.0e18 ||
         std::fabs(static_cast<double>(c.block_stride)) * static_cast<double>(c.num_blocks) > 9.0e18)
@@ -132,6 +137,7 @@ int validate_caches(const kvcs_cache *caches, int32_t num_caches,
     spans.push_back({c.layer, c.head_offset,
                      static_cast<int64_t>(c.head_offset) + c.num_heads});
   }
+  if (states != 0 && states != num_caches) return KVCS_EINVAL;
   std::sort(spans.begin(), spans.end(), [](const Span &a, const Span &b) {
     return a.layer != b.layer ? a.layer < b.layer : a.lo < b.lo;
   });
@@ -162,7 +168,7 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
   d.layout = c.layout;
   d.heads = c.num_heads;
   d.hb = c.head_bytes;
-  d.page_bytes = static_cast<u64>(block_size) * c.num_heads * c.head_bytes;
+  d.page_bytes = static_cast<u64>(page_bytes_of(c, block_size));
   d.half_stride = c.half_stride != 0
                       ? c.half_stride
                       : static_cast<long long>(c.num_blocks) * static_cast<long long>(d.page_bytes);
@@ -171,14 +177,18 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
   d.kbs = (c.layout == KVCS_LAYOUT_HND && c.kernel_block_size > 0) ? c.kernel_block_size
                                                                   : block_size;
   d.chunks = c.layout == KVCS_LAYOUT_XSPLIT ? c.head_bytes / 16 : 1;
-  d.halves = c.layout == KVCS_LAYOUT_LATENT ? 1 : 2;
-  d.P = (c.layout == KVCS_LAYOUT_LATENT ? c.head_bytes : 2 * c.head_bytes) / 8;
+  d.pbytes = c.layout == KVCS_LAYOUT_STATE ? c.piece_bytes : 8;
+  d.halves = (c.layout == KVCS_LAYOUT_LATENT || c.layout == KVCS_LAYOUT_STATE) ? 1 : 2;
+  d.P = c.layout == KVCS_LAYOUT_STATE
+            ? c.head_bytes / c.piece_bytes
+            : (c.layout == KVCS_LAYOUT_LATENT ? c.head_bytes : 2 * c.head_bytes) / 8;
   d.column = c.column;
   d.hb_shift = -1;
   for (int k = 0; k < 31; ++k)
     if (c.head_bytes == (1 << k)) d.hb_shift = k;
   // Units: cut a page into runs of about kUnitTargetBytes, as evenly as
-  // possible, of whole rows (NHD, latent) or whole heads (HND).
+  // possible, of whole rows (NHD, latent, state) or whole heads (HND,
+  // x-split).
   if (c.layout == KVCS_LAYOUT_HND || c.layout == KVCS_LAYOUT_XSPLIT) {
     d.rowb = c.layout == KVCS_LAYOUT_HND ? c.head_bytes : 16;
     const long long head = static_cast<long long>(block_size) * c.head_bytes;
@@ -187,9 +197,10 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
     d.rpu = (c.num_heads + d.upp - 1) / d.upp;
   } else {
     d.rowb = c.layout == KVCS_LAYOUT_NHD ? c.num_heads * c.head_bytes : c.head_bytes;
+    const int rows = c.layout == KVCS_LAYOUT_STATE ? c.num_heads : block_size;
     const int fit = std::max(1, kUnitTargetBytes / std::max(1, d.rowb));
-    d.upp = (block_size + fit - 1) / fit;
-    d.rpu = (block_size + d.upp - 1) / d.upp;
+    d.upp = (rows + fit - 1) / fit;
+    d.rpu = (rows + d.upp - 1) / d.upp;
   }
   return d;
 }
@@ -215,23 +226,22 @@ LaunchShape launch_shape(const kvcs_cache *caches, int lo, int hi, int block_siz
   LaunchShape ls;
   bool uniform = true;
   long long biggest = 16;
+  const DevCache d0 = make_dev_cache(caches[lo], block_size);
   for (int i = lo; i < hi; ++i) {
     const DevCache d = make_dev_cache(caches[i], block_size);
     ls.units_per_pos += static_cast<long long>(d.halves) * d.upp;
     ls.pages_per_pos += d.halves;
     biggest = std::max(biggest, unit_bytes(d, block_size));
     uniform = uniform && d.upp == 1 && caches[i].layout == caches[lo].layout &&
-              caches[i].column == caches[lo].column &&
-              make_dev_cache(caches[i], block_size).kbs ==
-                  make_dev_cache(caches[lo], block_size).kbs &&
+              caches[i].column == caches[lo].column && d.kbs == d0.kbs &&
               caches[i].num_heads == caches[lo].num_heads &&
-              caches[i].head_bytes == caches[lo].head_bytes;
+              caches[i].head_bytes == caches[lo].head_bytes &&
+              caches[i].piece_bytes == caches[lo].piece_bytes;
   }
   if (uniform) {
     // Every page fits a unit and all pages look alike: pack consecutive
     // pages of a position (e.g. a layer's K and V) into one unit.
-    const DevCache d = make_dev_cache(caches[lo], block_size);
-    const long long page = static_cast<long long>(d.page_bytes);
+    const long long page = static_cast<long long>(d0.page_bytes);
     const long long ppu = std::max<long long>(
         1, std::min<long long>(ls.pages_per_pos, kUnitTargetBytes / page));
     if (ppu > 1) {
@@ -253,61 +263,85 @@ int group_warps_for(int stages) {
   return gw;
 }
 
-int make_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
-              int64_t total_positions, int sms, Plan *plan) {
+// One kernel launch: a kernel and a run of (column-sorted) caches.
+struct Launch {
+  bool generic;
+  std::vector<kvcs_cache> caches;
+};
+
+// How a call runs: caches the bulk kernel can stage go to it (up to
+// kMaxCachesPerLaunch per launch), the rest to the generic kernel.  With
+// more than one launch, or the generic kernel, every result is added
+// atomically into an output zeroed first.
+struct Plan {
+  std::vector<Launch> launches;
+  int kernel = 0;         // 0 bulk only, 1 generic only, 2 both
+  int split = 0;          // bulk CTA ranges cut positions
+  int bulk_grid = 0;
+  int generic_grid = 0;
+  int stage_bytes = 0;    // of the first bulk launch
+  int stages = 0;
+  long long units = 0;    // units of the largest bulk launch
+  long long kv_bytes_max = 0;
+  bool all_atomic = false;
+  bool memset = false;
+};
+
+Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
+               int64_t total_positions, int sms) {
   Plan pl;
-  bool bulk = true;
-  long long bytes_per_pos = 0;
-  for (int32_t i = 0; i < num_caches; ++i) {
-    bulk = bulk && bulk_eligible(caches[i], block_size);
-    const long long halves = caches[i].layout == KVCS_LAYOUT_LATENT ? 1 : 2;
-    bytes_per_pos += halves * block_size * static_cast<long long>(caches[i].num_heads) *
-                     caches[i].head_bytes;
+  std::vector<kvcs_cache> bulk, gen;
+  for (const kvcs_cache &c : sorted) {
+    (bulk_eligible(c, block_size) ? bulk : gen).push_back(c);
+    const long long halves =
+        (c.layout == KVCS_LAYOUT_LATENT || c.layout == KVCS_LAYOUT_STATE) ? 1 : 2;
+    pl.kv_bytes_max += halves * page_bytes_of(c, block_size) * total_positions;
   }
-  pl.kernel = bulk ? 0 : 1;
-  pl.groups = (num_caches + kMaxCachesPerLaunch - 1) / kMaxCachesPerLaunch;
-  pl.kv_bytes_max = bytes_per_pos * total_positions;
+  for (const auto *set : {&bulk, &gen}) {
+    for (size_t lo = 0; lo < set->size(); lo += kMaxCachesPerLaunch) {
+      const size_t hi = std::min(set->size(), lo + kMaxCachesPerLaunch);
+      pl.launches.push_back({set == &gen, std::vector<kvcs_cache>(set->begin() + lo,
+                                                                  set->begin() + hi)});
+    }
+  }
+  pl.kernel = gen.empty() ? 0 : (bulk.empty() ? 1 : 2);
+  pl.all_atomic = pl.launches.size() > 1 || !gen.empty();
   if (sms < 1) sms = 1;
-  if (bulk) {
-    long long upp_max = 0;
-    for (int g = 0; g < pl.groups; ++g) {
-      const LaunchShape ls = launch_shape(
-          caches, g * kMaxCachesPerLaunch,
-          std::min(num_caches, (g + 1) * kMaxCachesPerLaunch), block_size);
-      upp_max = std::max(upp_max, ls.units_per_pos);
-      if (g == 0) {
+  if (!bulk.empty()) {
+    bool first = true;
+    for (const Launch &l : pl.launches) {
+      if (l.generic) continue;
+      const LaunchShape ls = launch_shape(l.caches.data(), 0,
+                                          static_cast<int>(l.caches.size()), block_size);
+      pl.units = std::max(pl.units, ls.units_per_pos * total_positions);
+      if (first) {
         pl.stage_bytes = ls.stage_bytes;
         pl.stages = ls.stages;
+        first = false;
       }
     }
-    pl.units = upp_max * total_positions;
     // Whole positions per CTA when that balances well (>= 95% of the even
     // split); otherwise split at unit granularity.
     const double per = static_cast<double>(total_positions) / sms;
     const double eff = per / std::ceil(per > 0 ? per : 1.0);
     if (total_positions >= sms && eff >= 0.95) {
       pl.split = 0;
-      pl.grid = sms;
+      pl.bulk_grid = sms;
     } else {
       pl.split = 1;
-      pl.grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, pl.units)));
+      pl.bulk_grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, pl.units)));
     }
-  } else {
-    pl.units = total_positions;
-    pl.split = 0;
-    pl.grid = static_cast<int>(std::max<long long>(
-        1, std::min<long long>(static_cast<long long>(sms) * 8, total_positions)));
   }
-  *plan = pl;
-  return KVCS_OK;
+  if (!gen.empty()) {
+    long long items = 0;
+    for (const Launch &l : pl.launches)
+      if (l.generic) items = std::max<long long>(items, total_positions * static_cast<long long>(l.caches.size()));
+    pl.generic_grid = static_cast<int>(std::max<long long>(
+        1, std::min<long long>(static_cast<long long>(sms) * 8, items)));
+  }
+  pl.memset = total_positions > 0 && (pl.all_atomic || (!bulk.empty() && pl.split));
+  return pl;
 }
-
-}  // namespace
-}  // namespace kvcs
-
-using namespace kvcs;
-
-namespace {
 
 // Shared body of kvcs_block_checksums and kvcs_group_checksums.
 int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block_size,
@@ -327,21 +361,17 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
 
   int sms = 0;
   if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
-  const std::vector<kvcs_cache> sorted = by_column(caches_in, num_caches);
-  const kvcs_cache *caches = sorted.data();
-  Plan pl;
-  make_plan(caches, num_caches, block_size, total_positions, sms, &pl);
+  const Plan pl = make_plan(by_column(caches_in, num_caches), block_size, total_positions, sms);
 
-  const bool all_atomic = pl.groups > 1;
-  if (all_atomic || (pl.kernel == 0 && pl.split)) {
+  if (pl.memset) {
     if (cudaMemsetAsync(outs->values, 0,
                         static_cast<size_t>(total_positions) * ncols * sizeof(uint64_t),
                         st) != cudaSuccess)
       return KVCS_ECUDA;
   }
 
-  long long min_nb = caches[0].num_blocks;
-  for (int32_t i = 1; i < num_caches; ++i) min_nb = std::min<long long>(min_nb, caches[i].num_blocks);
+  long long min_nb = caches_in[0].num_blocks;
+  for (int32_t i = 1; i < num_caches; ++i) min_nb = std::min<long long>(min_nb, caches_in[i].num_blocks);
 
   Params p;
   std::memset(&p, 0, sizeof(p));
@@ -356,22 +386,26 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
   p.min_num_blocks = min_nb;
   p.timeout_ns = kTimeoutNs;
   p.block_size = block_size;
-  p.all_atomic = all_atomic ? 1 : 0;
+  p.all_atomic = pl.all_atomic ? 1 : 0;
   p.num_columns = ncols;
+  p.state_call = caches_in[0].layout == KVCS_LAYOUT_STATE ? 1 : 0;
 
-  for (int g = 0; g < pl.groups; ++g) {
-    const int lo = g * kMaxCachesPerLaunch;
-    const int hi = std::min(num_caches, lo + kMaxCachesPerLaunch);
-    p.num_caches = hi - lo;
+  for (const Launch &l : pl.launches) {
+    const int n = static_cast<int>(l.caches.size());
+    p.num_caches = n;
     long long U = 0;
-    for (int i = lo; i < hi; ++i) {
-      p.caches[i - lo] = make_dev_cache(caches[i], block_size);
-      U += static_cast<long long>(p.caches[i - lo].halves) * p.caches[i - lo].upp;
+    bool general = false;
+    for (int i = 0; i < n; ++i) {
+      p.caches[i] = make_dev_cache(l.caches[i], block_size);
+      U += static_cast<long long>(p.caches[i].halves) * p.caches[i].upp;
+      general = general || l.caches[i].layout == KVCS_LAYOUT_HND ||
+                l.caches[i].layout == KVCS_LAYOUT_XSPLIT ||
+                l.caches[i].layout == KVCS_LAYOUT_STATE;
     }
     p.ppu = 1;
     p.pages_per_pos = 0;
-    if (pl.kernel == 0) {
-      const LaunchShape ls = launch_shape(caches, lo, hi, block_size);
+    if (!l.generic) {
+      const LaunchShape ls = launch_shape(l.caches.data(), 0, n, block_size);
       U = ls.units_per_pos;
       p.ppu = ls.ppu;
       p.pages_per_pos = ls.pages_per_pos;
@@ -380,16 +414,12 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
     }
     p.units_per_pos = U;
     p.total_units = U * total_positions;
-    if (pl.kernel == 0) {
+    if (!l.generic) {
       p.split = pl.split;
       p.group_warps = group_warps_for(p.stages);
       p.groups = kConsumerWarps / p.group_warps;
-      long long grid = pl.grid;
+      long long grid = pl.bulk_grid;
       if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
-      bool general = false;
-      for (int i = lo; i < hi; ++i)
-        general = general || caches[i].layout == KVCS_LAYOUT_HND ||
-                  caches[i].layout == KVCS_LAYOUT_XSPLIT;
       const size_t smem = bulk_smem_bytes(p.stages, p.stage_bytes);
       if (general)
         kvcs_bulk_kernel<true><<<static_cast<unsigned>(grid), kBulkThreads, smem, st>>>(p);
@@ -397,7 +427,7 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
         kvcs_bulk_kernel<false><<<static_cast<unsigned>(grid), kBulkThreads, smem, st>>>(p);
     } else {
       p.split = 0;
-      kvcs_generic_kernel<<<static_cast<unsigned>(pl.grid), kGenericThreads, 0, st>>>(p);
+      kvcs_generic_kernel<<<static_cast<unsigned>(pl.generic_grid), kGenericThreads, 0, st>>>(p);
     }
     if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -428,6 +458,9 @@ int columns_of(const kvcs_cache *caches, int32_t num_caches) {
 }
 
 }  // namespace
+}  // namespace kvcs
+
+using namespace kvcs;
 
 extern "C" {
 
@@ -440,20 +473,18 @@ int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
   if (sms <= 0) {
     if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
   }
-  const std::vector<kvcs_cache> sorted = by_column(caches, num_caches);
-  Plan pl;
-  make_plan(sorted.data(), num_caches, block_size, total_positions, sms, &pl);
+  const Plan pl = make_plan(by_column(caches, num_caches), block_size, total_positions, sms);
   std::memset(info, 0, sizeof(*info));
   info->kernel = pl.kernel;
-  info->split = pl.kernel == 0 ? pl.split : 0;
-  info->launches = total_positions > 0 ? pl.groups : 0;
-  info->memsets = (total_positions > 0 && (pl.groups > 1 || (pl.kernel == 0 && pl.split))) ? 1 : 0;
-  info->grid = pl.grid;
-  info->threads = pl.kernel == 0 ? kBulkThreads : kGenericThreads;
-  info->smem_bytes = pl.kernel == 0 ? bulk_smem_bytes(pl.stages, pl.stage_bytes) : 0;
-  info->stage_bytes = pl.kernel == 0 ? pl.stage_bytes : 0;
-  info->stages = pl.kernel == 0 ? pl.stages : 0;
-  info->units = pl.units;
+  info->split = pl.kernel != 1 ? pl.split : 0;
+  info->launches = total_positions > 0 ? static_cast<int32_t>(pl.launches.size()) : 0;
+  info->memsets = pl.memset ? 1 : 0;
+  info->grid = pl.kernel == 1 ? pl.generic_grid : pl.bulk_grid;
+  info->threads = pl.kernel == 1 ? kGenericThreads : kBulkThreads;
+  info->smem_bytes = pl.kernel != 1 ? bulk_smem_bytes(pl.stages, pl.stage_bytes) : 0;
+  info->stage_bytes = pl.kernel != 1 ? pl.stage_bytes : 0;
+  info->stages = pl.kernel != 1 ? pl.stages : 0;
+  info->units = pl.kernel == 1 ? total_positions : pl.units;
   info->kv_bytes_max = pl.kv_bytes_max;
   return KVCS_OK;
 }

@@ -51,6 +51,7 @@ constexpr int kLayoutNHD = 0;
 constexpr int kLayoutHND = 1;
 constexpr int kLayoutLatent = 2;
 constexpr int kLayoutXSplit = 3;
+constexpr int kLayoutState = 4;
 
 constexpr u32 kStatusBadBlockId = 1u;
 constexpr u32 kStatusBadRequests = 2u;
@@ -78,6 +79,8 @@ struct DevCache {
   int column;       // replica-key column the cache adds into
   int kbs;          // HND: slots per kernel sub-block (block_size if none)
   int chunks;       // HND: 1; x-split: 16-byte chunks per head (hb / 16)
+  int pbytes;       // piece bytes: 8, or a state's element bytes (2 or 4)
+  int pad;
 };
 
 struct Params {
@@ -105,6 +108,7 @@ struct Params {
                              // the same geometry and a page fits a unit
   int pages_per_pos;         // sum of halves over the caches
   int num_columns;           // replica-key columns of the output
+  int state_call;            // the caches hold Mamba states (block position 0)
   DevCache caches[kMaxCachesPerLaunch];
 };
 
@@ -213,10 +217,13 @@ __device__ PosInfo position_info(const Params &p, long long pos, const ReqCursor
     return pi;
   }
   const long long q = c.fp + (pos - c.po0);
-  // Tokens of this block below num_tokens: slots [0, nv).
+  // Tokens of this block below num_tokens: slots [0, nv).  A Mamba state
+  // block is the running state at position 0, whatever num_tokens is.
   const long long bs = p.block_size;
   long long nv = 0;
-  if (q <= c.nt / bs) {  // q * bs <= nt without overflow
+  if (p.state_call) {
+    nv = q == 0 ? 1 : 0;
+  } else if (q <= c.nt / bs) {  // q * bs <= nt without overflow
     nv = c.nt - q * bs;
     if (nv > bs) nv = bs;
   }
@@ -286,7 +293,44 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
   const int half_pieces = half * (C.hb >> 3);
   const int rowb = t.rowb;
   u64 acc = 0;
-  if (!kGeneral || (C.layout != kLayoutHND && C.layout != kLayoutXSplit)) {
+  if (kGeneral && C.layout == kLayoutState) {
+    // Mamba state unit: rows [first, first + count) of the state, each a
+    // slice of global row head_offset + row whose pieces are 2- or 4-byte
+    // elements weighted 2e+1 by element index e.  The 16-byte column `col`
+    // of a row holds elements e0 = col*k .. e0+k-1; with A = sum x_i and
+    // B = sum i x_i over them it adds (2 e0 + 1) A + 2 B.  Summed over a
+    // thread's columns of one row that is SA + 2k SCA + 2 SB with
+    // SA = sum A, SCA = sum col A, SB = sum B (adds and small multiplies
+    // only); the row factor m0 + 2 row multiplies it once per row.
+    const int nrows = m.count;
+    const u32 r0 = static_cast<u32>(m.first);
+    const u64 per = static_cast<u64>(16 / C.pbytes);
+    for (int r = t.rl; r < nrows; r += t.rstep) {
+      u64 SA = 0, SCA = 0, SB = 0;
+      const unsigned char *rowp = stage + static_cast<size_t>(r) * rowb;
+      for (int col = t.col0; col < t.cols; col += t.cstep) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(rowp + (col << 4));
+        u64 A, Bk;
+        if (C.pbytes == 2) {
+          const u32 a = (v.x & 0xffffu) + (v.x >> 16) + (v.y & 0xffffu) + (v.y >> 16) +
+                        (v.z & 0xffffu) + (v.z >> 16) + (v.w & 0xffffu) + (v.w >> 16);
+          const u32 b = (v.x >> 16) + 2u * (v.y & 0xffffu) + 3u * (v.y >> 16) +
+                        4u * (v.z & 0xffffu) + 5u * (v.z >> 16) + 6u * (v.w & 0xffffu) +
+                        7u * (v.w >> 16);
+          A = a;
+          Bk = b;
+        } else {
+          A = static_cast<u64>(v.x) + v.y + v.z + v.w;
+          Bk = static_cast<u64>(v.y) + 2ull * v.z + 3ull * v.w;
+        }
+        SA += A;
+        SCA += static_cast<u64>(static_cast<u32>(col)) * A;
+        SB += Bk;
+      }
+      const u64 mrow = C.m0 + 2ull * static_cast<u64>(r0 + static_cast<u32>(r));
+      acc += mrow * (SA + 2ull * per * SCA + 2ull * SB);
+    }
+  } else if (!kGeneral || (C.layout != kLayoutHND && C.layout != kLayoutXSplit)) {
     const int nrows = m.count;
     const u32 r0 = static_cast<u32>(m.first);
     for (int col = t.col0; col < t.cols; col += t.cstep) {
@@ -526,6 +570,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             count = max(0, min(C.rpu, C.heads - first));
             pbytes = static_cast<u32>(count) * static_cast<u32>(cur.nv) *
                      static_cast<u32>(C.hb);
+          } else if (kGeneral && C.layout == kLayoutState) {
+            count = max(0, min(C.rpu, C.heads - first));
+            pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
           } else {
             count = max(0, min(C.rpu, cur.nv - first));
             pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
@@ -738,13 +785,23 @@ constexpr int bulk_smem_bytes(int stages, int stage_bytes) {
 }
 
 // ---------------------------------------------------------------------------
-// Generic kernel: direct 8-byte loads, any geometry the ABI accepts
+// Generic kernel: direct loads, any geometry the ABI accepts
 // ---------------------------------------------------------------------------
 //
-// Used when a cache is not 16-byte aligned, has per-head bytes that are not
-// a multiple of 16, or rows larger than a stage.  One CTA per position
-// (grid-stride), each thread striding over the block's valid pieces in
-// logical order (slot, head, piece) and weighting each piece directly.
+// Used for caches the bulk kernel cannot stage: pools or strides not 16-byte
+// aligned, per-head bytes not a multiple of 16, rows larger than a stage,
+// state rows of any size.  Work items are (position, cache) pairs, taken
+// grid-stride by CTAs of 256 threads; a CTA's threads stride over the item's
+// valid pieces in logical order and weight each piece directly.  Each item's
+// sum is added with a 64-bit atomic into the pre-zeroed output word of its
+// (position, column), so a few positions with large states still spread
+// over the whole GPU.
+__device__ __forceinline__ u64 load_piece(const unsigned char *p, int bytes) {
+  if (bytes == 8) return __ldg(reinterpret_cast<const u64 *>(p));
+  if (bytes == 4) return __ldg(reinterpret_cast<const unsigned int *>(p));
+  return __ldg(reinterpret_cast<const unsigned short *>(p));
+}
+
 __global__ void __launch_bounds__(kGenericThreads)
     kvcs_generic_kernel(const __grid_constant__ Params p) {
   __shared__ u64 red[kGenericThreads / 32];
@@ -754,9 +811,13 @@ __global__ void __launch_bounds__(kGenericThreads)
     if (p.pos_offsets[0] != 0 || p.pos_offsets[p.num_requests] != p.total_positions)
       set_status(p, kStatusBadRequests);
   }
-  for (long long pos = blockIdx.x; pos < p.total_positions; pos += gridDim.x) {
+  const long long items = p.total_positions * p.num_caches;
+  for (long long item = blockIdx.x; item < items; item += gridDim.x) {
+    const long long pos = item / p.num_caches;
+    const int ci = static_cast<int>(item - pos * p.num_caches);
+    const DevCache &C = p.caches[ci];
     // every thread derives the same position info (uniform loads)
-    long long r = find_request(p, pos);
+    const long long r = find_request(p, pos);
     long long q = 0, b = 0, nv = 0;
     bool ok = r >= 0;
     if (ok) {
@@ -766,63 +827,81 @@ __global__ void __launch_bounds__(kGenericThreads)
       if (p.first_position[r] < 0) ok = false;
       if (q <= nt / bs) nv = min(nt - q * bs, bs);
     }
-    if (tid == 0) {
-      if (r < 0 || (ok == false)) set_status(p, kStatusBadRequests);
+    if (tid == 0 && ci == 0) {
+      if (!ok) set_status(p, kStatusBadRequests);
       else if (b < 0 || b >= p.min_num_blocks) set_status(p, kStatusBadBlockId);
     }
     if (ok && (b < 0 || b >= p.min_num_blocks)) ok = false;
-    for (int col = 0; col < p.num_columns; ++col) {
-      u64 acc = 0;
-      if (ok && nv > 0) {
-        const u64 t0 = static_cast<u64>(q) * static_cast<u64>(bs);
-        for (int ci = 0; ci < p.num_caches; ++ci) {
-          const DevCache &C = p.caches[ci];
-          if (C.column != col) continue;
-          const long long P = C.P;
-          const long long per_slot = static_cast<long long>(C.heads) * P;
-          const long long n = nv * per_slot;
-          const int hp = C.hb >> 3;  // pieces per half
-          for (long long idx = tid; idx < n; idx += kGenericThreads) {
-            const long long slot = idx / per_slot;
-            const long long rem = idx - slot * per_slot;
-            const long long h = rem / P;
-            const long long pc = rem - h * P;
-            long long off;
-            if (C.layout == kLayoutLatent) {
-              off = b * C.block_stride + slot * C.hb + 8 * pc;
-            } else {
-              const long long half = pc >= hp ? 1 : 0;
-              const long long e = (pc - half * hp) * 8;
-              const long long page = half * C.half_stride + b * C.block_stride;
-              if (C.layout == kLayoutNHD) {
-                off = page + (slot * C.heads + h) * C.hb + e;
-              } else if (C.layout == kLayoutXSplit) {
-                off = page + ((h * (C.hb >> 4) + (e >> 4)) * bs + slot) * 16 + (e & 15);
-              } else {
-                const long long sb = slot / C.kbs;
-                off = page + ((sb * C.heads + h) * C.kbs + (slot - sb * C.kbs)) * C.hb + e;
-              }
-            }
-            const u64 x = __ldg(reinterpret_cast<const u64 *>(C.base + off));
-            const u64 j = (t0 + static_cast<u64>(slot)) * static_cast<u64>(P) +
-                          static_cast<u64>(pc);
-            const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
-            acc += x * ((2ull * j + 1ull) * mh);
+    u64 acc = 0;
+    if (ok && C.layout == kLayoutState) {
+      // a state block lives at position 0 only; rows are its slices and
+      // its elements are the pieces
+      if (q == 0) {
+        const long long P = C.P;
+        const unsigned char *blk = C.base + b * C.block_stride;
+        if (P <= 64) {
+          // short rows (e.g. conv states): one row per thread
+          for (long long row = tid; row < C.heads; row += kGenericThreads) {
+            const unsigned char *rp = blk + row * C.hb;
+            u64 s = 0;
+            for (long long pc = 0; pc < P; ++pc)
+              s += load_piece(rp + pc * C.pbytes, C.pbytes) * (2ull * static_cast<u64>(pc) + 1ull);
+            acc += s * (C.m0 + 2ull * static_cast<u64>(row));
+          }
+        } else {
+          // long rows: the CTA strides over each row's elements
+          for (long long row = 0; row < C.heads; ++row) {
+            const unsigned char *rp = blk + row * C.hb;
+            u64 s = 0;
+            for (long long pc = tid; pc < P; pc += kGenericThreads)
+              s += load_piece(rp + pc * C.pbytes, C.pbytes) * (2ull * static_cast<u64>(pc) + 1ull);
+            acc += s * (C.m0 + 2ull * static_cast<u64>(row));
           }
         }
       }
-      acc = warp_sum(acc);
-      if ((tid & 31) == 0) red[tid >> 5] = acc;
-      __syncthreads();
-      if (tid == 0) {
-        u64 total = 0;
-        for (int w = 0; w < kGenericThreads / 32; ++w) total += red[w];
-        const long long dst = pos * p.num_columns + col;
-        if (p.all_atomic) atomicAdd(p.out + dst, total);
-        else p.out[dst] = total;
+    } else if (ok && nv > 0) {
+      const u64 t0 = static_cast<u64>(q) * static_cast<u64>(bs);
+      const long long P = C.P;
+      const long long per_slot = static_cast<long long>(C.heads) * P;
+      const long long n = nv * per_slot;
+      const int hp = C.hb >> 3;  // pieces per half
+      for (long long idx = tid; idx < n; idx += kGenericThreads) {
+        const long long slot = idx / per_slot;
+        const long long rem = idx - slot * per_slot;
+        const long long h = rem / P;
+        const long long pc = rem - h * P;
+        long long off;
+        if (C.layout == kLayoutLatent) {
+          off = b * C.block_stride + slot * C.hb + 8 * pc;
+        } else {
+          const long long half = pc >= hp ? 1 : 0;
+          const long long e = (pc - half * hp) * 8;
+          const long long page = half * C.half_stride + b * C.block_stride;
+          if (C.layout == kLayoutNHD) {
+            off = page + (slot * C.heads + h) * C.hb + e;
+          } else if (C.layout == kLayoutXSplit) {
+            off = page + ((h * (C.hb >> 4) + (e >> 4)) * bs + slot) * 16 + (e & 15);
+          } else {
+            const long long sb = slot / C.kbs;
+            off = page + ((sb * C.heads + h) * C.kbs + (slot - sb * C.kbs)) * C.hb + e;
+          }
+        }
+        const u64 x = __ldg(reinterpret_cast<const u64 *>(C.base + off));
+        const u64 j = (t0 + static_cast<u64>(slot)) * static_cast<u64>(P) +
+                      static_cast<u64>(pc);
+        const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
+        acc += x * ((2ull * j + 1ull) * mh);
       }
-      __syncthreads();
     }
+    acc = warp_sum(acc);
+    if ((tid & 31) == 0) red[tid >> 5] = acc;
+    __syncthreads();
+    if (tid == 0) {
+      u64 total = 0;
+      for (int w = 0; w < kGenericThreads / 32; ++w) total += red[w];
+      if (total) atomicAdd(p.out + pos * p.num_columns + C.column, total);
+    }
+    __syncthreads();
   }
 }
 

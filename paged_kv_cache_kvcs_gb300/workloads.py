@@ -29,6 +29,7 @@ LAYOUT_NHD = 0
 LAYOUT_HND = 1
 LAYOUT_LATENT = 2
 LAYOUT_XSPLIT = 3   # [2, num_blocks, heads, head_bytes / 16, block_size, 16]
+LAYOUT_STATE = 4    # [num_blocks, rows, row_bytes]: Mamba running state
 
 # Value recipes for pool bytes.  Every one produces raw bits that are only
 # ever read back as bytes.
@@ -53,6 +54,7 @@ class CacheSpec:
     block_stride: int = 0   # bytes between blocks' pages (0: packed)
     kernel_block_size: int = 0  # HND sub-block slots (0: none)
     v_pool: torch.Tensor | None = None  # separate V tensor, if any
+    piece_bytes: int = 0    # state element bytes (2 or 4); 0 for KV caches
 
 
 @dataclass
@@ -349,3 +351,46 @@ def invariance(seed: int = 0, device="cpu", num_requests: int = 16,
             wl("invariance_consumer", "consumer", out["consumer"], consumer_bs),
             wl("invariance_shard0", "shard", out["shard0"], producer_bs),
             wl("invariance_shard1", "shard", out["shard1"], producer_bs))
+
+
+# ---------------------------------------------------------------------------
+# Mamba running states
+# ---------------------------------------------------------------------------
+
+def mamba2(seed: int = 0, device="cpu", num_requests: int = 64, layers: int = 64,
+           ssm_heads: int = 80, head_dim: int = 64, d_state: int = 128,
+           conv_dim: int = 5376, conv_width: int = 4, spare_blocks: int = 3,
+           first_positions=None, positions_per_request: int = 1) -> Workload:
+    """Mamba2-shaped running states (d_inner 5120, 80 heads of 64, d_state
+    128, conv width 4): per layer an SSM state with one row per head
+    (head_dim x d_state fp32 values, 4-byte elements; 32 KiB) and a conv
+    state with one row per conv channel (conv_width - 1 bf16 values, 2-byte
+    elements), numbered consecutively within the layer (SSM rows, then conv
+    rows).  One state block per request at block position 0, block ids a
+    seeded permutation of the pool; values are random bits."""
+    device = torch.device(device)
+    g = _cpu_gen(seed)
+    R = num_requests
+    per = positions_per_request
+    po = torch.arange(0, (R + 1) * per, per, dtype=torch.int64)
+    fp = torch.tensor(list(first_positions) if first_positions is not None else [0] * R,
+                      dtype=torch.int64)
+    nt = torch.full((R,), 1000, dtype=torch.int64)
+    nb = R * per + spare_blocks
+    bids = torch.randperm(nb, generator=g)[:R * per].to(torch.int32)
+    dg = _dev_gen(seed, device)
+    ssm_row = head_dim * d_state * 4
+    conv_row = (conv_width - 1) * 2
+    caches = []
+    for li in range(layers):
+        ssm = fill_bytes(nb * ssm_heads * ssm_row, BITS16, dg, device)
+        conv = fill_bytes(nb * conv_dim * conv_row, BITS16, dg, device)
+        caches.append(CacheSpec(ssm, nb, LAYOUT_STATE, li, 0, ssm_heads, ssm_row,
+                                piece_bytes=4))
+        caches.append(CacheSpec(conv, nb, LAYOUT_STATE, li, ssm_heads, conv_dim, conv_row,
+                                piece_bytes=2))
+    return Workload("mamba2", 16, caches, po.to(device), fp.to(device), nt.to(device),
+                    bids.to(device),
+                    info=dict(layers=layers, heads=ssm_heads + conv_dim, head_bytes=ssm_row,
+                              block_size=16, kind=BITS16, layout=LAYOUT_STATE,
+                              requests=R, seed=seed))

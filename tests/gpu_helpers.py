@@ -32,11 +32,13 @@ def sampled_oracle_inputs(wl, positions):
     caches = []
     dev_ids = ids.to(wl.pos_offsets.device)
     for c in wl.caches:
-        halves = 1 if c.layout == W.LAYOUT_LATENT else 2
-        page = wl.block_size * c.num_heads * c.head_bytes
+        state = c.layout == W.LAYOUT_STATE
+        halves = 1 if c.layout in (W.LAYOUT_LATENT, W.LAYOUT_STATE) else 2
+        page = (1 if state else wl.block_size) * c.num_heads * c.head_bytes
         pages = c.pool.view(halves, c.num_blocks, page)[:, dev_ids]
         caches.append(OracleCache(host_bytes(pages), k, c.layout, c.layer,
-                                  c.head_offset, c.num_heads, c.head_bytes))
+                                  c.head_offset, c.num_heads, c.head_bytes,
+                                  getattr(c, "piece_bytes", 0) or 8))
     reqs = OracleRequests(list(range(k + 1)), q.tolist(), nt.tolist(), list(range(k)))
     return pos.numpy(), caches, reqs
 

@@ -39,8 +39,9 @@ def test_version_and_strerror():
 class FakeCache:
     def __init__(self, base=1 << 20, num_blocks=100, layout=0, layer=0,
                  head_offset=0, num_heads=8, head_bytes=256, column=0,
-                 half_stride=0, block_stride=0, kernel_block_size=0):
+                 half_stride=0, block_stride=0, kernel_block_size=0, piece_bytes=0):
         self.column = column
+        self.piece_bytes = piece_bytes
         self.half_stride = half_stride
         self.block_stride = block_stride
         self.kernel_block_size = kernel_block_size
@@ -100,7 +101,14 @@ def test_validation_codes():
     # x-split: 16-byte chunks
     assert code_of([FakeCache(layout=3)]) == 0
     assert code_of([FakeCache(layout=3, head_bytes=24)]) == K.KVCS_EINVAL
+    # Mamba states: 2- or 4-byte elements, not mixed with KV caches
     assert code_of([FakeCache(layout=4)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layout=4, num_heads=100, head_bytes=6, piece_bytes=2)]) == 0
+    assert code_of([FakeCache(layout=4, head_bytes=6, piece_bytes=4)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layout=4, head_bytes=8, piece_bytes=8)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(layer=0, layout=4, head_bytes=8, piece_bytes=4),
+                    FakeCache(layer=1)]) == K.KVCS_EINVAL
+    assert code_of([FakeCache(piece_bytes=2)]) == K.KVCS_EINVAL
     # strides that are 8- but not 16-byte multiples fall back to the generic kernel
     assert plan([FakeCache(block_stride=page + 8)])["kernel"] == 1
     assert plan([FakeCache(block_stride=page + 16)])["kernel"] == 0
@@ -152,9 +160,25 @@ def test_plan_shapes():
     p = plan([FakeCache(layer=0, head_bytes=128), FakeCache(layer=1, head_bytes=64)],
              positions=10)
     assert p["units"] == 10 * 4
-    # odd per-head bytes, or rows too wide to stage: generic kernel
-    assert plan([FakeCache(head_bytes=24)])["kernel"] == 1
+    # odd per-head bytes, or rows too wide to stage: generic kernel, whose
+    # per-(position, cache) sums are added into a zeroed output
+    p = plan([FakeCache(head_bytes=24)])
+    assert p["kernel"] == 1 and p["memsets"] == 1 and p["launches"] == 1
     assert plan([FakeCache(num_heads=512, head_bytes=256)])["kernel"] == 1
+    # some caches for each kernel: two launches
+    p = plan([FakeCache(layer=0), FakeCache(layer=1, head_bytes=24)])
+    assert p["kernel"] == 2 and p["launches"] == 2 and p["memsets"] == 1
+    # Mamba-like states: 32 KiB fp32 rows (bulk) and 6-byte conv rows (generic)
+    ssm = [FakeCache(layer=i, layout=4, num_heads=80, head_bytes=32768, piece_bytes=4,
+                     head_offset=0) for i in range(4)]
+    conv = [FakeCache(layer=i, layout=4, num_heads=5376, head_bytes=6, piece_bytes=2,
+                      head_offset=80) for i in range(4)]
+    p = plan(ssm, positions=64)
+    assert p["kernel"] == 0 and p["split"] == 1 and p["stage_bytes"] == 32768
+    assert p["units"] == 64 * 4 * 80
+    assert plan(conv, positions=64)["kernel"] == 1
+    p = plan(ssm + conv, positions=64)
+    assert p["kernel"] == 2 and p["launches"] == 2
     # more caches than one launch takes
     p = plan([FakeCache(layer=i, num_heads=1, head_bytes=16) for i in range(300)])
     assert p["launches"] == 3 and p["memsets"] == 1
