@@ -68,6 +68,44 @@ def make_workload(name: str, seed: int, device):
     raise SystemExit(f"unknown config {name}")
 
 
+def relayout(wl, layout: str):
+    """The same KV in another memory layout (NHD source pools; data
+    movement with torch only, before any timing)."""
+    import dataclasses
+    from paged_kv_cache_kvcs_gb300 import workloads as W
+    if layout == "nhd":
+        return wl
+    caches = []
+    for c in wl.caches:
+        assert c.layout == W.LAYOUT_NHD
+        bs, H, hb, nb = wl.block_size, c.num_heads, c.head_bytes, c.num_blocks
+        page = bs * H * hb
+        v = c.pool.view(2, nb, bs, H, hb)
+        if layout == "hnd":
+            pool = v.permute(0, 1, 3, 2, 4).contiguous().view(-1)
+            caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_HND))
+        elif layout == "hnd_sub4":
+            pool = v.view(2, nb, bs // 4, 4, H, hb).permute(0, 1, 2, 4, 3, 5).contiguous().view(-1)
+            caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_HND,
+                                              kernel_block_size=4))
+        elif layout == "interleaved":   # [num_blocks, 2, page]
+            pool = v.view(2, nb, page).transpose(0, 1).contiguous().view(-1)
+            caches.append(dataclasses.replace(c, pool=pool, half_stride=page,
+                                              block_stride=2 * page))
+        elif layout == "separate_kv":
+            k, vv = v[0].contiguous().view(-1), v[1].contiguous().view(-1)
+            caches.append(dataclasses.replace(c, pool=k, v_pool=vv))
+        elif layout == "xsplit":
+            pool = v.view(2, nb, bs, H, hb // 16, 16).permute(0, 1, 3, 4, 2, 5).contiguous().view(-1)
+            caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_XSPLIT))
+        else:
+            raise SystemExit(f"unknown layout {layout}")
+        c.pool = None               # free the NHD copy
+    torch.cuda.empty_cache()
+    return type(wl)(wl.name, wl.block_size, caches, wl.pos_offsets, wl.first_position,
+                    wl.num_tokens, wl.block_ids, {**wl.info, "relayout": layout})
+
+
 def kv_bytes(wl) -> int:
     """Algorithmic KV bytes one step reads: valid tokens of every position
     times the bytes a token occupies across all caches (for Mamba states:
@@ -368,16 +406,47 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = make_workload(args.config, args.seed + rank, dev)
+    if args.layout != "nhd":
+        wl = relayout(wl, args.layout)
+    if args.columns > 1:
+        for i, c in enumerate(wl.caches):
+            c.column = i % args.columns
     stream = torch.cuda.Stream(dev)
     out = torch.empty(wl.num_positions, dtype=torch.int64, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions)
     nbytes = kv_bytes(wl)
-    ck = kvcs.workload_checksummer(wl)
     raw_stream = stream.cuda_stream
+    if args.columns > 1 or args.verify:
+        # the replica-key path: one column per key, plus (--verify) the
+        # tagged row sums compared with stored values in the same call
+        ncols = max(1, args.columns)
+        values = torch.empty((wl.num_positions, ncols), dtype=torch.int64, device=dev)
+        extras = {}
+        if args.verify:
+            n = wl.num_positions
+            g = torch.Generator(device=dev).manual_seed(args.seed)
+            hashes = torch.randint(0, 256, (n, 32), dtype=torch.uint8, device=dev, generator=g)
+            tags = kvcs.block_checksum_tags(hashes, 0x5EED)
+            stored = torch.empty(n, dtype=torch.int64, device=dev)
+            kvcs.group_checksums(wl.caches, wl.block_size, wl.pos_offsets, wl.first_position,
+                                 wl.num_tokens, wl.block_ids, ncols, values=values,
+                                 row_sums=stored, tags=tags, total_positions=n)
+            extras = dict(tags=tags, expected=stored,
+                          mismatch=torch.empty(n, dtype=torch.uint8, device=dev),
+                          mismatch_count=torch.zeros(1, dtype=torch.int32, device=dev))
 
-    def step():
-        ck(out, status, raw_stream)
+        def step():
+            kvcs.group_checksums(wl.caches, wl.block_size, wl.pos_offsets,
+                                 wl.first_position, wl.num_tokens, wl.block_ids, ncols,
+                                 values=values, status=status, stream=raw_stream,
+                                 total_positions=wl.num_positions, **extras)
+        ck = None
+    else:
+        ck = kvcs.workload_checksummer(wl)
+
+        def step():
+            ck(out, status, raw_stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -443,7 +512,7 @@ def run_ours(args, ws, rank, local):
 
     # ---- end to end: host buffers through the public API ----
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and ck is not None:
         e2e = run_e2e(args, wl, dev, stream, ws, ck)
 
     if rank != 0:
@@ -458,7 +527,9 @@ def run_ours(args, ws, rank, local):
         "dtype": "u64", "data": "synthetic",
         "blocks_per_s": round(job_blocks / total_s, 1),
         "hbm_frac_of_nominal_8tbs": round(value / ws / NOMINAL_HBM_GBS, 4),
-        "config": {**describe(wl, args.config), "parallelism": f"replicas{ws}"},
+        "config": {**describe(wl, args.config), "parallelism": f"replicas{ws}",
+                   "memory_layout": args.layout, "columns": max(1, args.columns),
+                   "verify": bool(args.verify)},
         "plan": {k: plan[k] for k in ("kernel", "split", "launches", "memsets", "grid",
                                       "threads", "smem_bytes", "stage_bytes", "units")},
         "gpu_launches": int(launches),
@@ -560,6 +631,13 @@ def main():
     ap.add_argument("--copy-streams", type=int, default=4)
     ap.add_argument("--sweep", action="store_true",
                     help="also time the first 1, 2, 4, ... requests alone")
+    ap.add_argument("--layout", default="nhd",
+                    choices=("nhd", "hnd", "hnd_sub4", "interleaved", "separate_kv", "xsplit"),
+                    help="re-lay-out the (NHD) workload's pools before timing")
+    ap.add_argument("--columns", type=int, default=1,
+                    help="replica-key columns (caches assigned round-robin)")
+    ap.add_argument("--verify", action="store_true",
+                    help="time the tagged row sums and their comparison too")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

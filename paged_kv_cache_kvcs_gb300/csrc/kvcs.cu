@@ -45,14 +45,13 @@ cudaError_t device_setup(int *sms) {
   std::call_once(d.once, [&d, dev]() {
     int n = 0;
     d.err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (d.err == cudaSuccess)
-      d.err = cudaFuncSetAttribute(kvcs_bulk_kernel<false>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kSmemLimit);
-    if (d.err == cudaSuccess)
-      d.err = cudaFuncSetAttribute(kvcs_bulk_kernel<true>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kSmemLimit);
+    for (const void *fn : {reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamXSplit>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamState>)})
+      if (d.err == cudaSuccess)
+        d.err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemLimit);
     d.sms = n;
   });
   *sms = d.sms;
@@ -263,16 +262,28 @@ int group_warps_for(int stages) {
   return gw;
 }
 
-// One kernel launch: a kernel and a run of (column-sorted) caches.
+// Layout family of a cache (which instance of the bulk kernel stages it).
+int family_of(const kvcs_cache &c) {
+  switch (c.layout) {
+    case KVCS_LAYOUT_HND: return kFamHnd;
+    case KVCS_LAYOUT_XSPLIT: return kFamXSplit;
+    case KVCS_LAYOUT_STATE: return kFamState;
+    default: return kFamRows;
+  }
+}
+
+// One kernel launch: a kernel (the generic one, or the bulk instance of one
+// layout family) and a run of (column-sorted) caches.
 struct Launch {
   bool generic;
+  int family;
   std::vector<kvcs_cache> caches;
 };
 
-// How a call runs: caches the bulk kernel can stage go to it (up to
-// kMaxCachesPerLaunch per launch), the rest to the generic kernel.  With
-// more than one launch, or the generic kernel, every result is added
-// atomically into an output zeroed first.
+// How a call runs: caches the bulk kernel can stage go to its instance for
+// their layout family (up to kMaxCachesPerLaunch per launch), the rest to
+// the generic kernel.  With more than one launch, or the generic kernel,
+// every result is added atomically into an output zeroed first.
 struct Plan {
   std::vector<Launch> launches;
   int kernel = 0;         // 0 bulk only, 1 generic only, 2 both
@@ -290,18 +301,25 @@ struct Plan {
 Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
                int64_t total_positions, int sms) {
   Plan pl;
-  std::vector<kvcs_cache> bulk, gen;
+  std::vector<kvcs_cache> fam[4], gen;
+  std::vector<kvcs_cache> bulk;
   for (const kvcs_cache &c : sorted) {
-    (bulk_eligible(c, block_size) ? bulk : gen).push_back(c);
+    if (bulk_eligible(c, block_size)) {
+      fam[family_of(c)].push_back(c);
+      bulk.push_back(c);
+    } else {
+      gen.push_back(c);
+    }
     const long long halves =
         (c.layout == KVCS_LAYOUT_LATENT || c.layout == KVCS_LAYOUT_STATE) ? 1 : 2;
     pl.kv_bytes_max += halves * page_bytes_of(c, block_size) * total_positions;
   }
-  for (const auto *set : {&bulk, &gen}) {
-    for (size_t lo = 0; lo < set->size(); lo += kMaxCachesPerLaunch) {
-      const size_t hi = std::min(set->size(), lo + kMaxCachesPerLaunch);
-      pl.launches.push_back({set == &gen, std::vector<kvcs_cache>(set->begin() + lo,
-                                                                  set->begin() + hi)});
+  for (int f = 0; f <= 4; ++f) {
+    const std::vector<kvcs_cache> &set = f < 4 ? fam[f] : gen;
+    for (size_t lo = 0; lo < set.size(); lo += kMaxCachesPerLaunch) {
+      const size_t hi = std::min(set.size(), lo + kMaxCachesPerLaunch);
+      pl.launches.push_back({f == 4, f < 4 ? f : 0,
+                             std::vector<kvcs_cache>(set.begin() + lo, set.begin() + hi)});
     }
   }
   pl.kernel = gen.empty() ? 0 : (bulk.empty() ? 1 : 2);
@@ -394,13 +412,9 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
     const int n = static_cast<int>(l.caches.size());
     p.num_caches = n;
     long long U = 0;
-    bool general = false;
     for (int i = 0; i < n; ++i) {
       p.caches[i] = make_dev_cache(l.caches[i], block_size);
       U += static_cast<long long>(p.caches[i].halves) * p.caches[i].upp;
-      general = general || l.caches[i].layout == KVCS_LAYOUT_HND ||
-                l.caches[i].layout == KVCS_LAYOUT_XSPLIT ||
-                l.caches[i].layout == KVCS_LAYOUT_STATE;
     }
     p.ppu = 1;
     p.pages_per_pos = 0;
@@ -421,10 +435,13 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       long long grid = pl.bulk_grid;
       if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
       const size_t smem = bulk_smem_bytes(p.stages, p.stage_bytes);
-      if (general)
-        kvcs_bulk_kernel<true><<<static_cast<unsigned>(grid), kBulkThreads, smem, st>>>(p);
-      else
-        kvcs_bulk_kernel<false><<<static_cast<unsigned>(grid), kBulkThreads, smem, st>>>(p);
+      const dim3 gd(static_cast<unsigned>(grid));
+      switch (l.family) {
+        case kFamHnd: kvcs_bulk_kernel<kFamHnd><<<gd, kBulkThreads, smem, st>>>(p); break;
+        case kFamXSplit: kvcs_bulk_kernel<kFamXSplit><<<gd, kBulkThreads, smem, st>>>(p); break;
+        case kFamState: kvcs_bulk_kernel<kFamState><<<gd, kBulkThreads, smem, st>>>(p); break;
+        default: kvcs_bulk_kernel<kFamRows><<<gd, kBulkThreads, smem, st>>>(p); break;
+      }
     } else {
       p.split = 0;
       kvcs_generic_kernel<<<static_cast<unsigned>(pl.generic_grid), kGenericThreads, 0, st>>>(p);

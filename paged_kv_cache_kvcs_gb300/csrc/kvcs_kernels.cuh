@@ -53,6 +53,14 @@ constexpr int kLayoutLatent = 2;
 constexpr int kLayoutXSplit = 3;
 constexpr int kLayoutState = 4;
 
+// Layout families: each has its own instance of the bulk kernel holding only
+// its own staging and reduction code (a kernel holding every path ran the
+// common NHD case 11% slower).
+constexpr int kFamRows = 0;    // NHD and latent: rows of a page
+constexpr int kFamHnd = 1;     // HND: heads of a page (optionally sub-blocked)
+constexpr int kFamXSplit = 2;  // x-split: heads of 16-byte chunks
+constexpr int kFamState = 3;   // Mamba states: rows of a state
+
 constexpr u32 kStatusBadBlockId = 1u;
 constexpr u32 kStatusBadRequests = 2u;
 constexpr u32 kStatusTimeout = 4u;
@@ -262,11 +270,15 @@ struct ThreadMap {
   int cstep;   // column stride
   int rl;      // first row
   int rstep;   // row stride
+  int gtid;    // thread index within the consumer group
+  int nt;      // threads per consumer group
 };
 
 __device__ __forceinline__ void make_map(ThreadMap &t, int rowb, int gtid,
                                          int group_threads) {
   t.rowb = rowb;
+  t.gtid = gtid;
+  t.nt = group_threads;
   t.cols = rowb >> 4;
   if (t.cols <= group_threads) {
     t.rstep = group_threads / t.cols;
@@ -282,9 +294,43 @@ __device__ __forceinline__ void make_map(ThreadMap &t, int rowb, int gtid,
   }
 }
 
+// Running sums S, T, U over slots [s_lo, s_hi) of one (head, 16-byte column)
+// group whose slot s is staged at p0 + (s - s_off) * stride (s >= s_off);
+// four independent shared loads per iteration.
+__device__ __forceinline__ void accum_slots(const unsigned char *p0, size_t stride,
+                                            int s_lo, int s_hi, int s_off, u64 &S,
+                                            u64 &T, u64 &U) {
+  int s = s_lo;
+  for (; s + 3 < s_hi; s += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      v[k] = *reinterpret_cast<const uint4 *>(p0 + static_cast<size_t>(s + k - s_off) * stride);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
+      const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
+      const u64 X = x0 + x1;
+      S += X;
+      U += x1;
+      T += static_cast<u64>(static_cast<u32>(s + k)) * X;
+    }
+  }
+  for (; s < s_hi; ++s) {
+    const uint4 v =
+        *reinterpret_cast<const uint4 *>(p0 + static_cast<size_t>(s - s_off) * stride);
+    const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
+    const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
+    const u64 X = x0 + x1;
+    S += X;
+    U += x1;
+    T += static_cast<u64>(static_cast<u32>(s)) * X;
+  }
+}
+
 // This thread's share of one staged unit's contribution to the block
 // checksum (see the reformulation at the top of this file).
-template <bool kGeneral>
+template <int kFam>
 __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
                                         int half, const unsigned char *stage,
                                         const ThreadMap &t, u64 bsz) {
@@ -293,7 +339,7 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
   const int half_pieces = half * (C.hb >> 3);
   const int rowb = t.rowb;
   u64 acc = 0;
-  if (kGeneral && C.layout == kLayoutState) {
+  if constexpr (kFam == kFamState) {
     // Mamba state unit: rows [first, first + count) of the state, each a
     // slice of global row head_offset + row whose pieces are 2- or 4-byte
     // elements weighted 2e+1 by element index e.  The 16-byte column `col`
@@ -330,7 +376,7 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
       const u64 mrow = C.m0 + 2ull * static_cast<u64>(r0 + static_cast<u32>(r));
       acc += mrow * (SA + 2ull * per * SCA + 2ull * SB);
     }
-  } else if (!kGeneral || (C.layout != kLayoutHND && C.layout != kLayoutXSplit)) {
+  } else if constexpr (kFam == kFamRows) {
     const int nrows = m.count;
     const u32 r0 = static_cast<u32>(m.first);
     for (int col = t.col0; col < t.cols; col += t.cstep) {
@@ -376,47 +422,46 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
       acc += mh * (B * S + 2ull * P * T + 2ull * U);
     }
   } else {
-    // HND unit: heads [first, first + count), each with nv staged rows
-    // (slots 0 .. nv-1) of hb bytes, packed head after head.  An x-split
-    // unit is the same with every head cut into `chunks` 16-byte columns:
-    // staged [head][chunk][nv][16], one row per (head, chunk, slot).  Rows
-    // are grouped per (head, chunk); a group's head and piece pair are
-    // fixed, so it keeps the running sums and is weighted once.
+    // HND and x-split units: heads [first, first + count) staged as they lie
+    // in the page, all block_size slots of them (the valid ones are the
+    // first nv):
+    //   HND       [sub-block][head][kbs][hb]   (one sub-block unless the
+    //             attention kernel splits blocks)
+    //   x-split   [head][chunk][block_size][16]
+    // A thread owns whole groups (head, 16-byte column of the head's bytes):
+    // head and piece pair are fixed for a group, so the thread walks its nv
+    // slots with the running sums and weights the group once.
     const int nv = m.nv;
-    const int nrows = m.count * C.chunks * nv;
-    for (int col = t.col0; col < t.cols; col += t.cstep) {
-      int r = t.rl;
-      if (r >= nrows) continue;
-      int hh = r / nv;
-      int slot = r - hh * nv;
+    const int bsi = static_cast<int>(bsz);
+    const int cpr = C.hb >> 4;                 // 16-byte columns per head
+    const int groups = m.count * cpr;
+    for (int g = t.gtid; g < groups; g += t.nt) {
+      const int hl = g / cpr;
+      const int col = g - hl * cpr;
       u64 S = 0, T = 0, U = 0;
-      const unsigned char *sp = stage + static_cast<size_t>(r) * rowb + (col << 4);
-      const size_t step = static_cast<size_t>(t.rstep) * rowb;
-      while (true) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(sp);
-        const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
-        const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
-        const u64 X = x0 + x1;
-        S += X;
-        U += x1;
-        T += static_cast<u64>(static_cast<u32>(slot)) * X;
-        r += t.rstep;
-        sp += step;
-        slot += t.rstep;
-        if (slot >= nv || r >= nrows) {
-          const int head = hh / C.chunks;
-          const int chunk = hh - head * C.chunks;
-          const u64 mh = C.m0 + 2ull * static_cast<u64>(m.first + head);
-          const u64 B =
-              2ull * (t0P + static_cast<u64>(((col + chunk) << 1) + half_pieces)) + 1ull;
-          acc += mh * (B * S + 2ull * P * T + 2ull * U);
-          S = T = U = 0;
-          if (r >= nrows) break;
-          const int adv = slot / nv;
-          hh += adv;
-          slot -= adv * nv;
+      if constexpr (kFam == kFamXSplit) {
+        // the group's slots are one contiguous run of 16-byte rows; start
+        // at a group-dependent slot so a warp's reads spread over the banks
+        const unsigned char *gp = stage + static_cast<size_t>(g) * bsi * 16;
+        const int s0 = g % nv;
+        accum_slots(gp, 16, s0, nv, 0, S, T, U);
+        accum_slots(gp, 16, 0, s0, 0, S, T, U);
+      } else if (C.kbs == bsi) {
+        accum_slots(stage + static_cast<size_t>(hl) * bsi * C.hb + (col << 4),
+                    static_cast<size_t>(C.hb), 0, nv, 0, S, T, U);
+      } else {
+        // sub-block sb holds slots [sb*kbs, (sb+1)*kbs) of every head
+        const size_t sub_bytes = static_cast<size_t>(m.count) * C.kbs * C.hb;
+        for (int sb = 0; sb * C.kbs < nv; ++sb) {
+          const unsigned char *p0 = stage + sb * sub_bytes +
+                                    static_cast<size_t>(hl) * C.kbs * C.hb + (col << 4);
+          accum_slots(p0, static_cast<size_t>(C.hb), sb * C.kbs, min(nv, (sb + 1) * C.kbs),
+                      sb * C.kbs, S, T, U);
         }
       }
+      const u64 mh = C.m0 + 2ull * static_cast<u64>(m.first + hl);
+      const u64 B = 2ull * (t0P + static_cast<u64>((col << 1) + half_pieces)) + 1ull;
+      acc += mh * (B * S + 2ull * P * T + 2ull * U);
     }
   }
   return acc;
@@ -480,10 +525,8 @@ __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
 // Every wait is bounded; a wait that runs out sets KVCS_STATUS_TIMEOUT and
 // the kernel returns without hanging.
 //
-// kGeneral = false is the instance for launches whose caches are all NHD or
-// latent: it carries no HND or x-split code, which keeps the common path's
-// register allocation and scheduling independent of the rarer layouts.
-template <bool kGeneral>
+// kFam is the layout family of every cache in the launch.
+template <int kFam>
 __global__ void __launch_bounds__(kBulkThreads, 1)
     kvcs_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -565,17 +608,26 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         if (!cur.skip) {
           const int first = sub * C.rpu;
           int count;
-          u32 pbytes;   // valid bytes of one page of the unit
-          if (kGeneral && (C.layout == kLayoutHND || C.layout == kLayoutXSplit)) {
+          u32 pbytes;   // bytes copied per page of the unit
+          u32 pstride;  // bytes a page of the unit occupies in the stage
+          if constexpr (kFam == kFamHnd || kFam == kFamXSplit) {
+            // whole-slot runs of the unit's heads, staged as in memory
             count = max(0, min(C.rpu, C.heads - first));
-            pbytes = static_cast<u32>(count) * static_cast<u32>(cur.nv) *
-                     static_cast<u32>(C.hb);
-          } else if (kGeneral && C.layout == kLayoutState) {
+            pstride = static_cast<u32>(count) * static_cast<u32>(bs) * static_cast<u32>(C.hb);
+            pbytes = pstride;
+            if (kFam == kFamHnd && C.kbs != bs) {
+              const int nsb = (cur.nv + C.kbs - 1) / C.kbs;  // sub-blocks with valid slots
+              pbytes = static_cast<u32>(count) * static_cast<u32>(nsb * C.kbs) *
+                       static_cast<u32>(C.hb);
+            }
+          } else if constexpr (kFam == kFamState) {
             count = max(0, min(C.rpu, C.heads - first));
             pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
+            pstride = pbytes;
           } else {
             count = max(0, min(C.rpu, cur.nv - first));
             pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
+            pstride = pbytes;
           }
           if (pbytes > 0) {
             if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
@@ -601,49 +653,26 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               const unsigned char *page = D.base +
                   static_cast<long long>(phalf) * D.half_stride +
                   cur.block * D.block_stride;
-              if (kGeneral && D.layout == kLayoutHND) {
-                // A page is [sub-block][heads][kbs][hb] (one sub-block of
-                // block_size slots unless the attention kernel splits
-                // blocks); stage each head's valid slots as one packed run.
-                const u64 head_run = static_cast<u64>(D.kbs) * D.hb;
-                if (cur.nv == bs && D.kbs == bs) {
-                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * head_run,
-                                pbytes, fb, policy);
-                } else {
-                  const u64 sub_bytes = static_cast<u64>(D.heads) * head_run;
-                  for (int h = 0; h < count; ++h) {
-                    const unsigned char *src = page + static_cast<u64>(first + h) * head_run;
-                    u32 d = dst + static_cast<u32>(h * cur.nv) * D.hb;
-                    for (int s0 = 0; s0 < cur.nv; s0 += D.kbs) {
-                      const u32 n = static_cast<u32>(min(D.kbs, cur.nv - s0)) * D.hb;
-                      ptx::bulk_g2s(d, src, n, fb, policy);
-                      d += n;
-                      src += sub_bytes;
-                    }
-                  }
-                }
-              } else if (kGeneral && D.layout == kLayoutXSplit) {
-                // A page is [heads][chunks][block_size][16]: stage each
-                // (head, chunk) run of valid slots packed, [h][c][nv][16].
-                const u64 head_bytes_page = static_cast<u64>(bs) * D.hb;
-                if (cur.nv == bs) {
-                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * head_bytes_page,
-                                pbytes, fb, policy);
-                } else {
-                  const u32 run = static_cast<u32>(cur.nv) * 16u;
-                  const unsigned char *src = page + static_cast<u64>(first) * head_bytes_page;
-                  for (int hc = 0; hc < count * D.chunks; ++hc) {
-                    ptx::bulk_g2s(dst, src, run, fb, policy);
-                    dst += run;
-                    src += static_cast<u64>(bs) * 16u;
-                  }
-                  dst -= static_cast<u32>(count * D.chunks) * run;
-                }
+              if (kFam == kFamHnd && D.kbs != bs) {
+                // [sub-block][heads][kbs][hb]: in each sub-block that holds
+                // valid slots the unit's heads are one contiguous run
+                const u64 sub_page = static_cast<u64>(D.heads) * D.kbs * D.hb;
+                const u32 run = static_cast<u32>(count) * static_cast<u32>(D.kbs * D.hb);
+                for (int sb = 0; sb * D.kbs < cur.nv; ++sb)
+                  ptx::bulk_g2s(dst + static_cast<u32>(sb) * run,
+                                page + static_cast<u64>(sb) * sub_page +
+                                    static_cast<u64>(first) * D.kbs * D.hb,
+                                run, fb, policy);
+              } else if (kFam == kFamHnd || kFam == kFamXSplit) {
+                // [heads][block_size][hb] or [heads][chunks][block_size][16]:
+                // the unit's heads are one contiguous run of whole slots
+                ptx::bulk_g2s(dst, page + static_cast<u64>(first) * bs * D.hb, pstride,
+                              fb, policy);
               } else {
                 ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes,
                               fb, policy);
               }
-              dst += pbytes;
+              dst += pstride;
               if (++phalf == D.halves) {
                 phalf = 0;
                 ++pci;
@@ -754,9 +783,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     for (int k = 0; k < m.npages; ++k) {
       const DevCache &C = p.caches[ci];
       if (C.rowb != map.rowb) make_map(map, C.rowb, gtid, gw * 32);
-      v += unit_sum<kGeneral>(C, m, half, sp, map, bsz);
-      sp += (kGeneral && (C.layout == kLayoutHND || C.layout == kLayoutXSplit))
-                ? static_cast<size_t>(m.count) * m.nv * C.hb
+      v += unit_sum<kFam>(C, m, half, sp, map, bsz);
+      sp += (kFam == kFamHnd || kFam == kFamXSplit)
+                ? static_cast<size_t>(m.count) * static_cast<size_t>(bsz) * C.hb
                 : static_cast<size_t>(m.count) * C.rowb;
       if (++half == C.halves) {
         half = 0;
