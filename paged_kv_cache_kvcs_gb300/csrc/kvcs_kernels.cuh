@@ -328,6 +328,99 @@ __device__ __forceinline__ void accum_slots(const unsigned char *p0, size_t stri
   }
 }
 
+// As accum_slots over all nv slots of an x-split group (a contiguous run of
+// 16-byte rows at gp), starting at slot s0 and wrapping: groups start at
+// different slots so a warp's reads spread over the shared-memory banks;
+// four independent loads per iteration.
+__device__ __forceinline__ void accum_slots_rotated(const unsigned char *gp, int s0,
+                                                    int nv, u64 &S, u64 &T, u64 &U) {
+  int k = 0;
+  for (; k + 3 < nv; k += 4) {
+    int sl[4];
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      sl[i] = s0 + k + i;
+      if (sl[i] >= nv) sl[i] -= nv;
+      v[i] = *reinterpret_cast<const uint4 *>(gp + static_cast<size_t>(sl[i]) * 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const u64 x0 = (static_cast<u64>(v[i].y) << 32) | v[i].x;
+      const u64 x1 = (static_cast<u64>(v[i].w) << 32) | v[i].z;
+      const u64 X = x0 + x1;
+      S += X;
+      U += x1;
+      T += static_cast<u64>(static_cast<u32>(sl[i])) * X;
+    }
+  }
+  for (; k < nv; ++k) {
+    int sl = s0 + k;
+    if (sl >= nv) sl -= nv;
+    const uint4 v = *reinterpret_cast<const uint4 *>(gp + static_cast<size_t>(sl) * 16);
+    const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
+    const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
+    const u64 X = x0 + x1;
+    S += X;
+    U += x1;
+    T += static_cast<u64>(static_cast<u32>(sl)) * X;
+  }
+}
+
+// As accum_slots for an HND group in a sub-blocked stage: slot s of the
+// group is at p0 + (s / kbs) * sub_bytes + (s % kbs) * hb; four independent
+// loads per iteration, whatever sub-blocks they fall in.
+__device__ __forceinline__ void accum_slots_sub(const unsigned char *p0, int hb, int kbs,
+                                                size_t sub_bytes, int nv, u64 &S, u64 &T,
+                                                u64 &U) {
+  int s = 0;
+  // When kbs is a multiple of 4 a batch of four slots never straddles a
+  // sub-block: track (sub-block, offset) incrementally, one address a batch.
+  const bool whole = (kbs & 3) == 0;
+  int sb4 = 0, so4 = 0;
+  for (; s + 3 < nv; s += 4) {
+    uint4 v[4];
+    if (whole) {
+      const unsigned char *b = p0 + sb4 * sub_bytes + static_cast<size_t>(so4) * hb;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        v[i] = *reinterpret_cast<const uint4 *>(b + static_cast<size_t>(i) * hb);
+      so4 += 4;
+      if (so4 == kbs) {
+        so4 = 0;
+        ++sb4;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int sb = (s + i) / kbs;
+        v[i] = *reinterpret_cast<const uint4 *>(
+            p0 + sb * sub_bytes + static_cast<size_t>(s + i - sb * kbs) * hb);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const u64 x0 = (static_cast<u64>(v[i].y) << 32) | v[i].x;
+      const u64 x1 = (static_cast<u64>(v[i].w) << 32) | v[i].z;
+      const u64 X = x0 + x1;
+      S += X;
+      U += x1;
+      T += static_cast<u64>(static_cast<u32>(s + i)) * X;
+    }
+  }
+  for (; s < nv; ++s) {
+    const int sb = s / kbs;
+    const uint4 v = *reinterpret_cast<const uint4 *>(
+        p0 + sb * sub_bytes + static_cast<size_t>(s - sb * kbs) * hb);
+    const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
+    const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
+    const u64 X = x0 + x1;
+    S += X;
+    U += x1;
+    T += static_cast<u64>(static_cast<u32>(s)) * X;
+  }
+}
+
 // This thread's share of one staged unit's contribution to the block
 // checksum (see the reformulation at the top of this file).
 template <int kFam>
@@ -443,21 +536,14 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
         // the group's slots are one contiguous run of 16-byte rows; start
         // at a group-dependent slot so a warp's reads spread over the banks
         const unsigned char *gp = stage + static_cast<size_t>(g) * bsi * 16;
-        const int s0 = g % nv;
-        accum_slots(gp, 16, s0, nv, 0, S, T, U);
-        accum_slots(gp, 16, 0, s0, 0, S, T, U);
+        accum_slots_rotated(gp, g % nv, nv, S, T, U);
       } else if (C.kbs == bsi) {
         accum_slots(stage + static_cast<size_t>(hl) * bsi * C.hb + (col << 4),
                     static_cast<size_t>(C.hb), 0, nv, 0, S, T, U);
       } else {
         // sub-block sb holds slots [sb*kbs, (sb+1)*kbs) of every head
-        const size_t sub_bytes = static_cast<size_t>(m.count) * C.kbs * C.hb;
-        for (int sb = 0; sb * C.kbs < nv; ++sb) {
-          const unsigned char *p0 = stage + sb * sub_bytes +
-                                    static_cast<size_t>(hl) * C.kbs * C.hb + (col << 4);
-          accum_slots(p0, static_cast<size_t>(C.hb), sb * C.kbs, min(nv, (sb + 1) * C.kbs),
-                      sb * C.kbs, S, T, U);
-        }
+        accum_slots_sub(stage + static_cast<size_t>(hl) * C.kbs * C.hb + (col << 4), C.hb,
+                        C.kbs, static_cast<size_t>(m.count) * C.kbs * C.hb, nv, S, T, U);
       }
       const u64 mh = C.m0 + 2ull * static_cast<u64>(m.first + hl);
       const u64 B = 2ull * (t0P + static_cast<u64>((col << 1) + half_pieces)) + 1ull;
@@ -655,14 +741,19 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                   cur.block * D.block_stride;
               if (kFam == kFamHnd && D.kbs != bs) {
                 // [sub-block][heads][kbs][hb]: in each sub-block that holds
-                // valid slots the unit's heads are one contiguous run
+                // valid slots the unit's heads are one contiguous run; when
+                // the unit has every head those runs are one range
                 const u64 sub_page = static_cast<u64>(D.heads) * D.kbs * D.hb;
                 const u32 run = static_cast<u32>(count) * static_cast<u32>(D.kbs * D.hb);
-                for (int sb = 0; sb * D.kbs < cur.nv; ++sb)
-                  ptx::bulk_g2s(dst + static_cast<u32>(sb) * run,
-                                page + static_cast<u64>(sb) * sub_page +
-                                    static_cast<u64>(first) * D.kbs * D.hb,
-                                run, fb, policy);
+                if (count == D.heads) {
+                  ptx::bulk_g2s(dst, page, pbytes, fb, policy);
+                } else {
+                  for (int sb = 0; sb * D.kbs < cur.nv; ++sb)
+                    ptx::bulk_g2s(dst + static_cast<u32>(sb) * run,
+                                  page + static_cast<u64>(sb) * sub_page +
+                                      static_cast<u64>(first) * D.kbs * D.hb,
+                                  run, fb, policy);
+                }
               } else if (kFam == kFamHnd || kFam == kFamXSplit) {
                 // [heads][block_size][hb] or [heads][chunks][block_size][16]:
                 // the unit's heads are one contiguous run of whole slots
