@@ -399,6 +399,90 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_write(args, ws, rank, local):
+    """The KV write fused with the checksum (kvcs_write_kv): a prefill chunk
+    of new tokens written into every layer's paged pool in one call, each
+    token's checksum share added to its block's running word.  Compared with
+    the same write without the running words, and with writing and then
+    checksumming the written blocks in a separate pass."""
+    import paged_kv_cache_kvcs_gb300 as kvcs
+    from paged_kv_cache_kvcs_gb300 import workloads as W
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    layers, heads, hb, bs = 32, 8, 256, 16
+    R, L = 32, 512                         # requests x new tokens each
+    g = torch.Generator().manual_seed(args.seed + rank)
+    nb = R * L // bs + 64
+    perm = torch.randperm(nb, generator=g)
+    tables = perm[:R * L // bs].view(R, L // bs)
+    t = torch.arange(L)
+    slots = (tables[:, t // bs] * bs + t % bs).reshape(-1).to(dev)
+    pos = t.repeat(R).to(dev)
+    n = R * L
+    dg = torch.Generator(device=dev).manual_seed(args.seed + 1)
+    caches = [W.CacheSpec(torch.zeros(2 * nb * bs * heads * hb, dtype=torch.uint8, device=dev),
+                          nb, W.LAYOUT_NHD, li, 0, heads, hb) for li in range(layers)]
+    keys = [torch.randn((n, heads, hb // 2), dtype=torch.bfloat16, device=dev, generator=dg)
+            for _ in range(layers)]
+    vals = [torch.randn((n, heads, hb // 2), dtype=torch.bfloat16, device=dev, generator=dg)
+            for _ in range(layers)]
+    sums = torch.zeros(nb, dtype=torch.int64, device=dev)
+    # the written blocks as checksum positions (for the unfused comparison)
+    po = torch.arange(0, (R + 1) * (L // bs), L // bs, dtype=torch.int64, device=dev)
+    fp = torch.zeros(R, dtype=torch.int64, device=dev)
+    nt = torch.full((R,), L, dtype=torch.int64, device=dev)
+    bids = tables.reshape(-1).to(torch.int32).to(dev)
+    ck = kvcs.Checksummer(caches, bs, po, fp, nt, bids, R * L // bs)
+    out = torch.empty(R * L // bs, dtype=torch.int64, device=dev)
+    stream = torch.cuda.Stream(dev)
+    raw = stream.cuda_stream
+
+    def timed(fn, k):
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(k):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / 1e3 / k
+
+    fused = lambda: kvcs.write_kv(caches, bs, keys, vals, slots, pos, block_sums=sums,
+                                  stream=raw)
+    plain = lambda: kvcs.write_kv(caches, bs, keys, vals, slots, pos, stream=raw)
+
+    def unfused():
+        plain()
+        ck(out, None, raw)
+
+    launches0 = kvcs.launch_count()
+    t_fused = timed(fused, args.steps)
+    launches = (kvcs.launch_count() - launches0) // (args.steps + max(3, args.warmup))
+    t_plain = timed(plain, args.steps)
+    t_unfused = timed(unfused, args.steps)
+    moved = 2 * n * layers * 2 * heads * hb          # bytes read + written
+    if rank != 0:
+        return
+    line = {"metric": "KV write fused with the block checksum, GB/s of bytes read + written",
+            "value": round(moved / t_fused / 1e9, 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_fused * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u64", "data": "synthetic",
+            "config": {"workload": "llama3_8b_prefill_write", "layers": layers,
+                       "kv_heads": heads, "head_bytes": hb, "block_size": bs,
+                       "requests": R, "new_tokens_per_request": L,
+                       "bytes_moved_per_step": moved},
+            "gpu_launches_per_step": launches,
+            "write_only_ms": round(t_plain * 1e3, 4),
+            "write_then_checksum_ms": round(t_unfused * 1e3, 4),
+            "fused_vs_write_only": round(t_plain / t_fused, 4),
+            "fused_vs_write_then_checksum": round(t_unfused / t_fused, 4)}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, ws, rank, local):
     import paged_kv_cache_kvcs_gb300 as kvcs
 
@@ -649,6 +733,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, ws, rank)
+        elif args.config == "llama3_8b_write":
+            run_write(args, ws, rank, local)
         else:
             run_ours(args, ws, rank, local)
     finally:

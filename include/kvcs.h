@@ -255,6 +255,48 @@ int kvcs_block_checksum_tags(const void *block_hashes, int64_t hash_stride,
                              int64_t n, uint64_t fingerprint, uint64_t *tags,
                              void *stream);
 
+/*
+ * kvcs_write_kv -- write new tokens' K and V into layers' paged caches and
+ * add each written token's share of its block's checksum to a running word
+ * per physical block.
+ *
+ * The write is the KV-cache page's reshape_and_cache step (section
+ * "逻辑到物理地址映射"): token i goes to slot slot_mapping[i] =
+ * block * block_size + offset of every cache; a negative slot is a padding
+ * token and is skipped.  Because the piece index j = t*P + p runs token by
+ * token (the checksum page, item 1), a block's checksum is a sum over its
+ * tokens, each token adding sum_h m_h sum_p x_p (2(t*P + p) + 1) with t its
+ * position in the request.  So a running word per physical block, zeroed by
+ * the caller when the block is allocated and added into for every layer of
+ * the group, holds the checksum of the tokens written to the block so far --
+ * with no second read of the cache.  One call can write all layers (the
+ * receive side of a KV transfer) or one layer (a forward pass).
+ *
+ *   caches        HOST array of num_caches descriptors (NHD, HND, XSPLIT or
+ *                 LATENT) sharing the block table
+ *   keys, values  HOST arrays of num_caches DEVICE pointers:
+ *                 [num_tokens][num_heads][head_bytes] each (token stride
+ *                 num_heads * head_bytes bytes); for a LATENT cache keys[k]
+ *                 is [num_tokens][row_bytes] and values[k] must be NULL
+ *   slot_mapping  DEVICE int64[num_tokens]
+ *   positions     DEVICE int64[num_tokens]: each token's position in its
+ *                 request
+ *   block_sums    DEVICE uint64[min over caches of num_blocks] or NULL
+ *                 (write only)
+ *   status        DEVICE word or NULL: KVCS_STATUS_BAD_BLOCK_ID for a slot
+ *                 past a pool (token skipped), KVCS_STATUS_BAD_REQUESTS for
+ *                 a negative position (token written, not checksummed)
+ *   stream        a cudaStream_t
+ *
+ * Re-writing a slot adds its token again: roll back the running word (or
+ * re-zero and re-checksum the block) when tokens are overwritten.
+ */
+int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+                  int64_t num_tokens, const void *const *keys,
+                  const void *const *values, const int64_t *slot_mapping,
+                  const int64_t *positions, uint64_t *block_sums, uint32_t *status,
+                  void *stream);
+
 /* Which kernel and launch shape kvcs_block_checksums would use.  Filled by
  * kvcs_plan; no CUDA work is enqueued. */
 typedef struct kvcs_plan_info {

@@ -79,6 +79,10 @@ SIGNATURES = {
     "kvcs_block_checksum_tags": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
         ctypes.c_void_p, ctypes.c_void_p]),
+    "kvcs_write_kv": (ctypes.c_int, [
+        ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+        ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "kvcs_plan": (ctypes.c_int, [
         ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(kvcs_plan_info)]),
@@ -378,3 +382,41 @@ def block_checksum_tags(block_hashes, fingerprint: int, tags=None, stream=None):
     if rc != KVCS_OK:
         raise KvcsError(rc, "kvcs_block_checksum_tags")
     return tags
+
+
+def write_kv(caches, block_size: int, keys, values, slot_mapping, positions,
+             block_sums=None, status=None, stream=None) -> None:
+    """Torch front end of ``kvcs_write_kv`` over one cache or a list of
+    caches: ``keys``/``values`` are CUDA tensors ``[num_tokens, heads,
+    head_size]`` (any dtype; their bytes are written), one per cache, with
+    ``values[k]`` None for a latent cache; ``slot_mapping`` and ``positions``
+    int64 CUDA tensors; ``block_sums`` an int64 CUDA tensor of running words
+    (uint64 bits) or None."""
+    import torch
+    if not isinstance(caches, (list, tuple)):
+        caches, keys, values = [caches], [keys], [values]
+    n = slot_mapping.numel()
+    for c, k, v in zip(caches, keys, values):
+        _check_pool(c, block_size)
+        row = c.num_heads * c.head_bytes
+        for name, t in (("key", k), ("value", v)):
+            if t is not None and not (t.is_cuda and t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CUDA tensor")
+            if t is not None and t.numel() * t.element_size() < n * row:
+                raise ValueError(f"{name} is smaller than num_tokens rows")
+    for name, t in (("slot_mapping", slot_mapping), ("positions", positions)):
+        if not (t.is_cuda and t.dtype == torch.int64 and t.is_contiguous() and t.numel() == n):
+            raise ValueError(f"{name} must be a contiguous CUDA int64 tensor of num_tokens")
+    if block_sums is not None and block_sums.numel() < min(c.num_blocks for c in caches):
+        raise ValueError("block_sums needs one word per block")
+    if stream is None:
+        stream = torch.cuda.current_stream(slot_mapping.device).cuda_stream
+    arr = cache_array(caches)
+    kp = (ctypes.c_void_p * len(caches))(*[_ptr(k) for k in keys])
+    vp = (ctypes.c_void_p * len(caches))(*[_ptr(v) for v in values])
+    rc = load_library().kvcs_write_kv(arr, len(caches), block_size, n, kp, vp,
+                                      slot_mapping.data_ptr() if n else None,
+                                      positions.data_ptr() if n else None,
+                                      _ptr(block_sums), _ptr(status), stream)
+    if rc != KVCS_OK:
+        raise KvcsError(rc, "kvcs_write_kv")

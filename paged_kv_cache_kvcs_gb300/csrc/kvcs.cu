@@ -544,6 +544,65 @@ int kvcs_block_checksum_tags(const void *block_hashes, int64_t hash_stride,
   return KVCS_OK;
 }
 
+int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+                  int64_t num_tokens, const void *const *keys,
+                  const void *const *values, const int64_t *slot_mapping,
+                  const int64_t *positions, uint64_t *block_sums, uint32_t *status,
+                  void *stream) {
+  if (!caches || num_caches < 1 || num_tokens < 0 || !keys || !values) return KVCS_EINVAL;
+  std::vector<kvcs_cache> plain(caches, caches + num_caches);
+  for (kvcs_cache &c : plain) c.column = 0;  // running words are per block
+  int rc = validate_caches(plain.data(), num_caches, block_size, 1);
+  if (rc != KVCS_OK) return rc;
+  auto al = [](const void *ptr, uintptr_t a) { return reinterpret_cast<uintptr_t>(ptr) % a == 0; };
+  bool a16 = true;
+  long long min_nb = caches[0].num_blocks;
+  for (int32_t k = 0; k < num_caches; ++k) {
+    const kvcs_cache &c = caches[k];
+    if (c.layout == KVCS_LAYOUT_STATE) return KVCS_EINVAL;  // states are not per token
+    const bool latent = c.layout == KVCS_LAYOUT_LATENT;
+    if (num_tokens > 0 && (!keys[k] || (latent ? values[k] != nullptr : values[k] == nullptr)))
+      return KVCS_EINVAL;
+    if (!al(keys[k], 8) || (values[k] && !al(values[k], 8))) return KVCS_EINVAL;
+    min_nb = std::min<long long>(min_nb, c.num_blocks);
+    // 16-byte moves when every address involved stays 16-byte aligned
+    a16 = a16 && al(c.base, 16) && al(keys[k], 16) && (!values[k] || al(values[k], 16)) &&
+          c.head_bytes % 16 == 0 && c.half_stride % 16 == 0 && c.block_stride % 16 == 0;
+  }
+  if (block_sums && !al(block_sums, 8)) return KVCS_EINVAL;
+  if (num_tokens == 0) return KVCS_OK;
+  if (!slot_mapping || !positions) return KVCS_EINVAL;
+  int sms = 0;
+  if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
+  WriteParams w;
+  std::memset(&w, 0, sizeof(w));
+  w.slots = reinterpret_cast<const long long *>(slot_mapping);
+  w.positions = reinterpret_cast<const long long *>(positions);
+  w.block_sums = reinterpret_cast<u64 *>(block_sums);
+  w.status = status;
+  w.num_tokens = num_tokens;
+  w.num_blocks = min_nb;
+  w.block_size = block_size;
+  w.chunk = a16 ? 16 : 8;
+  for (int32_t lo = 0; lo < num_caches; lo += kMaxWriteCaches) {
+    const int n = std::min(kMaxWriteCaches, num_caches - lo);
+    w.num_caches = n;
+    for (int k = 0; k < n; ++k) {
+      w.c[k] = make_dev_cache(caches[lo + k], block_size);
+      w.key[k] = static_cast<const unsigned char *>(keys[lo + k]);
+      w.value[k] = static_cast<const unsigned char *>(values[lo + k]);
+    }
+    const long long warps_per_cta = kWriteThreads / 32;
+    const long long grid = std::min<long long>((num_tokens + warps_per_cta - 1) / warps_per_cta,
+                                               8LL * sms);
+    kvcs_write_kernel<<<static_cast<unsigned>(std::max<long long>(1, grid)), kWriteThreads, 0,
+                        static_cast<cudaStream_t>(stream)>>>(w);
+    if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return KVCS_OK;
+}
+
 int kvcs_selftest_wait_timeout(uint32_t *status, int64_t limit_ns, void *stream) {
   if (!status || limit_ns <= 0 || limit_ns > 2000000000LL) return KVCS_EINVAL;
   kvcs_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(

@@ -1026,6 +1026,120 @@ __global__ void __launch_bounds__(kGenericThreads)
 }
 
 // ---------------------------------------------------------------------------
+// KV write fused with the checksum (reshape_and_cache + running block sums)
+// ---------------------------------------------------------------------------
+
+constexpr int kMaxWriteCaches = 64;
+
+struct WriteParams {
+  const long long *slots;      // slot_mapping
+  const long long *positions;  // token positions in their requests
+  u64 *block_sums;             // running word per physical block, or null
+  u32 *status;
+  long long num_tokens;
+  long long num_blocks;        // smallest pool of the call
+  int block_size;
+  int num_caches;
+  int chunk;                   // 16 or 8: bytes moved per thread per step
+  DevCache c[kMaxWriteCaches];
+  const unsigned char *key[kMaxWriteCaches];    // [num_tokens][heads][hb]
+  const unsigned char *value[kMaxWriteCaches];  // same, or null (latent)
+};
+
+constexpr int kWriteThreads = 256;
+
+// Destination of byte offset `off` of head `h`'s K (or V) row of a token at
+// slot `o` of a page, for each layout.
+__device__ __forceinline__ long long write_offset(const DevCache &C, long long bs,
+                                                  long long o, long long h, long long e) {
+  if (C.layout == kLayoutNHD) return (o * C.heads + h) * C.hb + e;
+  if (C.layout == kLayoutHND) {
+    const long long sb = o / C.kbs;
+    return ((sb * C.heads + h) * C.kbs + (o - sb * C.kbs)) * C.hb + e;
+  }
+  if (C.layout == kLayoutXSplit) return ((h * (C.hb >> 4) + (e >> 4)) * bs + o) * 16 + (e & 15);
+  return o * C.hb + e;  // latent
+}
+
+// A warp per token (grid-stride over warps): for every cache of the call it
+// moves the token's K and V rows into the page slot, four 16-byte chunks per
+// lane in flight, and weights the pieces it moved; the token's total over
+// all caches goes into its block's running word with one atomic add.
+__global__ void __launch_bounds__(kWriteThreads)
+    kvcs_write_kernel(const __grid_constant__ WriteParams w) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (kWriteThreads / 32);
+  const long long bs = w.block_size;
+  const int ch = w.chunk;
+  for (long long i = blockIdx.x * (kWriteThreads / 32) + (threadIdx.x >> 5); i < w.num_tokens;
+       i += warps) {
+    const long long slot = w.slots[i];
+    if (slot < 0) continue;  // padding token
+    const long long b = slot / bs;
+    const long long o = slot - b * bs;
+    if (b >= w.num_blocks) {
+      if (lane == 0 && w.status) atomicOr(w.status, kStatusBadBlockId);
+      continue;
+    }
+    const long long t = w.positions[i];
+    if (t < 0 && lane == 0 && w.status) atomicOr(w.status, kStatusBadRequests);
+    u64 acc = 0;
+    for (int ci = 0; ci < w.num_caches; ++ci) {
+      const DevCache &C = w.c[ci];
+      const long long row = static_cast<long long>(C.heads) * C.hb;
+      const u64 tP = static_cast<u64>(t) * static_cast<u64>(C.P);
+      for (int half = 0; half < C.halves; ++half) {
+        const unsigned char *src = (half ? w.value[ci] : w.key[ci]) + i * row;
+        unsigned char *page = const_cast<unsigned char *>(C.base) + half * C.half_stride +
+                              b * C.block_stride;
+        const u64 hp = static_cast<u64>(half) * (C.hb >> 3);
+        for (long long base = static_cast<long long>(lane) * ch; base < row;
+             base += 4LL * 32 * ch) {
+          // up to four chunks per lane, loads first
+          uint4 v[4];
+          long long offs[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            offs[k] = base + static_cast<long long>(k) * 32 * ch;
+            if (offs[k] < row) {
+              if (ch == 16) {
+                v[k] = *reinterpret_cast<const uint4 *>(src + offs[k]);
+              } else {
+                const u64 x = *reinterpret_cast<const u64 *>(src + offs[k]);
+                v[k] = make_uint4(static_cast<u32>(x), static_cast<u32>(x >> 32), 0u, 0u);
+              }
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const long long off = offs[k];
+            if (off >= row) break;
+            const long long h = C.hb_shift >= 0 ? (off >> C.hb_shift) : off / C.hb;
+            const long long e = off - h * C.hb;
+            unsigned char *dst = page + write_offset(C, bs, o, h, e);
+            const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
+            const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
+            const u64 w0 = 2ull * (tP + static_cast<u64>(e >> 3) + hp) + 1ull;
+            if (ch == 16) {
+              *reinterpret_cast<uint4 *>(dst) = v[k];
+              const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
+              acc += mh * (x0 * w0 + x1 * (w0 + 2ull));
+            } else {
+              *reinterpret_cast<u64 *>(dst) = x0;
+              acc += mh * (x0 * w0);
+            }
+          }
+        }
+      }
+    }
+    if (w.block_sums != nullptr && t >= 0) {
+      acc = warp_sum(acc);
+      if (lane == 0) atomicAdd(w.block_sums + b, acc);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Row sums, tags and verification (offloaded-KV checks)
 // ---------------------------------------------------------------------------
 

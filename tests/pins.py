@@ -433,7 +433,34 @@ def pin_sensitivity(form):
     assert all(a != b for a, b in zip(sw, base))
 
 
+def pin_token_additivity(form):
+    """A block's checksum grows token by token: c with num_tokens = n minus c
+    with n - 1 equals c of the same block when only token n - 1's bytes are
+    kept (j = t*P + p runs over tokens), for every layout."""
+    for layout, hb in ((W.LAYOUT_NHD, 16), (W.LAYOUT_HND, 8), (W.LAYOUT_LATENT, 24)):
+        bs = 4
+        _, caches, r = random_pool_case(53, layout, layers=2, heads=2 if layout != 2 else 1,
+                                        hb=hb, bs=bs, lengths=[11], spare=0)
+        for n in range(1, 12):
+            q = (n - 1) // bs                       # block position of token n-1
+            blk = r.block_ids[q]
+            one = OracleRequests([0, 1], [q], [n], [blk])
+            prev = OracleRequests([0, 1], [q], [n - 1], [blk])
+            cn = int(form(caches, bs, one)[0][0])
+            cp = int(form(caches, bs, prev)[0][0])
+            kept = []
+            for c in caches:
+                d = np.zeros_like(c.data)
+                v_src = pool_view(c.data, c.layout, c.num_blocks, bs, c.num_heads, c.head_bytes)
+                v_dst = pool_view(d, c.layout, c.num_blocks, bs, c.num_heads, c.head_bytes)
+                v_dst[:, blk, (n - 1) % bs] = v_src[:, blk, (n - 1) % bs]
+                kept.append(OracleCache(d, c.num_blocks, c.layout, c.layer, c.head_offset,
+                                        c.num_heads, c.head_bytes))
+            ct = int(form(kept, bs, one)[0][0])
+            assert (cn - cp) % (1 << 64) == ct, (layout, n)
+
+
 ALL_PINS = [pin_hand_examples, pin_zero, pin_constant_pieces, pin_single_piece,
             pin_brute_force_stream, pin_additivity, pin_layout_invariance,
             pin_tp_pp_partials, pin_first_position, pin_past_num_tokens,
-            pin_bad_block_id, pin_sensitivity]
+            pin_bad_block_id, pin_sensitivity, pin_token_additivity]

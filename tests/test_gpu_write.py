@@ -1,0 +1,154 @@
+"""The KV write fused with the checksum (kvcs_write_kv) through the C ABI:
+the written pools equal a plain scatter (data movement with torch), and the
+running word of every block equals the oracle's block checksum of the
+tokens written to it, for every layout."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import W, OracleCache, OracleRequests, c_form, host_bytes
+import paged_kv_cache_kvcs_gb300 as K
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def u64(t):
+    return t.cpu().numpy().view(np.uint64)
+
+
+def to_canonical(c, bs):
+    """A pool in its declared layout -> canonical NHD [2, nb, bs, H, hb] (or
+    latent [nb, bs, row]) bytes, via torch views."""
+    nb, H, hb = c.num_blocks, c.num_heads, c.head_bytes
+    if c.layout == W.LAYOUT_LATENT:
+        return c.pool.view(nb, bs, hb)
+    if c.layout == W.LAYOUT_NHD:
+        return c.pool.view(2, nb, bs, H, hb)
+    if c.layout == W.LAYOUT_HND:
+        kbs = c.kernel_block_size or bs
+        v = c.pool.view(2, nb, bs // kbs, H, kbs, hb).permute(0, 1, 2, 4, 3, 5)
+        return v.reshape(2, nb, bs, H, hb)
+    v = c.pool.view(2, nb, H, hb // 16, bs, 16).permute(0, 1, 4, 2, 3, 5)
+    return v.reshape(2, nb, bs, H, hb)
+
+
+@pytest.mark.parametrize("layout,hb,kbs", [
+    (W.LAYOUT_NHD, 64, 0), (W.LAYOUT_NHD, 24, 0), (W.LAYOUT_HND, 64, 0),
+    (W.LAYOUT_HND, 32, 4), (W.LAYOUT_XSPLIT, 64, 0), (W.LAYOUT_LATENT, 1152, 0),
+    (W.LAYOUT_LATENT, 40, 0)])
+def test_write_matches_scatter_and_oracle(layout, hb, kbs):
+    bs, layers = 16, 2
+    heads = 1 if layout == W.LAYOUT_LATENT else 4
+    lengths = [37, 5, 18]
+    g = torch.Generator().manual_seed(11)
+    nb = 12
+    ids = torch.randperm(nb, generator=g)[:sum(-(-n // bs) for n in lengths)].tolist()
+    tables, k = [], 0
+    for n in lengths:
+        tables.append(ids[k:k + -(-n // bs)])
+        k += -(-n // bs)
+    halves = 1 if layout == W.LAYOUT_LATENT else 2
+    caches = [W.CacheSpec(torch.zeros(halves * nb * bs * heads * hb, dtype=torch.uint8,
+                                      device=DEV), nb, layout, li, 0, heads, hb,
+                          kernel_block_size=kbs) for li in range(layers)]
+    ref = [torch.zeros_like(c.pool).view(*to_canonical(c, bs).shape) for c in caches]
+    sums = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    # tokens (request, position), written in three shuffled calls with
+    # padding tokens mixed in
+    toks = [(r, t) for r, n in enumerate(lengths) for t in range(n)]
+    order = torch.randperm(len(toks), generator=g).tolist()
+    for part in (order[:20], order[20:45], order[45:]):
+        sel = [toks[i] for i in part]
+        slots = [tables[r][t // bs] * bs + t % bs for r, t in sel] + [-1, -5]
+        pos = [t for _, t in sel] + [3, 0]
+        n = len(slots)
+        slot_t = torch.tensor(slots, dtype=torch.int64, device=DEV)
+        pos_t = torch.tensor(pos, dtype=torch.int64, device=DEV)
+        for li, c in enumerate(caches):
+            if layout == W.LAYOUT_LATENT:
+                key = torch.randint(0, 256, (n, hb), dtype=torch.uint8, generator=g).to(DEV)
+                val = None
+            else:
+                key = torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8,
+                                    generator=g).to(DEV)
+                val = torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8,
+                                    generator=g).to(DEV)
+            K.write_kv(c, bs, key, val, slot_t, pos_t, block_sums=sums, status=status)
+            for j, s in enumerate(slots):
+                if s < 0:
+                    continue
+                b, o = s // bs, s % bs
+                if layout == W.LAYOUT_LATENT:
+                    ref[li][b, o] = key[j]
+                else:
+                    ref[li][0, b, o] = key[j]
+                    ref[li][1, b, o] = val[j]
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for li, c in enumerate(caches):
+        assert torch.equal(to_canonical(c, bs).contiguous(), ref[li].contiguous()), li
+    # every written block's running word is the oracle's block checksum
+    ocaches = [OracleCache(host_bytes(r), nb, W.LAYOUT_LATENT if layout == W.LAYOUT_LATENT
+                           else W.LAYOUT_NHD, li, 0, heads, hb)
+               for li, r in enumerate(ref)]
+    po = [0]
+    for tb in tables:
+        po.append(po[-1] + len(tb))
+    reqs = OracleRequests(po, [0] * len(lengths), lengths, [b for tb in tables for b in tb])
+    exp, _ = c_form(ocaches, bs, reqs)
+    got = u64(sums)
+    for q, b in enumerate(reqs.block_ids):
+        assert got[b] == np.uint64(exp[q]), (q, b)
+    unused = set(range(nb)) - set(reqs.block_ids)
+    assert all(got[b] == 0 for b in unused)
+
+
+def test_write_flags_bad_slots_and_positions():
+    nb, bs, heads, hb = 4, 8, 2, 32
+    c = W.CacheSpec(torch.zeros(2 * nb * bs * heads * hb, dtype=torch.uint8, device=DEV),
+                    nb, W.LAYOUT_NHD, 0, 0, heads, hb)
+    key = torch.ones((3, heads, hb), dtype=torch.uint8, device=DEV)
+    sums = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    K.write_kv(c, bs, key, key.clone(), torch.tensor([nb * bs + 3, 5, 9], device=DEV),
+               torch.tensor([0, -2, 1], device=DEV), block_sums=sums, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & K.KVCS_STATUS_BAD_BLOCK_ID
+    assert int(st.item()) & K.KVCS_STATUS_BAD_REQUESTS
+    # slot 5 (negative position) was written but not summed; slot 9 both
+    pool = c.pool.view(2, nb, bs, heads, hb)
+    assert int(pool[0, 0, 5].sum()) == heads * hb and int(pool[0, 1, 1].sum()) == heads * hb
+    assert int(sums[0].item()) == 0 and int(sums[1].item()) != 0
+
+
+def test_all_layers_in_one_call_equals_layer_by_layer():
+    bs, nb, heads, hb, layers = 16, 20, 8, 256, 5
+    g = torch.Generator().manual_seed(21)
+    n = 300
+    slots = torch.randperm(nb * bs, generator=g)[:n].to(DEV)
+    pos = torch.randint(0, 4096, (n,), generator=g).to(DEV)
+    keys = [torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8, generator=g).to(DEV)
+            for _ in range(layers)]
+    vals = [torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8, generator=g).to(DEV)
+            for _ in range(layers)]
+
+    def fresh():
+        return [W.CacheSpec(torch.zeros(2 * nb * bs * heads * hb, dtype=torch.uint8,
+                                        device=DEV), nb, W.LAYOUT_NHD, li, 0, heads, hb)
+                for li in range(layers)]
+
+    a, b = fresh(), fresh()
+    sa = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    sb = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    K.write_kv(a, bs, keys, vals, slots, pos, block_sums=sa)
+    for c, k, v in zip(b, keys, vals):
+        K.write_kv(c, bs, k, v, slots, pos, block_sums=sb)
+    torch.cuda.synchronize()
+    assert torch.equal(sa, sb)
+    for ca, cb in zip(a, b):
+        assert torch.equal(ca.pool, cb.pool)
