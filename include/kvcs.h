@@ -290,6 +290,12 @@ int kvcs_block_checksum_tags(const void *block_hashes, int64_t hash_stride,
  *
  * Re-writing a slot adds its token again: roll back the running word (or
  * re-zero and re-checksum the block) when tokens are overwritten.
+ *
+ * Returns KVCS_EINVAL for the argument errors of kvcs_block_checksums, a
+ * STATE cache, a missing key pointer, a value pointer given for a LATENT
+ * cache (or missing for another), or key/value pointers not 8-byte aligned;
+ * KVCS_EUNSUPPORTED when a token's row (num_heads * head_bytes) is 1 GiB or
+ * more.
  */
 int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
                   int64_t num_tokens, const void *const *keys,

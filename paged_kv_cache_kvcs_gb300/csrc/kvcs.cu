@@ -564,6 +564,9 @@ int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_si
     if (num_tokens > 0 && (!keys[k] || (latent ? values[k] != nullptr : values[k] == nullptr)))
       return KVCS_EINVAL;
     if (!al(keys[k], 8) || (values[k] && !al(values[k], 8))) return KVCS_EINVAL;
+    // the kernel indexes a token's row with 32-bit offsets
+    if (static_cast<long long>(c.num_heads) * c.head_bytes >= (1LL << 30))
+      return KVCS_EUNSUPPORTED;
     min_nb = std::min<long long>(min_nb, c.num_blocks);
     // 16-byte moves when every address involved stays 16-byte aligned
     a16 = a16 && al(c.base, 16) && al(keys[k], 16) && (!values[k] || al(values[k], 16)) &&
@@ -584,21 +587,39 @@ int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_si
   w.num_blocks = min_nb;
   w.block_size = block_size;
   w.chunk = a16 ? 16 : 8;
-  for (int32_t lo = 0; lo < num_caches; lo += kMaxWriteCaches) {
-    const int n = std::min(kMaxWriteCaches, num_caches - lo);
-    w.num_caches = n;
-    for (int k = 0; k < n; ++k) {
-      w.c[k] = make_dev_cache(caches[lo + k], block_size);
-      w.key[k] = static_cast<const unsigned char *>(keys[lo + k]);
-      w.value[k] = static_cast<const unsigned char *>(values[lo + k]);
+  // caches by layout family (NHD and latent share one), each family in
+  // launches of at most kMaxWriteCaches caches
+  const int families[3] = {KVCS_LAYOUT_NHD, KVCS_LAYOUT_HND, KVCS_LAYOUT_XSPLIT};
+  auto family = [](int layout) {
+    return layout == KVCS_LAYOUT_LATENT ? static_cast<int>(KVCS_LAYOUT_NHD) : layout;
+  };
+  // a warp per token; CTAs beyond the resident ones start as others retire
+  const long long warps_per_cta = kWriteThreads / 32;
+  const unsigned grid = static_cast<unsigned>(std::max<long long>(
+      1, std::min<long long>((num_tokens + warps_per_cta - 1) / warps_per_cta, 32LL * sms)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int fam : families) {
+    std::vector<int32_t> members;
+    for (int32_t k = 0; k < num_caches; ++k)
+      if (family(caches[k].layout) == fam) members.push_back(k);
+    for (size_t lo = 0; lo < members.size(); lo += kMaxWriteCaches) {
+      const int n = static_cast<int>(std::min<size_t>(kMaxWriteCaches, members.size() - lo));
+      w.num_caches = n;
+      for (int k = 0; k < n; ++k) {
+        const int32_t m = members[lo + k];
+        w.c[k] = make_dev_cache(caches[m], block_size);
+        w.key[k] = static_cast<const unsigned char *>(keys[m]);
+        w.value[k] = static_cast<const unsigned char *>(values[m]);
+      }
+      if (fam == KVCS_LAYOUT_HND)
+        kvcs_write_kernel<kLayoutHND><<<grid, kWriteThreads, 0, st>>>(w);
+      else if (fam == KVCS_LAYOUT_XSPLIT)
+        kvcs_write_kernel<kLayoutXSplit><<<grid, kWriteThreads, 0, st>>>(w);
+      else
+        kvcs_write_kernel<kLayoutNHD><<<grid, kWriteThreads, 0, st>>>(w);
+      if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
+      g_launches.fetch_add(1, std::memory_order_relaxed);
     }
-    const long long warps_per_cta = kWriteThreads / 32;
-    const long long grid = std::min<long long>((num_tokens + warps_per_cta - 1) / warps_per_cta,
-                                               8LL * sms);
-    kvcs_write_kernel<<<static_cast<unsigned>(std::max<long long>(1, grid)), kWriteThreads, 0,
-                        static_cast<cudaStream_t>(stream)>>>(w);
-    if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
   }
   return KVCS_OK;
 }

@@ -1047,25 +1047,95 @@ struct WriteParams {
 };
 
 constexpr int kWriteThreads = 256;
+constexpr int kWriteBatch = 8;  // chunks per lane in flight
 
-// Destination of byte offset `off` of head `h`'s K (or V) row of a token at
-// slot `o` of a page, for each layout.
-__device__ __forceinline__ long long write_offset(const DevCache &C, long long bs,
-                                                  long long o, long long h, long long e) {
-  if (C.layout == kLayoutNHD) return (o * C.heads + h) * C.hb + e;
-  if (C.layout == kLayoutHND) {
+// One cache's K and V rows of one token: moved into the page slot `o` of
+// block `b` by the calling warp, up to eight chunks per lane in flight (the
+// K and V chunks of one batch together); returns the lane's share of the
+// token's checksum term for this cache.  Byte `off` of a row (head
+// h = off / hb, byte e = off mod hb) goes to, per layout:
+//   NHD, latent  o*row + off
+//   HND          ((o/kbs*heads + h)*kbs + o mod kbs)*hb + e
+//   x-split      (off/16)*bs*16 + o*16 + off mod 16
+template <int kLayout>
+__device__ __forceinline__ u64 write_token_rows(const DevCache &C, const unsigned char *srck,
+                                                const unsigned char *srcv, long long bs,
+                                                long long b, long long o, u64 t, int ch,
+                                                int lane) {
+  const int row = C.heads * C.hb;
+  const int nh = row / ch;          // chunks per half
+  const int n = nh * C.halves;      // chunks of the token
+  unsigned char *page = const_cast<unsigned char *>(C.base) + b * C.block_stride;
+  long long slot_base;              // address of byte 0 of head 0 of slot o
+  long long head_step = 0;          // HND: bytes between heads
+  if (kLayout == kLayoutHND) {
     const long long sb = o / C.kbs;
-    return ((sb * C.heads + h) * C.kbs + (o - sb * C.kbs)) * C.hb + e;
+    slot_base = (sb * C.heads * C.kbs + (o - sb * C.kbs)) * C.hb;
+    head_step = static_cast<long long>(C.kbs - 1) * C.hb;
+  } else if (kLayout == kLayoutXSplit) {
+    slot_base = o * 16;
+  } else {
+    slot_base = o * row;
   }
-  if (C.layout == kLayoutXSplit) return ((h * (C.hb >> 4) + (e >> 4)) * bs + o) * 16 + (e & 15);
-  return o * C.hb + e;  // latent
+  const u64 tP = t * static_cast<u64>(C.P);
+  u64 acc = 0;
+  for (int base = lane; base < n; base += kWriteBatch * 32) {
+    uint4 v[kWriteBatch];
+#pragma unroll
+    for (int k = 0; k < kWriteBatch; ++k) {
+      const int idx = base + 32 * k;
+      if (idx < n) {
+        const bool hv = idx >= nh;
+        const unsigned char *src = (hv ? srcv : srck) + (idx - (hv ? nh : 0)) * ch;
+        if (ch == 16) {
+          v[k] = *reinterpret_cast<const uint4 *>(src);
+        } else {
+          const u64 x = *reinterpret_cast<const u64 *>(src);
+          v[k] = make_uint4(static_cast<u32>(x), static_cast<u32>(x >> 32), 0u, 0u);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kWriteBatch; ++k) {
+      const int idx = base + 32 * k;
+      if (idx >= n) break;
+      const int half = idx >= nh ? 1 : 0;
+      const int off = (idx - half * nh) * ch;
+      const int h = C.hb_shift >= 0 ? (off >> C.hb_shift) : off / C.hb;
+      const int e = off - h * C.hb;
+      long long d;
+      if (kLayout == kLayoutHND) {
+        d = slot_base + off + h * head_step;
+      } else if (kLayout == kLayoutXSplit) {
+        d = slot_base + static_cast<long long>(off >> 4) * bs * 16 + (off & 15);
+      } else {
+        d = slot_base + off;
+      }
+      unsigned char *dst = page + half * C.half_stride + d;
+      const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
+      const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
+      const u64 w0 = 2ull * (tP + static_cast<u64>((e >> 3) + half * (C.hb >> 3))) + 1ull;
+      if (ch == 16) {
+        *reinterpret_cast<uint4 *>(dst) = v[k];
+        const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
+        acc += mh * (x0 * w0 + x1 * (w0 + 2ull));
+      } else {
+        *reinterpret_cast<u64 *>(dst) = x0;
+        acc += mh * (x0 * w0);
+      }
+    }
+  }
+  return acc;
 }
 
-// A warp per token (grid-stride over warps): for every cache of the call it
-// moves the token's K and V rows into the page slot, four 16-byte chunks per
-// lane in flight, and weights the pieces it moved; the token's total over
-// all caches goes into its block's running word with one atomic add.
-__global__ void __launch_bounds__(kWriteThreads)
+// A warp per token (grid-stride over warps): for every cache of the launch
+// it moves the token's K and V rows into the page slot and weights the
+// pieces it moved; the token's total over those caches goes into its block's
+// running word with one atomic add.  One instance per layout family (NHD
+// and latent, HND, x-split); a call with several families makes one launch
+// per family.
+template <int kLayout>
+__global__ void __launch_bounds__(kWriteThreads, 2)
     kvcs_write_kernel(const __grid_constant__ WriteParams w) {
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (kWriteThreads / 32);
@@ -1087,50 +1157,8 @@ __global__ void __launch_bounds__(kWriteThreads)
     for (int ci = 0; ci < w.num_caches; ++ci) {
       const DevCache &C = w.c[ci];
       const long long row = static_cast<long long>(C.heads) * C.hb;
-      const u64 tP = static_cast<u64>(t) * static_cast<u64>(C.P);
-      for (int half = 0; half < C.halves; ++half) {
-        const unsigned char *src = (half ? w.value[ci] : w.key[ci]) + i * row;
-        unsigned char *page = const_cast<unsigned char *>(C.base) + half * C.half_stride +
-                              b * C.block_stride;
-        const u64 hp = static_cast<u64>(half) * (C.hb >> 3);
-        for (long long base = static_cast<long long>(lane) * ch; base < row;
-             base += 4LL * 32 * ch) {
-          // up to four chunks per lane, loads first
-          uint4 v[4];
-          long long offs[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            offs[k] = base + static_cast<long long>(k) * 32 * ch;
-            if (offs[k] < row) {
-              if (ch == 16) {
-                v[k] = *reinterpret_cast<const uint4 *>(src + offs[k]);
-              } else {
-                const u64 x = *reinterpret_cast<const u64 *>(src + offs[k]);
-                v[k] = make_uint4(static_cast<u32>(x), static_cast<u32>(x >> 32), 0u, 0u);
-              }
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const long long off = offs[k];
-            if (off >= row) break;
-            const long long h = C.hb_shift >= 0 ? (off >> C.hb_shift) : off / C.hb;
-            const long long e = off - h * C.hb;
-            unsigned char *dst = page + write_offset(C, bs, o, h, e);
-            const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
-            const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
-            const u64 w0 = 2ull * (tP + static_cast<u64>(e >> 3) + hp) + 1ull;
-            if (ch == 16) {
-              *reinterpret_cast<uint4 *>(dst) = v[k];
-              const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
-              acc += mh * (x0 * w0 + x1 * (w0 + 2ull));
-            } else {
-              *reinterpret_cast<u64 *>(dst) = x0;
-              acc += mh * (x0 * w0);
-            }
-          }
-        }
-      }
+      acc += write_token_rows<kLayout>(C, w.key[ci] + i * row, w.value[ci] + i * row, bs, b, o,
+                                       static_cast<u64>(t), ch, lane);
     }
     if (w.block_sums != nullptr && t >= 0) {
       acc = warp_sum(acc);

@@ -152,3 +152,91 @@ def test_all_layers_in_one_call_equals_layer_by_layer():
     assert torch.equal(sa, sb)
     for ca, cb in zip(a, b):
         assert torch.equal(ca.pool, cb.pool)
+
+
+def _oracle_sums(caches, refs, bs, tables, lengths):
+    """Oracle block checksums of the blocks in `tables` from canonical pools."""
+    ocaches = []
+    for c, r in zip(caches, refs):
+        lay = W.LAYOUT_LATENT if c.layout == W.LAYOUT_LATENT else W.LAYOUT_NHD
+        ocaches.append(OracleCache(host_bytes(r), c.num_blocks, lay, c.layer, c.head_offset,
+                                   c.num_heads, c.head_bytes))
+    po = [0]
+    for tb in tables:
+        po.append(po[-1] + len(tb))
+    reqs = OracleRequests(po, [0] * len(lengths), lengths, [b for tb in tables for b in tb])
+    exp, _ = c_form(ocaches, bs, reqs)
+    return reqs.block_ids, exp
+
+
+def test_mixed_layouts_in_one_call():
+    """NHD, HND in kernel sub-blocks, x-split and latent caches written by one
+    call (one launch per layout family) add into the same running words."""
+    bs, nb = 16, 10
+    specs = [(W.LAYOUT_NHD, 4, 64, 0), (W.LAYOUT_HND, 4, 32, 4), (W.LAYOUT_XSPLIT, 2, 48, 0),
+             (W.LAYOUT_LATENT, 1, 72, 0), (W.LAYOUT_NHD, 2, 16, 0)]
+    caches = []
+    for li, (lay, heads, hb, kbs) in enumerate(specs):
+        halves = 1 if lay == W.LAYOUT_LATENT else 2
+        caches.append(W.CacheSpec(torch.zeros(halves * nb * bs * heads * hb, dtype=torch.uint8,
+                                              device=DEV), nb, lay, li, 0, heads, hb,
+                                  kernel_block_size=kbs))
+    lengths = [40, 23]
+    g = torch.Generator().manual_seed(5)
+    ids = torch.randperm(nb, generator=g).tolist()
+    tables = [ids[0:3], ids[3:5]]
+    sel = [(r, t) for r, n in enumerate(lengths) for t in range(n)]
+    slots = torch.tensor([tables[r][t // bs] * bs + t % bs for r, t in sel], device=DEV)
+    pos = torch.tensor([t for _, t in sel], device=DEV)
+    n = len(sel)
+    keys, vals = [], []
+    for c in caches:
+        if c.layout == W.LAYOUT_LATENT:
+            keys.append(torch.randint(0, 256, (n, c.head_bytes), dtype=torch.uint8,
+                                      generator=g).to(DEV))
+            vals.append(None)
+        else:
+            keys.append(torch.randint(0, 256, (n, c.num_heads, c.head_bytes), dtype=torch.uint8,
+                                      generator=g).to(DEV))
+            vals.append(torch.randint(0, 256, (n, c.num_heads, c.head_bytes),
+                                      dtype=torch.uint8, generator=g).to(DEV))
+    sums = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    K.write_kv(caches, bs, keys, vals, slots, pos, block_sums=sums)
+    torch.cuda.synchronize()
+    refs = [to_canonical(c, bs).contiguous() for c in caches]
+    block_ids, exp = _oracle_sums(caches, refs, bs, tables, lengths)
+    got = u64(sums)
+    for q, b in enumerate(block_ids):
+        assert got[b] == np.uint64(exp[q]), (q, b)
+    # the written rows landed where the layouts put them
+    sl = slots.cpu()
+    for c, k, v, r in zip(caches, keys, vals, refs):
+        if c.layout == W.LAYOUT_LATENT:
+            assert torch.equal(r[sl // bs, sl % bs].cpu(), k.cpu())
+        else:
+            assert torch.equal(r[0, sl // bs, sl % bs].cpu(), k.cpu())
+            assert torch.equal(r[1, sl // bs, sl % bs].cpu(), v.cpu())
+
+
+def test_more_caches_than_one_launch_holds():
+    """70 caches of one family take two launches; the words still add up."""
+    bs, nb, layers, hb = 8, 6, 70, 16
+    g = torch.Generator().manual_seed(8)
+    caches = [W.CacheSpec(torch.zeros(nb * bs * hb, dtype=torch.uint8, device=DEV), nb,
+                          W.LAYOUT_LATENT, li, 0, 1, hb) for li in range(layers)]
+    lengths = [13]
+    tables = [[4, 1]]
+    slots = torch.tensor([tables[0][t // bs] * bs + t % bs for t in range(13)], device=DEV)
+    pos = torch.arange(13, device=DEV)
+    keys = [torch.randint(0, 256, (13, hb), dtype=torch.uint8, generator=g).to(DEV)
+            for _ in range(layers)]
+    sums = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    l0 = K.launch_count()
+    K.write_kv(caches, bs, keys, [None] * layers, slots, pos, block_sums=sums)
+    torch.cuda.synchronize()
+    assert K.launch_count() - l0 == 2
+    refs = [to_canonical(c, bs).contiguous() for c in caches]
+    block_ids, exp = _oracle_sums(caches, refs, bs, tables, lengths)
+    got = u64(sums)
+    for q, b in enumerate(block_ids):
+        assert got[b] == np.uint64(exp[q]), (q, b)
