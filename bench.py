@@ -229,11 +229,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, units_per_launch: int):
+def profiled_traffic(workload: str, units_per_launch: int, kernel: str = "kvcs_bulk_kernel"):
     """DRAM bytes per launch from the committed ncu summary of this workload's
     kernel, scaled to this launch by units processed; None when the summary
     is missing or was taken on different kernel sources."""
-    f = ROOT / "profiles" / f"kvcs_bulk_kernel_{workload}.md"
+    f = ROOT / "profiles" / f"{kernel}_{workload}.md"
     if not f.exists():
         return None
     text = f.read_text()
@@ -410,7 +410,8 @@ def run_write(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     layers, heads, hb, bs = 32, 8, 256, 16
-    R, L = 32, 512                         # requests x new tokens each
+    # requests x new tokens each; the small case is the profiling size
+    R, L = (8, 512) if args.config == "llama3_8b_write_small" else (32, 512)
     g = torch.Generator().manual_seed(args.seed + rank)
     nb = R * L // bs + 64
     perm = torch.randperm(nb, generator=g)
@@ -459,13 +460,19 @@ def run_write(args, ws, rank, local):
         ck(out, None, raw)
 
     launches0 = kvcs.launch_count()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    t_wall0 = time.time()
     t_fused = timed(fused, args.steps)
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
     launches = (kvcs.launch_count() - launches0) // (args.steps + max(3, args.warmup))
     t_plain = timed(plain, args.steps)
     t_unfused = timed(unfused, args.steps)
     moved = 2 * n * layers * 2 * heads * hb          # bytes read + written
     if rank != 0:
         return
+    peak, peak_kind = measured_peak()
+    achieved = moved / t_fused / 1e9
     line = {"metric": "KV write fused with the block checksum, GB/s of bytes read + written",
             "value": round(moved / t_fused / 1e9, 2), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
@@ -474,8 +481,17 @@ def run_write(args, ws, rank, local):
             "config": {"workload": "llama3_8b_prefill_write", "layers": layers,
                        "kv_heads": heads, "head_bytes": hb, "block_size": bs,
                        "requests": R, "new_tokens_per_request": L,
-                       "bytes_moved_per_step": moved},
+                       "bytes_moved_per_step": moved,
+                       "l2": "new K/V and written pages far above the 129 MB L2; no flush"},
             "gpu_launches_per_step": launches,
+            "gpu_launches": launches * args.steps,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": profiled_traffic("llama3_8b_write", n,
+                                                     kernel="kvcs_write_kernel"),
+                         "kernel": "kvcs_write_kernel", "launch_ms": round(t_fused * 1e3, 4)},
+            "clocks": clocks,
             "write_only_ms": round(t_plain * 1e3, 4),
             "write_then_checksum_ms": round(t_unfused * 1e3, 4),
             "fused_vs_write_only": round(t_plain / t_fused, 4),
@@ -733,7 +749,7 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, ws, rank)
-        elif args.config == "llama3_8b_write":
+        elif args.config in ("llama3_8b_write", "llama3_8b_write_small"):
             run_write(args, ws, rank, local)
         else:
             run_ours(args, ws, rank, local)
