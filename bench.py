@@ -654,10 +654,13 @@ def run_ours(args, ws, rank, local):
 
 
 def run_e2e(args, wl, dev, stream, ws, ck):
-    """Each step: pinned host -> device copies of every KV pool (spread over
-    several copy streams, so several copy engines work at once) and of the
-    request tables, the checksum call, and a device -> host read of the
-    checksums and the status word."""
+    """Each step: pinned host -> device copies of every KV pool and of the
+    request tables, the checksum, and a device -> host read of the checksums
+    and the status word.  The layers arrive in ``--e2e-groups`` groups, as a
+    layer-wise KV load delivers them: each group's checksum is added into the
+    position words (KVCS_OUT_ACCUMULATE) as soon as that group has landed,
+    while the next group is still on the host link."""
+    import paged_kv_cache_kvcs_gb300 as kvcs
     host_pools = [torch.empty(c.pool.numel(), dtype=torch.uint8, pin_memory=True)
                   for c in wl.caches]
     for h, c in zip(host_pools, wl.caches):
@@ -671,25 +674,31 @@ def run_e2e(args, wl, dev, stream, ws, ck):
     h2d = sum(h.numel() for h in host_pools) + sum(t.numel() * t.element_size() for t in host_tabs)
     d2h = host_out.numel() * 8 + 4
     steps = max(1, min(args.steps, args.e2e_steps))
-    copy_streams = [torch.cuda.Stream(dev) for _ in range(max(1, args.copy_streams))]
+    ngroups = max(1, min(args.e2e_groups, len(wl.caches)))
+    bounds = [len(wl.caches) * g // ngroups for g in range(ngroups + 1)]
+    groups = [list(range(bounds[g], bounds[g + 1])) for g in range(ngroups)]
+    group_ck = [kvcs.Checksummer([wl.caches[i] for i in grp], wl.block_size, wl.pos_offsets,
+                                 wl.first_position, wl.num_tokens, wl.block_ids,
+                                 wl.num_positions) for grp in groups]
+    copy_stream = torch.cuda.Stream(dev)
     raw = stream.cuda_stream
 
     def one():
         go = torch.cuda.Event()
         go.record(stream)                 # the previous step's reads are done
-        for i, (h, c) in enumerate(zip(host_pools, wl.caches)):
-            cs = copy_streams[i % len(copy_streams)]
-            cs.wait_event(go)
-            with torch.cuda.stream(cs):
-                c.pool.copy_(h, non_blocking=True)
-        for h, t in zip(host_tabs, tabs):
-            t.copy_(h, non_blocking=True)
-        for cs in copy_streams:
-            done = torch.cuda.Event()
-            done.record(cs)
-            stream.wait_event(done)
+        copy_stream.wait_event(go)
+        with torch.cuda.stream(copy_stream):
+            for h, t in zip(host_tabs, tabs):
+                t.copy_(h, non_blocking=True)
         status.zero_()
-        ck(out, status, raw)
+        for g, grp in enumerate(groups):
+            with torch.cuda.stream(copy_stream):
+                for i in grp:
+                    wl.caches[i].pool.copy_(host_pools[i], non_blocking=True)
+            landed = torch.cuda.Event()
+            landed.record(copy_stream)
+            stream.wait_event(landed)
+            group_ck[g](out, status, raw, accumulate=g > 0)
         host_out.copy_(out, non_blocking=True)
         host_status.copy_(status, non_blocking=True)
 
@@ -713,8 +722,9 @@ def run_e2e(args, wl, dev, stream, ws, ck):
     return {"value": round(total / secs / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps, "ms_per_step": round(secs / steps * 1e3, 3),
-            "copy_streams": len(copy_streams),
-            "what": "pinned-host KV pools + block tables -> device, checksum, "
+            "layer_groups": ngroups,
+            "what": "pinned-host KV pools + block tables -> device in layer groups, "
+                    "each group checksummed (accumulating) as it lands, "
                     "checksums -> pinned host, every step"}
 
 
@@ -728,7 +738,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--copy-streams", type=int, default=4)
+    ap.add_argument("--e2e-groups", type=int, default=8,
+                    help="layer groups the end-to-end load delivers and checksums")
     ap.add_argument("--sweep", action="store_true",
                     help="also time the first 1, 2, 4, ... requests alone")
     ap.add_argument("--layout", default="nhd",

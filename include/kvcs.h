@@ -208,10 +208,22 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
  * each row's partials summed (KVChecksumGroup, field stored), XORed with the
  * block's tag (function block_checksum_tags) so that it matches only the
  * block it was stored for.
+ *
+ * KVCS_OUT_ACCUMULATE in flags adds this call's partials into values
+ * (mod 2^64) instead of overwriting them.  Block checksums are sums over
+ * layers (the checksum page, item 2), so a caller that receives KV layer by
+ * layer (the connector page: start_load_kv with per-layer events,
+ * wait_for_layer_load) can checksum each layer group as it lands, on the
+ * stream that waits for that group, and end with the full checksum.  A
+ * position with no valid token, or with a bad block id, then adds nothing.
+ * Row sums, tags and the comparison, when asked for, are computed from
+ * values as they stand after the add.
  */
+#define KVCS_OUT_ACCUMULATE 1
+
 typedef struct kvcs_outputs {
   int32_t num_columns;       /* >= 1 and <= 64 */
-  int32_t reserved;          /* must be 0 */
+  int32_t flags;             /* 0 or KVCS_OUT_ACCUMULATE; other bits invalid */
   uint64_t *values;          /* required: [total_positions][num_columns] */
   uint64_t *row_sums;        /* or NULL: [total_positions], sum of the row's
                                 values XOR tags[i] (when tags is given) */

@@ -29,6 +29,8 @@ KVCS_STATUS_BAD_BLOCK_ID = 1
 KVCS_STATUS_BAD_REQUESTS = 2
 KVCS_STATUS_TIMEOUT = 4
 
+KVCS_OUT_ACCUMULATE = 1
+
 
 class kvcs_cache(ctypes.Structure):
     _fields_ = [("base", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
@@ -40,7 +42,7 @@ class kvcs_cache(ctypes.Structure):
 
 
 class kvcs_outputs(ctypes.Structure):
-    _fields_ = [("num_columns", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    _fields_ = [("num_columns", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("values", ctypes.c_void_p), ("row_sums", ctypes.c_void_p),
                 ("tags", ctypes.c_void_p), ("expected", ctypes.c_void_p),
                 ("mismatch", ctypes.c_void_p), ("mismatch_count", ctypes.c_void_p)]
@@ -276,11 +278,23 @@ class Checksummer:
                                   first_position.data_ptr(), num_tokens.data_ptr(),
                                   block_ids.data_ptr())
         self._fn = load_library().kvcs_block_checksums
+        self._group_fn = load_library().kvcs_group_checksums
         self._reqs_ref = ctypes.byref(self.reqs)
 
-    def __call__(self, out, status=None, stream: int | None = None):
+    def __call__(self, out, status=None, stream: int | None = None, accumulate: bool = False):
         """Enqueue one call writing ``out`` (int64/uint64 CUDA tensor of at
-        least ``total_positions`` words) on ``stream`` (a raw handle)."""
+        least ``total_positions`` words) on ``stream`` (a raw handle);
+        ``accumulate`` adds this call's checksums into ``out`` instead."""
+        if accumulate:
+            outs = kvcs_outputs(1, KVCS_OUT_ACCUMULATE,
+                                out.data_ptr() if self.total_positions > 0 else None)
+            rc = self._group_fn(self.caches, self.num_caches, self.block_size, self._reqs_ref,
+                                self.total_positions, ctypes.byref(outs),
+                                status.data_ptr() if status is not None else None,
+                                stream or None)
+            if rc != KVCS_OK:
+                raise KvcsError(rc, "kvcs_group_checksums")
+            return out
         rc = self._fn(self.caches, self.num_caches, self.block_size, self._reqs_ref,
                       self.total_positions,
                       out.data_ptr() if self.total_positions > 0 else None,
@@ -329,12 +343,13 @@ def group_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
                     num_tokens, block_ids, num_columns: int, values=None,
                     row_sums=None, tags=None, expected=None, mismatch=None,
                     mismatch_count=None, status=None, stream=None,
-                    total_positions: int | None = None):
+                    total_positions: int | None = None, accumulate: bool = False):
     """Torch front end of ``kvcs_group_checksums``.  Each cache names its
     replica-key ``column``; returns ``values`` (int64 CUDA tensor
     ``[total_positions, num_columns]`` holding uint64 bits).  ``row_sums``,
     ``tags``, ``expected`` are int64 CUDA tensors of ``total_positions``;
-    ``mismatch`` a uint8 one; ``mismatch_count`` an int32 one-element one."""
+    ``mismatch`` a uint8 one; ``mismatch_count`` an int32 one-element one.
+    ``accumulate`` adds the partials into the given ``values``."""
     import torch
     for c in caches:
         _check_pool(c, block_size)
@@ -342,9 +357,12 @@ def group_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
         total_positions = int(pos_offsets[-1].item())
     dev = pos_offsets.device
     if values is None:
+        if accumulate:
+            raise ValueError("accumulate needs the values to add into")
         values = torch.empty((max(total_positions, 0), num_columns), dtype=torch.int64,
                              device=dev)
-    outs = kvcs_outputs(num_columns, 0, values.data_ptr() if total_positions > 0 else None,
+    outs = kvcs_outputs(num_columns, KVCS_OUT_ACCUMULATE if accumulate else 0,
+                        values.data_ptr() if total_positions > 0 else None,
                         _ptr(row_sums), _ptr(tags), _ptr(expected), _ptr(mismatch),
                         _ptr(mismatch_count))
     reqs = kvcs_requests(pos_offsets.numel() - 1, pos_offsets.data_ptr(),

@@ -299,7 +299,7 @@ struct Plan {
 };
 
 Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
-               int64_t total_positions, int sms) {
+               int64_t total_positions, int sms, bool accumulate = false) {
   Plan pl;
   std::vector<kvcs_cache> fam[4], gen;
   std::vector<kvcs_cache> bulk;
@@ -323,7 +323,8 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
     }
   }
   pl.kernel = gen.empty() ? 0 : (bulk.empty() ? 1 : 2);
-  pl.all_atomic = pl.launches.size() > 1 || !gen.empty();
+  // accumulating calls add every result into the caller's values
+  pl.all_atomic = accumulate || pl.launches.size() > 1 || !gen.empty();
   if (sms < 1) sms = 1;
   if (!bulk.empty()) {
     bool first = true;
@@ -357,7 +358,8 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
     pl.generic_grid = static_cast<int>(std::max<long long>(
         1, std::min<long long>(static_cast<long long>(sms) * 8, items)));
   }
-  pl.memset = total_positions > 0 && (pl.all_atomic || (!bulk.empty() && pl.split));
+  pl.memset = !accumulate && total_positions > 0 &&
+              (pl.all_atomic || (!bulk.empty() && pl.split));
   return pl;
 }
 
@@ -365,7 +367,8 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
 int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block_size,
                   const kvcs_requests *reqs, int64_t total_positions,
                   const kvcs_outputs *outs, uint32_t *status, cudaStream_t st) {
-  if (!outs || outs->reserved != 0) return KVCS_EINVAL;
+  if (!outs || (outs->flags & ~KVCS_OUT_ACCUMULATE) != 0) return KVCS_EINVAL;
+  const bool accumulate = (outs->flags & KVCS_OUT_ACCUMULATE) != 0;
   const int ncols = outs->num_columns;
   int rc = validate_caches(caches_in, num_caches, block_size, ncols);
   if (rc != KVCS_OK) return rc;
@@ -379,7 +382,8 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
 
   int sms = 0;
   if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
-  const Plan pl = make_plan(by_column(caches_in, num_caches), block_size, total_positions, sms);
+  const Plan pl = make_plan(by_column(caches_in, num_caches), block_size, total_positions, sms,
+                            accumulate);
 
   if (pl.memset) {
     if (cudaMemsetAsync(outs->values, 0,

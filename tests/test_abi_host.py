@@ -30,6 +30,17 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, name), name
 
 
+def test_header_constants_match_the_binding():
+    text = HEADER.read_text()
+    consts = {m.group(1): int(m.group(2).rstrip("u"))
+              for m in re.finditer(r"#define (KVCS_[A-Z_]+) \(?(-?[0-9]+u?)\)?", text)}
+    consts.update({m.group(1): int(m.group(2))
+                   for m in re.finditer(r"(KVCS_LAYOUT_[A-Z]+) = ([0-9]+)", text)})
+    assert len(consts) >= 15, consts
+    for name, value in consts.items():
+        assert getattr(B, name) == value, name
+
+
 def test_version_and_strerror():
     assert K.version() >> 16 == 1
     for code in (K.KVCS_OK, K.KVCS_EINVAL, K.KVCS_EUNSUPPORTED, K.KVCS_ECUDA, 99):
@@ -197,6 +208,10 @@ def test_group_and_tags_reject_bad_arguments_without_cuda():
     assert lib.kvcs_group_checksums(arr, 2, 16, ctypes.byref(reqs), 4,
                                     ctypes.byref(outs), None, None) == K.KVCS_EINVAL
     outs = B.kvcs_outputs(65, 0, 128, None, None, None, None, None)
+    assert lib.kvcs_group_checksums(arr, 2, 16, ctypes.byref(reqs), 4,
+                                    ctypes.byref(outs), None, None) == K.KVCS_EINVAL
+    # unknown output flags
+    outs = B.kvcs_outputs(2, 2, 128, None, None, None, None, None)
     assert lib.kvcs_group_checksums(arr, 2, 16, ctypes.byref(reqs), 4,
                                     ctypes.byref(outs), None, None) == K.KVCS_EINVAL
     assert lib.kvcs_block_checksum_tags(64, 4, 3, 0, 128, None) == K.KVCS_EINVAL
