@@ -65,6 +65,8 @@ def make_workload(name: str, seed: int, device):
         return W.tiny(seed, device)
     if name == "mamba2":                # Mamba2-shaped running states, 10.9 GB
         return W.mamba2(seed, device)
+    if name == "mamba2_small":          # 16 requests, 2.7 GB: ncu captures
+        return W.mamba2(seed, device, num_requests=16)
     raise SystemExit(f"unknown config {name}")
 
 

@@ -922,6 +922,53 @@ __device__ __forceinline__ u64 load_piece(const unsigned char *p, int bytes) {
   return __ldg(reinterpret_cast<const unsigned short *>(p));
 }
 
+// A state block whose rows are short, read as a flat run of 16-byte chunks
+// (the block starts 16-byte aligned and its size is a multiple of 16): the
+// chunk's elements are walked in order, each weighted 2e+1 by its index e
+// within its row, and a row's part is multiplied by the row factor when the
+// row ends or the chunk does.  Element sizes 2 and 4 divide 16, so no
+// element straddles two chunks.
+template <int kPb>
+__device__ __forceinline__ u64 state_chunk_sum(const uint4 v, long long c, u32 epr, u64 m0) {
+  constexpr u32 kEpc = 16 / kPb;  // elements per chunk
+  const u32 w[4] = {v.x, v.y, v.z, v.w};
+  const u32 e0 = static_cast<u32>(c) * kEpc;
+  const u32 row = e0 / epr;
+  u32 e = e0 - row * epr;
+  u64 mrow = m0 + 2ull * row;
+  u64 part = 0, acc = 0;
+#pragma unroll
+  for (u32 k = 0; k < kEpc; ++k) {
+    const u32 x = kPb == 2 ? (w[k >> 1] >> ((k & 1) * 16)) & 0xffffu : w[k];
+    part += static_cast<u64>(x) * (2u * e + 1u);
+    if (++e == epr) {
+      acc += mrow * part;
+      part = 0;
+      e = 0;
+      mrow += 2ull;
+    }
+  }
+  return acc + mrow * part;
+}
+
+template <int kPb>
+__device__ __forceinline__ u64 state_flat_sum(const unsigned char *blk, long long nchunks,
+                                              u32 epr, u64 m0, int tid) {
+  const uint4 *src = reinterpret_cast<const uint4 *>(blk);
+  u64 acc = 0;
+  long long c = tid;
+  // four chunks per thread in flight
+  for (; c + 3 * kGenericThreads < nchunks; c += 4 * kGenericThreads) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = __ldg(src + c + k * kGenericThreads);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc += state_chunk_sum<kPb>(v[k], c + k * kGenericThreads, epr, m0);
+  }
+  for (; c < nchunks; c += kGenericThreads) acc += state_chunk_sum<kPb>(__ldg(src + c), c, epr, m0);
+  return acc;
+}
+
 __global__ void __launch_bounds__(kGenericThreads)
     kvcs_generic_kernel(const __grid_constant__ Params p) {
   __shared__ u64 red[kGenericThreads / 32];
@@ -959,8 +1006,14 @@ __global__ void __launch_bounds__(kGenericThreads)
       if (q == 0) {
         const long long P = C.P;
         const unsigned char *blk = C.base + b * C.block_stride;
-        if (P <= 64) {
-          // short rows (e.g. conv states): one row per thread
+        const long long bytes = static_cast<long long>(C.heads) * C.hb;
+        if (P <= 64 && (reinterpret_cast<uintptr_t>(blk) & 15) == 0 && (bytes & 15) == 0 &&
+            bytes / C.pbytes < (1LL << 31)) {
+          // short rows (e.g. conv states), aligned: flat 16-byte chunks
+          acc = C.pbytes == 2 ? state_flat_sum<2>(blk, bytes >> 4, static_cast<u32>(P), C.m0, tid)
+                              : state_flat_sum<4>(blk, bytes >> 4, static_cast<u32>(P), C.m0, tid);
+        } else if (P <= 64) {
+          // short rows, unaligned: one row per thread
           for (long long row = tid; row < C.heads; row += kGenericThreads) {
             const unsigned char *rp = blk + row * C.hb;
             u64 s = 0;

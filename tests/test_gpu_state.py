@@ -66,6 +66,22 @@ def test_whole_position_mode_and_the_position_rule():
     assert got[0] != 0 and got[4] != 0
 
 
+@pytest.mark.parametrize("row,pb,rows", [
+    (6, 2, 64), (6, 2, 8), (2, 2, 40), (12, 4, 4), (20, 4, 36), (62, 2, 24), (4, 4, 100),
+    (6, 2, 50), (12, 4, 5), (10, 2, 7), (6, 2, 4096), (12, 4, 2048)])
+def test_short_state_rows_generic_kernel(row, pb, rows):
+    """Short rows in the generic kernel: blocks whose size is a multiple of
+    16 bytes are read as flat 16-byte chunks, others one row per thread."""
+    g = torch.Generator(device=DEV).manual_seed(row * 1000 + rows)
+    base = small(8, num_requests=5)
+    nb = base.caches[0].num_blocks
+    caches = [W.CacheSpec(W.fill_bytes(nb * rows * row, W.BITS16, g, torch.device(DEV)), nb,
+                          W.LAYOUT_STATE, li, 5, rows, row, piece_bytes=pb) for li in range(3)]
+    wl = W.Workload("short", 16, caches, base.pos_offsets, base.first_position,
+                    base.num_tokens, base.block_ids)
+    check(wl, kernel=1)
+
+
 def test_unknown_split_is_one_row_per_shard():
     # a whole shard's state (here 96 KiB) as a single row
     g = torch.Generator(device=DEV).manual_seed(6)
