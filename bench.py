@@ -498,6 +498,14 @@ def run_write(args, ws, rank, local):
             "write_then_checksum_ms": round(t_unfused * 1e3, 4),
             "fused_vs_write_only": round(t_plain / t_fused, 4),
             "fused_vs_write_then_checksum": round(t_unfused / t_fused, 4)}
+    if ws == 1 and not args.no_cpu_baseline:
+        # the oracle computing the same block words from the written pages
+        cores = host_cores()
+        wl = W.Workload("llama3_8b_prefill_write", bs, caches, po, fp, nt, bids)
+        gbs, bps, desc = oracle_timed(wl, args.cpu_seconds, cores, args.seed)
+        line["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s of written KV checksummed",
+                                "cores": cores, "kind": "oracle", "blocks_per_s": round(bps, 2),
+                                "sample": desc}
     print(json.dumps(line), flush=True)
 
 
@@ -538,11 +546,13 @@ def run_ours(args, ws, rank, local):
                           mismatch=torch.empty(n, dtype=torch.uint8, device=dev),
                           mismatch_count=torch.zeros(1, dtype=torch.int32, device=dev))
 
+        n_pos = wl.num_positions       # read once: the property syncs the device
+
         def step():
             kvcs.group_checksums(wl.caches, wl.block_size, wl.pos_offsets,
                                  wl.first_position, wl.num_tokens, wl.block_ids, ncols,
                                  values=values, status=status, stream=raw_stream,
-                                 total_positions=wl.num_positions, **extras)
+                                 total_positions=n_pos, **extras)
         ck = None
     else:
         ck = kvcs.workload_checksummer(wl)

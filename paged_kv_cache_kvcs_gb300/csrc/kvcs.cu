@@ -48,7 +48,8 @@ cudaError_t device_setup(int *sms) {
     for (const void *fn : {reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamXSplit>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamState>)})
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamState>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndSub>)})
       if (d.err == cudaSuccess)
         d.err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kSmemLimit);
@@ -263,9 +264,11 @@ int group_warps_for(int stages) {
 }
 
 // Layout family of a cache (which instance of the bulk kernel stages it).
-int family_of(const kvcs_cache &c) {
+int family_of(const kvcs_cache &c, int block_size) {
   switch (c.layout) {
-    case KVCS_LAYOUT_HND: return kFamHnd;
+    case KVCS_LAYOUT_HND:
+      return c.kernel_block_size > 0 && c.kernel_block_size != block_size ? kFamHndSub
+                                                                          : kFamHnd;
     case KVCS_LAYOUT_XSPLIT: return kFamXSplit;
     case KVCS_LAYOUT_STATE: return kFamState;
     default: return kFamRows;
@@ -301,11 +304,11 @@ struct Plan {
 Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
                int64_t total_positions, int sms, bool accumulate = false) {
   Plan pl;
-  std::vector<kvcs_cache> fam[4], gen;
+  std::vector<kvcs_cache> fam[kNumFamilies], gen;
   std::vector<kvcs_cache> bulk;
   for (const kvcs_cache &c : sorted) {
     if (bulk_eligible(c, block_size)) {
-      fam[family_of(c)].push_back(c);
+      fam[family_of(c, block_size)].push_back(c);
       bulk.push_back(c);
     } else {
       gen.push_back(c);
@@ -314,11 +317,11 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
         (c.layout == KVCS_LAYOUT_LATENT || c.layout == KVCS_LAYOUT_STATE) ? 1 : 2;
     pl.kv_bytes_max += halves * page_bytes_of(c, block_size) * total_positions;
   }
-  for (int f = 0; f <= 4; ++f) {
-    const std::vector<kvcs_cache> &set = f < 4 ? fam[f] : gen;
+  for (int f = 0; f <= kNumFamilies; ++f) {
+    const std::vector<kvcs_cache> &set = f < kNumFamilies ? fam[f] : gen;
     for (size_t lo = 0; lo < set.size(); lo += kMaxCachesPerLaunch) {
       const size_t hi = std::min(set.size(), lo + kMaxCachesPerLaunch);
-      pl.launches.push_back({f == 4, f < 4 ? f : 0,
+      pl.launches.push_back({f == kNumFamilies, f < kNumFamilies ? f : 0,
                              std::vector<kvcs_cache>(set.begin() + lo, set.begin() + hi)});
     }
   }
@@ -444,6 +447,7 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
         case kFamHnd: kvcs_bulk_kernel<kFamHnd><<<gd, kBulkThreads, smem, st>>>(p); break;
         case kFamXSplit: kvcs_bulk_kernel<kFamXSplit><<<gd, kBulkThreads, smem, st>>>(p); break;
         case kFamState: kvcs_bulk_kernel<kFamState><<<gd, kBulkThreads, smem, st>>>(p); break;
+        case kFamHndSub: kvcs_bulk_kernel<kFamHndSub><<<gd, kBulkThreads, smem, st>>>(p); break;
         default: kvcs_bulk_kernel<kFamRows><<<gd, kBulkThreads, smem, st>>>(p); break;
       }
     } else {

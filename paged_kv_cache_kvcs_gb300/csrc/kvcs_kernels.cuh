@@ -57,9 +57,16 @@ constexpr int kLayoutState = 4;
 // its own staging and reduction code (a kernel holding every path ran the
 // common NHD case 11% slower).
 constexpr int kFamRows = 0;    // NHD and latent: rows of a page
-constexpr int kFamHnd = 1;     // HND: heads of a page (optionally sub-blocked)
+constexpr int kFamHnd = 1;     // HND: heads of a page
 constexpr int kFamXSplit = 2;  // x-split: heads of 16-byte chunks
 constexpr int kFamState = 3;   // Mamba states: rows of a state
+constexpr int kFamHndSub = 4;  // HND in kernel sub-blocks: heads of each sub-block
+constexpr int kNumFamilies = 5;
+
+// Families whose units are runs of whole heads, all block_size slots of them.
+__host__ __device__ constexpr bool head_family(int fam) {
+  return fam == kFamHnd || fam == kFamHndSub || fam == kFamXSplit;
+}
 
 constexpr u32 kStatusBadBlockId = 1u;
 constexpr u32 kStatusBadRequests = 2u;
@@ -537,7 +544,7 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
         // at a group-dependent slot so a warp's reads spread over the banks
         const unsigned char *gp = stage + static_cast<size_t>(g) * bsi * 16;
         accum_slots_rotated(gp, g % nv, nv, S, T, U);
-      } else if (C.kbs == bsi) {
+      } else if constexpr (kFam == kFamHnd) {
         accum_slots(stage + static_cast<size_t>(hl) * bsi * C.hb + (col << 4),
                     static_cast<size_t>(C.hb), 0, nv, 0, S, T, U);
       } else {
@@ -696,12 +703,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           int count;
           u32 pbytes;   // bytes copied per page of the unit
           u32 pstride;  // bytes a page of the unit occupies in the stage
-          if constexpr (kFam == kFamHnd || kFam == kFamXSplit) {
+          if constexpr (head_family(kFam)) {
             // whole-slot runs of the unit's heads, staged as in memory
             count = max(0, min(C.rpu, C.heads - first));
             pstride = static_cast<u32>(count) * static_cast<u32>(bs) * static_cast<u32>(C.hb);
             pbytes = pstride;
-            if (kFam == kFamHnd && C.kbs != bs) {
+            if constexpr (kFam == kFamHndSub) {
               const int nsb = (cur.nv + C.kbs - 1) / C.kbs;  // sub-blocks with valid slots
               pbytes = static_cast<u32>(count) * static_cast<u32>(nsb * C.kbs) *
                        static_cast<u32>(C.hb);
@@ -739,7 +746,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               const unsigned char *page = D.base +
                   static_cast<long long>(phalf) * D.half_stride +
                   cur.block * D.block_stride;
-              if (kFam == kFamHnd && D.kbs != bs) {
+              if constexpr (kFam == kFamHndSub) {
                 // [sub-block][heads][kbs][hb]: in each sub-block that holds
                 // valid slots the unit's heads are one contiguous run; when
                 // the unit has every head those runs are one range
@@ -754,7 +761,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                                       static_cast<u64>(first) * D.kbs * D.hb,
                                   run, fb, policy);
                 }
-              } else if (kFam == kFamHnd || kFam == kFamXSplit) {
+              } else if constexpr (head_family(kFam)) {
                 // [heads][block_size][hb] or [heads][chunks][block_size][16]:
                 // the unit's heads are one contiguous run of whole slots
                 ptx::bulk_g2s(dst, page + static_cast<u64>(first) * bs * D.hb, pstride,
@@ -875,7 +882,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       const DevCache &C = p.caches[ci];
       if (C.rowb != map.rowb) make_map(map, C.rowb, gtid, gw * 32);
       v += unit_sum<kFam>(C, m, half, sp, map, bsz);
-      sp += (kFam == kFamHnd || kFam == kFamXSplit)
+      sp += head_family(kFam)
                 ? static_cast<size_t>(m.count) * static_cast<size_t>(bsz) * C.hb
                 : static_cast<size_t>(m.count) * C.rowb;
       if (++half == C.halves) {
