@@ -451,24 +451,40 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
     const int nrows = m.count;
     const u32 r0 = static_cast<u32>(m.first);
     const u64 per = static_cast<u64>(16 / C.pbytes);
+    const bool two = C.pbytes == 2;
+    auto column = [two](const uint4 v, u64 &A, u64 &Bk) {
+      if (two) {
+        A = (v.x & 0xffffu) + (v.x >> 16) + (v.y & 0xffffu) + (v.y >> 16) +
+            (v.z & 0xffffu) + (v.z >> 16) + (v.w & 0xffffu) + (v.w >> 16);
+        Bk = (v.x >> 16) + 2u * (v.y & 0xffffu) + 3u * (v.y >> 16) + 4u * (v.z & 0xffffu) +
+             5u * (v.z >> 16) + 6u * (v.w & 0xffffu) + 7u * (v.w >> 16);
+      } else {
+        A = static_cast<u64>(v.x) + v.y + v.z + v.w;
+        Bk = static_cast<u64>(v.y) + 2ull * v.z + 3ull * v.w;
+      }
+    };
     for (int r = t.rl; r < nrows; r += t.rstep) {
       u64 SA = 0, SCA = 0, SB = 0;
       const unsigned char *rowp = stage + static_cast<size_t>(r) * rowb;
-      for (int col = t.col0; col < t.cols; col += t.cstep) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(rowp + (col << 4));
-        u64 A, Bk;
-        if (C.pbytes == 2) {
-          const u32 a = (v.x & 0xffffu) + (v.x >> 16) + (v.y & 0xffffu) + (v.y >> 16) +
-                        (v.z & 0xffffu) + (v.z >> 16) + (v.w & 0xffffu) + (v.w >> 16);
-          const u32 b = (v.x >> 16) + 2u * (v.y & 0xffffu) + 3u * (v.y >> 16) +
-                        4u * (v.z & 0xffffu) + 5u * (v.z >> 16) + 6u * (v.w & 0xffffu) +
-                        7u * (v.w >> 16);
-          A = a;
-          Bk = b;
-        } else {
-          A = static_cast<u64>(v.x) + v.y + v.z + v.w;
-          Bk = static_cast<u64>(v.y) + 2ull * v.z + 3ull * v.w;
+      int col = t.col0;
+      // four columns per iteration: four independent shared loads in flight
+      for (; col + 3 * t.cstep < t.cols; col += 4 * t.cstep) {
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          v[k] = *reinterpret_cast<const uint4 *>(rowp + ((col + k * t.cstep) << 4));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          u64 A, Bk;
+          column(v[k], A, Bk);
+          SA += A;
+          SCA += static_cast<u64>(static_cast<u32>(col + k * t.cstep)) * A;
+          SB += Bk;
         }
+      }
+      for (; col < t.cols; col += t.cstep) {
+        u64 A, Bk;
+        column(*reinterpret_cast<const uint4 *>(rowp + (col << 4)), A, Bk);
         SA += A;
         SCA += static_cast<u64>(static_cast<u32>(col)) * A;
         SB += Bk;
