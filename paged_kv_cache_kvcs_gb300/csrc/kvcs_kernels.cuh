@@ -509,13 +509,13 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
       const unsigned char *sp = stage + static_cast<size_t>(t.rl) * rowb + (col << 4);
       const size_t step = static_cast<size_t>(t.rstep) * rowb;
       int r = t.rl;
-      // four rows per iteration: four independent shared loads in flight
-      for (; r + 3 * t.rstep < nrows; r += 4 * t.rstep, sp += 4 * step) {
-        uint4 v[4];
+      // eight rows per iteration: eight independent shared loads in flight
+      for (; r + 7 * t.rstep < nrows; r += 8 * t.rstep, sp += 8 * step) {
+        uint4 v[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const uint4 *>(sp + k * step);
+        for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const uint4 *>(sp + k * step);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
           const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
           const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
           const u64 X = x0 + x1;
