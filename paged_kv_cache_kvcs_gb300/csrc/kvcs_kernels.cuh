@@ -303,18 +303,18 @@ __device__ __forceinline__ void make_map(ThreadMap &t, int rowb, int gtid,
 
 // Running sums S, T, U over slots [s_lo, s_hi) of one (head, 16-byte column)
 // group whose slot s is staged at p0 + (s - s_off) * stride (s >= s_off);
-// four independent shared loads per iteration.
+// eight independent shared loads per iteration.
 __device__ __forceinline__ void accum_slots(const unsigned char *p0, size_t stride,
                                             int s_lo, int s_hi, int s_off, u64 &S,
                                             u64 &T, u64 &U) {
   int s = s_lo;
-  for (; s + 3 < s_hi; s += 4) {
-    uint4 v[4];
+  for (; s + 7 < s_hi; s += 8) {
+    uint4 v[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < 8; ++k)
       v[k] = *reinterpret_cast<const uint4 *>(p0 + static_cast<size_t>(s + k - s_off) * stride);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < 8; ++k) {
       const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
       const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
       const u64 X = x0 + x1;
@@ -375,38 +375,42 @@ __device__ __forceinline__ void accum_slots_rotated(const unsigned char *gp, int
 }
 
 // As accum_slots for an HND group in a sub-blocked stage: slot s of the
-// group is at p0 + (s / kbs) * sub_bytes + (s % kbs) * hb; four independent
+// group is at p0 + (s / kbs) * sub_bytes + (s % kbs) * hb; eight independent
 // loads per iteration, whatever sub-blocks they fall in.
 __device__ __forceinline__ void accum_slots_sub(const unsigned char *p0, int hb, int kbs,
                                                 size_t sub_bytes, int nv, u64 &S, u64 &T,
                                                 u64 &U) {
   int s = 0;
-  // When kbs is a multiple of 4 a batch of four slots never straddles a
-  // sub-block: track (sub-block, offset) incrementally, one address a batch.
+  // When kbs is a multiple of 4 a run of four slots never straddles a
+  // sub-block: track (sub-block, offset) incrementally, one address per run,
+  // two runs (eight independent loads) per iteration.
   const bool whole = (kbs & 3) == 0;
   int sb4 = 0, so4 = 0;
-  for (; s + 3 < nv; s += 4) {
-    uint4 v[4];
+  for (; s + 7 < nv; s += 8) {
+    uint4 v[8];
     if (whole) {
-      const unsigned char *b = p0 + sb4 * sub_bytes + static_cast<size_t>(so4) * hb;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        v[i] = *reinterpret_cast<const uint4 *>(b + static_cast<size_t>(i) * hb);
-      so4 += 4;
-      if (so4 == kbs) {
-        so4 = 0;
-        ++sb4;
+      for (int run = 0; run < 2; ++run) {
+        const unsigned char *b = p0 + sb4 * sub_bytes + static_cast<size_t>(so4) * hb;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          v[run * 4 + i] = *reinterpret_cast<const uint4 *>(b + static_cast<size_t>(i) * hb);
+        so4 += 4;
+        if (so4 == kbs) {
+          so4 = 0;
+          ++sb4;
+        }
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         const int sb = (s + i) / kbs;
         v[i] = *reinterpret_cast<const uint4 *>(
             p0 + sb * sub_bytes + static_cast<size_t>(s + i - sb * kbs) * hb);
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const u64 x0 = (static_cast<u64>(v[i].y) << 32) | v[i].x;
       const u64 x1 = (static_cast<u64>(v[i].w) << 32) | v[i].z;
       const u64 X = x0 + x1;

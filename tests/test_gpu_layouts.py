@@ -96,12 +96,13 @@ def test_padded_blocks(layout, pad):
     assert st == 0 and np.array_equal(got, exp)
 
 
-@pytest.mark.parametrize("kbs", [1, 4, 8, 16])
+@pytest.mark.parametrize("bs,kbs", [(16, 1), (16, 4), (16, 8), (16, 16), (48, 12), (48, 6),
+                                    (32, 2)])
 @pytest.mark.parametrize("hb", [64, 24])
-def test_hnd_kernel_sub_blocks(kbs, hb):
+def test_hnd_kernel_sub_blocks(bs, kbs, hb):
     """HND blocks split into block_size / kbs sub-blocks:
     [2, num_blocks, sub, heads, kbs, hb]."""
-    bs, heads = 16, 4
+    heads = 4
     wl, exp = canonical(4, W.LAYOUT_HND, hb=hb, bs=bs, heads=heads)
     r = bs // kbs
     caches = []
