@@ -342,11 +342,11 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
         first = false;
       }
     }
-    // Whole positions per CTA when that balances well (>= 95% of the even
+    // Whole positions per CTA when that balances well (>= 99% of the even
     // split); otherwise split at unit granularity.
     const double per = static_cast<double>(total_positions) / sms;
     const double eff = per / std::ceil(per > 0 ? per : 1.0);
-    if (total_positions >= sms && eff >= 0.95) {
+    if (total_positions >= sms && eff >= 0.99) {
       pl.split = 0;
       pl.bulk_grid = sms;
     } else {
