@@ -412,50 +412,88 @@ def run_write(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     layers, heads, hb, bs = 32, 8, 256, 16
-    # requests x new tokens each; the small case is the profiling size
-    R, L = (8, 512) if args.config == "llama3_8b_write_small" else (32, 512)
     g = torch.Generator().manual_seed(args.seed + rank)
-    nb = R * L // bs + 64
-    perm = torch.randperm(nb, generator=g)
-    tables = perm[:R * L // bs].view(R, L // bs)
-    t = torch.arange(L)
-    slots = (tables[:, t // bs] * bs + t % bs).reshape(-1).to(dev)
-    pos = t.repeat(R).to(dev)
+    decode = args.config == "llama3_8b_write_decode"
+    if decode:
+        # one new token for each of 256 requests, at lengths 512..4095
+        R, L = 256, 1
+        lens = torch.randint(512, 4096, (R,), generator=g)
+        nb = R + 64
+        tables = torch.randperm(nb, generator=g)[:R].view(R, 1)   # the last block
+        slots = (tables[:, 0] * bs + lens % bs).to(dev)
+        pos = lens.to(dev)
+        po_step = 1
+        fp = (lens // bs).to(dev)
+        nt = (lens + 1).to(dev)
+    else:
+        # requests x new tokens each; the small case is the profiling size
+        R, L = (8, 512) if args.config == "llama3_8b_write_small" else (32, 512)
+        nb = R * L // bs + 64
+        perm = torch.randperm(nb, generator=g)
+        tables = perm[:R * L // bs].view(R, L // bs)
+        t = torch.arange(L)
+        slots = (tables[:, t // bs] * bs + t % bs).reshape(-1).to(dev)
+        pos = t.repeat(R).to(dev)
+        po_step = L // bs
+        fp = torch.zeros(R, dtype=torch.int64, device=dev)
+        nt = torch.full((R,), L, dtype=torch.int64, device=dev)
     n = R * L
     dg = torch.Generator(device=dev).manual_seed(args.seed + 1)
+    lay = {"nhd": (W.LAYOUT_NHD, 0), "hnd": (W.LAYOUT_HND, 0), "hnd_sub4": (W.LAYOUT_HND, 4),
+           "xsplit": (W.LAYOUT_XSPLIT, 0)}.get(args.layout)
+    if lay is None:
+        raise SystemExit(f"the write bench has no layout {args.layout}")
     caches = [W.CacheSpec(torch.zeros(2 * nb * bs * heads * hb, dtype=torch.uint8, device=dev),
-                          nb, W.LAYOUT_NHD, li, 0, heads, hb) for li in range(layers)]
+                          nb, lay[0], li, 0, heads, hb, kernel_block_size=lay[1])
+              for li in range(layers)]
     keys = [torch.randn((n, heads, hb // 2), dtype=torch.bfloat16, device=dev, generator=dg)
             for _ in range(layers)]
     vals = [torch.randn((n, heads, hb // 2), dtype=torch.bfloat16, device=dev, generator=dg)
             for _ in range(layers)]
     sums = torch.zeros(nb, dtype=torch.int64, device=dev)
     # the written blocks as checksum positions (for the unfused comparison)
-    po = torch.arange(0, (R + 1) * (L // bs), L // bs, dtype=torch.int64, device=dev)
-    fp = torch.zeros(R, dtype=torch.int64, device=dev)
-    nt = torch.full((R,), L, dtype=torch.int64, device=dev)
+    po = torch.arange(0, (R + 1) * po_step, po_step, dtype=torch.int64, device=dev)
     bids = tables.reshape(-1).to(torch.int32).to(dev)
-    ck = kvcs.Checksummer(caches, bs, po, fp, nt, bids, R * L // bs)
-    out = torch.empty(R * L // bs, dtype=torch.int64, device=dev)
+    ck = kvcs.Checksummer(caches, bs, po, fp, nt, bids, R * po_step)
+    out = torch.empty(R * po_step, dtype=torch.int64, device=dev)
     stream = torch.cuda.Stream(dev)
     raw = stream.cuda_stream
+
+    # the decode step's data fits in L2: flush it before every timed step,
+    # outside the events, by reading a 256 MB buffer (a read leaves no dirty
+    # lines whose write-back would land inside the timed step)
+    scrub = torch.ones(32 << 20, dtype=torch.int64, device=dev) if decode else None
+    scrub_out = torch.empty((), dtype=torch.int64, device=dev)
 
     def timed(fn, k):
         with torch.cuda.stream(stream):
             for _ in range(max(3, args.warmup)):
                 fn()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(k):
-                fn()
-            e1.record(stream)
+            if scrub is None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(k):
+                    fn()
+                e1.record(stream)
+            else:
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(k)]
+                for a, b in ev:
+                    torch.sum(scrub, dim=0, out=scrub_out)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / 1e3 / k
+        if scrub is None:
+            return e0.elapsed_time(e1) / 1e3 / k
+        return sum(a.elapsed_time(b) for a, b in ev) / 1e3 / k
 
-    fused = lambda: kvcs.write_kv(caches, bs, keys, vals, slots, pos, block_sums=sums,
-                                  stream=raw)
-    plain = lambda: kvcs.write_kv(caches, bs, keys, vals, slots, pos, stream=raw)
+    # prepared calls, as an engine with fixed buffers makes them
+    fused_w = kvcs.KVWriter(caches, bs, keys, vals, slots, pos, block_sums=sums)
+    plain_w = kvcs.KVWriter(caches, bs, keys, vals, slots, pos)
+    fused = lambda: fused_w(raw)
+    plain = lambda: plain_w(raw)
 
     def unfused():
         plain()
@@ -480,11 +518,13 @@ def run_write(args, ws, rank, local):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t_fused * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u64", "data": "synthetic",
-            "config": {"workload": "llama3_8b_prefill_write", "layers": layers,
+            "config": {"workload": "llama3_8b_decode_write" if decode
+                       else "llama3_8b_prefill_write", "layers": layers,
                        "kv_heads": heads, "head_bytes": hb, "block_size": bs,
                        "requests": R, "new_tokens_per_request": L,
-                       "bytes_moved_per_step": moved,
-                       "l2": "new K/V and written pages far above the 129 MB L2; no flush"},
+                       "bytes_moved_per_step": moved, "memory_layout": args.layout,
+                       "l2": "L2 flushed (256 MB read) before every timed step" if decode
+                       else "new K/V and written pages far above the 129 MB L2; no flush"},
             "gpu_launches_per_step": launches,
             "gpu_launches": launches * args.steps,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -786,7 +826,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, ws, rank)
-        elif args.config in ("llama3_8b_write", "llama3_8b_write_small"):
+        elif args.config in ("llama3_8b_write", "llama3_8b_write_small",
+                             "llama3_8b_write_decode"):
             run_write(args, ws, rank, local)
         else:
             run_ours(args, ws, rank, local)

@@ -18,4 +18,4 @@ from ._binding import (  # noqa: F401
     kvcs_requests, launch_count, load_library, plan_for, selftest_wait_timeout,
     strerror, version,
     workload_checksums, Checksummer, workload_checksummer, kvcs_outputs,
-    group_checksums, block_checksum_tags, write_kv)
+    group_checksums, block_checksum_tags, write_kv, KVWriter)

@@ -438,3 +438,49 @@ def write_kv(caches, block_size: int, keys, values, slot_mapping, positions,
                                       _ptr(block_sums), _ptr(status), stream)
     if rc != KVCS_OK:
         raise KvcsError(rc, "kvcs_write_kv")
+
+
+class KVWriter:
+    """A ``kvcs_write_kv`` call prepared once for fixed caches and fixed
+    new-token buffers (as a serving engine keeps them): the arguments are
+    checked and marshalled here, so each call is a single ctypes call.  The
+    buffers may be refilled in place between calls; ``num_tokens`` may be
+    lowered per call (the first tokens of the buffers are written)."""
+
+    def __init__(self, caches, block_size: int, keys, values, slot_mapping, positions,
+                 block_sums=None, status=None):
+        if not isinstance(caches, (list, tuple)):
+            caches, keys, values = [caches], [keys], [values]
+        write_kv(caches, block_size, keys, values, slot_mapping[:0], positions[:0],
+                 block_sums, status)                     # argument checks only
+        n = slot_mapping.numel()
+        for c, k, v in zip(caches, keys, values):
+            row = c.num_heads * c.head_bytes
+            for t in (k, v):
+                if t is not None and t.numel() * t.element_size() < n * row:
+                    raise ValueError("key/value buffers are smaller than the slot mapping")
+        if positions.numel() != n:
+            raise ValueError("positions and slot_mapping differ in length")
+        self._keep = (list(caches), list(keys), list(values), slot_mapping, positions,
+                      block_sums, status)
+        self.max_tokens = n
+        self.num_caches = len(caches)
+        self.block_size = block_size
+        self.caches = cache_array(caches)
+        self.kp = (ctypes.c_void_p * len(caches))(*[_ptr(k) for k in keys])
+        self.vp = (ctypes.c_void_p * len(caches))(*[_ptr(v) for v in values])
+        self.slots = slot_mapping.data_ptr()
+        self.pos = positions.data_ptr()
+        self.sums = _ptr(block_sums)
+        self.status = _ptr(status)
+        self._fn = load_library().kvcs_write_kv
+
+    def __call__(self, stream: int | None = None, num_tokens: int | None = None):
+        n = self.max_tokens if num_tokens is None else num_tokens
+        if not 0 <= n <= self.max_tokens:
+            raise ValueError("num_tokens outside the prepared buffers")
+        rc = self._fn(self.caches, self.num_caches, self.block_size, n, self.kp, self.vp,
+                      self.slots if n else None, self.pos if n else None, self.sums,
+                      self.status, stream or None)
+        if rc != KVCS_OK:
+            raise KvcsError(rc, "kvcs_write_kv")

@@ -601,10 +601,8 @@ int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_si
   auto family = [](int layout) {
     return layout == KVCS_LAYOUT_LATENT ? static_cast<int>(KVCS_LAYOUT_NHD) : layout;
   };
-  // a warp per token; CTAs beyond the resident ones start as others retire
+  // a warp per item; CTAs beyond the resident ones start as others retire
   const long long warps_per_cta = kWriteThreads / 32;
-  const unsigned grid = static_cast<unsigned>(std::max<long long>(
-      1, std::min<long long>((num_tokens + warps_per_cta - 1) / warps_per_cta, 32LL * sms)));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   for (int fam : families) {
     std::vector<int32_t> members;
@@ -619,10 +617,30 @@ int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_si
         w.key[k] = static_cast<const unsigned char *>(keys[m]);
         w.value[k] = static_cast<const unsigned char *>(values[m]);
       }
+      // enough (token, run of caches) items for about 64 warps per SM
+      const long long want = 64LL * sms;
+      const long long runs = std::min<long long>(n, std::max<long long>(
+                                                        1, (want + num_tokens - 1) / num_tokens));
+      w.caches_per_item = static_cast<int>((n + runs - 1) / runs);
+      const long long witems = num_tokens * ((n + w.caches_per_item - 1) / w.caches_per_item);
+      const unsigned grid = static_cast<unsigned>(std::max<long long>(
+          1, std::min<long long>((witems + warps_per_cta - 1) / warps_per_cta, 32LL * sms)));
+      // x-split: a warp per (cache, 32 tokens, run of heads) item, the runs
+      // short enough for about 64 warps per SM
+      int max_heads = 1;
+      for (int k = 0; k < n; ++k) max_heads = std::max(max_heads, w.c[k].heads);
+      const long long xbase = (num_tokens + 31) / 32 * n;
+      const long long xruns = std::min<long long>(
+          max_heads, std::max<long long>(1, (want + xbase - 1) / xbase));
+      w.heads_per_item = static_cast<int>((max_heads + xruns - 1) / xruns);
+      w.head_chunks = (max_heads + w.heads_per_item - 1) / w.heads_per_item;
+      const unsigned xgrid = static_cast<unsigned>(std::max<long long>(
+          1, std::min<long long>((xbase * w.head_chunks + warps_per_cta - 1) / warps_per_cta,
+                                 32LL * sms)));
       if (fam == KVCS_LAYOUT_HND)
         kvcs_write_kernel<kLayoutHND><<<grid, kWriteThreads, 0, st>>>(w);
       else if (fam == KVCS_LAYOUT_XSPLIT)
-        kvcs_write_kernel<kLayoutXSplit><<<grid, kWriteThreads, 0, st>>>(w);
+        kvcs_write_xsplit_kernel<<<xgrid, kWriteThreads, 0, st>>>(w);
       else
         kvcs_write_kernel<kLayoutNHD><<<grid, kWriteThreads, 0, st>>>(w);
       if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;

@@ -240,3 +240,33 @@ def test_more_caches_than_one_launch_holds():
     got = u64(sums)
     for q, b in enumerate(block_ids):
         assert got[b] == np.uint64(exp[q]), (q, b)
+
+
+def test_prepared_writer_matches_write_kv():
+    """KVWriter (arguments marshalled once) writes and sums exactly as
+    write_kv, for all prepared tokens and for a leading subset."""
+    bs, nb, heads, hb, layers, n = 16, 10, 2, 64, 3, 40
+    g = torch.Generator().manual_seed(31)
+    slots = torch.randperm(nb * bs, generator=g)[:n].to(DEV)
+    pos = torch.randint(0, 300, (n,), generator=g).to(DEV)
+    keys = [torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8, generator=g).to(DEV)
+            for _ in range(layers)]
+    vals = [torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8, generator=g).to(DEV)
+            for _ in range(layers)]
+
+    def fresh():
+        return [W.CacheSpec(torch.zeros(2 * nb * bs * heads * hb, dtype=torch.uint8,
+                                        device=DEV), nb, W.LAYOUT_HND, li, 0, heads, hb)
+                for li in range(layers)]
+
+    for count in (n, 17, 0):
+        a, b = fresh(), fresh()
+        sa = torch.zeros(nb, dtype=torch.int64, device=DEV)
+        sb = torch.zeros(nb, dtype=torch.int64, device=DEV)
+        K.KVWriter(a, bs, keys, vals, slots, pos, block_sums=sa)(num_tokens=count)
+        K.write_kv(b, bs, [k[:count] for k in keys], [v[:count] for v in vals], slots[:count],
+                   pos[:count], block_sums=sb)
+        torch.cuda.synchronize()
+        assert torch.equal(sa, sb)
+        for ca, cb in zip(a, b):
+            assert torch.equal(ca.pool, cb.pool)
