@@ -1139,7 +1139,7 @@ constexpr int kWriteBatch = 8;  // chunks per lane in flight
 // h = off / hb, byte e = off mod hb) goes to, per layout:
 //   NHD, latent  o*row + off
 //   HND          ((o/kbs*heads + h)*kbs + o mod kbs)*hb + e
-//   x-split      (off/16)*bs*16 + o*16 + off mod 16
+// (x-split pages have their own kernel below.)
 template <int kLayout>
 __device__ __forceinline__ u64 write_token_rows(const DevCache &C, const unsigned char *srck,
                                                 const unsigned char *srcv, long long bs,
@@ -1155,8 +1155,6 @@ __device__ __forceinline__ u64 write_token_rows(const DevCache &C, const unsigne
     const long long sb = o / C.kbs;
     slot_base = (sb * C.heads * C.kbs + (o - sb * C.kbs)) * C.hb;
     head_step = static_cast<long long>(C.kbs - 1) * C.hb;
-  } else if (kLayout == kLayoutXSplit) {
-    slot_base = o * 16;
   } else {
     slot_base = o * row;
   }
@@ -1186,14 +1184,8 @@ __device__ __forceinline__ u64 write_token_rows(const DevCache &C, const unsigne
       const int off = (idx - half * nh) * ch;
       const int h = C.hb_shift >= 0 ? (off >> C.hb_shift) : off / C.hb;
       const int e = off - h * C.hb;
-      long long d;
-      if (kLayout == kLayoutHND) {
-        d = slot_base + off + h * head_step;
-      } else if (kLayout == kLayoutXSplit) {
-        d = slot_base + static_cast<long long>(off >> 4) * bs * 16 + (off & 15);
-      } else {
-        d = slot_base + off;
-      }
+      const long long d = kLayout == kLayoutHND ? slot_base + off + h * head_step
+                                                : slot_base + off;
       unsigned char *dst = page + half * C.half_stride + d;
       const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
       const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
