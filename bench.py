@@ -411,51 +411,26 @@ def run_write(args, ws, rank, local):
     from paged_kv_cache_kvcs_gb300 import workloads as W
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    layers, heads, hb, bs = 32, 8, 256, 16
-    g = torch.Generator().manual_seed(args.seed + rank)
     decode = args.config == "llama3_8b_write_decode"
-    if decode:
-        # one new token for each of 256 requests, at lengths 512..4095
-        R, L = 256, 1
-        lens = torch.randint(512, 4096, (R,), generator=g)
-        nb = R + 64
-        tables = torch.randperm(nb, generator=g)[:R].view(R, 1)   # the last block
-        slots = (tables[:, 0] * bs + lens % bs).to(dev)
-        pos = lens.to(dev)
-        po_step = 1
-        fp = (lens // bs).to(dev)
-        nt = (lens + 1).to(dev)
-    else:
-        # requests x new tokens each; the small case is the profiling size
-        R, L = (8, 512) if args.config == "llama3_8b_write_small" else (32, 512)
-        nb = R * L // bs + 64
-        perm = torch.randperm(nb, generator=g)
-        tables = perm[:R * L // bs].view(R, L // bs)
-        t = torch.arange(L)
-        slots = (tables[:, t // bs] * bs + t % bs).reshape(-1).to(dev)
-        pos = t.repeat(R).to(dev)
-        po_step = L // bs
-        fp = torch.zeros(R, dtype=torch.int64, device=dev)
-        nt = torch.full((R,), L, dtype=torch.int64, device=dev)
-    n = R * L
-    dg = torch.Generator(device=dev).manual_seed(args.seed + 1)
     lay = {"nhd": (W.LAYOUT_NHD, 0), "hnd": (W.LAYOUT_HND, 0), "hnd_sub4": (W.LAYOUT_HND, 4),
            "xsplit": (W.LAYOUT_XSPLIT, 0)}.get(args.layout)
     if lay is None:
         raise SystemExit(f"the write bench has no layout {args.layout}")
-    caches = [W.CacheSpec(torch.zeros(2 * nb * bs * heads * hb, dtype=torch.uint8, device=dev),
-                          nb, lay[0], li, 0, heads, hb, kernel_block_size=lay[1])
-              for li in range(layers)]
-    keys = [torch.randn((n, heads, hb // 2), dtype=torch.bfloat16, device=dev, generator=dg)
-            for _ in range(layers)]
-    vals = [torch.randn((n, heads, hb // 2), dtype=torch.bfloat16, device=dev, generator=dg)
-            for _ in range(layers)]
+    wb = W.llama3_8b_write(args.seed + rank, dev, kind="decode" if decode else "prefill",
+                           num_requests=8 if args.config == "llama3_8b_write_small" else None,
+                           layout=lay[0], kernel_block_size=lay[1])
+    caches, keys, vals, slots, pos = wb.caches, wb.keys, wb.values, wb.slot_mapping, wb.positions
+    bs, nb, layers = wb.block_size, wb.num_blocks, len(wb.caches)
+    heads, hb = wb.info["heads"], wb.info["head_bytes"]
+    R = wb.info["requests"]
+    n = slots.numel()
+    L = n // R
+    po, fp, nt, bids = wb.pos_offsets, wb.first_position, wb.num_tokens, wb.block_ids
+    npos = int(bids.numel())
     sums = torch.zeros(nb, dtype=torch.int64, device=dev)
     # the written blocks as checksum positions (for the unfused comparison)
-    po = torch.arange(0, (R + 1) * po_step, po_step, dtype=torch.int64, device=dev)
-    bids = tables.reshape(-1).to(torch.int32).to(dev)
-    ck = kvcs.Checksummer(caches, bs, po, fp, nt, bids, R * po_step)
-    out = torch.empty(R * po_step, dtype=torch.int64, device=dev)
+    ck = kvcs.Checksummer(caches, bs, po, fp, nt, bids, npos)
+    out = torch.empty(npos, dtype=torch.int64, device=dev)
     stream = torch.cuda.Stream(dev)
     raw = stream.cuda_stream
 
@@ -530,8 +505,8 @@ def run_write(args, ws, rank, local):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
-                         "traffic": profiled_traffic("llama3_8b_write", n,
-                                                     kernel="kvcs_write_kernel"),
+                         "traffic": None if decode else profiled_traffic(
+                             "llama3_8b_write", n, kernel="kvcs_write_kernel"),
                          "kernel": "kvcs_write_kernel", "launch_ms": round(t_fused * 1e3, 4)},
             "clocks": clocks,
             "write_only_ms": round(t_plain * 1e3, 4),
@@ -541,8 +516,7 @@ def run_write(args, ws, rank, local):
     if ws == 1 and not args.no_cpu_baseline:
         # the oracle computing the same block words from the written pages
         cores = host_cores()
-        wl = W.Workload("llama3_8b_prefill_write", bs, caches, po, fp, nt, bids)
-        gbs, bps, desc = oracle_timed(wl, args.cpu_seconds, cores, args.seed)
+        gbs, bps, desc = oracle_timed(wb.checksum_workload(), args.cpu_seconds, cores, args.seed)
         line["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s of written KV checksummed",
                                 "cores": cores, "kind": "oracle", "blocks_per_s": round(bps, 2),
                                 "sample": desc}

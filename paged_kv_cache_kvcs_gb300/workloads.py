@@ -394,3 +394,79 @@ def mamba2(seed: int = 0, device="cpu", num_requests: int = 64, layers: int = 64
                     info=dict(layers=layers, heads=ssm_heads + conv_dim, head_bytes=ssm_row,
                               block_size=16, kind=BITS16, layout=LAYOUT_STATE,
                               requests=R, seed=seed))
+
+
+@dataclass
+class WriteBatch:
+    """New tokens to write into paged caches (the KV-cache page's
+    reshape_and_cache inputs), plus the written blocks as checksum
+    positions: request r's blocks are positions po[r]..po[r+1] starting at
+    block position fp[r], with nt[r] valid tokens."""
+
+    block_size: int
+    caches: list[CacheSpec]
+    keys: list[torch.Tensor]
+    values: list[torch.Tensor]
+    slot_mapping: torch.Tensor     # int64 [num_tokens]
+    positions: torch.Tensor        # int64 [num_tokens]
+    num_blocks: int
+    pos_offsets: torch.Tensor      # int64 [R+1]
+    first_position: torch.Tensor   # int64 [R]
+    num_tokens: torch.Tensor       # int64 [R]
+    block_ids: torch.Tensor        # int32 [pos_offsets[R]]
+    info: dict = field(default_factory=dict)
+
+    def checksum_workload(self) -> Workload:
+        return Workload("written", self.block_size, self.caches, self.pos_offsets,
+                        self.first_position, self.num_tokens, self.block_ids, self.info)
+
+
+def llama3_8b_write(seed: int = 0, device="cpu", kind: str = "prefill",
+                    num_requests: int | None = None, layout: int = LAYOUT_NHD,
+                    kernel_block_size: int = 0, layers: int = 32) -> WriteBatch:
+    """Llama-3-8B-shaped new tokens (8 KV heads, head_size 128, bf16
+    ``randn`` K and V, block_size 16) for ``layers`` zeroed pools.
+    ``prefill``: ``num_requests`` (default 32) requests of 512 new tokens at
+    positions 0..511, written to consecutive slots of seeded-permuted
+    blocks.  ``decode``: ``num_requests`` (default 256) requests of one new
+    token each at lengths uniform in [512, 4096), each in its own block."""
+    device = torch.device(device)
+    heads, hb, bs = 8, 256, 16
+    g = _cpu_gen(seed)
+    if kind == "decode":
+        R = num_requests or 256
+        lens = torch.randint(512, 4096, (R,), generator=g)
+        nb = R + 64
+        tables = torch.randperm(nb, generator=g)[:R].view(R, 1)
+        slots = tables[:, 0] * bs + lens % bs
+        pos = lens
+        per = 1
+        fp = lens // bs
+        nt = lens + 1
+    elif kind == "prefill":
+        R, L = num_requests or 32, 512
+        nb = R * L // bs + 64
+        tables = torch.randperm(nb, generator=g)[:R * L // bs].view(R, L // bs)
+        t = torch.arange(L)
+        slots = (tables[:, t // bs] * bs + t % bs).reshape(-1)
+        pos = t.repeat(R)
+        per = L // bs
+        fp = torch.zeros(R, dtype=torch.int64)
+        nt = torch.full((R,), L, dtype=torch.int64)
+    else:
+        raise ValueError(kind)
+    n = slots.numel()
+    dg = _dev_gen(seed, device)
+    caches = [CacheSpec(torch.zeros(2 * nb * bs * heads * hb, dtype=torch.uint8, device=device),
+                        nb, layout, li, 0, heads, hb, kernel_block_size=kernel_block_size)
+              for li in range(layers)]
+    keys = [torch.randn((n, heads, hb // 2), dtype=torch.bfloat16, device=device, generator=dg)
+            for _ in range(layers)]
+    vals = [torch.randn((n, heads, hb // 2), dtype=torch.bfloat16, device=device, generator=dg)
+            for _ in range(layers)]
+    po = torch.arange(0, (R + 1) * per, per, dtype=torch.int64)
+    return WriteBatch(bs, caches, keys, vals, slots.to(device), pos.to(device), nb,
+                      po.to(device), fp.to(device), nt.to(device),
+                      tables.reshape(-1).to(torch.int32).to(device),
+                      info=dict(kind=kind, requests=R, layers=layers, heads=heads,
+                                head_bytes=hb, block_size=bs, seed=seed))

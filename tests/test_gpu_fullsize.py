@@ -89,3 +89,31 @@ def test_invariance_full():
     assert np.array_equal(b[pos], exp)
     del prod, cons, s0, s1
     _free()
+
+
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_fused_write_full_size(kind):
+    """The benchmark's write steps (32 layers; 32 x 512 new tokens, or 256
+    requests x 1 token) through the prepared call it times: every written
+    block's running word equals a checksum pass over the written pools, and
+    sampled blocks equal the oracle."""
+    from gpu_helpers import oracle_sampled
+    wb = W.llama3_8b_write(0, DEV, kind=kind)
+    sums = torch.zeros(wb.num_blocks, dtype=torch.int64, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    K.KVWriter(wb.caches, wb.block_size, wb.keys, wb.values, wb.slot_mapping, wb.positions,
+               block_sums=sums, status=status)()
+    wl = wb.checksum_workload()
+    npos = int(wb.block_ids.numel())
+    out = torch.empty(npos, dtype=torch.int64, device=DEV)
+    K.Checksummer(wl.caches, wl.block_size, wl.pos_offsets, wl.first_position, wl.num_tokens,
+                  wl.block_ids, npos)(out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ids = wb.block_ids.long()
+    words = sums[ids]
+    assert torch.equal(words, out)
+    pos, exp, _ = oracle_sampled(wl, _sample(wl, 24))
+    assert np.array_equal(words.cpu().numpy().view(np.uint64)[pos], exp)
+    del wb, wl
+    _free()
