@@ -57,8 +57,12 @@ def make_workload(name: str, seed: int, device):
         return W.llama3_8b(seed, device, num_requests=19, min_len=1024, max_len=1024)
     if name == "mla":
         return W.mla(seed, device)
+    if name == "mla_small":            # 608 positions = 4 x 152, 2.7 GB: ncu captures
+        return W.mla(seed, device, num_requests=19, tokens=2048)
     if name == "llama3_70b":
         return W.llama3_70b(seed, device)
+    if name == "llama3_70b_small":     # 608 positions = 4 x 152, 1.6 GB: ncu captures
+        return W.llama3_70b(seed, device, num_requests=19, tokens=512)
     if name.startswith("llama3_70b_r"):  # request-count sweep point
         return W.llama3_70b(seed, device, num_requests=int(name[len("llama3_70b_r"):]))
     if name == "tiny":
