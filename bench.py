@@ -101,6 +101,11 @@ def relayout(wl, layout: str):
         elif layout == "separate_kv":
             k, vv = v[0].contiguous().view(-1), v[1].contiguous().view(-1)
             caches.append(dataclasses.replace(c, pool=k, v_pool=vv))
+        elif layout == "misaligned":   # NHD pools starting 8 bytes past a 16-byte boundary
+            buf = torch.empty(v.numel() + 8, dtype=torch.uint8, device=v.device)
+            pool = buf[8:]
+            pool.copy_(v.reshape(-1))
+            caches.append(dataclasses.replace(c, pool=pool))
         elif layout == "xsplit":
             pool = v.view(2, nb, bs, H, hb // 16, 16).permute(0, 1, 3, 4, 2, 5).contiguous().view(-1)
             caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_XSPLIT))
@@ -787,7 +792,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="also time the first 1, 2, 4, ... requests alone")
     ap.add_argument("--layout", default="nhd",
-                    choices=("nhd", "hnd", "hnd_sub4", "interleaved", "separate_kv", "xsplit"),
+                    choices=("nhd", "hnd", "hnd_sub4", "interleaved", "separate_kv", "xsplit",
+                             "misaligned"),
                     help="re-lay-out the (NHD) workload's pools before timing")
     ap.add_argument("--columns", type=int, default=1,
                     help="replica-key columns (caches assigned round-robin)")

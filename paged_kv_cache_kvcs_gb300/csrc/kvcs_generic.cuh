@@ -135,37 +135,82 @@ __global__ void __launch_bounds__(kGenericThreads)
         }
       }
     } else if (ok && nv > 0) {
-      const u64 t0 = static_cast<u64>(q) * static_cast<u64>(bs);
-      const long long P = C.P;
-      const long long per_slot = static_cast<long long>(C.heads) * P;
-      const long long n = nv * per_slot;
-      const int hp = C.hb >> 3;  // pieces per half
-      for (long long idx = tid; idx < n; idx += kGenericThreads) {
-        const long long slot = idx / per_slot;
-        const long long rem = idx - slot * per_slot;
-        const long long h = rem / P;
-        const long long pc = rem - h * P;
-        long long off;
-        if (C.layout == kLayoutLatent) {
-          off = b * C.block_stride + slot * C.hb + 8 * pc;
-        } else {
-          const long long half = pc >= hp ? 1 : 0;
-          const long long e = (pc - half * hp) * 8;
-          const long long page = half * C.half_stride + b * C.block_stride;
+      // A thread owns columns (head h, 8-byte word w of the head's K or V
+      // bytes): piece index p = half * hb/8 + w is fixed, so it walks its
+      // slots with running sums S = sum x and T = sum slot x and adds
+      // m_h ((2(t0 P + p) + 1) S + 2P T) once per column.  Few columns:
+      // several threads share a column, each taking every rstep-th slot.
+      const u64 t0P = static_cast<u64>(q) * static_cast<u64>(bs) * static_cast<u64>(C.P);
+      const u64 twoP = 2ull * static_cast<u64>(C.P);
+      const int hw = C.hb >> 3;         // words per head per half
+      const int cols = C.heads * hw;    // columns per half
+      int col0, cstep, s0, rstep;
+      if (cols >= kGenericThreads) {
+        col0 = tid; cstep = kGenericThreads; s0 = 0; rstep = 1;
+      } else {
+        rstep = kGenericThreads / cols;
+        s0 = tid / cols;
+        col0 = s0 < rstep ? tid - s0 * cols : cols;  // idle threads past rstep * cols
+        cstep = cols;
+      }
+      const int inv = static_cast<int>(nv);
+      for (int half = 0; half < C.halves; ++half) {
+        const unsigned char *page = C.base + half * C.half_stride + b * C.block_stride;
+        for (int col = col0; col < cols; col += cstep) {
+          const int h = col / hw;
+          const int wd = col - h * hw;
+          // address of slot s's word: colp + s * sstride, except for HND
+          // sub-blocks: colp + (s / kbs) * sub + (s % kbs) * hb
+          const unsigned char *colp;
+          long long sstride;
+          long long sub = 0;
           if (C.layout == kLayoutNHD) {
-            off = page + (slot * C.heads + h) * C.hb + e;
+            colp = page + static_cast<long long>(h) * C.hb + wd * 8;
+            sstride = static_cast<long long>(C.heads) * C.hb;
+          } else if (C.layout == kLayoutLatent) {
+            colp = page + wd * 8;
+            sstride = C.hb;
           } else if (C.layout == kLayoutXSplit) {
-            off = page + ((h * (C.hb >> 4) + (e >> 4)) * bs + slot) * 16 + (e & 15);
+            colp = page + (static_cast<long long>(h) * (C.hb >> 4) + (wd >> 1)) * bs * 16 +
+                   (wd & 1) * 8;
+            sstride = 16;
           } else {
-            const long long sb = slot / C.kbs;
-            off = page + ((sb * C.heads + h) * C.kbs + (slot - sb * C.kbs)) * C.hb + e;
+            colp = page + static_cast<long long>(h) * C.kbs * C.hb + wd * 8;
+            sstride = C.hb;
+            if (C.kbs != bs) sub = static_cast<long long>(C.heads) * C.kbs * C.hb;
           }
+          u64 S = 0, T = 0;
+          if (sub == 0) {
+            int s = s0;
+            for (; s + 3 * rstep < inv; s += 4 * rstep) {
+              u64 x[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                x[k] = __ldg(reinterpret_cast<const u64 *>(colp + (s + k * rstep) * sstride));
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                S += x[k];
+                T += static_cast<u64>(static_cast<u32>(s + k * rstep)) * x[k];
+              }
+            }
+            for (; s < inv; s += rstep) {
+              const u64 x = __ldg(reinterpret_cast<const u64 *>(colp + s * sstride));
+              S += x;
+              T += static_cast<u64>(static_cast<u32>(s)) * x;
+            }
+          } else {
+            for (int s = s0; s < inv; s += rstep) {
+              const int sb = s / C.kbs;
+              const u64 x = __ldg(reinterpret_cast<const u64 *>(
+                  colp + sb * sub + static_cast<long long>(s - sb * C.kbs) * sstride));
+              S += x;
+              T += static_cast<u64>(static_cast<u32>(s)) * x;
+            }
+          }
+          const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
+          const u64 B = 2ull * (t0P + static_cast<u64>(half * hw + wd)) + 1ull;
+          acc += mh * (B * S + twoP * T);
         }
-        const u64 x = __ldg(reinterpret_cast<const u64 *>(C.base + off));
-        const u64 j = (t0 + static_cast<u64>(slot)) * static_cast<u64>(P) +
-                      static_cast<u64>(pc);
-        const u64 mh = C.m0 + 2ull * static_cast<u64>(h);
-        acc += x * ((2ull * j + 1ull) * mh);
       }
     }
     acc = warp_sum(acc);

@@ -148,3 +148,42 @@ def test_xsplit_layout(hb, bs, pad):
     assert plan["kernel"] == (1 if pad else 0)
     got, st = run(with_caches(wl, caches))
     assert st == 0 and np.array_equal(got, exp)
+
+
+def _relaid(c, bs, kind):
+    """Bytes of canonical pool ``c`` (NHD, or latent) in layout ``kind``."""
+    if kind in ("nhd", "latent"):
+        return c.pool.clone(), dict()
+    v = c.pool.view(2, c.num_blocks, bs, c.num_heads, c.head_bytes)
+    if kind == "hnd":
+        return v.permute(0, 1, 3, 2, 4).contiguous().view(-1), dict(layout=W.LAYOUT_HND)
+    if kind == "hnd_sub4":
+        return (v.view(2, c.num_blocks, bs // 4, 4, c.num_heads, c.head_bytes)
+                .permute(0, 1, 2, 4, 3, 5).contiguous().view(-1),
+                dict(layout=W.LAYOUT_HND, kernel_block_size=4))
+    assert kind == "xsplit"
+    return (v.view(2, c.num_blocks, bs, c.num_heads, c.head_bytes // 16, 16)
+            .permute(0, 1, 3, 4, 2, 5).contiguous().view(-1), dict(layout=W.LAYOUT_XSPLIT))
+
+
+@pytest.mark.parametrize("kind", ["nhd", "hnd", "hnd_sub4", "xsplit", "latent"])
+@pytest.mark.parametrize("heads,hb", [(8, 256), (2, 32)])   # >= and < 256 word columns
+def test_misaligned_pools_every_layout(kind, heads, hb):
+    """Pools starting 8 bytes past a 16-byte boundary go to the generic
+    kernel in every layout and give the canonical checksums."""
+    bs = 16
+    if kind == "latent":
+        heads, hb = 1, hb * 4 + 8
+    wl, exp = canonical(9, W.LAYOUT_LATENT if kind == "latent" else W.LAYOUT_NHD, hb=hb,
+                        bs=bs, heads=heads, layers=2, lengths=(70, 33, 5))
+    caches, keep = [], []
+    for c in wl.caches:
+        data, extra = _relaid(c, bs, kind)
+        raw = torch.zeros(data.numel() + 8, dtype=torch.uint8, device=DEV)
+        raw[8:] = data
+        keep.append(raw)
+        caches.append(dataclasses.replace(c, pool=raw[8:], **extra))
+    wl2 = with_caches(wl, caches)
+    assert K.plan_for(wl2.caches, bs, wl2.num_positions)["kernel"] == 1
+    got, st = run(wl2)
+    assert st == 0 and np.array_equal(got, exp)
