@@ -231,12 +231,21 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources that make each profiled kernel: the host side that plans and
+# launches it, the shared device code and the kernel's own file.
+KERNEL_SOURCES = {
+    "kvcs_bulk_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_bulk.cuh"],
+    "kvcs_write_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_write.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str = "kvcs_bulk_kernel") -> str:
     h = hashlib.sha256()
     csrc = ROOT / "paged_kv_cache_kvcs_gb300" / "csrc"
-    for p in sorted(csrc.glob("*")):
-        h.update(p.name.encode())
-        h.update(p.read_bytes())
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        h.update((csrc / name).read_bytes())
+    h.update((ROOT / "include" / "kvcs.h").read_bytes())
     return h.hexdigest()[:16]
 
 
@@ -250,7 +259,7 @@ def profiled_traffic(workload: str, units_per_launch: int, kernel: str = "kvcs_b
     text = f.read_text()
     m_src = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
     m_b = re.search(r"dram_bytes_per_unit:\s*([0-9.eE+]+)", text)
-    if not (m_src and m_b) or m_src.group(1) != kernel_source_hash():
+    if not (m_src and m_b) or m_src.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_b.group(1)) * units_per_launch
 
