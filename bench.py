@@ -149,7 +149,10 @@ def describe(wl, name) -> dict:
             "kv_recipe": i.get("kind"), "requests": wl.num_requests,
             "positions": wl.num_positions, "kv_bytes": kv_bytes(wl),
             "seed": i.get("seed"),
-            "l2": "KV working set far above the 129 MB L2; no flush between steps"}
+            "l2": ("KV working set far above the 129 MB L2; no flush between steps"
+                   if kv_bytes(wl) > (1 << 30) else
+                   "KV working set within a few L2 sizes; steps run back to back "
+                   "(a latency case, not a bandwidth figure)")}
 
 
 # ---------------------------------------------------------------------------
