@@ -252,6 +252,42 @@ def pin_single_piece(form):
             assert [int(a) for a in vals] == exp, (layout, ci, q, slot, h, p)
 
 
+def pin_single_piece_far_position(form):
+    """The single-piece closed form at block positions so far into the
+    request (first position 2^60 + 3) that t P passes 2^64: the weight
+    2(tP + p) + 1 is taken mod 2^64, like every other product."""
+    rng = random.Random(12)
+    far = (1 << 60) + 3
+    for layout, hb, heads in ((W.LAYOUT_NHD, 16, 2), (W.LAYOUT_HND, 24, 2),
+                              (W.LAYOUT_LATENT, 32, 1)):
+        bs, n = 4, 14
+        _, caches, r = random_pool_case(4, layout, heads=heads, hb=hb, bs=bs, lengths=[n],
+                                        layers=1, layer_numbers=[7], head_offset=1)
+        rf = OracleRequests(r.pos_offsets, [far], [far * bs + n], r.block_ids)
+        P = hb // 8 if layout == W.LAYOUT_LATENT else hb // 4
+        for _ in range(10):
+            q = rng.randrange(len(r.block_ids))
+            slot = rng.randrange(bs)
+            h = rng.randrange(heads)
+            p = rng.randrange(P)
+            x = rng.getrandbits(64) | 1
+            c0 = OracleCache(np.zeros_like(caches[0].data), caches[0].num_blocks,
+                             caches[0].layout, caches[0].layer, caches[0].head_offset,
+                             caches[0].num_heads, caches[0].head_bytes)
+            v = pool_view(c0.data, layout, c0.num_blocks, bs, c0.num_heads, hb)
+            half, piece = (0, p) if (layout == W.LAYOUT_LATENT or p < hb // 8) \
+                else (1, p - hb // 8)
+            put_piece(v, half, r.block_ids[q], slot, h, piece, x)
+            vals, _ = form([c0], bs, rf)
+            t = (far + q) * bs + slot
+            assert t * P > 1 << 64
+            exp = [0] * len(vals)
+            if q * bs + slot < n:
+                m = 2 * (c0.layer * H + c0.head_offset + h) + 1
+                exp[q] = (x * m * (2 * (t * P + p) + 1)) % (1 << 64)
+            assert [int(a) for a in vals] == exp, (layout, q, slot, h, p)
+
+
 def pin_brute_force_stream(form):
     for latent, layouts in ((False, (W.LAYOUT_NHD, W.LAYOUT_HND)), (True, (W.LAYOUT_LATENT,))):
         lengths = [9, 1, 16]
@@ -461,6 +497,6 @@ def pin_token_additivity(form):
 
 
 ALL_PINS = [pin_hand_examples, pin_zero, pin_constant_pieces, pin_single_piece,
-            pin_brute_force_stream, pin_additivity, pin_layout_invariance,
+            pin_single_piece_far_position, pin_brute_force_stream, pin_additivity, pin_layout_invariance,
             pin_tp_pp_partials, pin_first_position, pin_past_num_tokens,
             pin_bad_block_id, pin_sensitivity, pin_token_additivity]

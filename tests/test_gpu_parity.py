@@ -82,6 +82,8 @@ BULK = [
          lengths=(33, 100), extra_positions=(1, 0)),  # 1 KiB pages, 7 per unit
     dict(layout=W.LAYOUT_NHD, layers=6, heads=4, head_bytes=1024, block_size=2,
          lengths=(11, 4)),                            # 8 KiB pages, 4 per unit
+    dict(layout=W.LAYOUT_NHD, layers=2, heads=2, head_bytes=64, block_size=16,
+         lengths=((1 << 57) * 16 + 37,), first_positions=(1 << 57,)),  # t P wraps 2^64
 ]
 
 
@@ -117,6 +119,8 @@ GENERIC = [
          lengths=(40,), extra_positions=(1,)),
     dict(layout=W.LAYOUT_HND, layers=1, heads=2, head_bytes=256, block_size=512,
          lengths=(600,)),                             # head run > 64 KiB
+    dict(layout=W.LAYOUT_NHD, layers=2, heads=3, head_bytes=24, block_size=16,
+         lengths=((1 << 57) * 16 + 20,), first_positions=(1 << 57,)),  # t P wraps 2^64
 ]
 
 

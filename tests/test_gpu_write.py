@@ -270,3 +270,34 @@ def test_prepared_writer_matches_write_kv():
         assert torch.equal(sa, sb)
         for ca, cb in zip(a, b):
             assert torch.equal(ca.pool, cb.pool)
+
+
+@pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_XSPLIT, W.LAYOUT_LATENT])
+def test_write_far_positions_wrap(layout):
+    """Token positions near 2^61 (t P past 2^64): the running word equals
+    the oracle's block checksum, all products taken mod 2^64."""
+    bs, nb, heads, hb = 16, 3, 2, 64
+    if layout == W.LAYOUT_LATENT:
+        heads, hb = 1, 96
+    far = 1 << 57
+    g = torch.Generator().manual_seed(41)
+    halves = 1 if layout == W.LAYOUT_LATENT else 2
+    c = W.CacheSpec(torch.zeros(halves * nb * bs * heads * hb, dtype=torch.uint8, device=DEV),
+                    nb, layout, 3, 0, heads, hb)
+    n = 13
+    slots = torch.arange(n, device=DEV) + 2 * bs           # block 2, slots 0..12
+    pos = torch.arange(n, device=DEV) + far * bs
+    key = torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8, generator=g).to(DEV)
+    val = None if layout == W.LAYOUT_LATENT else \
+        torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8, generator=g).to(DEV)
+    if layout == W.LAYOUT_LATENT:
+        key = key.view(n, hb)
+    sums = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    K.write_kv(c, bs, key, val, slots, pos, block_sums=sums)
+    torch.cuda.synchronize()
+    canon = to_canonical(c, bs).contiguous()
+    oc = OracleCache(host_bytes(canon), nb, W.LAYOUT_LATENT if layout == W.LAYOUT_LATENT
+                     else W.LAYOUT_NHD, 3, 0, heads, hb)
+    exp, st = c_form([oc], bs, OracleRequests([0, 1], [far], [far * bs + n], [2]))
+    assert st == 0
+    assert u64(sums)[2] == np.uint64(exp[0])
