@@ -242,13 +242,24 @@ KERNEL_SOURCES = {
 }
 
 
-def kernel_source_hash(kernel: str = "kvcs_bulk_kernel") -> str:
+def source_code(text: str) -> str:
+    """C/C++ source without its comments and blank lines (so that a comment
+    edit does not count as a kernel change)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.strip() for line in text.splitlines() if line.strip())
+
+
+def kernel_source_hash(kernel: str = "kvcs_bulk_kernel", read=None) -> str:
+    """SHA-256 prefix of the code (comments stripped) of the sources that
+    make ``kernel``; ``read(path)`` returns a file's text (default: the
+    working tree)."""
+    read = read or (lambda rel: (ROOT / rel).read_text())
     h = hashlib.sha256()
-    csrc = ROOT / "paged_kv_cache_kvcs_gb300" / "csrc"
     for name in KERNEL_SOURCES[kernel]:
         h.update(name.encode())
-        h.update((csrc / name).read_bytes())
-    h.update((ROOT / "include" / "kvcs.h").read_bytes())
+        h.update(source_code(read(f"paged_kv_cache_kvcs_gb300/csrc/{name}")).encode())
+    h.update(source_code(read("include/kvcs.h")).encode())
     return h.hexdigest()[:16]
 
 

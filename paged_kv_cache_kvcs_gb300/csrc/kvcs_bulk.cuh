@@ -339,18 +339,21 @@ __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
 // ---------------------------------------------------------------------------
 //
 // Persistent: CTA g owns a contiguous range of work units.  A unit is a run
-// of whole rows of one page (one block's K, its V, or its latent rows), or
-// of whole heads for HND, of about 16 KiB; the stage size is the launch's
-// largest unit, and as many stages as fit in shared memory form a ring.
-// When the positions outnumber the CTAs the ranges are whole positions and
-// every result is stored once, without atomics; otherwise the ranges are cut
-// at unit granularity and positions shared by two CTAs are combined with
-// 64-bit atomics into the pre-zeroed output.
+// of whole rows of one page (one block's K, its V, its latent rows or its
+// state rows), or of whole heads for HND and x-split, of at most about
+// 48 KiB; when every page of the launch fits a unit and all look alike,
+// consecutive pages of a position are packed into one unit.  The stage size
+// is the launch's largest unit, and as many stages as fit in shared memory
+// form a ring.  When the positions balance over the CTAs the ranges are
+// whole positions and every result is stored once, without atomics;
+// otherwise the ranges are cut at unit granularity and positions shared by
+// two CTAs are combined with 64-bit atomics into the pre-zeroed output.
 //
 // Warp 0, lane 0 is the producer: it walks the range, turns (position,
 // cache, half) into page addresses through the block table and issues one
-// bulk copy per unit (one per head for a partial HND block) into the next
-// stage, signalling the stage's "full" mbarrier by transaction bytes.  The
+// bulk copy per page of the unit (one per sub-block for a partial-head run
+// of an HND page in kernel sub-blocks) into the next stage, signalling the
+// stage's "full" mbarrier by transaction bytes.  The
 // consumer warps form `groups` groups of `group_warps` warps; emitted unit i
 // goes to group i % groups, which reduces it, adds its share into the
 // position's accumulator slot and releases the stage on its "empty" mbarrier.
