@@ -365,7 +365,8 @@ const char *kvcs_strerror(int code);
  * threads).  Memsets are not counted. */
 uint64_t kvcs_launch_count(void);
 
-/* ABI version: (major << 16) | minor. */
+/* ABI version: (major << 16) | minor.  Minor 2 added kvcs_write_kv and
+ * kvcs_outputs.flags (KVCS_OUT_ACCUMULATE; the field was reserved, 0). */
 int32_t kvcs_version(void);
 
 #ifdef __cplusplus

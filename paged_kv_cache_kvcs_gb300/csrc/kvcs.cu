@@ -671,6 +671,6 @@ const char *kvcs_strerror(int code) {
 
 uint64_t kvcs_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int32_t kvcs_version(void) { return (1 << 16) | 1; }
+int32_t kvcs_version(void) { return (1 << 16) | 2; }
 
 }  // extern "C"
