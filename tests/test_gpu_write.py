@@ -301,3 +301,35 @@ def test_write_far_positions_wrap(layout):
     exp, st = c_form([oc], bs, OracleRequests([0, 1], [far], [far * bs + n], [2]))
     assert st == 0
     assert u64(sums)[2] == np.uint64(exp[0])
+
+
+@pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND, W.LAYOUT_XSPLIT])
+def test_write_with_8_byte_aligned_buffers(layout):
+    """Key and value buffers 8 bytes off a 16-byte boundary: the write moves
+    8-byte pieces, with the same pools and running words as aligned buffers."""
+    bs, nb, heads, hb, n = 16, 6, 2, 64, 37
+    g = torch.Generator().manual_seed(51)
+    slots = torch.randperm(nb * bs, generator=g)[:n].to(DEV)
+    pos = torch.randint(0, 2000, (n,), generator=g).to(DEV)
+    key = torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8, generator=g).to(DEV)
+    val = torch.randint(0, 256, (n, heads, hb), dtype=torch.uint8, generator=g).to(DEV)
+
+    def offset8(t):
+        raw = torch.zeros(t.numel() + 8, dtype=torch.uint8, device=DEV)
+        raw[8:] = t.reshape(-1)
+        return raw[8:].view(t.shape)
+
+    def cache():
+        return W.CacheSpec(torch.zeros(2 * nb * bs * heads * hb, dtype=torch.uint8, device=DEV),
+                           nb, layout, 1, 0, heads, hb)
+
+    a, b = cache(), cache()
+    sa = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    sb = torch.zeros(nb, dtype=torch.int64, device=DEV)
+    K.write_kv(a, bs, key, val, slots, pos, block_sums=sa)
+    k8, v8 = offset8(key), offset8(val)
+    assert k8.data_ptr() % 16 == 8
+    K.write_kv(b, bs, k8, v8, slots, pos, block_sums=sb)
+    torch.cuda.synchronize()
+    assert torch.equal(a.pool, b.pool)
+    assert torch.equal(sa, sb)
