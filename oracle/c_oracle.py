@@ -21,7 +21,8 @@ class _OracleCacheC(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
                 ("layout", ctypes.c_int32), ("layer", ctypes.c_int32),
                 ("head_offset", ctypes.c_int32), ("num_heads", ctypes.c_int32),
-                ("head_bytes", ctypes.c_int32), ("piece_bytes", ctypes.c_int32)]
+                ("head_bytes", ctypes.c_int32), ("piece_bytes", ctypes.c_int32),
+                ("kernel_block_size", ctypes.c_int32)]
 
 
 _lib = None
@@ -60,7 +61,8 @@ def block_checksums(caches: Sequence[OracleCache], block_size: int,
     for k, (c, d) in enumerate(zip(caches, datas)):
         arr[k] = _OracleCacheC(d.ctypes.data, c.num_blocks, c.layout, c.layer,
                                c.head_offset, c.num_heads, c.head_bytes,
-                               getattr(c, "piece_bytes", 8))
+                               getattr(c, "piece_bytes", 8),
+                               getattr(c, "kernel_block_size", 0))
     po = np.ascontiguousarray(requests.pos_offsets, dtype=np.int64)
     fp = np.ascontiguousarray(requests.first_position, dtype=np.int64)
     nt = np.ascontiguousarray(requests.num_tokens, dtype=np.int64)

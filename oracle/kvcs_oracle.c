@@ -25,8 +25,10 @@
 #include <stdlib.h>
 
 #define ORACLE_LAYOUT_NHD 0    /* pool [2][num_blocks][block_size][heads][head_bytes] */
-#define ORACLE_LAYOUT_HND 1    /* pool [2][num_blocks][heads][block_size][head_bytes] */
+#define ORACLE_LAYOUT_HND 1    /* pool [2][num_blocks][heads][block_size][head_bytes], or
+                                  [2][num_blocks][block_size/kbs][heads][kbs][head_bytes] */
 #define ORACLE_LAYOUT_LATENT 2 /* pool [num_blocks][block_size][row_bytes] */
+#define ORACLE_LAYOUT_XSPLIT 3 /* pool [2][num_blocks][heads][head_bytes/16][block_size][16] */
 #define ORACLE_LAYOUT_STATE 4  /* pool [num_blocks][rows][row_bytes]: Mamba state */
 
 #define ORACLE_H 65536u /* MAX_KV_HEADS_PER_LAYER */
@@ -41,6 +43,7 @@ typedef struct oracle_cache {
   int32_t num_heads;
   int32_t head_bytes; /* K (= V) bytes per head per token; latent/state: row bytes */
   int32_t piece_bytes; /* state: element bytes (2 or 4); else ignored (8) */
+  int32_t kernel_block_size; /* HND: slots per kernel sub-block; 0: none */
 } oracle_cache;
 
 /* Tokens of the request's first num_tokens that block `position` holds. */
@@ -73,10 +76,17 @@ static uint64_t piece_at(const oracle_cache *c, int64_t block_size,
       byte -= hb;
     }
     int64_t page = kv * c->num_blocks + block;
-    if (c->layout == ORACLE_LAYOUT_NHD)
+    if (c->layout == ORACLE_LAYOUT_NHD) {
       off = ((page * block_size + slot) * c->num_heads + head) * hb + byte;
-    else
-      off = ((page * c->num_heads + head) * block_size + slot) * hb + byte;
+    } else if (c->layout == ORACLE_LAYOUT_XSPLIT) {
+      /* x elements make 16 bytes: [heads][head_bytes/16][block_size][16] */
+      off = (((page * c->num_heads + head) * (hb / 16) + byte / 16) * block_size + slot) * 16 +
+            byte % 16;
+    } else {
+      int64_t kbs = c->kernel_block_size > 0 ? c->kernel_block_size : block_size;
+      off = (((page * (block_size / kbs) + slot / kbs) * c->num_heads + head) * kbs +
+             slot % kbs) * hb + byte;
+    }
   }
   uint64_t x = 0;
   for (int k = 0; k < 8; ++k) x |= (uint64_t)c->data[off + k] << (8 * k);
@@ -215,7 +225,12 @@ int oracle_block_checksums(const oracle_cache *caches, int32_t num_caches,
         (int64_t)c->head_offset + c->num_heads > (int64_t)ORACLE_H)
       return -1;
     if (c->layout == ORACLE_LAYOUT_LATENT && c->num_heads != 1) return -1;
-    if (c->layout < 0 || c->layout > 2) return -1; /* 3 (x-split) is a GPU-side layout */
+    if (c->layout < 0 || c->layout > 3) return -1;
+    if (c->layout == ORACLE_LAYOUT_XSPLIT && c->head_bytes % 16) return -1;
+    if (c->kernel_block_size != 0 &&
+        (c->layout != ORACLE_LAYOUT_HND || c->kernel_block_size < 0 ||
+         block_size % c->kernel_block_size))
+      return -1;
   }
   if (pos_offsets[0] != 0) return -1;
   for (int64_t r = 0; r < num_requests; ++r)

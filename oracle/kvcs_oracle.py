@@ -55,8 +55,11 @@ MAX_KV_HEADS_PER_LAYER = 1 << 16
 BLOCK_CHECKSUM_BYTES = 8
 
 LAYOUT_NHD = 0     # pool [2, num_blocks, block_size, num_heads, head_bytes]
-LAYOUT_HND = 1     # pool [2, num_blocks, num_heads, block_size, head_bytes]
+LAYOUT_HND = 1     # pool [2, num_blocks, num_heads, block_size, head_bytes], or with
+                   # kernel sub-blocks [2, num_blocks, block_size / kbs, num_heads, kbs,
+                   # head_bytes]
 LAYOUT_LATENT = 2  # pool [num_blocks, block_size, row_bytes]
+LAYOUT_XSPLIT = 3  # pool [2, num_blocks, num_heads, head_bytes / 16, block_size, 16]
 LAYOUT_STATE = 4   # pool [num_blocks, rows, row_bytes]: Mamba running state
 
 STATUS_BAD_BLOCK_ID = 1
@@ -87,6 +90,7 @@ class OracleCache:
     num_heads: int
     head_bytes: int
     piece_bytes: int = 8
+    kernel_block_size: int = 0   # HND: slots per kernel sub-block (0: none)
 
 
 @dataclass(frozen=True)
@@ -128,7 +132,10 @@ def piece_byte_offset(cache: OracleCache, block_size: int, block: int,
     for local head ``head`` in physical block ``block``.
 
     The logical order (K bytes then V bytes of the head, token by token) is
-    fixed by the definition; the memory order comes from the declared layout.
+    fixed by the definition; the memory order comes from the declared layout
+    (page "【vLLM 源码解析】KV Cache": section "reshape kv_cache" for the
+    block-size split into kernel blocks, section on reshape_and_cache for the
+    key layout with x elements of 16 bytes, here read for K and V alike).
     """
     hb = cache.head_bytes
     byte = 8 * p
@@ -141,7 +148,14 @@ def piece_byte_offset(cache: OracleCache, block_size: int, block: int,
     if cache.layout == LAYOUT_NHD:
         return ((page * block_size + slot) * cache.num_heads + head) * hb + byte
     if cache.layout == LAYOUT_HND:
-        return ((page * cache.num_heads + head) * block_size + slot) * hb + byte
+        kbs = cache.kernel_block_size or block_size
+        sub, within = divmod(slot, kbs)
+        return (((page * (block_size // kbs) + sub) * cache.num_heads + head) * kbs +
+                within) * hb + byte
+    if cache.layout == LAYOUT_XSPLIT:
+        chunk, inner = divmod(byte, 16)
+        return (((page * cache.num_heads + head) * (hb // 16) + chunk) * block_size +
+                slot) * 16 + inner
     raise ValueError(f"unknown layout {cache.layout}")
 
 
@@ -202,6 +216,14 @@ def check_cache(cache: OracleCache, block_size: int) -> None:
         raise ValueError("per-token bytes must be a positive multiple of 8")
     if cache.layout == LAYOUT_LATENT and cache.num_heads != 1:
         raise ValueError("a latent cache has exactly one head")
+    if cache.layout == LAYOUT_XSPLIT and cache.head_bytes % 16:
+        raise ValueError("x-split heads are whole 16-byte chunks")
+    if cache.kernel_block_size and (cache.layout != LAYOUT_HND or
+                                    cache.kernel_block_size < 0 or
+                                    block_size % cache.kernel_block_size):
+        raise ValueError("kernel blocks split an HND block evenly")
+    if cache.layout not in (LAYOUT_NHD, LAYOUT_HND, LAYOUT_LATENT, LAYOUT_XSPLIT):
+        raise ValueError(f"unknown layout {cache.layout}")
     if cache.head_offset < 0 or cache.num_heads < 1:
         raise ValueError("bad head range")
     if cache.head_offset + cache.num_heads > MAX_KV_HEADS_PER_LAYER:

@@ -28,7 +28,8 @@ def host_bytes(t) -> np.ndarray:
 def oracle_caches(caches) -> list[OracleCache]:
     return [OracleCache(host_bytes(c.pool), c.num_blocks, c.layout, c.layer,
                         c.head_offset, c.num_heads, c.head_bytes,
-                        getattr(c, "piece_bytes", 0) or 8) for c in caches]
+                        getattr(c, "piece_bytes", 0) or 8,
+                        getattr(c, "kernel_block_size", 0)) for c in caches]
 
 
 def oracle_requests(wl) -> OracleRequests:

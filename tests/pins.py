@@ -328,21 +328,40 @@ def _swap(case, bs):
 
 
 def pin_layout_invariance(form):
+    """The same KV in every memory layout gives the same checksums (the
+    paragraph on TP ranks and layouts): NHD, HND, HND in kernel sub-blocks of
+    1 and 2 slots, and x-split ([heads][head_bytes/16][block_size][16]).  The
+    other layouts are the NHD pool permuted by numpy, each permutation
+    written from the layout's shape."""
     lengths = [10, 3]
-    _, _, cases = logical_case(29, (W.LAYOUT_NHD, W.LAYOUT_HND), layers=2,
-                               heads=3, hb=16, bs_list=(4, 4), lengths=lengths)
-    a, _ = form(*_swap(cases[(W.LAYOUT_NHD, 4)], 4))
-    # same block ids for both so positions line up: rebuild HND with NHD's table
-    caches_n, rn = cases[(W.LAYOUT_NHD, 4)]
-    caches_h = []
-    for c in caches_n:
-        v = pool_view(c.data, c.layout, c.num_blocks, 4, c.num_heads, c.head_bytes)
-        hnd = np.ascontiguousarray(v.transpose(0, 1, 3, 2, 4)).reshape(-1)
-        caches_h.append(OracleCache(hnd, c.num_blocks, W.LAYOUT_HND, c.layer,
-                                    c.head_offset, c.num_heads, c.head_bytes))
-    b, _ = form(caches_h, 4, rn)
-    assert [int(x) for x in a] == [int(x) for x in b]
+    bs, heads, hb = 4, 3, 32
+    _, _, cases = logical_case(29, (W.LAYOUT_NHD,), layers=2, heads=heads, hb=hb,
+                               bs_list=(bs,), lengths=lengths)
+    caches_n, rn = cases[(W.LAYOUT_NHD, bs)]
+    a, _ = form(caches_n, bs, rn)
     assert any(int(x) for x in a)
+
+    def relaid(layout, perm_of, kbs=0):
+        out = []
+        for c in caches_n:
+            v = c.data.reshape(2, c.num_blocks, bs, heads, hb)     # [kv, block, slot, head, byte]
+            out.append(OracleCache(np.ascontiguousarray(perm_of(v)).reshape(-1), c.num_blocks,
+                                   layout, c.layer, c.head_offset, heads, hb,
+                                   kernel_block_size=kbs))
+        return out
+
+    variants = [
+        relaid(W.LAYOUT_HND, lambda v: v.transpose(0, 1, 3, 2, 4)),
+        relaid(W.LAYOUT_XSPLIT, lambda v: v.reshape(2, v.shape[1], bs, heads, hb // 16, 16)
+               .transpose(0, 1, 3, 4, 2, 5)),
+    ]
+    for kbs in (1, 2):
+        variants.append(relaid(
+            W.LAYOUT_HND, lambda v, k=kbs: v.reshape(2, v.shape[1], bs // k, k, heads, hb)
+            .transpose(0, 1, 2, 4, 3, 5), kbs=kbs))
+    for caches in variants:
+        b, _ = form(caches, bs, rn)
+        assert [int(x) for x in a] == [int(x) for x in b], caches[0].layout
 
 
 def pin_tp_pp_partials(form):

@@ -187,3 +187,20 @@ def test_misaligned_pools_every_layout(kind, heads, hb):
     assert K.plan_for(wl2.caches, bs, wl2.num_positions)["kernel"] == 1
     got, st = run(wl2)
     assert st == 0 and np.array_equal(got, exp)
+
+
+@pytest.mark.parametrize("layout,kbs,hb,bs", [(W.LAYOUT_XSPLIT, 0, 64, 16),
+                                              (W.LAYOUT_XSPLIT, 0, 48, 7),
+                                              (W.LAYOUT_HND, 4, 64, 16),
+                                              (W.LAYOUT_HND, 3, 24, 12),
+                                              (W.LAYOUT_HND, 8, 256, 32)])
+def test_xsplit_and_sub_blocks_against_the_oracle_directly(layout, kbs, hb, bs):
+    """Random pools read as x-split or sub-blocked HND by both the GPU and
+    the oracle (which addresses these layouts itself)."""
+    from gpu_helpers import full_oracle
+    wl = W.random_case(12, DEV, layout=layout, layers=3, heads=4, head_bytes=hb,
+                       block_size=bs, lengths=(70, 33, 5))
+    wl = with_caches(wl, [dataclasses.replace(c, kernel_block_size=kbs) for c in wl.caches])
+    exp, est = full_oracle(wl)
+    got, st = run(wl)
+    assert st == est == 0 and np.array_equal(got, exp)

@@ -29,6 +29,21 @@ def test_c_equals_python(case, seed):
 
 
 @pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("layout,kbs,hb,bs", [(W.LAYOUT_XSPLIT, 0, 32, 5),
+                                              (W.LAYOUT_XSPLIT, 0, 16, 1),
+                                              (W.LAYOUT_HND, 2, 24, 6),
+                                              (W.LAYOUT_HND, 1, 8, 3)])
+def test_c_equals_python_xsplit_and_sub_blocks(seed, layout, kbs, hb, bs):
+    import dataclasses
+    wl = W.random_case(seed, "cpu", layout=layout, layers=2, heads=2, head_bytes=hb,
+                       block_size=bs, lengths=(13, 4), first_positions=(1, 0))
+    wl = dataclasses.replace(wl, caches=[dataclasses.replace(c, kernel_block_size=kbs)
+                                         for c in wl.caches])
+    caches, reqs = oracle_inputs(wl)
+    assert c_form(caches, wl.block_size, reqs) == py_form(caches, wl.block_size, reqs)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
 def test_tiny_workload(seed):
     wl = W.tiny(seed)
     caches, reqs = oracle_inputs(wl)

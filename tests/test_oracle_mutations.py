@@ -33,6 +33,25 @@ def _block_ignored(cache, bs, block, slot, head, p):
     return ORIG["piece_byte_offset"](cache, bs, 0, slot, head, p)
 
 
+def _xsplit_axes_swapped(cache, bs, block, slot, head, p):
+    if cache.layout != O.LAYOUT_XSPLIT:
+        return ORIG["piece_byte_offset"](cache, bs, block, slot, head, p)
+    hb = cache.head_bytes
+    byte = 8 * p
+    kv = 0
+    if byte >= hb:
+        kv, byte = 1, byte - hb
+    page = kv * cache.num_blocks + block
+    chunk, inner = divmod(byte, 16)   # slot and chunk axes swapped
+    return (((page * cache.num_heads + head) * bs + slot) * (hb // 16) + chunk) * 16 + inner
+
+
+def _sub_blocks_ignored(cache, bs, block, slot, head, p):
+    import dataclasses
+    return ORIG["piece_byte_offset"](dataclasses.replace(cache, kernel_block_size=0), bs,
+                                     block, slot, head, p)
+
+
 ORIG = {name: getattr(O, name) for name in (
     "piece_byte_offset", "piece_weight", "piece_index", "token_position",
     "slice_factor", "num_valid_tokens", "pieces_per_token", "read_piece")}
@@ -60,6 +79,8 @@ MUTANTS = {
     "nhd_transposed": ("piece_byte_offset", _nhd_transposed),
     "v_then_k": ("piece_byte_offset", _v_then_k),
     "block_id_ignored": ("piece_byte_offset", _block_ignored),
+    "xsplit_axes_swapped": ("piece_byte_offset", _xsplit_axes_swapped),
+    "sub_blocks_ignored": ("piece_byte_offset", _sub_blocks_ignored),
     "big_endian": ("read_piece", lambda c, off: int.from_bytes(
         bytes(c.data[off:off + 8]), "big")),
 }
