@@ -81,3 +81,27 @@ def test_captured_write_matches_direct_write():
         assert torch.equal(sa, sb)
         for ca, cb in zip(a, b):
             assert torch.equal(ca.pool, cb.pool)
+
+
+def test_concurrent_calls_on_several_streams():
+    """Calls enqueued on four streams at once (their kernels may overlap)
+    give the results of the same calls made one at a time."""
+    wls = [W.random_case(20 + k, DEV, layers=3, heads=4, head_bytes=64,
+                         lengths=(300, 41, 77), layout=(W.LAYOUT_NHD, W.LAYOUT_HND)[k % 2])
+           for k in range(4)]
+    ref = []
+    for wl in wls:
+        out = torch.empty(wl.num_positions, dtype=torch.int64, device=DEV)
+        K.workload_checksums(wl, out=out)
+        ref.append(out)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in wls]
+    cks = [K.Checksummer(wl.caches, wl.block_size, wl.pos_offsets, wl.first_position,
+                         wl.num_tokens, wl.block_ids, wl.num_positions) for wl in wls]
+    outs = [torch.zeros_like(r) for r in ref]
+    for _ in range(5):
+        for ck, out, s in zip(cks, outs, streams):
+            ck(out, None, s.cuda_stream)
+    torch.cuda.synchronize()
+    for out, r in zip(outs, ref):
+        assert torch.equal(out, r)
