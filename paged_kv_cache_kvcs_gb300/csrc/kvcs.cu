@@ -2,9 +2,10 @@
 // validation, launch planning and the exported C ABI declared in kvcs.h.
 //
 // The library allocates no memory.  Every call validates its host arguments
-// before touching CUDA, plans one or more launches of one kernel and enqueues
-// them (plus, when CTAs share positions, one cudaMemsetAsync of the output)
-// on the caller's stream.
+// before touching CUDA, plans its kernel launches (the bulk-copy kernel per
+// layout family, the generic kernel, the row-sum epilogue; or the write
+// kernels) and enqueues them, plus, when CTAs or launches share positions,
+// one cudaMemsetAsync of the output, on the caller's stream.
 
 #include <cuda_runtime.h>
 
