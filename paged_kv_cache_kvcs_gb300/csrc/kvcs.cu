@@ -61,6 +61,9 @@ cudaError_t device_setup(int *sms) {
 }
 
 constexpr int kMaxColumns = 64;
+// Positions of at most this many bytes, fewer than the SMs, are read one per
+// CTA: split mode's memset and atomics would cost more than the imbalance.
+constexpr long long kSmallPositionBytes = 128 * 1024;
 
 // Bytes of one page: one block of K, of V, of latent rows, or of state rows.
 long long page_bytes_of(const kvcs_cache &c, int block_size) {
@@ -350,6 +353,11 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
     if (total_positions >= sms && eff >= 0.99) {
       pl.split = 0;
       pl.bulk_grid = sms;
+    } else if (total_positions < sms &&
+               pl.kv_bytes_max <= kSmallPositionBytes * total_positions) {
+      // few small positions: one CTA each, no memset and no atomics
+      pl.split = 0;
+      pl.bulk_grid = static_cast<int>(total_positions);
     } else {
       pl.split = 1;
       pl.bulk_grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, pl.units)));

@@ -163,10 +163,16 @@ def test_plan_shapes():
     # HND with 16 KiB per head (block_size 64): three heads per unit
     p = plan([FakeCache(layout=1, layer=i) for i in range(4)], bs=64, positions=500)
     assert p["units"] == 500 * 4 * 2 * 3 and p["stage_bytes"] == 49152
-    # tiny pages (4 KiB): all four pages of a position in one unit
+    # tiny pages (4 KiB): all four pages of a position in one unit; few small
+    # positions are read one per CTA, with no memset
     p = plan([FakeCache(layer=i, num_heads=2, head_bytes=128) for i in range(2)],
              positions=7)
-    assert p["units"] == 7 and p["stage_bytes"] == 16384 and p["split"] == 1
+    assert p["units"] == 7 and p["stage_bytes"] == 16384 and p["split"] == 0
+    assert p["grid"] == 7 and p["memsets"] == 0
+    # ... but positions over 128 KiB, fewer than the SMs, are split at units
+    p = plan([FakeCache(layer=i, num_heads=2, head_bytes=128) for i in range(20)],
+             positions=100)
+    assert p["split"] == 1 and p["memsets"] == 1 and p["grid"] == 152
     # mixed geometry: no packing
     p = plan([FakeCache(layer=0, head_bytes=128), FakeCache(layer=1, head_bytes=64)],
              positions=10)
