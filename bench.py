@@ -450,14 +450,18 @@ def run_write(args, ws, rank, local):
     from paged_kv_cache_kvcs_gb300 import workloads as W
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    decode = args.config == "llama3_8b_write_decode"
+    # decode: one new token per request; "_layer": one layer per call, as a
+    # forward pass writes it
+    decode = args.config.startswith("llama3_8b_write_decode")
+    one_layer = args.config == "llama3_8b_write_decode_layer"
     lay = {"nhd": (W.LAYOUT_NHD, 0), "hnd": (W.LAYOUT_HND, 0), "hnd_sub4": (W.LAYOUT_HND, 4),
            "xsplit": (W.LAYOUT_XSPLIT, 0)}.get(args.layout)
     if lay is None:
         raise SystemExit(f"the write bench has no layout {args.layout}")
     wb = W.llama3_8b_write(args.seed + rank, dev, kind="decode" if decode else "prefill",
                            num_requests=8 if args.config == "llama3_8b_write_small" else None,
-                           layout=lay[0], kernel_block_size=lay[1])
+                           layout=lay[0], kernel_block_size=lay[1],
+                           layers=1 if one_layer else 32)
     caches, keys, vals, slots, pos = wb.caches, wb.keys, wb.values, wb.slot_mapping, wb.positions
     bs, nb, layers = wb.block_size, wb.num_blocks, len(wb.caches)
     heads, hb = wb.info["heads"], wb.info["head_bytes"]
@@ -532,8 +536,9 @@ def run_write(args, ws, rank, local):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t_fused * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u64", "data": "synthetic",
-            "config": {"workload": "llama3_8b_decode_write" if decode
-                       else "llama3_8b_prefill_write", "layers": layers,
+            "config": {"workload": ("llama3_8b_decode_write_one_layer" if one_layer else
+                                    "llama3_8b_decode_write" if decode
+                                    else "llama3_8b_prefill_write"), "layers": layers,
                        "kv_heads": heads, "head_bytes": hb, "block_size": bs,
                        "requests": R, "new_tokens_per_request": L,
                        "bytes_moved_per_step": moved, "memory_layout": args.layout,
@@ -841,7 +846,7 @@ def main():
         if args.impl == "reference":
             run_reference(args, ws, rank)
         elif args.config in ("llama3_8b_write", "llama3_8b_write_small",
-                             "llama3_8b_write_decode"):
+                             "llama3_8b_write_decode", "llama3_8b_write_decode_layer"):
             run_write(args, ws, rank, local)
         else:
             run_ours(args, ws, rank, local)
