@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(kWriteThreads, 2)
     const long long i = it - static_cast<long long>(chunk) * w.num_tokens;
     const int c_lo = chunk * cpi;
     const int c_hi = min(w.num_caches, c_lo + cpi);
+    // both table loads in flight together
     const long long slot = w.slots[i];
+    const long long t = w.positions[i];
     if (slot < 0) continue;  // padding token
     const long long b = slot / bs;
     const long long o = slot - b * bs;
@@ -134,7 +136,6 @@ __global__ void __launch_bounds__(kWriteThreads, 2)
       if (lane == 0 && chunk == 0 && w.status) atomicOr(w.status, kStatusBadBlockId);
       continue;
     }
-    const long long t = w.positions[i];
     if (t < 0 && lane == 0 && chunk == 0 && w.status) atomicOr(w.status, kStatusBadRequests);
     u64 acc = 0;
     for (int ci = c_lo; ci < c_hi; ++ci) {
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(kWriteThreads, 2)
     long long b = 0, o = 0, t = -1;
     if (live) {
       const long long slot = w.slots[i];
+      const long long ti = w.positions[i];   // both table loads in flight together
       live = slot >= 0;  // padding token
       if (live) {
         b = slot / bs;
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(kWriteThreads, 2)
           if (ci == 0 && hk == 0 && w.status) atomicOr(w.status, kStatusBadBlockId);
           live = false;
         } else {
-          t = w.positions[i];
+          t = ti;
           if (ci == 0 && hk == 0 && t < 0 && w.status)
             atomicOr(w.status, kStatusBadRequests);
         }
