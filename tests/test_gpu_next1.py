@@ -129,3 +129,21 @@ def test_verify_detects_moved_blocks_and_changed_bytes():
     view[0, blk, 0, 1, 5] ^= 0x40
     mm, cnt = check()
     assert cnt == 1 and mm.nonzero()[0].tolist() == [20]
+
+
+@pytest.mark.parametrize("layout,kbs", [(W.LAYOUT_HND, 0), (W.LAYOUT_HND, 4),
+                                        (W.LAYOUT_XSPLIT, 0), (W.LAYOUT_LATENT, 0)])
+def test_columns_in_every_layout(layout, kbs):
+    """Replica-key columns of HND (with and without kernel sub-blocks),
+    x-split and latent caches, against the oracle reading those layouts."""
+    import dataclasses
+    hb = 96 if layout == W.LAYOUT_LATENT else 64
+    wl = W.random_case(7, DEV, layout=layout, layers=4, heads=2, head_bytes=hb, block_size=16,
+                       lengths=(70, 33, 5))
+    caches = [dataclasses.replace(c, column=i % 2, kernel_block_size=kbs)
+              for i, c in enumerate(wl.caches)]
+    wl = W.Workload(wl.name, wl.block_size, caches, wl.pos_offsets, wl.first_position,
+                    wl.num_tokens, wl.block_ids)
+    values = _group(wl, 2)
+    torch.cuda.synchronize()
+    assert np.array_equal(u64(values).reshape(-1, 2), _oracle_values(wl, 2))
