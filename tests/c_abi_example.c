@@ -6,8 +6,10 @@
  * each block position's checksum has the closed form
  *   c = (t1^2 - t0^2) P^2 * sum_{layer, head} (2 (layer * 65536 + head) + 1)
  * mod 2^64, with t0 = position * 16 and t1 = min(t0 + 16, 37).  The program
- * also checks that bad arguments are refused before any CUDA work and that
- * an out-of-pool block id is flagged in the status word.
+ * also checks that bad arguments are refused before any CUDA work, that an
+ * out-of-pool block id is flagged in the status word, and that writing the
+ * same tokens into empty pools with kvcs_write_kv leaves each block's
+ * running word at the same closed form.
  *
  * Build: nvcc -o c_abi_example c_abi_example.c -I<repo>/include -L<lib dir>
  *        -lkvcs -Xlinker -rpath,<lib dir>
@@ -119,8 +121,63 @@ int main(void) {
   CHECK(status & KVCS_STATUS_BAD_BLOCK_ID, "bad block id flagged");
   CHECK(out[1] == 0, "bad position reads 0");
 
-  printf("c abi ok: 3 block checksums equal the closed form (version %d.%d)\n",
-         kvcs_version() >> 16, kvcs_version() & 0xffff);
+  /* the fused write: the same 37 tokens (all pieces 1) into empty pools;
+   * every written block's running word must be the same closed form */
+  void *empty[2], *keys[2], *vals[2];
+  const size_t tok_bytes = (size_t)ntok * heads * head_bytes;
+  uint8_t *host_tok = (uint8_t *)calloc(tok_bytes, 1);
+  CHECK(host_tok != NULL, "host allocation");
+  for (size_t i = 0; i < tok_bytes; i += 8) host_tok[i] = 1;
+  kvcs_cache wcaches[2];
+  memcpy(wcaches, caches, sizeof(caches));
+  for (int l = 0; l < layers; ++l) {
+    CHECK(cudaMalloc(&empty[l], pool_bytes) == cudaSuccess, "cudaMalloc pool");
+    cudaMemset(empty[l], 0, pool_bytes);
+    CHECK(cudaMalloc(&keys[l], tok_bytes) == cudaSuccess, "cudaMalloc keys");
+    CHECK(cudaMalloc(&vals[l], tok_bytes) == cudaSuccess, "cudaMalloc values");
+    cudaMemcpy(keys[l], host_tok, tok_bytes, cudaMemcpyHostToDevice);
+    cudaMemcpy(vals[l], host_tok, tok_bytes, cudaMemcpyHostToDevice);
+    wcaches[l].base = empty[l];
+  }
+  int64_t h_slots[37], h_pos[37];
+  for (int t = 0; t < ntok; ++t) {
+    h_slots[t] = (int64_t)h_ids[t / bs] * bs + t % bs;
+    h_pos[t] = t;
+  }
+  int64_t *d_slots, *d_pos;
+  uint64_t *d_sums;
+  CHECK(cudaMalloc((void **)&d_slots, sizeof(h_slots)) == cudaSuccess, "cudaMalloc");
+  CHECK(cudaMalloc((void **)&d_pos, sizeof(h_pos)) == cudaSuccess, "cudaMalloc");
+  CHECK(cudaMalloc((void **)&d_sums, nb * sizeof(uint64_t)) == cudaSuccess, "cudaMalloc");
+  cudaMemcpy(d_slots, h_slots, sizeof(h_slots), cudaMemcpyHostToDevice);
+  cudaMemcpy(d_pos, h_pos, sizeof(h_pos), cudaMemcpyHostToDevice);
+  cudaMemset(d_sums, 0, nb * sizeof(uint64_t));
+  cudaMemset(d_status, 0, sizeof(uint32_t));
+  rc = kvcs_write_kv(wcaches, layers, bs, ntok, (const void *const *)keys,
+                     (const void *const *)vals, d_slots, d_pos, d_sums, d_status, NULL);
+  CHECK(rc == KVCS_OK, "kvcs_write_kv");
+  uint64_t sums[5];
+  cudaMemcpy(sums, d_sums, sizeof(sums), cudaMemcpyDeviceToHost);
+  cudaMemcpy(&status, d_status, sizeof(status), cudaMemcpyDeviceToHost);
+  CHECK(status == 0, "write status clear");
+  for (int q = 0; q < 3; ++q) {
+    const uint64_t t0 = (uint64_t)q * bs;
+    const uint64_t t1 = t0 + bs < (uint64_t)ntok ? t0 + bs : (uint64_t)ntok;
+    CHECK(sums[h_ids[q]] == (t1 * t1 - t0 * t0) * P * P * msum, "running word = closed form");
+  }
+  CHECK(sums[1] == 0 && sums[2] == 0, "unwritten blocks stay 0");
+
+  printf("c abi ok: 3 block checksums and 3 fused-write block words equal the closed form "
+         "(version %d.%d)\n", kvcs_version() >> 16, kvcs_version() & 0xffff);
+  for (int l = 0; l < layers; ++l) {
+    cudaFree(empty[l]);
+    cudaFree(keys[l]);
+    cudaFree(vals[l]);
+  }
+  cudaFree(d_slots);
+  cudaFree(d_pos);
+  cudaFree(d_sums);
+  free(host_tok);
   for (int l = 0; l < layers; ++l) cudaFree(pools[l]);
   cudaFree(d_po);
   cudaFree(d_fp);
