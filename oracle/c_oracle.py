@@ -22,7 +22,8 @@ class _OracleCacheC(ctypes.Structure):
                 ("layout", ctypes.c_int32), ("layer", ctypes.c_int32),
                 ("head_offset", ctypes.c_int32), ("num_heads", ctypes.c_int32),
                 ("head_bytes", ctypes.c_int32), ("piece_bytes", ctypes.c_int32),
-                ("kernel_block_size", ctypes.c_int32)]
+                ("kernel_block_size", ctypes.c_int32), ("half_stride", ctypes.c_int64),
+                ("block_stride", ctypes.c_int64)]
 
 
 _lib = None
@@ -62,7 +63,8 @@ def block_checksums(caches: Sequence[OracleCache], block_size: int,
         arr[k] = _OracleCacheC(d.ctypes.data, c.num_blocks, c.layout, c.layer,
                                c.head_offset, c.num_heads, c.head_bytes,
                                getattr(c, "piece_bytes", 8),
-                               getattr(c, "kernel_block_size", 0))
+                               getattr(c, "kernel_block_size", 0),
+                               getattr(c, "half_stride", 0), getattr(c, "block_stride", 0))
     po = np.ascontiguousarray(requests.pos_offsets, dtype=np.int64)
     fp = np.ascontiguousarray(requests.first_position, dtype=np.int64)
     nt = np.ascontiguousarray(requests.num_tokens, dtype=np.int64)

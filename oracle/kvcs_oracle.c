@@ -44,6 +44,8 @@ typedef struct oracle_cache {
   int32_t head_bytes; /* K (= V) bytes per head per token; latent/state: row bytes */
   int32_t piece_bytes; /* state: element bytes (2 or 4); else ignored (8) */
   int32_t kernel_block_size; /* HND: slots per kernel sub-block; 0: none */
+  int64_t half_stride;  /* bytes from a block's K page to its V page; 0: packed */
+  int64_t block_stride; /* bytes between blocks' pages; 0: packed */
 } oracle_cache;
 
 /* Tokens of the request's first num_tokens that block `position` holds. */
@@ -66,27 +68,26 @@ static uint64_t piece_at(const oracle_cache *c, int64_t block_size,
                          int64_t p) {
   int64_t hb = c->head_bytes;
   int64_t byte = 8 * p;
-  int64_t off;
+  int64_t kv = 0;
+  if (c->layout != ORACLE_LAYOUT_LATENT && byte >= hb) {
+    kv = 1;
+    byte -= hb;
+  }
+  /* the page of (kv, block); explicit strides place it anywhere in the pool */
+  int64_t page_bytes = block_size * c->num_heads * hb;
+  int64_t half = c->half_stride ? c->half_stride : c->num_blocks * page_bytes;
+  int64_t stride = c->block_stride ? c->block_stride : page_bytes;
+  int64_t off = kv * half + block * stride;
   if (c->layout == ORACLE_LAYOUT_LATENT) {
-    off = (block * block_size + slot) * hb + byte;
+    off += slot * hb + byte;
+  } else if (c->layout == ORACLE_LAYOUT_NHD) {
+    off += (slot * c->num_heads + head) * hb + byte;
+  } else if (c->layout == ORACLE_LAYOUT_XSPLIT) {
+    /* x elements make 16 bytes: [heads][head_bytes/16][block_size][16] */
+    off += ((head * (hb / 16) + byte / 16) * block_size + slot) * 16 + byte % 16;
   } else {
-    int64_t kv = 0;
-    if (byte >= hb) {
-      kv = 1;
-      byte -= hb;
-    }
-    int64_t page = kv * c->num_blocks + block;
-    if (c->layout == ORACLE_LAYOUT_NHD) {
-      off = ((page * block_size + slot) * c->num_heads + head) * hb + byte;
-    } else if (c->layout == ORACLE_LAYOUT_XSPLIT) {
-      /* x elements make 16 bytes: [heads][head_bytes/16][block_size][16] */
-      off = (((page * c->num_heads + head) * (hb / 16) + byte / 16) * block_size + slot) * 16 +
-            byte % 16;
-    } else {
-      int64_t kbs = c->kernel_block_size > 0 ? c->kernel_block_size : block_size;
-      off = (((page * (block_size / kbs) + slot / kbs) * c->num_heads + head) * kbs +
-             slot % kbs) * hb + byte;
-    }
+    int64_t kbs = c->kernel_block_size > 0 ? c->kernel_block_size : block_size;
+    off += ((slot / kbs * c->num_heads + head) * kbs + slot % kbs) * hb + byte;
   }
   uint64_t x = 0;
   for (int k = 0; k < 8; ++k) x |= (uint64_t)c->data[off + k] << (8 * k);
@@ -112,7 +113,8 @@ static uint64_t slice_checksum(const oracle_cache *c, int64_t block_size,
 /* Element p (little-endian, unsigned) of local row `row` of a state block. */
 static uint64_t state_piece(const oracle_cache *c, int64_t block, int64_t row,
                             int64_t p) {
-  int64_t off = (block * c->num_heads + row) * c->head_bytes + p * c->piece_bytes;
+  int64_t stride = c->block_stride ? c->block_stride : (int64_t)c->num_heads * c->head_bytes;
+  int64_t off = block * stride + row * c->head_bytes + p * c->piece_bytes;
   uint64_t x = 0;
   for (int k = 0; k < c->piece_bytes; ++k) x |= (uint64_t)c->data[off + k] << (8 * k);
   return x;
@@ -226,6 +228,7 @@ int oracle_block_checksums(const oracle_cache *caches, int32_t num_caches,
       return -1;
     if (c->layout == ORACLE_LAYOUT_LATENT && c->num_heads != 1) return -1;
     if (c->layout < 0 || c->layout > 3) return -1;
+    if (c->half_stride < 0 || c->block_stride < 0) return -1;
     if (c->layout == ORACLE_LAYOUT_XSPLIT && c->head_bytes % 16) return -1;
     if (c->kernel_block_size != 0 &&
         (c->layout != ORACLE_LAYOUT_HND || c->kernel_block_size < 0 ||

@@ -91,6 +91,8 @@ class OracleCache:
     head_bytes: int
     piece_bytes: int = 8
     kernel_block_size: int = 0   # HND: slots per kernel sub-block (0: none)
+    half_stride: int = 0         # bytes from a block's K page to its V page (0: packed)
+    block_stride: int = 0        # bytes between blocks' pages (0: packed)
 
 
 @dataclass(frozen=True)
@@ -139,24 +141,38 @@ def piece_byte_offset(cache: OracleCache, block_size: int, block: int,
     """
     hb = cache.head_bytes
     byte = 8 * p
-    if cache.layout == LAYOUT_LATENT:
-        return (block * block_size + slot) * hb + byte
     kv = 0
-    if byte >= hb:
+    if cache.layout != LAYOUT_LATENT and byte >= hb:
         kv, byte = 1, byte - hb
-    page = kv * cache.num_blocks + block
+    base = page_start(cache, block_size, kv, block)
+    if cache.layout == LAYOUT_LATENT:
+        return base + slot * hb + byte
     if cache.layout == LAYOUT_NHD:
-        return ((page * block_size + slot) * cache.num_heads + head) * hb + byte
+        return base + (slot * cache.num_heads + head) * hb + byte
     if cache.layout == LAYOUT_HND:
         kbs = cache.kernel_block_size or block_size
         sub, within = divmod(slot, kbs)
-        return (((page * (block_size // kbs) + sub) * cache.num_heads + head) * kbs +
-                within) * hb + byte
+        return base + ((sub * cache.num_heads + head) * kbs + within) * hb + byte
     if cache.layout == LAYOUT_XSPLIT:
         chunk, inner = divmod(byte, 16)
-        return (((page * cache.num_heads + head) * (hb // 16) + chunk) * block_size +
-                slot) * 16 + inner
+        return base + ((head * (hb // 16) + chunk) * block_size + slot) * 16 + inner
     raise ValueError(f"unknown layout {cache.layout}")
+
+
+def page_bytes(cache: OracleCache, block_size: int) -> int:
+    """Bytes of one page: one block's K, its V, or its latent rows."""
+    return block_size * cache.num_heads * cache.head_bytes
+
+
+def page_start(cache: OracleCache, block_size: int, kv: int, block: int) -> int:
+    """Byte offset of the page holding half ``kv`` (0: K, 1: V) of ``block``:
+    by default the pool is all K pages then all V pages; explicit strides
+    place a block's pages anywhere (e.g. K and V interleaved per block, or
+    padded blocks)."""
+    page = page_bytes(cache, block_size)
+    half = cache.half_stride or cache.num_blocks * page
+    stride = cache.block_stride or page
+    return kv * half + block * stride
 
 
 def read_piece(cache: OracleCache, offset: int) -> int:
@@ -228,8 +244,11 @@ def check_cache(cache: OracleCache, block_size: int) -> None:
         raise ValueError("bad head range")
     if cache.head_offset + cache.num_heads > MAX_KV_HEADS_PER_LAYER:
         raise ValueError("a layer with more than H KV heads is excluded")
+    if cache.half_stride < 0 or cache.block_stride < 0:
+        raise ValueError("strides are byte offsets within the one pool array")
     halves = 1 if cache.layout == LAYOUT_LATENT else 2
-    need = halves * cache.num_blocks * block_size * cache.num_heads * cache.head_bytes
+    need = page_start(cache, block_size, halves - 1, cache.num_blocks - 1) + \
+        page_bytes(cache, block_size)
     if cache.data.size < need:
         raise ValueError("pool smaller than its declared geometry")
 
@@ -237,7 +256,8 @@ def check_cache(cache: OracleCache, block_size: int) -> None:
 def state_piece(cache: OracleCache, block: int, row: int, p: int) -> int:
     """Element ``p`` of local row ``row`` of a state block, read unsigned."""
     w = cache.piece_bytes
-    off = (block * cache.num_heads + row) * cache.head_bytes + w * p
+    stride = cache.block_stride or cache.num_heads * cache.head_bytes
+    off = block * stride + row * cache.head_bytes + w * p
     return int.from_bytes(bytes(cache.data[off:off + w]), "little")
 
 

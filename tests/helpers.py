@@ -26,10 +26,22 @@ def host_bytes(t) -> np.ndarray:
 
 
 def oracle_caches(caches) -> list[OracleCache]:
-    return [OracleCache(host_bytes(c.pool), c.num_blocks, c.layout, c.layer,
-                        c.head_offset, c.num_heads, c.head_bytes,
-                        getattr(c, "piece_bytes", 0) or 8,
-                        getattr(c, "kernel_block_size", 0)) for c in caches]
+    """Host copies of the pools.  A separate V tensor is appended to the K
+    bytes (data movement only), its pages then half_stride = len(K) bytes
+    after the K pages."""
+    out = []
+    for c in caches:
+        data = host_bytes(c.pool)
+        half = getattr(c, "half_stride", 0)
+        v_pool = getattr(c, "v_pool", None)
+        if v_pool is not None:
+            half = data.size
+            data = np.concatenate([data, host_bytes(v_pool)])
+        out.append(OracleCache(data, c.num_blocks, c.layout, c.layer, c.head_offset,
+                               c.num_heads, c.head_bytes, getattr(c, "piece_bytes", 0) or 8,
+                               getattr(c, "kernel_block_size", 0), half,
+                               getattr(c, "block_stride", 0)))
+    return out
 
 
 def oracle_requests(wl) -> OracleRequests:

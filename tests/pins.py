@@ -22,6 +22,7 @@ with independent code so a bug shared by a form and a pin is unlikely.
 
 from __future__ import annotations
 
+import dataclasses
 import json
 import random
 from pathlib import Path
@@ -330,8 +331,9 @@ def _swap(case, bs):
 def pin_layout_invariance(form):
     """The same KV in every memory layout gives the same checksums (the
     paragraph on TP ranks and layouts): NHD, HND, HND in kernel sub-blocks of
-    1 and 2 slots, and x-split ([heads][head_bytes/16][block_size][16]).  The
-    other layouts are the NHD pool permuted by numpy, each permutation
+    1 and 2 slots, x-split ([heads][head_bytes/16][block_size][16]), and NHD
+    pages placed by explicit strides (K and V interleaved per block; padded
+    blocks).  The other layouts are the NHD pool rearranged by numpy, each
     written from the layout's shape."""
     lengths = [10, 3]
     bs, heads, hb = 4, 3, 32
@@ -359,6 +361,23 @@ def pin_layout_invariance(form):
         variants.append(relaid(
             W.LAYOUT_HND, lambda v, k=kbs: v.reshape(2, v.shape[1], bs // k, k, heads, hb)
             .transpose(0, 1, 2, 4, 3, 5), kbs=kbs))
+    # explicit strides: K and V interleaved per block ([block][kv][page]),
+    # and blocks padded by 24 bytes
+    page = bs * heads * hb
+    inter = []
+    for c in caches_n:
+        v = c.data.reshape(2, c.num_blocks, page).transpose(1, 0, 2)
+        inter.append(dataclasses.replace(c, data=np.ascontiguousarray(v).reshape(-1),
+                                         half_stride=page, block_stride=2 * page))
+    variants.append(inter)
+    padded = []
+    for c in caches_n:
+        buf = np.zeros((2, c.num_blocks, page + 24), dtype=np.uint8)
+        buf[:, :, :page] = c.data.reshape(2, c.num_blocks, page)
+        padded.append(dataclasses.replace(c, data=buf.reshape(-1),
+                                          half_stride=c.num_blocks * (page + 24),
+                                          block_stride=page + 24))
+    variants.append(padded)
     for caches in variants:
         b, _ = form(caches, bs, rn)
         assert [int(x) for x in a] == [int(x) for x in b], caches[0].layout

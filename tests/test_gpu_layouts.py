@@ -204,3 +204,42 @@ def test_xsplit_and_sub_blocks_against_the_oracle_directly(layout, kbs, hb, bs):
     exp, est = full_oracle(wl)
     got, st = run(wl)
     assert st == est == 0 and np.array_equal(got, exp)
+
+
+@pytest.mark.parametrize("kind", ["interleaved", "separate", "separate_v_first", "padded16",
+                                  "padded8"])
+@pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND])
+def test_strided_pools_against_the_oracle_directly(kind, layout):
+    """Pages placed by explicit strides or in separate K and V tensors, read
+    by the GPU and by the oracle (which takes the strides itself; a separate
+    V tensor is appended to the K bytes on the host)."""
+    from gpu_helpers import full_oracle
+    wl = W.random_case(13, DEV, layout=layout, layers=3, heads=4, head_bytes=64,
+                       block_size=16, lengths=(70, 33, 5))
+    caches, keep = [], []
+    for c in wl.caches:
+        pb = page_bytes(wl, c)
+        halves = c.pool.view(2, c.num_blocks, pb)
+        if kind == "interleaved":
+            pool = halves.transpose(0, 1).contiguous().view(-1)
+            caches.append(dataclasses.replace(c, pool=pool, half_stride=pb, block_stride=2 * pb))
+        elif kind.startswith("separate"):
+            if kind == "separate_v_first":
+                v = halves[1].clone()
+                k = halves[0].clone()
+            else:
+                k = halves[0].clone()
+                v = halves[1].clone()
+            keep.append((k, v))
+            caches.append(dataclasses.replace(c, pool=k.view(-1), v_pool=v.view(-1)))
+        else:
+            pad = 16 if kind == "padded16" else 8
+            stride = pb + pad
+            buf = torch.zeros(2 * c.num_blocks * stride, dtype=torch.uint8, device=DEV)
+            buf.view(2 * c.num_blocks, stride)[:, :pb] = halves.reshape(2 * c.num_blocks, pb)
+            caches.append(dataclasses.replace(c, pool=buf, block_stride=stride,
+                                              half_stride=c.num_blocks * stride))
+    wl2 = with_caches(wl, caches)
+    exp, est = full_oracle(wl2)
+    got, st = run(wl2)
+    assert st == est == 0 and np.array_equal(got, exp)

@@ -59,3 +59,26 @@ def test_threads_do_not_change_results():
     one = c_form(caches, wl.block_size, reqs, threads=1)
     for t in (2, 3, 7, 64):
         assert c_form(caches, wl.block_size, reqs, threads=t) == one
+
+
+@pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND, W.LAYOUT_LATENT, W.LAYOUT_XSPLIT])
+def test_c_equals_python_with_strides(layout):
+    """Pages placed by explicit strides: K and V interleaved per block with
+    padding."""
+    import dataclasses
+    import numpy as np
+    hb = 32
+    heads = 1 if layout == W.LAYOUT_LATENT else 2
+    wl = W.random_case(3, "cpu", layout=layout, layers=2, heads=heads, head_bytes=hb,
+                       block_size=4, lengths=(11, 6))
+    caches, reqs = oracle_inputs(wl)
+    page = 4 * heads * hb
+    halves = 1 if layout == W.LAYOUT_LATENT else 2
+    strided = []
+    for c in caches:
+        buf = np.zeros((c.num_blocks, halves, page + 16), dtype=np.uint8)
+        buf[:, :, :page] = c.data.reshape(halves, c.num_blocks, page).transpose(1, 0, 2)
+        strided.append(dataclasses.replace(c, data=buf.reshape(-1), half_stride=page + 16,
+                                           block_stride=halves * (page + 16)))
+    a = py_form(caches, 4, reqs)
+    assert c_form(strided, 4, reqs) == py_form(strided, 4, reqs) == a

@@ -81,6 +81,8 @@ MUTANTS = {
     "block_id_ignored": ("piece_byte_offset", _block_ignored),
     "xsplit_axes_swapped": ("piece_byte_offset", _xsplit_axes_swapped),
     "sub_blocks_ignored": ("piece_byte_offset", _sub_blocks_ignored),
+    "strides_ignored": ("page_start", lambda c, bs, kv, block:
+                        (kv * c.num_blocks + block) * O.page_bytes(c, bs)),
     "big_endian": ("read_piece", lambda c, off: int.from_bytes(
         bytes(c.data[off:off + 8]), "big")),
 }
