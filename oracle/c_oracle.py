@@ -18,7 +18,8 @@ from .kvcs_oracle import OracleCache, OracleRequests
 
 
 class _OracleCacheC(ctypes.Structure):
-    _fields_ = [("data", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
+    _fields_ = [("data", ctypes.c_void_p), ("data_bytes", ctypes.c_int64),
+                ("num_blocks", ctypes.c_int64),
                 ("layout", ctypes.c_int32), ("layer", ctypes.c_int32),
                 ("head_offset", ctypes.c_int32), ("num_heads", ctypes.c_int32),
                 ("head_bytes", ctypes.c_int32), ("piece_bytes", ctypes.c_int32),
@@ -60,7 +61,7 @@ def block_checksums(caches: Sequence[OracleCache], block_size: int,
     datas = [np.ascontiguousarray(c.data, dtype=np.uint8) for c in caches]
     arr = (_OracleCacheC * max(1, len(caches)))()
     for k, (c, d) in enumerate(zip(caches, datas)):
-        arr[k] = _OracleCacheC(d.ctypes.data, c.num_blocks, c.layout, c.layer,
+        arr[k] = _OracleCacheC(d.ctypes.data, d.size, c.num_blocks, c.layout, c.layer,
                                c.head_offset, c.num_heads, c.head_bytes,
                                getattr(c, "piece_bytes", 8),
                                getattr(c, "kernel_block_size", 0),

@@ -36,6 +36,7 @@
 
 typedef struct oracle_cache {
   const uint8_t *data; /* host bytes of the whole pool */
+  int64_t data_bytes;  /* how many bytes `data` holds */
   int64_t num_blocks;
   int32_t layout;
   int32_t layer;
@@ -197,9 +198,26 @@ static void *run_job(void *arg) {
   return NULL;
 }
 
+/* Bytes the pool must hold for every page its geometry addresses: up to the
+ * end of the last block's last page (state: the last block's rows). */
+static int64_t pool_bytes_needed(const oracle_cache *c, int64_t block_size) {
+  if (c->num_blocks == 0) return 0;
+  if (c->layout == ORACLE_LAYOUT_STATE) {
+    int64_t state = (int64_t)c->num_heads * c->head_bytes;
+    int64_t stride = c->block_stride ? c->block_stride : state;
+    return (c->num_blocks - 1) * stride + state;
+  }
+  int64_t page_bytes = block_size * c->num_heads * (int64_t)c->head_bytes;
+  int64_t half = c->half_stride ? c->half_stride : c->num_blocks * page_bytes;
+  int64_t stride = c->block_stride ? c->block_stride : page_bytes;
+  int64_t last_half = c->layout == ORACLE_LAYOUT_LATENT ? 0 : 1;
+  return last_half * half + (c->num_blocks - 1) * stride + page_bytes;
+}
+
 /*
  * One uint64 per global position index into out[pos_offsets[num_requests]].
- * Returns 0, or -1 for arguments the definition does not cover.  *status gets
+ * Returns 0, or -1 for arguments the definition does not cover or a pool
+ * smaller than its declared geometry.  *status gets
  * ORACLE_STATUS_BAD_BLOCK_ID if some position's block id is outside
  * [0, num_blocks) of some cache (that position's output is 0).
  * num_threads <= 0 means one thread.
@@ -215,11 +233,14 @@ int oracle_block_checksums(const oracle_cache *caches, int32_t num_caches,
     return -1;
   for (int32_t k = 0; k < num_caches; ++k) {
     const oracle_cache *c = &caches[k];
+    if (c->num_blocks < 0 || c->data_bytes < 0 || (c->data_bytes > 0 && !c->data))
+      return -1;
     if (c->layout == ORACLE_LAYOUT_STATE) {
       if ((c->piece_bytes != 2 && c->piece_bytes != 4) || c->head_bytes <= 0 ||
           c->head_bytes % c->piece_bytes || c->num_heads < 1 || c->head_offset < 0 ||
-          (int64_t)c->head_offset + c->num_heads > (int64_t)ORACLE_H)
+          (int64_t)c->head_offset + c->num_heads > (int64_t)ORACLE_H || c->block_stride < 0)
         return -1;
+      if (pool_bytes_needed(c, block_size) > c->data_bytes) return -1;
       continue;
     }
     if (c->head_bytes <= 0 || c->head_bytes % 8 || c->num_heads < 1 ||
@@ -234,6 +255,7 @@ int oracle_block_checksums(const oracle_cache *caches, int32_t num_caches,
         (c->layout != ORACLE_LAYOUT_HND || c->kernel_block_size < 0 ||
          block_size % c->kernel_block_size))
       return -1;
+    if (pool_bytes_needed(c, block_size) > c->data_bytes) return -1;
   }
   if (pos_offsets[0] != 0) return -1;
   for (int64_t r = 0; r < num_requests; ++r)

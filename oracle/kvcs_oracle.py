@@ -13,18 +13,18 @@ docstring items 1 and 2, the attributes ``MAX_KV_HEADS_PER_LAYER`` and
 reduced mod 2**64 only where the definition says "mod 2**64", so this form is
 the slow, obviously-correct ground truth for small inputs.
 
-Definition restated (same page, module docstring):
+Definition restated in this module's words (same page, module docstring):
 
-* A *slice* is the KV of one layer and one KV head inside one block: the K and
-  the V of the block's tokens for that head, one token after another (per
-  token: the K bytes of the head, then its V bytes) and cut into little-endian
-  8-byte pieces.  Piece ``p`` of the token at request position ``t`` has index
-  ``j = t*P + p`` where ``P`` is the number of pieces per token.
+* For each (layer, KV head) pair, a block holds one *slice*.  Its bytes are,
+  for each token of the block in turn, that head's K bytes followed by its V
+  bytes.  Reading them as consecutive little-endian 64-bit words gives the
+  pieces; the word ``p`` of the token at request position ``t`` has index
+  ``j = t*P + p``, with ``P`` words per token.
 * ``s = sum_j x_j * (2*j + 1) mod 2**64``  (item 1).
 * ``c = sum_{layer, head} m * s mod 2**64`` with
   ``m = 2*(layer*H + head) + 1`` and ``H = MAX_KV_HEADS_PER_LAYER = 1 << 16``
   (item 2; the attribute list of the same page).
-* Slots of the last block at or past ``num_tokens`` are left out of the sum
+* A slot whose token index is ``num_tokens`` or more contributes nothing
   (dataclass ``KVChecksumBlocks``, field ``num_tokens``).
 
 Readings where the page is silent:
@@ -113,9 +113,10 @@ class OracleRequests:
 
 
 def num_valid_tokens(position: int, block_size: int, num_tokens: int) -> int:
-    """How many of the request's first ``num_tokens`` tokens block
-    ``position`` holds (function ``num_valid_tokens``): the block's slots are
-    tokens ``position*block_size + slot``; count those below ``num_tokens``."""
+    """Count of the block's slots that carry a token (function
+    ``num_valid_tokens``): slot ``slot`` of block ``position`` is token
+    ``position*block_size + slot``, and only tokens below ``num_tokens``
+    exist."""
     return sum(1 for slot in range(block_size)
                if token_position(position, block_size, slot) < num_tokens)
 
@@ -225,7 +226,13 @@ def check_cache(cache: OracleCache, block_size: int) -> None:
         if cache.head_offset < 0 or cache.num_heads < 1 or \
                 cache.head_offset + cache.num_heads > MAX_KV_HEADS_PER_LAYER:
             raise ValueError("bad row range")
-        if cache.data.size < cache.num_blocks * cache.num_heads * cache.head_bytes:
+        if cache.block_stride < 0:
+            raise ValueError("strides are byte offsets within the one pool array")
+        state = cache.num_heads * cache.head_bytes
+        need = 0
+        if cache.num_blocks > 0:
+            need = (cache.num_blocks - 1) * (cache.block_stride or state) + state
+        if cache.data.size < need:
             raise ValueError("pool smaller than its declared geometry")
         return
     if cache.head_bytes <= 0 or cache.head_bytes % 8:
@@ -247,8 +254,10 @@ def check_cache(cache: OracleCache, block_size: int) -> None:
     if cache.half_stride < 0 or cache.block_stride < 0:
         raise ValueError("strides are byte offsets within the one pool array")
     halves = 1 if cache.layout == LAYOUT_LATENT else 2
-    need = page_start(cache, block_size, halves - 1, cache.num_blocks - 1) + \
-        page_bytes(cache, block_size)
+    need = 0
+    if cache.num_blocks > 0:
+        need = page_start(cache, block_size, halves - 1, cache.num_blocks - 1) + \
+            page_bytes(cache, block_size)
     if cache.data.size < need:
         raise ValueError("pool smaller than its declared geometry")
 
