@@ -155,6 +155,14 @@ def describe(wl, name) -> dict:
                    "(a latency case, not a bandwidth figure)")}
 
 
+def arm_config(wl, args, ws) -> dict:
+    """The ``config`` object of a line: the workload and how it is run (the
+    same keys in both arms)."""
+    return {**describe(wl, args.config), "parallelism": f"replicas{ws}",
+            "memory_layout": args.layout, "columns": max(1, args.columns),
+            "verify": bool(args.verify)}
+
+
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
@@ -329,9 +337,11 @@ def host_cores() -> int:
 
 def _oracle_inputs(wl, n: int, seed: int):
     """Host inputs of the oracle for ``n`` random block positions of the
-    workload (only the pages they read), and the KV bytes they hold."""
+    workload (only the pages they read): (caches, requests, KV bytes they
+    hold, number of positions, the positions)."""
     import numpy as np
     from oracle.kvcs_oracle import OracleCache, OracleRequests
+    from paged_kv_cache_kvcs_gb300 import workloads as W
 
     rng = np.random.default_rng(seed)
     P = wl.num_positions
@@ -340,54 +350,55 @@ def _oracle_inputs(wl, n: int, seed: int):
     req = torch.searchsorted(po, pos, right=True) - 1
     q = wl.first_position.cpu()[req] + (pos - po[req])
     nt = wl.num_tokens.cpu()[req]
-    ids = wl.block_ids.cpu()[pos].to(torch.int64).to(wl.block_ids.device)
+    ids = wl.block_ids.cpu()[pos].to(torch.int64)
     caches = []
     state = bool(wl.caches) and wl.caches[0].layout == 4
     for c in wl.caches:
-        halves = 1 if c.layout in (2, 4) else 2
-        page = (1 if state else wl.block_size) * c.num_heads * c.head_bytes
-        pages = c.pool.view(halves, c.num_blocks, page)[:, ids].cpu().numpy()
+        pages = W.gather_pages(c, wl.block_size, ids).cpu().numpy()
         caches.append(OracleCache(pages.reshape(-1), len(pos), c.layout, c.layer,
                                   c.head_offset, c.num_heads, c.head_bytes,
-                                  c.piece_bytes or 8))
+                                  c.piece_bytes or 8, c.kernel_block_size))
     reqs = OracleRequests(list(range(len(pos) + 1)), q.tolist(), nt.tolist(),
                           list(range(len(pos))))
     if state:
         per_state = sum(c.num_heads * c.head_bytes for c in wl.caches)
-        return caches, reqs, per_state * int((q == 0).sum()), len(pos)
+        return caches, reqs, per_state * int((q == 0).sum()), len(pos), pos.numpy()
     per_token = sum((1 if c.layout == 2 else 2) * c.num_heads * c.head_bytes
                     for c in wl.caches)
     bs = wl.block_size
     valid = sum(max(0, min(bs, int(t) - int(qq) * bs)) for qq, t in zip(q, nt))
-    return caches, reqs, valid * per_token, len(pos)
+    return caches, reqs, valid * per_token, len(pos), pos.numpy()
 
 
 def oracle_run(wl, n: int, threads: int, seed: int):
     """One timed oracle run over ``n`` random positions: (seconds, KV bytes,
     positions)."""
     from oracle import c_oracle
-    caches, reqs, nbytes, npos = _oracle_inputs(wl, n, seed)
+    caches, reqs, nbytes, npos, _ = _oracle_inputs(wl, n, seed)
     t0 = time.perf_counter()
     c_oracle.block_checksums(caches, wl.block_size, reqs, num_threads=threads)
     return time.perf_counter() - t0, nbytes, npos
 
 
-def oracle_timed(wl, seconds: float, threads: int, seed: int):
+def oracle_timed(wl, seconds: float, threads: int, seed: int) -> dict:
     """About ``seconds`` of oracle work on one sample of the workload (the
-    sample is repeated when the whole workload takes less): (GB/s,
-    blocks/s, description)."""
+    sample is repeated when the whole workload takes less).  Returns GB/s,
+    blocks/s, a description, and the sampled positions with the oracle's
+    values there (for checking the GPU's output)."""
     from oracle import c_oracle
     n = oracle_calibrate(wl, seconds, threads, seed)
-    caches, reqs, nbytes, npos = _oracle_inputs(wl, n, seed + 7)
+    caches, reqs, nbytes, npos, pos = _oracle_inputs(wl, n, seed + 7)
     spent, runs = 0.0, 0
+    vals = None
     while runs == 0 or (spent < 0.8 * seconds and runs < 100):
         t0 = time.perf_counter()
-        c_oracle.block_checksums(caches, wl.block_size, reqs, num_threads=threads)
+        vals, _ = c_oracle.block_checksums(caches, wl.block_size, reqs, num_threads=threads)
         spent += time.perf_counter() - t0
         runs += 1
     desc = (f"{npos} random block positions of the workload ({nbytes / 1e9:.2f} GB "
             f"of KV), {runs} oracle run(s) totalling {spent:.1f} s on {threads} threads")
-    return nbytes * runs / spent / 1e9, npos * runs / spent, desc
+    return {"gbs": nbytes * runs / spent / 1e9, "bps": npos * runs / spent, "desc": desc,
+            "positions": pos, "values": vals}
 
 
 def oracle_calibrate(wl, seconds: float, threads: int, seed: int) -> int:
@@ -398,6 +409,42 @@ def oracle_calibrate(wl, seconds: float, threads: int, seed: int) -> int:
         if dt >= 0.5 * seconds or npos >= wl.num_positions:
             return max(1, min(wl.num_positions, int(round(n * seconds / max(dt, 1e-4)))))
         n = min(wl.num_positions, max(2 * n, int(n * 0.6 * seconds / max(dt, 1e-4))))
+
+
+def python_oracle_tiny(seed: int) -> dict:
+    """The pure-Python oracle over the whole tiny workload (2 layers, 2 heads,
+    one request of 100 tokens), timed on one host thread."""
+    from oracle import kvcs_oracle
+    from oracle.kvcs_oracle import OracleCache, OracleRequests
+    from paged_kv_cache_kvcs_gb300 import workloads as W
+    wl = W.tiny(seed, "cpu")
+    caches = [OracleCache(c.pool.numpy(), c.num_blocks, c.layout, c.layer, c.head_offset,
+                          c.num_heads, c.head_bytes) for c in wl.caches]
+    reqs = OracleRequests(wl.pos_offsets.tolist(), wl.first_position.tolist(),
+                          wl.num_tokens.tolist(), wl.block_ids.tolist())
+    runs, spent = 0, 0.0
+    while runs == 0 or (spent < 1.0 and runs < 20):
+        t0 = time.perf_counter()
+        kvcs_oracle.block_checksums(caches, wl.block_size, reqs)
+        spent += time.perf_counter() - t0
+        runs += 1
+    nbytes = kv_bytes(wl)
+    return {"value": round(nbytes * runs / spent / 1e9, 6), "unit": "GB/s", "cores": 1,
+            "kind": "oracle (pure Python, exact ints)",
+            "blocks_per_s": round(wl.num_positions * runs / spent, 2),
+            "sample": f"the whole tiny workload ({nbytes} B of KV, {wl.num_positions} "
+                      f"positions), {runs} run(s) totalling {spent:.2f} s"}
+
+
+def parity_check(got, positions, expected) -> dict:
+    """The timed run's output at the oracle's sampled positions: how many
+    positions were compared and how many differ (bit for bit)."""
+    import numpy as np
+    g = np.asarray(got).view(np.uint64)
+    e = np.asarray(expected, dtype=np.uint64)
+    bad = int(np.count_nonzero(g[positions] != e))
+    return {"positions": int(len(positions)), "mismatches": bad,
+            "against": "C oracle at the cpu_baseline sample's positions"}
 
 
 # ---------------------------------------------------------------------------
@@ -416,7 +463,7 @@ def run_reference(args, ws, rank):
     # sample of positions gathered to the host once
     per_step = min(1.5, max(0.005, 90.0 / (args.warmup + args.steps)))
     n = oracle_calibrate(wl, per_step, cores, args.seed)
-    caches, reqs, nbytes, npos = _oracle_inputs(wl, n, args.seed + 1)
+    caches, reqs, nbytes, npos, _ = _oracle_inputs(wl, n, args.seed + 1)
     times = []
     for k in range(args.warmup + args.steps):
         t0 = time.perf_counter()
@@ -432,7 +479,7 @@ def run_reference(args, ws, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u64", "data": "synthetic",
             "blocks_per_s": round(statistics.mean(t[1] for t in times), 3),
-            "config": describe(wl, args.config),
+            "config": arm_config(wl, args, ws),
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 3), "unit": "GB/s",
@@ -560,35 +607,36 @@ def run_write(args, ws, rank, local):
     if ws == 1 and not args.no_cpu_baseline:
         # the oracle computing the same block words from the written pages
         cores = host_cores()
-        gbs, bps, desc = oracle_timed(wb.checksum_workload(), args.cpu_seconds, cores, args.seed)
-        line["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s of written KV checksummed",
-                                "cores": cores, "kind": "oracle", "blocks_per_s": round(bps, 2),
-                                "sample": desc}
+        ot = oracle_timed(wb.checksum_workload(), args.cpu_seconds, cores, args.seed)
+        line["cpu_baseline"] = {"value": round(ot["gbs"], 3),
+                                "unit": "GB/s of written KV checksummed",
+                                "cores": cores, "kind": "oracle",
+                                "blocks_per_s": round(ot["bps"], 2), "sample": ot["desc"]}
+        # the timed call once more on zeroed running words (every timed step
+        # added its terms again), read at the sampled blocks
+        with torch.cuda.stream(stream):
+            sums.zero_()
+            fused()
+        torch.cuda.synchronize(dev)
+        words = sums[bids.long()].cpu().numpy()
+        line["parity"] = parity_check(words, ot["positions"], ot["values"])
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, ws, rank, local):
+def time_checksums(wl, args, dev, stream, ws, rank, steps, warmup, clocks=True) -> dict:
+    """Warm-up, then ``steps`` timed calls over the whole workload, each
+    bracketed by CUDA events on the launching stream (after a barrier and a
+    synchronize).  The output buffer keeps the last timed call's result."""
     import paged_kv_cache_kvcs_gb300 as kvcs
-
-    kvcs.load_library()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    wl = make_workload(args.config, args.seed + rank, dev)
-    if args.layout != "nhd":
-        wl = relayout(wl, args.layout)
-    if args.columns > 1:
-        for i, c in enumerate(wl.caches):
-            c.column = i % args.columns
-    stream = torch.cuda.Stream(dev)
     out = torch.empty(wl.num_positions, dtype=torch.int64, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions)
-    nbytes = kv_bytes(wl)
     raw_stream = stream.cuda_stream
+    ncols = max(1, args.columns)
+    values = None
     if args.columns > 1 or args.verify:
         # the replica-key path: one column per key, plus (--verify) the
         # tagged row sums compared with stored values in the same call
-        ncols = max(1, args.columns)
         values = torch.empty((wl.num_positions, ncols), dtype=torch.int64, device=dev)
         extras = {}
         if args.verify:
@@ -603,7 +651,6 @@ def run_ours(args, ws, rank, local):
             extras = dict(tags=tags, expected=stored,
                           mismatch=torch.empty(n, dtype=torch.uint8, device=dev),
                           mismatch_count=torch.zeros(1, dtype=torch.int32, device=dev))
-
         n_pos = wl.num_positions       # read once: the property syncs the device
 
         def step():
@@ -619,23 +666,21 @@ def run_ours(args, ws, rank, local):
             ck(out, status, raw_stream)
 
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
     torch.cuda.synchronize(dev)
     if int(status.item()) != 0:
         raise SystemExit(f"status {int(status.item())} during warm-up")
 
-    # ---- device-timed region: K steps, events on the launching stream ----
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(torch.cuda.current_device() if ws == 1 else local) \
-        if rank == 0 else None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if (clocks and rank == 0) else None
     barrier(ws)
     torch.cuda.synchronize(dev)
     launches0 = kvcs.launch_count()
     t_wall0 = time.time()
     with torch.cuda.stream(stream):
-        for k in range(args.steps):
+        for k in range(steps):
             starts[k].record(stream)
             step()
             ends[k].record(stream)
@@ -643,98 +688,190 @@ def run_ours(args, ws, rank, local):
     t_wall1 = time.time()
     barrier(ws)
     launches = kvcs.launch_count() - launches0
-    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
-    per = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
-    total_s = starts[0].elapsed_time(ends[-1]) / 1e3
-    total_s = all_max(total_s, ws)
-    job_bytes = all_sum(nbytes * args.steps, ws)
+    clk = sampler.stop(t_wall0, t_wall1) if sampler else None
+    if int(status.item()) != 0:
+        raise SystemExit(f"status {int(status.item())} during the timed steps")
+    per = [a.elapsed_time(b) / 1e3 for a, b in zip(starts, ends)]
+    total_s = all_max(starts[0].elapsed_time(ends[-1]) / 1e3, ws)
+    if values is not None:
+        # a position's checksum is its row of column partials summed mod 2^64
+        import numpy as np
+        result = values.cpu().numpy().view(np.uint64).sum(axis=1, dtype=np.uint64)
+    else:
+        result = out.cpu().numpy()
+    return {"total_s": total_s, "launch_s": statistics.mean(per), "launches": int(launches),
+            "clocks": clk, "plan": plan, "nbytes": kv_bytes(wl), "ck": ck, "out": out,
+            "status": status, "result": result}
+
+
+def request_sweep(wl, stream, out, status) -> list:
+    """The first 1, 2, 4, ... requests of the workload alone: GB/s per call
+    timed back to back, and the same call replayed from a CUDA graph."""
+    import paged_kv_cache_kvcs_gb300 as kvcs
+    raw_stream = stream.cuda_stream
+    sweep = []
+    n = 1
+    while n <= wl.num_requests:
+        sub = type(wl)(wl.name, wl.block_size, wl.caches, wl.pos_offsets[:n + 1],
+                       wl.first_position[:n], wl.num_tokens[:n],
+                       wl.block_ids[:int(wl.pos_offsets[n])], wl.info)
+        sck = kvcs.workload_checksummer(sub)
+        sb = kv_bytes(sub)
+        k = max(10, min(500, int(2e10 / max(sb, 1))))
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                sck(out, status, raw_stream)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(k):
+                sck(out, status, raw_stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / k
+        # the same call captured in a CUDA graph (no host work per step)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            sck(out, status, raw_stream)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                graph.replay()
+            e0.record(stream)
+            for _ in range(k):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        tg = e0.elapsed_time(e1) / 1e3 / k
+        sp = kvcs.plan_for(sub.caches, sub.block_size, sub.num_positions)
+        sweep.append({"requests": n, "kv_bytes": sb, "ms": round(t * 1e3, 4),
+                      "gbs": round(sb / t / 1e9, 1), "graph_ms": round(tg * 1e3, 4),
+                      "graph_gbs": round(sb / tg / 1e9, 1), "split": sp["split"]})
+        n *= 2
+    if int(status.item()) != 0:
+        raise SystemExit(f"status {int(status.item())} during the sweep")
+    return sweep
+
+
+def roofline_of(r, workload: str) -> dict:
+    peak, peak_kind = measured_peak()
+    achieved = r["nbytes"] / r["launch_s"] / 1e9
+    plan = r["plan"]
+    return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(workload, plan["units"]),
+            "kernel": "kvcs_bulk_kernel" if plan["kernel"] == 0 else "kvcs_generic_kernel",
+            "launch_ms": round(r["launch_s"] * 1e3, 4)}
+
+
+def cpu_leg(wl, r, seconds: float, seed: int) -> tuple[dict, dict]:
+    """The oracle on all host cores over a sample of the workload, and the
+    timed run's output checked against it at the sampled positions."""
+    cores = host_cores()
+    ot = oracle_timed(wl, seconds, cores, seed)
+    base = {"value": round(ot["gbs"], 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "blocks_per_s": round(ot["bps"], 2), "sample": ot["desc"]}
+    return base, parity_check(r["result"], ot["positions"], ot["values"])
+
+
+def oracle_one_thread(wl, seconds: float, seed: int) -> dict:
+    """The C oracle on one host thread over a sample of the workload."""
+    ot = oracle_timed(wl, seconds, 1, seed + 11)
+    return {"value": round(ot["gbs"], 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "blocks_per_s": round(ot["bps"], 2), "sample": ot["desc"]}
+
+
+def other_configs(args, dev, stream) -> dict:
+    """The DeepSeek-V3-shaped MLA and Llama-3-70B-shaped fp8 workloads, each
+    timed on its own (the previous one freed first), with the oracle on a
+    sample and the 70B request-count sweep."""
+    res = {}
+    for name in ("mla", "llama3_70b"):
+        torch.cuda.empty_cache()
+        wl = make_workload(name, args.seed, dev)
+        r = time_checksums(wl, args, dev, stream, 1, 0, args.steps, args.warmup)
+        entry = {"workload": describe(wl, name),
+                 "value": round(r["nbytes"] * args.steps / r["total_s"] / 1e9, 2),
+                 "unit": "GB/s",
+                 "ms_per_step": round(r["total_s"] / args.steps * 1e3, 4),
+                 "blocks_per_s": round(wl.num_positions * args.steps / r["total_s"], 1),
+                 "gpu_launches": r["launches"],
+                 "plan": {k: r["plan"][k] for k in ("kernel", "split", "launches", "memsets",
+                                                    "grid", "stage_bytes", "units")},
+                 "roofline": roofline_of(r, name), "clocks": r["clocks"]}
+        if name == "llama3_70b":
+            entry["sweep"] = request_sweep(wl, stream, r["out"], r["status"])
+        if not args.no_cpu_baseline:
+            entry["cpu_baseline"], entry["parity"] = cpu_leg(wl, r, args.other_cpu_seconds,
+                                                             args.seed)
+        res[name] = entry
+        del wl, r
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, ws, rank, local):
+    import paged_kv_cache_kvcs_gb300 as kvcs
+
+    kvcs.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = make_workload(args.config, args.seed + rank, dev)
+    if args.layout != "nhd":
+        wl = relayout(wl, args.layout)
+    if args.columns > 1:
+        for i, c in enumerate(wl.caches):
+            c.column = i % args.columns
+    stream = torch.cuda.Stream(dev)
+    r = time_checksums(wl, args, dev, stream, ws, rank, args.steps, args.warmup)
+    total_s = r["total_s"]
+    job_bytes = all_sum(r["nbytes"] * args.steps, ws)
     job_blocks = all_sum(wl.num_positions * args.steps, ws)
     value = job_bytes / total_s / 1e9
-    launch_s = statistics.mean(per)
 
-    # ---- request-count sweep: the first n requests of the workload ----
-    sweep = None
-    if args.sweep:
-        sweep = []
-        n = 1
-        while n <= wl.num_requests:
-            sub = type(wl)(wl.name, wl.block_size, wl.caches, wl.pos_offsets[:n + 1],
-                           wl.first_position[:n], wl.num_tokens[:n],
-                           wl.block_ids[:int(wl.pos_offsets[n])], wl.info)
-            sck = kvcs.workload_checksummer(sub)
-            sb = kv_bytes(sub)
-            k = max(10, min(500, int(2e10 / max(sb, 1))))
-            with torch.cuda.stream(stream):
-                for _ in range(5):
-                    sck(out, status, raw_stream)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(k):
-                    sck(out, status, raw_stream)
-                e1.record(stream)
-            torch.cuda.synchronize(dev)
-            t = e0.elapsed_time(e1) / 1e3 / k
-            # the same call captured in a CUDA graph (no host work per step)
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                sck(out, status, raw_stream)
-            with torch.cuda.stream(stream):
-                for _ in range(5):
-                    graph.replay()
-                e0.record(stream)
-                for _ in range(k):
-                    graph.replay()
-                e1.record(stream)
-            torch.cuda.synchronize(dev)
-            tg = e0.elapsed_time(e1) / 1e3 / k
-            sp = kvcs.plan_for(sub.caches, sub.block_size, sub.num_positions)
-            sweep.append({"requests": n, "kv_bytes": sb, "ms": round(t * 1e3, 4),
-                          "gbs": round(sb / t / 1e9, 1), "graph_ms": round(tg * 1e3, 4),
-                          "graph_gbs": round(sb / tg / 1e9, 1), "split": sp["split"]})
-            n *= 2
+    sweep = request_sweep(wl, stream, r["out"], r["status"]) if args.sweep else None
 
     # ---- end to end: host buffers through the public API ----
     e2e = None
-    if not args.no_e2e and ck is not None:
-        e2e = run_e2e(args, wl, dev, stream, ws, ck)
+    if not args.no_e2e and r["ck"] is not None:
+        e2e = run_e2e(args, wl, dev, stream, ws, r["ck"])
 
     if rank != 0:
         return
-    peak, peak_kind = measured_peak()
-    achieved = nbytes / launch_s / 1e9
-    traffic = profiled_traffic(args.config, plan["units"])
+    plan = r["plan"]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 4),
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u64", "data": "synthetic",
         "blocks_per_s": round(job_blocks / total_s, 1),
         "hbm_frac_of_nominal_8tbs": round(value / ws / NOMINAL_HBM_GBS, 4),
-        "config": {**describe(wl, args.config), "parallelism": f"replicas{ws}",
-                   "memory_layout": args.layout, "columns": max(1, args.columns),
-                   "verify": bool(args.verify)},
+        "config": arm_config(wl, args, ws),
         "plan": {k: plan[k] for k in ("kernel", "split", "launches", "memsets", "grid",
                                       "threads", "smem_bytes", "stage_bytes", "units")},
-        "gpu_launches": int(launches),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "kernel": "kvcs_bulk_kernel" if plan["kernel"] == 0
-                     else "kvcs_generic_kernel",
-                     "launch_ms": round(launch_s * 1e3, 4)},
-        "clocks": clocks,
+        "gpu_launches": r["launches"],
+        "roofline": roofline_of(r, args.config),
+        "clocks": r["clocks"],
         "e2e": e2e,
     }
     if sweep is not None:
         line["sweep"] = sweep
     if ws == 1 and not args.no_cpu_baseline:
-        cores = host_cores()
-        gbs, bps, desc = oracle_timed(wl, args.cpu_seconds, cores, args.seed)
-        line["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": cores,
-                                "kind": "oracle", "blocks_per_s": round(bps, 2),
-                                "sample": desc}
+        line["cpu_baseline"], line["parity"] = cpu_leg(wl, r, args.cpu_seconds, args.seed)
+        line["cpu_baseline"]["one_thread"] = oracle_one_thread(wl, args.other_cpu_seconds,
+                                                               args.seed)
+        line["cpu_baseline"]["python_tiny"] = python_oracle_tiny(args.seed)
+    headline = (args.config == "llama3_8b" and args.layout == "nhd" and args.columns <= 1
+                and not args.verify)
+    if ws == 1 and headline and not args.no_other_configs:
+        del wl, r
+        line["other_configs"] = other_configs(args, dev, stream)
     print(json.dumps(line), flush=True)
+    bad = [k for k, v in [("headline", line.get("parity"))] +
+           [(k, v.get("parity")) for k, v in line.get("other_configs", {}).items()]
+           if v and v["mismatches"]]
+    if bad:
+        raise SystemExit(f"GPU output differs from the oracle on: {', '.join(bad)}")
 
 
 def run_e2e(args, wl, dev, stream, ws, ck):
@@ -836,6 +973,11 @@ def main():
                     help="time the tagged row sums and their comparison too")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--other-cpu-seconds", type=float, default=4.0,
+                    help="oracle seconds per extra workload and for the one-thread figure")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="time only the chosen workload (the default line also times "
+                         "the MLA and 70B workloads and the 70B request sweep)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

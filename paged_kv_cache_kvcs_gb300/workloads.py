@@ -79,6 +79,24 @@ class Workload:
         return int(self.pos_offsets.numel() - 1)
 
 
+def gather_pages(cache: CacheSpec, block_size: int, ids: torch.Tensor) -> torch.Tensor:
+    """The pages of blocks ``ids`` of one cache, packed one after another:
+    uint8 ``[halves, len(ids), page]`` on the pool's device (data movement
+    only).  Pages are found the way the cache places them: default packing,
+    explicit half/block strides, or a separate V tensor."""
+    state = cache.layout == LAYOUT_STATE
+    halves = 1 if cache.layout in (LAYOUT_LATENT, LAYOUT_STATE) else 2
+    page = (1 if state else block_size) * cache.num_heads * cache.head_bytes
+    bstride = cache.block_stride or page
+    ids = ids.to(cache.pool.device, torch.int64)
+    if cache.v_pool is not None:
+        return torch.stack([torch.as_strided(t, (cache.num_blocks, page), (bstride, 1))[ids]
+                            for t in (cache.pool, cache.v_pool)])
+    hstride = cache.half_stride or cache.num_blocks * page
+    view = torch.as_strided(cache.pool, (halves, cache.num_blocks, page), (hstride, bstride, 1))
+    return view[:, ids]
+
+
 def _cpu_gen(seed: int) -> torch.Generator:
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)

@@ -30,6 +30,8 @@ def test_reference_arm_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
     assert d["config"]["workload"] == "tiny_paged_kv_checksum"
+    # the same config keys as our arm's line
+    assert {"parallelism", "memory_layout", "columns", "verify"} <= set(d["config"])
 
 
 def test_warmup_below_three_is_refused():
@@ -42,7 +44,7 @@ def test_warmup_below_three_is_refused():
 @pytest.mark.gpu
 def test_our_arm_line():
     d = run("--config", "llama3_8b_small", "--steps", "5", "--warmup", "3", "--e2e-steps", "1",
-            "--cpu-seconds", "1")
+            "--cpu-seconds", "1", "--other-cpu-seconds", "0.5")
     assert BASE_KEYS | {"roofline", "clocks", "gpu_launches", "ms_per_step"} <= set(d)
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
@@ -52,6 +54,12 @@ def test_our_arm_line():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     c = d["clocks"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(c)
+    # the timed call's output against the oracle's sampled values
+    assert d["parity"]["positions"] > 0 and d["parity"]["mismatches"] == 0
+    cb = d["cpu_baseline"]
+    assert cb["one_thread"]["cores"] == 1 and cb["one_thread"]["value"] > 0
+    assert cb["python_tiny"]["value"] > 0
+    assert {"parallelism", "memory_layout", "columns", "verify"} <= set(d["config"])
 
 
 @pytest.mark.gpu
@@ -60,3 +68,12 @@ def test_write_line():
             "--cpu-seconds", "1")
     assert {"metric", "value", "unit", "roofline", "clocks", "cpu_baseline", "gpu_launches"} <= set(d)
     assert d["gpu_launches"] == 5 and d["roofline"]["kernel"] == "kvcs_write_kernel"
+    assert d["parity"]["positions"] > 0 and d["parity"]["mismatches"] == 0
+
+
+@pytest.mark.gpu
+def test_replica_columns_line_checks_its_output():
+    d = run("--config", "llama3_8b_small", "--steps", "3", "--warmup", "3", "--no-e2e",
+            "--columns", "2", "--verify", "--cpu-seconds", "1", "--other-cpu-seconds", "0.5")
+    assert d["parity"]["positions"] > 0 and d["parity"]["mismatches"] == 0
+    assert "other_configs" not in d

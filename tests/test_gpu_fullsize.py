@@ -1,6 +1,8 @@
 """The full-size workloads in the launch configuration the benchmark times
-(one call over every cache and request): sampled positions against the
-oracle, plus properties that hold at any size."""
+(one call over every cache and request), compared with the oracle at every
+block position: one exact 64-bit value per position (page
+"vllm.distributed.kv_transfer.kv_checksum.checksum", module docstring
+item 2), so the whole output must be equal bit for bit."""
 
 import numpy as np
 import pytest
@@ -13,23 +15,16 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _sample(wl, n=48, seed=0):
-    g = np.random.default_rng(seed)
-    P = wl.num_positions
-    po = wl.pos_offsets.cpu().numpy()
-    last = po[1:] - 1                       # partial last blocks
-    pick = set(g.choice(P, size=min(n, P), replace=False).tolist())
-    pick |= set(last[:8].tolist()) | {0, P - 1}
-    return sorted(pick)
-
-
-def _check(wl, n=48):
-    from gpu_helpers import gpu_checksums, oracle_sampled
+def _check_all(wl):
+    """Library output of one call over ``wl`` equals the oracle at every
+    position; returns the output."""
+    from gpu_helpers import gpu_checksums, oracle_every_position
     got, st = gpu_checksums(wl)
     assert st == 0
-    pos, exp, est = oracle_sampled(wl, _sample(wl, n))
+    exp, est = oracle_every_position(wl)
     assert est == 0
-    assert np.array_equal(got[pos], exp)
+    bad = np.flatnonzero(got != exp)
+    assert bad.size == 0, f"{bad.size} of {got.size} positions differ, first {bad[:8].tolist()}"
     return got
 
 
@@ -42,7 +37,7 @@ def test_llama3_8b_full():
     wl = W.llama3_8b(0, DEV)
     plan = K.plan_for(wl.caches, wl.block_size, wl.num_positions)
     assert plan["kernel"] == 0 and plan["launches"] == 1
-    got = _check(wl)
+    got = _check_all(wl)
     assert np.count_nonzero(got) == got.size
     del wl
     _free()
@@ -50,44 +45,55 @@ def test_llama3_8b_full():
 
 def test_mla_full():
     wl = W.mla(0, DEV)
-    _check(wl, n=24)
+    _check_all(wl)
     del wl
     _free()
 
 
 def test_llama3_70b_full_and_sweep():
+    """Every position of the 43 GB workload, and the request-count sweep
+    (the first n requests alone, in the launch mode the sweep times: split
+    at unit granularity for few requests) equal to the prefix of the
+    oracle-checked full result."""
     wl = W.llama3_70b(0, DEV)
     from gpu_helpers import gpu_checksums
-    full = _check(wl, n=24)
-    # request-count sweep: the first n requests alone give the same values
-    for n in (1, 2, 8, 32):
+    full = _check_all(wl)
+    for n in (1, 2, 4, 8, 16, 32, 64):
         sub = W.Workload(wl.name, wl.block_size, wl.caches, wl.pos_offsets[:n + 1],
                          wl.first_position[:n], wl.num_tokens[:n],
                          wl.block_ids[:int(wl.pos_offsets[n])])
         got, st = gpu_checksums(sub)
         assert st == 0
-        assert np.array_equal(got, full[:got.size])
+        assert np.array_equal(got, full[:got.size]), n
     del wl
     _free()
 
 
 def test_invariance_full():
     """16 requests of 3000 tokens, 8B-shaped: producer bs16 NHD, consumer
-    bs64 HND, two TP shards; per-token-range sums match bit for bit."""
-    from gpu_helpers import gpu_checksums, oracle_sampled
+    bs64 HND, two TP shards.  Each variant equals the oracle at every
+    position, and per-token-range sums match bit for bit."""
+    from gpu_helpers import gpu_checksums
     prod, cons, s0, s1 = W.invariance(0, DEV)
-    a, _ = gpu_checksums(prod)
-    b, _ = gpu_checksums(cons)
-    c0, _ = gpu_checksums(s0)
-    c1, _ = gpu_checksums(s1)
+    a = _check_all(prod)
+    b = _check_all(cons)
+    c0 = _check_all(s0)
+    c1 = _check_all(s1)
     assert np.array_equal(c0 + c1, a)
     pa = a.reshape(16, 188)
     pb = b.reshape(16, 47)
     sums = np.add.reduceat(pa, np.arange(0, 188, 4), axis=1, dtype=np.uint64)
     assert np.array_equal(sums, pb)
-    pos, exp, _ = oracle_sampled(cons, list(range(0, 752, 37)) + [46, 751])
-    assert np.array_equal(b[pos], exp)
     del prod, cons, s0, s1
+    _free()
+
+
+def test_mamba2_full():
+    """The Mamba2-shaped states (SSM rows on the bulk kernel, conv rows on
+    the generic kernel, one call), every position against the oracle."""
+    wl = W.mamba2(0, DEV, num_requests=64)
+    _check_all(wl)
+    del wl
     _free()
 
 
@@ -95,9 +101,9 @@ def test_invariance_full():
 def test_fused_write_full_size(kind):
     """The benchmark's write steps (32 layers; 32 x 512 new tokens, or 256
     requests x 1 token) through the prepared call it times: every written
-    block's running word equals a checksum pass over the written pools, and
-    sampled blocks equal the oracle."""
-    from gpu_helpers import oracle_sampled
+    block's running word equals a checksum pass over the written pools and
+    the oracle over the written pages."""
+    from gpu_helpers import oracle_every_position
     wb = W.llama3_8b_write(0, DEV, kind=kind)
     sums = torch.zeros(wb.num_blocks, dtype=torch.int64, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -113,7 +119,8 @@ def test_fused_write_full_size(kind):
     ids = wb.block_ids.long()
     words = sums[ids]
     assert torch.equal(words, out)
-    pos, exp, _ = oracle_sampled(wl, _sample(wl, 24))
-    assert np.array_equal(words.cpu().numpy().view(np.uint64)[pos], exp)
+    exp, est = oracle_every_position(wl)
+    assert est == 0
+    assert np.array_equal(words.cpu().numpy().view(np.uint64), exp)
     del wb, wl
     _free()

@@ -92,14 +92,3 @@ def test_unknown_split_is_one_row_per_shard():
     wl = W.Workload("shard", 16, caches, base.pos_offsets, base.first_position,
                     base.num_tokens, base.block_ids)
     check(wl, kernel=1)
-
-
-def test_mamba2_full_size_sampled():
-    from gpu_helpers import gpu_checksums, oracle_sampled
-    wl = W.mamba2(0, DEV, num_requests=64)
-    got, st = gpu_checksums(wl)
-    assert st == 0
-    pos, exp, _ = oracle_sampled(wl, [0, 17, 63])
-    assert np.array_equal(got[pos], exp)
-    del wl
-    torch.cuda.empty_cache()
