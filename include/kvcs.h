@@ -4,11 +4,11 @@
  * What it computes (page "vllm.distributed.kv_transfer.kv_checksum.checksum",
  * vLLM API docs, module docstring items 1 and 2):
  *
- *   A slice is the KV of one layer and one KV head inside one block: per
- *   token, that head's K bytes then its V bytes, token by token, cut into
- *   little-endian 8-byte pieces x_j with j = t*P + p (t = the token's
- *   position in the request, P = pieces per token, p = the piece within the
- *   token).  Its checksum is
+ *   Each (layer, KV head) pair owns one slice of a block.  Its bytes run
+ *   through the block's tokens in order, each token contributing the head's
+ *   K bytes and then its V bytes; the slice is read as consecutive
+ *   little-endian 64-bit words x_j, where j = t*P + p for word p of the token
+ *   at request position t and P words per token.  Its checksum is
  *       s = sum_j x_j * (2j + 1)                      mod 2^64
  *   and the block's checksum is
  *       c = sum_{layer, head} m * s                   mod 2^64,
@@ -148,7 +148,10 @@ typedef struct kvcs_requests {
                                  outside [0, num_columns) or a column with no
                                  cache, misaligned base, two caches covering
                                  the same (layer, global head) */
-#define KVCS_EUNSUPPORTED (-2) /* head_offset + num_heads > 65536 */
+#define KVCS_EUNSUPPORTED (-2) /* a geometry the library does not handle:
+                                 head_offset + num_heads > 65536 (any call),
+                                 or a token row (num_heads * head_bytes) of
+                                 1 GiB or more (kvcs_write_kv) */
 #define KVCS_ECUDA (-3)       /* a CUDA call failed (launch, attribute query);
                                  work may have been partly enqueued */
 
@@ -197,12 +200,13 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
  * Per-position outputs of kvcs_group_checksums.  All pointers are DEVICE
  * pointers owned by the caller.
  *
- * Replicated KV (MLA, or GQA with more TP ranks than KV heads) is tracked per
- * replica: a worker keeps one partial checksum per replica key
- * (replicas, replica_index) of the layers it covers (the checksum page,
- * paragraph on replicated KV; dataclass KVChecksumGroup, field values).  Each
- * cache names its column; values[i * num_columns + k] is position i's partial
- * over the caches of column k.
+ * When KV is replicated across ranks (an MLA latent cache, or GQA heads
+ * copied to several TP ranks), each replica is checked separately: the
+ * partial over a set of layers carries the (replicas, replica_index) key of
+ * those layers, and one partial is kept per key (the checksum page,
+ * paragraph on replicated KV; dataclass KVChecksumGroup, field values).  Here
+ * each cache names the column of its key; values[i * num_columns + k] is
+ * position i's partial over the caches of column k.
  *
  * A load of offloaded KV is checked against the checksums offloaded with it:
  * each row's partials summed (KVChecksumGroup, field stored), XORed with the

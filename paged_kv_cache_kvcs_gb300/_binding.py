@@ -182,8 +182,72 @@ def kvcs_plan(caches: ctypes.Array, num_caches: int, block_size: int,
     return info.as_dict()
 
 
+def _current_device():
+    import torch
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _check_tensor(name: str, t, dtypes, min_numel: int, device) -> None:
+    """``t`` is a contiguous CUDA tensor of one of ``dtypes`` on ``device``
+    holding at least ``min_numel`` elements: the kernels get only its
+    address, so a CPU tensor, another device's tensor or a short one must be
+    refused here."""
+    if not (getattr(t, "is_cuda", False) and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must be a {' or '.join(map(str, dtypes))} tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call runs on {device}")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call needs {min_numel}")
+
+
+def _check_requests(pos_offsets, first_position, num_tokens, block_ids,
+                    total_positions: int):
+    """The request table: int64 pos_offsets [R+1], first_position [R],
+    num_tokens [R] and int32 block_ids [>= total_positions], all on the
+    current CUDA device.  Returns that device."""
+    import torch
+    for name, t in (("pos_offsets", pos_offsets), ("first_position", first_position),
+                    ("num_tokens", num_tokens), ("block_ids", block_ids)):
+        if not getattr(t, "is_cuda", False):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if pos_offsets.numel() < 1:
+        raise ValueError("pos_offsets must hold num_requests + 1 elements")
+    dev = _current_device()
+    R = pos_offsets.numel() - 1
+    _check_tensor("pos_offsets", pos_offsets, (torch.int64,), R + 1, dev)
+    for name, t in (("first_position", first_position), ("num_tokens", num_tokens)):
+        _check_tensor(name, t, (torch.int64,), R, dev)
+        if t.numel() != R:
+            raise ValueError(f"{name} must hold one element per request ({R})")
+    if total_positions < 0:
+        raise ValueError("total_positions must be >= 0")
+    _check_tensor("block_ids", block_ids, (torch.int32,), total_positions, dev)
+    return dev
+
+
+def _check_status(status, dev) -> None:
+    import torch
+    if status is not None:
+        _check_tensor("status", status, (torch.int32, torch.uint32), 1, dev)
+
+
+WORDS = None
+
+
+def _words():
+    """dtypes that hold uint64 bits"""
+    global WORDS
+    if WORDS is None:
+        import torch
+        WORDS = (torch.int64, torch.uint64)
+    return WORDS
+
+
 def _check_pool(c, block_size: int) -> None:
-    """Every page the descriptor can address lies inside its tensor."""
+    """Every page the descriptor can address lies inside its tensor, on the
+    current device."""
     t = c.pool
     if isinstance(t, int):
         return
@@ -191,6 +255,10 @@ def _check_pool(c, block_size: int) -> None:
     for x in (t, v_pool):
         if x is not None and not (x.is_cuda and x.is_contiguous()):
             raise ValueError("cache pools must be contiguous CUDA tensors")
+    dev = _current_device()
+    for x in (t, v_pool):
+        if x is not None and x.device != dev:
+            raise ValueError(f"a cache pool is on {x.device}, the call runs on {dev}")
     page = (1 if c.layout == KVCS_LAYOUT_STATE else block_size) * c.num_heads * c.head_bytes
     bstride = getattr(c, "block_stride", 0) or page
     span = (c.num_blocks - 1) * bstride + page if c.num_blocks > 0 else 0
@@ -222,19 +290,16 @@ def block_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
     import torch
     for c in caches:
         _check_pool(c, block_size)
-    for name, t, dt in (("pos_offsets", pos_offsets, torch.int64),
-                        ("first_position", first_position, torch.int64),
-                        ("num_tokens", num_tokens, torch.int64),
-                        ("block_ids", block_ids, torch.int32)):
-        if not (t.is_cuda and t.dtype == dt and t.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
     if total_positions is None:
+        if not getattr(pos_offsets, "is_cuda", False) or pos_offsets.numel() < 1:
+            raise ValueError("pos_offsets must be a CUDA int64 tensor of num_requests + 1")
         total_positions = int(pos_offsets[-1].item())
-    dev = pos_offsets.device
+    dev = _check_requests(pos_offsets, first_position, num_tokens, block_ids, total_positions)
     if out is None:
         out = torch.empty(max(total_positions, 0), dtype=torch.int64, device=dev)
-    elif out.numel() < total_positions or out.dtype not in (torch.int64, torch.uint64):
-        raise ValueError("out must hold total_positions 64-bit words")
+    else:
+        _check_tensor("out", out, _words(), total_positions, dev)
+    _check_status(status, dev)
     reqs = kvcs_requests(pos_offsets.numel() - 1, pos_offsets.data_ptr(),
                          first_position.data_ptr(), num_tokens.data_ptr(),
                          block_ids.data_ptr())
@@ -260,15 +325,10 @@ class Checksummer:
 
     def __init__(self, caches: Sequence, block_size: int, pos_offsets,
                  first_position, num_tokens, block_ids, total_positions: int):
-        import torch
         for c in caches:
             _check_pool(c, block_size)
-        for name, t, dt in (("pos_offsets", pos_offsets, torch.int64),
-                            ("first_position", first_position, torch.int64),
-                            ("num_tokens", num_tokens, torch.int64),
-                            ("block_ids", block_ids, torch.int32)):
-            if not (t.is_cuda and t.dtype == dt and t.is_contiguous()):
-                raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+        self.device = _check_requests(pos_offsets, first_position, num_tokens, block_ids,
+                                      total_positions)
         self._keep = (list(caches), pos_offsets, first_position, num_tokens, block_ids)
         self.num_caches = len(caches)
         self.block_size = block_size
@@ -285,6 +345,14 @@ class Checksummer:
         """Enqueue one call writing ``out`` (int64/uint64 CUDA tensor of at
         least ``total_positions`` words) on ``stream`` (a raw handle);
         ``accumulate`` adds this call's checksums into ``out`` instead."""
+        if out.device != self.device or out.numel() < self.total_positions or \
+                out.dtype not in _words() or not out.is_contiguous():
+            _check_tensor("out", out, _words(), self.total_positions, self.device)
+        if status is not None and status.device != self.device:
+            _check_status(status, self.device)
+        import torch
+        if torch.cuda.current_device() != self.device.index:
+            raise ValueError(f"the call was prepared on {self.device}; make it current")
         if accumulate:
             outs = kvcs_outputs(1, KVCS_OUT_ACCUMULATE,
                                 out.data_ptr() if self.total_positions > 0 else None)
@@ -354,13 +422,27 @@ def group_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
     for c in caches:
         _check_pool(c, block_size)
     if total_positions is None:
+        if not getattr(pos_offsets, "is_cuda", False) or pos_offsets.numel() < 1:
+            raise ValueError("pos_offsets must be a CUDA int64 tensor of num_requests + 1")
         total_positions = int(pos_offsets[-1].item())
-    dev = pos_offsets.device
+    dev = _check_requests(pos_offsets, first_position, num_tokens, block_ids, total_positions)
+    if not 1 <= num_columns <= 64:
+        raise ValueError("num_columns must be in [1, 64]")
     if values is None:
         if accumulate:
             raise ValueError("accumulate needs the values to add into")
         values = torch.empty((max(total_positions, 0), num_columns), dtype=torch.int64,
                              device=dev)
+    else:
+        _check_tensor("values", values, _words(), total_positions * num_columns, dev)
+    for name, t in (("row_sums", row_sums), ("tags", tags), ("expected", expected)):
+        if t is not None:
+            _check_tensor(name, t, _words(), total_positions, dev)
+    if mismatch is not None:
+        _check_tensor("mismatch", mismatch, (torch.uint8, torch.bool), total_positions, dev)
+    if mismatch_count is not None:
+        _check_tensor("mismatch_count", mismatch_count, (torch.int32, torch.uint32), 1, dev)
+    _check_status(status, dev)
     outs = kvcs_outputs(num_columns, KVCS_OUT_ACCUMULATE if accumulate else 0,
                         values.data_ptr() if total_positions > 0 else None,
                         _ptr(row_sums), _ptr(tags), _ptr(expected), _ptr(mismatch),
@@ -425,8 +507,19 @@ def write_kv(caches, block_size: int, keys, values, slot_mapping, positions,
     for name, t in (("slot_mapping", slot_mapping), ("positions", positions)):
         if not (t.is_cuda and t.dtype == torch.int64 and t.is_contiguous() and t.numel() == n):
             raise ValueError(f"{name} must be a contiguous CUDA int64 tensor of num_tokens")
+    dev = _current_device()
+    for name, t in (("slot_mapping", slot_mapping), ("positions", positions)):
+        _check_tensor(name, t, (torch.int64,), n, dev)
+    for k, v in zip(keys, values):
+        for name, t in (("key", k), ("value", v)):
+            if t is not None and t.device != dev:
+                raise ValueError(f"a {name} tensor is on {t.device}, the call runs on {dev}")
     if block_sums is not None and block_sums.numel() < min(c.num_blocks for c in caches):
         raise ValueError("block_sums needs one word per block")
+    if block_sums is not None:
+        _check_tensor("block_sums", block_sums, _words(),
+                      min(c.num_blocks for c in caches), dev)
+    _check_status(status, dev)
     if stream is None:
         stream = torch.cuda.current_stream(slot_mapping.device).cuda_stream
     arr = cache_array(caches)

@@ -29,35 +29,42 @@ constexpr u64 kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
-  std::once_flag once;
+  std::mutex mu;
+  std::atomic<bool> done{false};  // set only once the setup succeeded
   int sms = 0;
-  cudaError_t err = cudaSuccess;
 };
 DeviceState g_dev[kMaxDevices];
 
 // SM count of the current device; sets the bulk kernel's shared-memory
-// attribute once per device.
+// attribute once per device.  A failed setup is not remembered: the next
+// call on that device tries again.
 cudaError_t device_setup(int *sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   DeviceState &d = g_dev[dev];
-  std::call_once(d.once, [&d, dev]() {
+  if (d.done.load(std::memory_order_acquire)) {
+    *sms = d.sms;
+    return cudaSuccess;
+  }
+  std::lock_guard<std::mutex> lock(d.mu);
+  if (!d.done.load(std::memory_order_relaxed)) {
     int n = 0;
-    d.err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     for (const void *fn : {reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamXSplit>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamState>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndSub>)})
-      if (d.err == cudaSuccess)
-        d.err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmemLimit);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return e;
     d.sms = n;
-  });
+    d.done.store(true, std::memory_order_release);
+  }
   *sms = d.sms;
-  return d.err;
+  return cudaSuccess;
 }
 
 constexpr int kMaxColumns = 64;
@@ -672,7 +679,9 @@ const char *kvcs_strerror(int code) {
   switch (code) {
     case KVCS_OK: return "success";
     case KVCS_EINVAL: return "invalid argument";
-    case KVCS_EUNSUPPORTED: return "unsupported: more than 65536 KV heads per layer";
+    case KVCS_EUNSUPPORTED:
+      return "unsupported geometry (global heads past 65536 per layer, or a token row of 1 GiB "
+             "or more in a write)";
     case KVCS_ECUDA: return "CUDA error";
     default: return "unknown error";
   }

@@ -80,3 +80,115 @@ def test_write_kv_rejects_before_any_cuda_call():
     assert call([FakeCache(), FakeCache()], [ok_k, ok_k], [ok_v, ok_v]) == K.KVCS_EINVAL
     # zero tokens: nothing to do
     assert call([FakeCache()], [ok_k], [ok_v], n=0) == K.KVCS_OK
+
+
+class FakeTensor:
+    """Enough of a CUDA tensor for the binding's argument checks (no GPU
+    here): its address is never dereferenced because every case below is
+    refused before the library is called."""
+
+    def __init__(self, n, dtype, dev=0):
+        self.n, self.dtype = n, dtype
+        self.device = torch.device("cuda", dev)
+        self.is_cuda = True
+
+    def numel(self):
+        return self.n
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return 1 << 20
+
+    def element_size(self):
+        return torch.empty(0, dtype=self.dtype).element_size()
+
+
+def _fake_tables(R=3, P=10, ids=None, fp=None, nt=None):
+    return (FakeTensor(R + 1, torch.int64), FakeTensor(R if fp is None else fp, torch.int64),
+            FakeTensor(R if nt is None else nt, torch.int64),
+            FakeTensor(P if ids is None else ids, torch.int32))
+
+
+class _Cache:
+    pool = 1 << 21
+    num_blocks, layout, layer, head_offset, num_heads, head_bytes = 16, 0, 0, 0, 2, 64
+
+
+@pytest.fixture
+def on_cuda0(monkeypatch):
+    monkeypatch.setattr(B, "_current_device", lambda: torch.device("cuda", 0))
+
+
+def test_group_checksums_refuses_cpu_tensors():
+    wl = W.tiny(0, "cpu")
+    with pytest.raises(ValueError, match="CUDA"):
+        K.group_checksums(wl.caches, wl.block_size, wl.pos_offsets, wl.first_position,
+                          wl.num_tokens, wl.block_ids, 1)
+
+
+@pytest.mark.parametrize("bad", ["block_ids_short", "first_position_count", "num_tokens_count",
+                                 "wrong_dtype", "other_device"])
+def test_request_tables_checked(on_cuda0, bad):
+    po, fp, nt, ids = _fake_tables()
+    if bad == "block_ids_short":
+        ids = FakeTensor(9, torch.int32)
+    elif bad == "first_position_count":
+        fp = FakeTensor(2, torch.int64)
+    elif bad == "num_tokens_count":
+        nt = FakeTensor(4, torch.int64)
+    elif bad == "wrong_dtype":
+        ids = FakeTensor(10, torch.int64)
+    else:
+        nt = FakeTensor(3, torch.int64, dev=1)
+    with pytest.raises(ValueError):
+        K.block_checksums([_Cache()], 16, po, fp, nt, ids, total_positions=10)
+    with pytest.raises(ValueError):
+        K.Checksummer([_Cache()], 16, po, fp, nt, ids, 10)
+    with pytest.raises(ValueError):
+        K.group_checksums([_Cache()], 16, po, fp, nt, ids, 1, total_positions=10)
+
+
+def test_block_checksums_output_checked(on_cuda0):
+    po, fp, nt, ids = _fake_tables()
+    for out in (FakeTensor(9, torch.int64), FakeTensor(10, torch.int32),
+                FakeTensor(10, torch.int64, dev=1)):
+        with pytest.raises(ValueError):
+            K.block_checksums([_Cache()], 16, po, fp, nt, ids, out=out, total_positions=10)
+    with pytest.raises(ValueError):
+        K.block_checksums([_Cache()], 16, po, fp, nt, ids, out=FakeTensor(10, torch.int64),
+                          status=FakeTensor(1, torch.int64), total_positions=10)
+
+
+def test_prepared_call_checks_its_output(on_cuda0):
+    po, fp, nt, ids = _fake_tables()
+    ck = K.Checksummer([_Cache()], 16, po, fp, nt, ids, 10)
+    for out in (FakeTensor(9, torch.int64), FakeTensor(10, torch.float64),
+                FakeTensor(10, torch.int64, dev=1)):
+        with pytest.raises(ValueError):
+            ck(out)
+
+
+@pytest.mark.parametrize("bad", ["values_short", "row_sums_short", "tags_short",
+                                 "expected_short", "mismatch_short", "mismatch_count_dtype",
+                                 "columns_zero", "columns_65"])
+def test_group_outputs_checked(on_cuda0, bad):
+    po, fp, nt, ids = _fake_tables()
+    n, cols = 10, 2
+    kw = dict(values=FakeTensor(n * cols, torch.int64), row_sums=FakeTensor(n, torch.int64),
+              tags=FakeTensor(n, torch.int64), expected=FakeTensor(n, torch.int64),
+              mismatch=FakeTensor(n, torch.uint8), mismatch_count=FakeTensor(1, torch.int32))
+    short = {"values_short": ("values", FakeTensor(n * cols - 1, torch.int64)),
+             "row_sums_short": ("row_sums", FakeTensor(n - 1, torch.int64)),
+             "tags_short": ("tags", FakeTensor(n - 1, torch.int64)),
+             "expected_short": ("expected", FakeTensor(n - 1, torch.int64)),
+             "mismatch_short": ("mismatch", FakeTensor(n - 1, torch.uint8)),
+             "mismatch_count_dtype": ("mismatch_count", FakeTensor(1, torch.int64))}
+    if bad in short:
+        k, v = short[bad]
+        kw[k] = v
+    else:
+        cols = 0 if bad == "columns_zero" else 65
+    with pytest.raises(ValueError):
+        K.group_checksums([_Cache()], 16, po, fp, nt, ids, cols, total_positions=n, **kw)
