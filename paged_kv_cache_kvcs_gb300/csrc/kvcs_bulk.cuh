@@ -624,13 +624,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
   while (true) {
     // fill f - 1 of this stage (another group's unit) must be released
     // before fill f can be told apart from fill f - 2
-    if (f > 0 && !ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]),
-                                         (f - 1u) & 1u, p.timeout_ns)) {
-      set_status(p, kStatusTimeout);
-      return;
-    }
-    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->full[s]), f & 1u, p.timeout_ns)) {
-      set_status(p, kStatusTimeout);
+    bool ok = f == 0 || ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]),
+                                               (f - 1u) & 1u, p.timeout_ns);
+    ok = ok && ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->full[s]), f & 1u, p.timeout_ns);
+    // Each lane waits on its own, so near the time limit lanes can disagree;
+    // the warp leaves as a whole if any lane gave up, so no lane reaches the
+    // full-mask shuffles below with others of its warp gone.
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) set_status(p, kStatusTimeout);
       return;
     }
     const UnitMeta m = hdr->meta[s];
