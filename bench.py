@@ -67,6 +67,12 @@ def make_workload(name: str, seed: int, device):
         return W.llama3_70b(seed, device, num_requests=int(name[len("llama3_70b_r"):]))
     if name == "tiny":
         return W.tiny(seed, device)
+    if name == "llama3_8b_decode_hnd":  # newest block of 16384 requests, 1 token each, HND
+        return W.llama3_8b_decode(seed, device)
+    if name == "llama3_8b_decode_nhd":
+        return W.llama3_8b_decode(seed, device, layout=W.LAYOUT_NHD)
+    if name == "llama3_8b_decode_hnd_small":   # 2048 requests: ncu captures
+        return W.llama3_8b_decode(seed, device, num_requests=2048)
     if name == "mamba2":                # Mamba2-shaped running states, 10.9 GB
         return W.mamba2(seed, device)
     if name == "mamba2_small":          # 16 requests, 2.7 GB: ncu captures
@@ -83,6 +89,13 @@ def relayout(wl, layout: str):
         return wl
     caches = []
     for c in wl.caches:
+        if layout == "misaligned":   # the same pools starting 8 bytes past a 16-byte boundary
+            buf = torch.empty(c.pool.numel() + 8, dtype=torch.uint8, device=c.pool.device)
+            pool = buf[8:]
+            pool.copy_(c.pool)
+            caches.append(dataclasses.replace(c, pool=pool))
+            c.pool = None
+            continue
         assert c.layout == W.LAYOUT_NHD
         bs, H, hb, nb = wl.block_size, c.num_heads, c.head_bytes, c.num_blocks
         page = bs * H * hb
@@ -101,11 +114,6 @@ def relayout(wl, layout: str):
         elif layout == "separate_kv":
             k, vv = v[0].contiguous().view(-1), v[1].contiguous().view(-1)
             caches.append(dataclasses.replace(c, pool=k, v_pool=vv))
-        elif layout == "misaligned":   # NHD pools starting 8 bytes past a 16-byte boundary
-            buf = torch.empty(v.numel() + 8, dtype=torch.uint8, device=v.device)
-            pool = buf[8:]
-            pool.copy_(v.reshape(-1))
-            caches.append(dataclasses.replace(c, pool=pool))
         elif layout == "xsplit":
             pool = v.view(2, nb, bs, H, hb // 16, 16).permute(0, 1, 3, 4, 2, 5).contiguous().view(-1)
             caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_XSPLIT))
@@ -247,6 +255,7 @@ def measured_peak():
 KERNEL_SOURCES = {
     "kvcs_bulk_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_bulk.cuh"],
     "kvcs_write_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_write.cuh"],
+    "kvcs_direct_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_direct.cuh"],
 }
 
 
@@ -699,7 +708,8 @@ def time_checksums(wl, args, dev, stream, ws, rank, steps, warmup, clocks=True) 
         result = values.cpu().numpy().view(np.uint64).sum(axis=1, dtype=np.uint64)
     else:
         result = out.cpu().numpy()
-    return {"total_s": total_s, "launch_s": statistics.mean(per), "launches": int(launches),
+    return {"state": bool(wl.caches) and wl.caches[0].layout == 4,
+            "total_s": total_s, "launch_s": statistics.mean(per), "launches": int(launches),
             "clocks": clk, "plan": plan, "nbytes": kv_bytes(wl), "ck": ck, "out": out,
             "status": status, "result": result}
 
@@ -752,14 +762,24 @@ def request_sweep(wl, stream, out, status) -> list:
     return sweep
 
 
+def direct_kernel_name(r) -> str:
+    """The kernel of a call the bulk kernel does not take: the direct-load
+    kernel for KV caches, the state-row kernel for Mamba states."""
+    return "kvcs_state_kernel" if r["state"] else "kvcs_direct_kernel"
+
+
 def roofline_of(r, workload: str) -> dict:
+    """The dominant kernel against the measured copy peak; ``workload`` names
+    the committed ncu summary that gives its DRAM traffic."""
     peak, peak_kind = measured_peak()
     achieved = r["nbytes"] / r["launch_s"] / 1e9
     plan = r["plan"]
+    kernel = direct_kernel_name(r) if plan["kernel"] == 1 else "kvcs_bulk_kernel"
+    traffic = (profiled_traffic(workload, plan["units"], kernel=kernel)
+               if kernel in KERNEL_SOURCES else None)
     return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(workload, plan["units"]),
-            "kernel": "kvcs_bulk_kernel" if plan["kernel"] == 0 else "kvcs_generic_kernel",
+            "traffic": traffic, "kernel": kernel,
             "launch_ms": round(r["launch_s"] * 1e3, 4)}
 
 
@@ -850,7 +870,8 @@ def run_ours(args, ws, rank, local):
         "plan": {k: plan[k] for k in ("kernel", "split", "launches", "memsets", "grid",
                                       "threads", "smem_bytes", "stage_bytes", "units")},
         "gpu_launches": r["launches"],
-        "roofline": roofline_of(r, args.config),
+        "roofline": roofline_of(r, args.config if args.layout == "nhd"
+                                else f"{args.config}_{args.layout}"),
         "clocks": r["clocks"],
         "e2e": e2e,
     }

@@ -3,7 +3,8 @@
 //
 // The library allocates no memory.  Every call validates its host arguments
 // before touching CUDA, plans its kernel launches (the bulk-copy kernel per
-// layout family, the generic kernel, the row-sum epilogue; or the write
+// layout family; the direct-load kernel for KV caches it cannot stage; the
+// state-row kernel for such state caches; the row-sum epilogue; or the write
 // kernels) and enqueues them, plus, when CTAs or launches share positions,
 // one cudaMemsetAsync of the output, on the caller's stream.
 
@@ -18,7 +19,11 @@
 #include <vector>
 
 #include "kvcs.h"
-#include "kvcs_kernels.cuh"
+#include "kvcs_bulk.cuh"
+#include "kvcs_direct.cuh"
+#include "kvcs_epilogue.cuh"
+#include "kvcs_state.cuh"
+#include "kvcs_write.cuh"
 
 namespace kvcs {
 namespace {
@@ -223,11 +228,12 @@ long long unit_bytes(const DevCache &d, int block_size) {
   return static_cast<long long>(d.rpu) * d.rowb;
 }
 
-// Shape of one bulk launch over caches [lo, hi): units per position, pages
-// per unit, stage size and count.
+// Shape of one bulk launch over caches [lo, hi): units per position,
+// whether pages are packed several to a stage, stage size and count.
 struct LaunchShape {
   long long units_per_pos = 0;
-  int ppu = 1;
+  int pack = 0;
+  int full_pages = 1;
   int pages_per_pos = 0;
   int stage_bytes = 0;
   int stages = 0;
@@ -250,16 +256,16 @@ LaunchShape launch_shape(const kvcs_cache *caches, int lo, int hi, int block_siz
               caches[i].piece_bytes == caches[lo].piece_bytes;
   }
   if (uniform) {
-    // Every page fits a unit and all pages look alike: pack consecutive
-    // pages of a position (e.g. a layer's K and V) into one unit.
+    // Every page fits a unit and all pages look alike: each page is a unit,
+    // and the producer packs consecutive pages of a position (e.g. a layer's
+    // K and V) into one stage as far as their valid bytes fit.  The stage
+    // holds as many whole pages as fit in the unit target.
     const long long page = static_cast<long long>(d0.page_bytes);
     const long long ppu = std::max<long long>(
         1, std::min<long long>(ls.pages_per_pos, kUnitTargetBytes / page));
-    if (ppu > 1) {
-      ls.ppu = static_cast<int>(ppu);
-      ls.units_per_pos = (ls.pages_per_pos + ls.ppu - 1) / ls.ppu;
-      biggest = ppu * page;
-    }
+    ls.pack = 1;
+    ls.full_pages = static_cast<int>(ppu);
+    biggest = std::max(biggest, ppu * page);
   }
   ls.stage_bytes = static_cast<int>((biggest + 127) / 128 * 128);
   ls.stages = std::min(kMaxStages, (kSmemLimit - kHeaderBytes) / ls.stage_bytes);
@@ -286,24 +292,31 @@ int family_of(const kvcs_cache &c, int block_size) {
   }
 }
 
-// One kernel launch: a kernel (the generic one, or the bulk instance of one
-// layout family) and a run of (column-sorted) caches.
+// One kernel launch: a kernel (the bulk instance of one layout family, the
+// direct-load kernel or the state-row kernel) and a run of (column-sorted)
+// caches.
+constexpr int kKernelBulk = 0;
+constexpr int kKernelDirect = 1;
+constexpr int kKernelState = 2;
+
 struct Launch {
-  bool generic;
+  int kernel;
   int family;
   std::vector<kvcs_cache> caches;
 };
 
 // How a call runs: caches the bulk kernel can stage go to its instance for
-// their layout family (up to kMaxCachesPerLaunch per launch), the rest to
-// the generic kernel.  With more than one launch, or the generic kernel,
-// every result is added atomically into an output zeroed first.
+// their layout family (up to kMaxCachesPerLaunch per launch), the other KV
+// caches to the direct-load kernel and the other state caches to the
+// state-row kernel.  With more than one launch, or a direct-load or
+// state-row launch, every result is added atomically into an output zeroed
+// first.
 struct Plan {
   std::vector<Launch> launches;
-  int kernel = 0;         // 0 bulk only, 1 generic only, 2 both
+  int kernel = 0;         // 0 bulk only, 1 direct loads only, 2 both
   int split = 0;          // bulk CTA ranges cut positions
   int bulk_grid = 0;
-  int generic_grid = 0;
+  int generic_grid = 0;   // direct-load or state-row kernel
   int stage_bytes = 0;    // of the first bulk launch
   int stages = 0;
   long long units = 0;    // units of the largest bulk launch
@@ -332,7 +345,10 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
     const std::vector<kvcs_cache> &set = f < kNumFamilies ? fam[f] : gen;
     for (size_t lo = 0; lo < set.size(); lo += kMaxCachesPerLaunch) {
       const size_t hi = std::min(set.size(), lo + kMaxCachesPerLaunch);
-      pl.launches.push_back({f == kNumFamilies, f < kNumFamilies ? f : 0,
+      const int kernel = f < kNumFamilies ? kKernelBulk
+                         : set[lo].layout == KVCS_LAYOUT_STATE ? kKernelState
+                                                                : kKernelDirect;
+      pl.launches.push_back({kernel, f < kNumFamilies ? f : 0,
                              std::vector<kvcs_cache>(set.begin() + lo, set.begin() + hi)});
     }
   }
@@ -343,7 +359,7 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
   if (!bulk.empty()) {
     bool first = true;
     for (const Launch &l : pl.launches) {
-      if (l.generic) continue;
+      if (l.kernel != kKernelBulk) continue;
       const LaunchShape ls = launch_shape(l.caches.data(), 0,
                                           static_cast<int>(l.caches.size()), block_size);
       pl.units = std::max(pl.units, ls.units_per_pos * total_positions);
@@ -372,10 +388,17 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
   }
   if (!gen.empty()) {
     long long items = 0;
-    for (const Launch &l : pl.launches)
-      if (l.generic) items = std::max<long long>(items, total_positions * static_cast<long long>(l.caches.size()));
+    for (const Launch &l : pl.launches) {
+      if (l.kernel == kKernelBulk) continue;
+      long long n = total_positions * static_cast<long long>(l.caches.size());
+      // the direct-load kernel takes pages, a warp each, eight warps a CTA
+      if (l.kernel == kKernelDirect) n = (2 * n + kDirectThreads / 32 - 1) / (kDirectThreads / 32);
+      items = std::max<long long>(items, n);
+    }
+    // a state cache is all state or all KV, so one kind of kernel runs here
+    const long long per_sm = gen[0].layout == KVCS_LAYOUT_STATE ? 8 : 4;
     pl.generic_grid = static_cast<int>(std::max<long long>(
-        1, std::min<long long>(static_cast<long long>(sms) * 8, items)));
+        1, std::min<long long>(static_cast<long long>(sms) * per_sm, items)));
   }
   pl.memset = !accumulate && total_positions > 0 &&
               (pl.all_atomic || (!bulk.empty() && pl.split));
@@ -439,19 +462,22 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       p.caches[i] = make_dev_cache(l.caches[i], block_size);
       U += static_cast<long long>(p.caches[i].halves) * p.caches[i].upp;
     }
-    p.ppu = 1;
+    p.pack = 0;
+    p.full_pages = 1;
     p.pages_per_pos = 0;
-    if (!l.generic) {
+    for (int i = 0; i < n; ++i) p.pages_per_pos += p.caches[i].halves;
+    if (l.kernel == kKernelBulk) {
       const LaunchShape ls = launch_shape(l.caches.data(), 0, n, block_size);
       U = ls.units_per_pos;
-      p.ppu = ls.ppu;
+      p.pack = ls.pack;
+      p.full_pages = ls.full_pages;
       p.pages_per_pos = ls.pages_per_pos;
       p.stage_bytes = ls.stage_bytes;
       p.stages = ls.stages;
     }
     p.units_per_pos = U;
     p.total_units = U * total_positions;
-    if (!l.generic) {
+    if (l.kernel == kKernelBulk) {
       p.split = pl.split;
       p.group_warps = group_warps_for(p.stages);
       p.groups = kConsumerWarps / p.group_warps;
@@ -466,9 +492,12 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
         case kFamHndSub: kvcs_bulk_kernel<kFamHndSub><<<gd, kBulkThreads, smem, st>>>(p); break;
         default: kvcs_bulk_kernel<kFamRows><<<gd, kBulkThreads, smem, st>>>(p); break;
       }
+    } else if (l.kernel == kKernelDirect) {
+      p.split = 0;
+      kvcs_direct_kernel<<<static_cast<unsigned>(pl.generic_grid), kDirectThreads, 0, st>>>(p);
     } else {
       p.split = 0;
-      kvcs_generic_kernel<<<static_cast<unsigned>(pl.generic_grid), kGenericThreads, 0, st>>>(p);
+      kvcs_state_kernel<<<static_cast<unsigned>(pl.generic_grid), kGenericThreads, 0, st>>>(p);
     }
     if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -521,7 +550,9 @@ int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
   info->launches = total_positions > 0 ? static_cast<int32_t>(pl.launches.size()) : 0;
   info->memsets = pl.memset ? 1 : 0;
   info->grid = pl.kernel == 1 ? pl.generic_grid : pl.bulk_grid;
-  info->threads = pl.kernel == 1 ? kGenericThreads : kBulkThreads;
+  info->threads = pl.kernel != 1 ? kBulkThreads
+                  : caches[0].layout == KVCS_LAYOUT_STATE ? kGenericThreads
+                                                           : kDirectThreads;
   info->smem_bytes = pl.kernel != 1 ? bulk_smem_bytes(pl.stages, pl.stage_bytes) : 0;
   info->stage_bytes = pl.kernel != 1 ? pl.stage_bytes : 0;
   info->stages = pl.kernel != 1 ? pl.stages : 0;

@@ -308,7 +308,8 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
         const unsigned char *gp = stage + static_cast<size_t>(g) * bsi * 16;
         accum_slots_rotated(gp, g % nv, nv, S, T, U);
       } else if constexpr (kFam == kFamHnd) {
-        accum_slots(stage + static_cast<size_t>(hl) * bsi * C.hb + (col << 4),
+        // heads staged one after another, nv slots each
+        accum_slots(stage + static_cast<size_t>(hl) * nv * C.hb + (col << 4),
                     static_cast<size_t>(C.hb), 0, nv, 0, S, T, U);
       } else {
         // sub-block sb holds slots [sb*kbs, (sb+1)*kbs) of every head
@@ -321,6 +322,23 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
     }
   }
   return acc;
+}
+
+// Pages of one position a stage holds in packed launches (every page alike,
+// each a unit): the host's count for full pages; for a partial block of the
+// row and HND families, as many pages as their valid bytes allow; a skipped
+// position is passed over at once.
+template <int kFam>
+__device__ __forceinline__ int stage_fit(const Params &p, const PosInfo &cur, int stage_bytes) {
+  if (!p.pack) return 1;
+  if (cur.skip) return 1 << 30;
+  if (cur.nv == p.block_size || (kFam != kFamRows && kFam != kFamHnd)) return p.full_pages;
+  const DevCache &C = p.caches[0];
+  const u32 bytes = kFam == kFamRows
+                        ? static_cast<u32>(cur.nv) * static_cast<u32>(C.rowb)
+                        : static_cast<u32>(C.heads) * static_cast<u32>(cur.nv) *
+                              static_cast<u32>(C.hb);
+  return max(1, static_cast<int>(static_cast<u32>(stage_bytes) / bytes));
 }
 
 // Write a finished (position, column) checksum: a plain store when this CTA
@@ -426,20 +444,21 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     bool aborted = false;
     if (u_begin < u_end) {
       long long pos = u_begin / U;
-      const int k = static_cast<int>(u_begin - pos * U);
       int ci = 0, half = 0, sub = 0;
-      if (p.ppu > 1) {
-        const int page = k * p.ppu;
-        ci = page / p.caches[0].halves;
-        half = page - ci * p.caches[0].halves;
-      } else {
-        int kk = k;
-        while (kk >= p.caches[ci].halves * p.caches[ci].upp) {
-          kk -= p.caches[ci].halves * p.caches[ci].upp;
-          ++ci;
+      {
+        int kk = static_cast<int>(u_begin - pos * U);
+        if (p.pack) {
+          // every cache has the same halves, one unit per page
+          ci = kk / p.caches[0].halves;
+          half = kk - ci * p.caches[0].halves;
+        } else {
+          while (kk >= p.caches[ci].halves * p.caches[ci].upp) {
+            kk -= p.caches[ci].halves * p.caches[ci].upp;
+            ++ci;
+          }
+          half = kk / p.caches[ci].upp;
+          sub = kk - half * p.caches[ci].upp;
         }
-        half = kk / p.caches[ci].upp;
-        sub = kk - half * p.caches[ci].upp;
       }
       ReqCursor rc;
       rc.r = -1;
@@ -448,30 +467,37 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       long long b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
       PosInfo cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
       int mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
+      int fit = stage_fit<kFam>(p, cur, SB);
       int slot = 0;
       u32 n_emit = 0;
       int col = p.caches[ci].column;
-      for (long long u = u_begin; u < u_end; ++u) {
+      for (long long u = u_begin; u < u_end;) {
         const DevCache &C = p.caches[ci];
         // One accumulator slot per (position, column); the caches arrive
         // sorted by column, so a column's units are consecutive.
         const long long dst = pos * p.num_columns + col;
-        int npg = 1;
-        if (p.ppu > 1) npg = min(p.ppu, p.pages_per_pos - (ci * C.halves + half));
+        const int first = sub * C.rpu;
+        int count = 0;
+        u32 pbytes = 0;   // bytes copied per page of the unit
+        u32 pstride = 0;  // bytes a page of the unit occupies in the stage
         if (!cur.skip) {
-          const int first = sub * C.rpu;
-          int count;
-          u32 pbytes;   // bytes copied per page of the unit
-          u32 pstride;  // bytes a page of the unit occupies in the stage
           if constexpr (head_family(kFam)) {
-            // whole-slot runs of the unit's heads, staged as in memory
             count = max(0, min(C.rpu, C.heads - first));
-            pstride = static_cast<u32>(count) * static_cast<u32>(bs) * static_cast<u32>(C.hb);
-            pbytes = pstride;
-            if constexpr (kFam == kFamHndSub) {
-              const int nsb = (cur.nv + C.kbs - 1) / C.kbs;  // sub-blocks with valid slots
-              pbytes = static_cast<u32>(count) * static_cast<u32>(nsb * C.kbs) *
-                       static_cast<u32>(C.hb);
+            if constexpr (kFam == kFamHnd) {
+              // each head's first nv slots (its valid ones), heads packed
+              // one after another in the stage
+              pstride = static_cast<u32>(count) * static_cast<u32>(cur.nv) *
+                        static_cast<u32>(C.hb);
+              pbytes = pstride;
+            } else {
+              // the unit's heads with all their slots, staged as in memory
+              pstride = static_cast<u32>(count) * static_cast<u32>(bs) * static_cast<u32>(C.hb);
+              pbytes = pstride;
+              if constexpr (kFam == kFamHndSub) {
+                const int nsb = (cur.nv + C.kbs - 1) / C.kbs;  // sub-blocks with valid slots
+                pbytes = static_cast<u32>(count) * static_cast<u32>(nsb * C.kbs) *
+                         static_cast<u32>(C.hb);
+              }
             }
           } else if constexpr (kFam == kFamState) {
             count = max(0, min(C.rpu, C.heads - first));
@@ -482,75 +508,110 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
             pstride = pbytes;
           }
-          if (pbytes > 0) {
-            if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
-                                        p.timeout_ns)) {
-              set_status(p, kStatusTimeout);
-              aborted = true;
-              break;
-            }
-            if (n_emit == 0) {
-              slot = static_cast<int>(seq % kRingSlots);
-              ++seq;
-              hdr->ring_acc[slot] = 0ull;
-              hdr->ring_cnt[slot] = 0u;
-            }
-            store_meta(&hdr->meta[s], dst, cur.q, ci, half, first, count, cur.nv,
-                       mode, slot, npg);
-            const u32 fb = ptx::smem_addr(&hdr->full[s]);
-            ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
-            u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
-            int pci = ci, phalf = half;
-            for (int k2 = 0; k2 < npg; ++k2) {
-              const DevCache &D = p.caches[pci];
-              const unsigned char *page = D.base +
-                  static_cast<long long>(phalf) * D.half_stride +
-                  cur.block * D.block_stride;
-              if constexpr (kFam == kFamHndSub) {
-                // [sub-block][heads][kbs][hb]: in each sub-block that holds
-                // valid slots the unit's heads are one contiguous run; when
-                // the unit has every head those runs are one range
-                const u64 sub_page = static_cast<u64>(D.heads) * D.kbs * D.hb;
-                const u32 run = static_cast<u32>(count) * static_cast<u32>(D.kbs * D.hb);
-                if (count == D.heads) {
-                  ptx::bulk_g2s(dst, page, pbytes, fb, policy);
-                } else {
-                  for (int sb = 0; sb * D.kbs < cur.nv; ++sb)
-                    ptx::bulk_g2s(dst + static_cast<u32>(sb) * run,
-                                  page + static_cast<u64>(sb) * sub_page +
-                                      static_cast<u64>(first) * D.kbs * D.hb,
-                                  run, fb, policy);
-                }
-              } else if constexpr (head_family(kFam)) {
-                // [heads][block_size][hb] or [heads][chunks][block_size][16]:
-                // the unit's heads are one contiguous run of whole slots
-                ptx::bulk_g2s(dst, page + static_cast<u64>(first) * bs * D.hb, pstride,
-                              fb, policy);
+        }
+        // Pages per unit: one, or, when the launch's pages all look alike and
+        // each is a unit, as many consecutive pages of the position (in this
+        // CTA's range) as the stage holds -- many more when blocks are
+        // partial.  A skipped position is passed over in one step.
+        int npg = 1;
+        // (the two forms of the test and of the cursor step below measured
+        // fastest for their families: rows a packed step per unit, heads the
+        // one-page step whenever a unit holds one page)
+        if (kFam == kFamRows ? p.pack != 0 : fit > 1) {
+          int left = p.pages_per_pos - (ci * C.halves + half);
+          if (u_end - u < left) left = static_cast<int>(u_end - u);
+          npg = max(1, min(left, fit));
+        }
+        if (pbytes > 0) {
+          if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
+                                      p.timeout_ns)) {
+            set_status(p, kStatusTimeout);
+            aborted = true;
+            break;
+          }
+          if (n_emit == 0) {
+            slot = static_cast<int>(seq % kRingSlots);
+            ++seq;
+            hdr->ring_acc[slot] = 0ull;
+            hdr->ring_cnt[slot] = 0u;
+          }
+          store_meta(&hdr->meta[s], dst, cur.q, ci, half, first, count, cur.nv,
+                     mode, slot, npg);
+          const u32 fb = ptx::smem_addr(&hdr->full[s]);
+          ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
+          u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
+          int pci = ci, phalf = half;
+          for (int k2 = 0; k2 < npg; ++k2) {
+            const DevCache &D = p.caches[pci];
+            const unsigned char *page = D.base +
+                static_cast<long long>(phalf) * D.half_stride +
+                cur.block * D.block_stride;
+            if constexpr (kFam == kFamHndSub) {
+              // [sub-block][heads][kbs][hb]: in each sub-block that holds
+              // valid slots the unit's heads are one contiguous run; when
+              // the unit has every head those runs are one range
+              const u64 sub_page = static_cast<u64>(D.heads) * D.kbs * D.hb;
+              const u32 run = static_cast<u32>(count) * static_cast<u32>(D.kbs * D.hb);
+              if (count == D.heads) {
+                ptx::bulk_g2s(dst, page, pbytes, fb, policy);
               } else {
-                ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes,
-                              fb, policy);
+                for (int sb = 0; sb * D.kbs < cur.nv; ++sb)
+                  ptx::bulk_g2s(dst + static_cast<u32>(sb) * run,
+                                page + static_cast<u64>(sb) * sub_page +
+                                    static_cast<u64>(first) * D.kbs * D.hb,
+                                run, fb, policy);
               }
-              dst += pstride;
-              if (++phalf == D.halves) {
-                phalf = 0;
-                ++pci;
+            } else if constexpr (kFam == kFamHnd) {
+              // [heads][block_size][hb]: a full block's heads are one
+              // contiguous run; a partial block's valid slots are one run of
+              // nv slots per head, copied one after another
+              const unsigned char *src = page + static_cast<u64>(first) * bs * D.hb;
+              if (cur.nv == bs) {
+                ptx::bulk_g2s(dst, src, pstride, fb, policy);
+              } else {
+                const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(D.hb);
+                const u64 hstep = static_cast<u64>(bs) * static_cast<u64>(D.hb);
+                for (int h = 0; h < count; ++h)
+                  ptx::bulk_g2s(dst + static_cast<u32>(h) * run, src + h * hstep, run, fb,
+                                policy);
               }
+            } else if constexpr (head_family(kFam)) {
+              // [heads][chunks][block_size][16]: the unit's heads are one
+              // contiguous run of whole slots
+              ptx::bulk_g2s(dst, page + static_cast<u64>(first) * bs * D.hb, pstride,
+                            fb, policy);
+            } else {
+              ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes,
+                            fb, policy);
             }
-            ++it;
-            ++n_emit;
-            if (++s == NS) {
-              s = 0;
-              ++f;
+            dst += pstride;
+            if (++phalf == D.halves) {
+              phalf = 0;
+              ++pci;
             }
           }
+          ++it;
+          ++n_emit;
+          if (++s == NS) {
+            s = 0;
+            ++f;
+          }
         }
-        // advance the cursor past this unit
+        // advance the cursor past this unit's npg host units
+        u += npg;
         bool pos_done = false;
-        if (p.ppu > 1) {
-          // every cache has C.halves halves when pages are packed
+        if (kFam == kFamRows && p.pack) {
+          // packed pages: every cache has C.halves halves
           const int flat = ci * C.halves + half + npg;
           ci = flat / C.halves;
           half = flat - ci * C.halves;
+          pos_done = ci >= p.num_caches;
+        } else if (npg > 1) {
+          half += npg;
+          while (half >= C.halves) {
+            half -= C.halves;
+            ++ci;
+          }
           pos_done = ci >= p.num_caches;
         } else if (++sub == C.upp) {
           sub = 0;
@@ -560,7 +621,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           }
         }
         if (pos_done) ci = 0;
-        if (pos_done || u + 1 == u_end || p.caches[ci].column != col) {
+        if (pos_done || u == u_end || p.caches[ci].column != col) {
           // close the (position, column): this thread's share of the count
           if (n_emit > 0) {
             const u32 delta = 0u - static_cast<u32>(p.group_warps) * n_emit;
@@ -572,13 +633,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           n_emit = 0;
         }
         col = p.caches[ci].column;
-        if (pos_done && u + 1 < u_end) {
+        if (pos_done && u < u_end) {
           ++pos;
           b_cur = b_next;
           b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
           req_seek(p, rc, pos);
           cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
           mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
+          fit = stage_fit<kFam>(p, cur, SB);
         }
       }
     }
@@ -643,7 +705,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       const DevCache &C = p.caches[ci];
       if (C.rowb != map.rowb) make_map(map, C.rowb, gtid, gw * 32);
       v += unit_sum<kFam>(C, m, half, sp, map, bsz);
-      sp += head_family(kFam)
+      sp += kFam == kFamHnd ? static_cast<size_t>(m.count) * static_cast<size_t>(m.nv) * C.hb
+            : head_family(kFam)
                 ? static_cast<size_t>(m.count) * static_cast<size_t>(bsz) * C.hb
                 : static_cast<size_t>(m.count) * C.rowb;
       if (++half == C.halves) {

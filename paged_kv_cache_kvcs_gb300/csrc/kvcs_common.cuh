@@ -120,8 +120,10 @@ struct Params {
   int stage_bytes;           // bytes per stage (multiple of 128)
   int group_warps;           // consumer warps per group: 1, 2, 4 or 8
   int groups;                // kConsumerWarps / group_warps, <= stages
-  int ppu;                   // pages per unit: > 1 only when every cache has
-                             // the same geometry and a page fits a unit
+  int pack;                  // 1: every cache has the same geometry and each
+                             // page is a unit; consecutive pages of a position
+                             // are packed into one stage as far as it holds
+  int full_pages;            // pack: full pages a stage holds
   int pages_per_pos;         // sum of halves over the caches
   int num_columns;           // replica-key columns of the output
   int state_call;            // the caches hold Mamba states (block position 0)
@@ -215,21 +217,22 @@ __device__ __forceinline__ void req_seek(const Params &p, ReqCursor &c, long lon
   req_load(p, c, r);
 }
 
-__device__ PosInfo position_info(const Params &p, long long pos, const ReqCursor &c,
-                                 long long b, long long u_begin, long long u_end) {
+// Block position, block and valid slots of global position `pos` (request
+// cursor `c` on it, block id `b`); bad tables set status bits when `report`.
+__device__ PosInfo position_info_quiet(const Params &p, long long pos, const ReqCursor &c,
+                                       long long b, bool report) {
   PosInfo pi;
-  pi.whole = (pos * p.units_per_pos >= u_begin) &&
-             ((pos + 1) * p.units_per_pos <= u_end);
+  pi.whole = false;
   pi.q = 0;
   pi.block = 0;
   pi.nv = 0;
   pi.skip = true;
   if (c.r < 0 || c.fp < 0) {
-    set_status(p, kStatusBadRequests);
+    if (report) set_status(p, kStatusBadRequests);
     return pi;
   }
   if (b < 0 || b >= p.min_num_blocks) {
-    set_status(p, kStatusBadBlockId);
+    if (report) set_status(p, kStatusBadBlockId);
     return pi;
   }
   const long long q = c.fp + (pos - c.po0);
@@ -247,6 +250,16 @@ __device__ PosInfo position_info(const Params &p, long long pos, const ReqCursor
   pi.block = b;
   pi.nv = static_cast<int>(nv);
   pi.skip = nv <= 0;
+  return pi;
+}
+
+// As position_info_quiet, for the bulk kernel's producer lane: also whether
+// every unit of the position lies in this CTA's range [u_begin, u_end).
+__device__ __forceinline__ PosInfo position_info(const Params &p, long long pos,
+                                                 const ReqCursor &c, long long b,
+                                                 long long u_begin, long long u_end) {
+  PosInfo pi = position_info_quiet(p, pos, c, b, true);
+  pi.whole = (pos * p.units_per_pos >= u_begin) && ((pos + 1) * p.units_per_pos <= u_end);
   return pi;
 }
 

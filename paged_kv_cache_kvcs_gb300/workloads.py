@@ -247,6 +247,20 @@ def llama3_70b(seed: int = 0, device="cpu", num_requests: int = 128,
                   kind=BYTES)
 
 
+def llama3_8b_decode(seed: int = 0, device="cpu", num_requests: int = 16384,
+                     layout: int = LAYOUT_HND) -> Workload:
+    """Decode-shaped checksums of freshly appended blocks: Llama-3-8B
+    geometry (32 layers, 8 KV heads, head_size 128 bf16 ``randn``, block_size
+    16), ``num_requests`` requests of ``16 k + 1`` tokens with ``k`` uniform
+    in [32, 255], each listing only its newest block (position ``k``), which
+    holds one token."""
+    g = _cpu_gen(seed + 2000)
+    ks = torch.randint(32, 256, (num_requests,), generator=g).tolist()
+    return _build("llama3_8b_decode", seed, device, layers=32, heads=8, head_bytes=256,
+                  block_size=16, lengths=[16 * k + 1 for k in ks], layout=layout,
+                  kind=BF16_NORMAL, first_positions=ks)
+
+
 def random_case(seed: int, device="cpu", *, layout: int = LAYOUT_NHD,
                 layers: int = 2, heads: int = 2, head_bytes: int = 32,
                 block_size: int = 16, lengths: Sequence[int] = (37,),

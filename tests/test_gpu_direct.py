@@ -1,0 +1,154 @@
+"""The direct-load kernel (KV pages the bulk-copy kernel cannot stage)
+against the oracle, through the C ABI: every layout, pools 0 or 8 bytes past
+a 16-byte boundary, rows that are 8 mod 16 bytes (chunks pair up over two
+rows), rows and head runs past a stage, pages whose alignment alternates
+with the block (strides 8 mod 16), ragged and empty positions, first
+positions past 2^57 (t P wraps 2^64).  Bit-exact uint64 equality."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import W
+import paged_kv_cache_kvcs_gb300 as K
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _shifted(wl, shift, block_pad=0):
+    """The same bytes at ``shift`` bytes past a 16-byte boundary, each page
+    followed by ``block_pad`` spare bytes (block stride = page + pad)."""
+    caches, keep = [], []
+    for c in wl.caches:
+        halves = 1 if c.layout == W.LAYOUT_LATENT else 2
+        page = wl.block_size * c.num_heads * c.head_bytes
+        stride = page + block_pad
+        raw = torch.zeros(halves * c.num_blocks * stride + shift + 16, dtype=torch.uint8,
+                          device=DEV)
+        pool = raw[shift:shift + halves * c.num_blocks * stride]
+        pool.view(halves * c.num_blocks, stride)[:, :page] = \
+            c.pool.view(halves * c.num_blocks, page)
+        keep.append(raw)
+        extra = dict(block_stride=stride, half_stride=c.num_blocks * stride) if block_pad else {}
+        caches.append(dataclasses.replace(c, pool=pool, **extra))
+    return W.Workload(wl.name, wl.block_size, caches, wl.pos_offsets, wl.first_position,
+                      wl.num_tokens, wl.block_ids, wl.info), keep
+
+
+def _check(wl):
+    from gpu_helpers import full_oracle, gpu_checksums
+    plan = K.plan_for(wl.caches, wl.block_size, wl.num_positions)
+    assert plan["kernel"] == 1, plan
+    got, st = gpu_checksums(wl)
+    exp, est = full_oracle(wl)
+    assert st == est == 0
+    bad = np.flatnonzero(got != exp)
+    assert bad.size == 0, f"{bad.size} of {got.size} differ, first {bad[:8].tolist()}"
+
+
+CASES = [
+    # (layout, heads, head_bytes, block_size, kernel_block_size)
+    (W.LAYOUT_NHD, 8, 256, 16, 0),      # the 8B-shaped row, 128 chunks
+    (W.LAYOUT_NHD, 3, 24, 16, 0),       # 72-byte rows: chunks pair over two rows
+    (W.LAYOUT_NHD, 1, 8, 5, 0),         # one word per row
+    (W.LAYOUT_NHD, 5, 40, 3, 0),        # 200-byte rows
+    (W.LAYOUT_LATENT, 1, 72, 16, 0),
+    (W.LAYOUT_LATENT, 1, 1152, 64, 0),  # the MLA row
+    (W.LAYOUT_HND, 8, 256, 16, 0),
+    (W.LAYOUT_HND, 3, 24, 7, 0),        # head runs alternate their alignment
+    (W.LAYOUT_HND, 2, 8, 16, 0),
+    (W.LAYOUT_HND, 4, 64, 16, 4),       # kernel sub-blocks
+    (W.LAYOUT_HND, 3, 24, 12, 3),
+    (W.LAYOUT_XSPLIT, 4, 64, 16, 0),
+    (W.LAYOUT_XSPLIT, 2, 48, 7, 0),
+]
+
+
+@pytest.mark.parametrize("shift", [0, 8])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"l{c[0]}h{c[1]}b{c[2]}bs{c[3]}k{c[4]}")
+def test_direct_kernel_matches_oracle(case, shift):
+    layout, heads, hb, bs, kbs = case
+    wl = W.random_case(21, DEV, layout=layout, layers=3, heads=heads, head_bytes=hb,
+                       block_size=bs, lengths=(70, 33, 5, bs), first_positions=(1, 0, 0, 0),
+                       extra_positions=(0, 1, 0, 0))
+    if kbs:
+        wl = W.Workload(wl.name, bs, [dataclasses.replace(c, kernel_block_size=kbs)
+                                      for c in wl.caches], wl.pos_offsets, wl.first_position,
+                        wl.num_tokens, wl.block_ids, wl.info)
+    aligned16 = hb % 16 == 0 and (layout != W.LAYOUT_NHD or (heads * hb) % 16 == 0)
+    if shift == 0 and aligned16:
+        # 16-byte geometry: force the direct kernel with blocks 8 mod 16 apart
+        wl, keep = _shifted(wl, 0, block_pad=8)
+    else:
+        wl, keep = _shifted(wl, shift)
+    _check(wl)
+
+
+@pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND])
+def test_rows_and_head_runs_past_a_stage(layout):
+    """128 KiB NHD rows (64 heads of 2 KiB) and 128 KiB HND head runs
+    (block_size 512): each lane owns several chunk columns."""
+    if layout == W.LAYOUT_NHD:
+        wl = W.random_case(22, DEV, layout=layout, layers=2, heads=64, head_bytes=2048,
+                           block_size=2, lengths=(5, 2))
+    else:
+        wl = W.random_case(22, DEV, layout=layout, layers=2, heads=2, head_bytes=256,
+                           block_size=512, lengths=(700, 3))
+    wl, keep = _shifted(wl, 8)
+    _check(wl)
+
+
+def test_many_positions_and_caches_misaligned():
+    """Thousands of positions over 16 layers, 8 bytes off: warps' page
+    ranges start and end inside positions and inside a position's caches."""
+    g = torch.Generator().manual_seed(5)
+    lengths = torch.randint(1, 400, (96,), generator=g).tolist()
+    wl = W.random_case(23, DEV, layout=W.LAYOUT_NHD, layers=16, heads=2, head_bytes=64,
+                       block_size=16, lengths=lengths)
+    wl, keep = _shifted(wl, 8)
+    _check(wl)
+
+
+def test_position_past_2_pow_57_misaligned():
+    wl = W.random_case(24, DEV, layout=W.LAYOUT_NHD, layers=2, heads=3, head_bytes=24,
+                       block_size=16, lengths=((1 << 57) * 16 + 20,),
+                       first_positions=(1 << 57,))
+    wl, keep = _shifted(wl, 8)
+    _check(wl)
+
+
+def test_bad_block_id_and_columns_misaligned():
+    """A bad block id gives 0 and the status bit; replica columns add per
+    column; an accumulating call adds onto earlier contents."""
+    from gpu_helpers import full_oracle
+    wl = W.random_case(25, DEV, layout=W.LAYOUT_NHD, layers=4, heads=2, head_bytes=24,
+                       block_size=8, lengths=(40, 17))
+    wl, keep = _shifted(wl, 8)
+    exp, _ = full_oracle(wl)
+    ids = wl.block_ids.clone()
+    ids[2] = wl.caches[0].num_blocks + 5
+    bad = W.Workload(wl.name, wl.block_size, wl.caches, wl.pos_offsets, wl.first_position,
+                     wl.num_tokens, ids, wl.info)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = K.workload_checksums(bad, status=status)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint64)
+    want = exp.copy()
+    want[2] = 0
+    assert int(status.item()) & K.KVCS_STATUS_BAD_BLOCK_ID
+    assert np.array_equal(got, want)
+    # two columns (layers 0-1 and 2-3), their row sum is the checksum
+    cols = [dataclasses.replace(c, column=i // 2) for i, c in enumerate(wl.caches)]
+    vals = K.group_checksums(cols, wl.block_size, wl.pos_offsets, wl.first_position,
+                             wl.num_tokens, wl.block_ids, 2)
+    torch.cuda.synchronize()
+    v = vals.cpu().numpy().view(np.uint64)
+    assert np.array_equal(v.sum(axis=1, dtype=np.uint64), exp)
+    # accumulate the same call onto the values: every word doubles
+    K.group_checksums(cols, wl.block_size, wl.pos_offsets, wl.first_position,
+                      wl.num_tokens, wl.block_ids, 2, values=vals, accumulate=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(vals.cpu().numpy().view(np.uint64), v * np.uint64(2))

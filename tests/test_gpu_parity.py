@@ -84,6 +84,14 @@ BULK = [
          lengths=(11, 4)),                            # 8 KiB pages, 4 per unit
     dict(layout=W.LAYOUT_NHD, layers=2, heads=2, head_bytes=64, block_size=16,
          lengths=((1 << 57) * 16 + 37,), first_positions=(1 << 57,)),  # t P wraps 2^64
+    # decode-shaped HND: each request lists only its newest block, holding
+    # 1, 2 or 15 tokens (only those slots are copied), plus full blocks
+    dict(layout=W.LAYOUT_HND, layers=3, heads=8, head_bytes=256, block_size=16,
+         lengths=[16 * k + 1 for k in range(40)] + [16 * 7 + 2, 16 * 3 + 15, 64],
+         first_positions=list(range(40)) + [7, 3, 0]),
+    dict(layout=W.LAYOUT_HND, layers=2, heads=2, head_bytes=64, block_size=16,
+         lengths=[16 * (k % 9) + 1 + (k % 3) for k in range(304)],
+         first_positions=[k % 9 for k in range(304)]),  # whole-position mode
 ]
 
 
