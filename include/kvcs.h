@@ -25,6 +25,12 @@
  *
  * Memory: the caller owns every buffer.  The library allocates nothing and
  * enqueues all work on the caller's stream; calls are asynchronous.
+ * Stream order: a call's kernels start only after the stream's earlier work
+ * has finished.  The checksum kernels let a following kernel that was
+ * launched with programmatic stream serialization start before they end;
+ * as with any programmatic dependent launch, such a kernel must wait for
+ * them (griddepcontrol.wait, cudaGridDependencySynchronize) before it reads
+ * what they write.
  * Thread safety: calls may be issued concurrently from several host threads
  * and streams; they share no mutable state apart from a launch counter.
  */
@@ -329,7 +335,9 @@ typedef struct kvcs_plan_info {
                             (output zeroed first, partial sums added with
                             64-bit atomics; the generic kernel always adds) */
   int32_t launches;      /* kernel launches per call (one per cache group) */
-  int32_t memsets;       /* cudaMemsetAsync calls per call (0 or 1) */
+  int32_t memsets;       /* output-zeroing launches per call (0 or 1): one
+                            small kernel before the checksum launches, which
+                            overlap it (programmatic dependent launch) */
   int32_t grid;          /* CTAs per kernel launch */
   int32_t threads;       /* threads per CTA */
   int32_t smem_bytes;    /* dynamic shared memory per CTA */
@@ -366,7 +374,7 @@ int kvcs_selftest_wait_timeout(uint32_t *status, int64_t limit_ns, void *stream)
 const char *kvcs_strerror(int code);
 
 /* Kernels this library has launched in this process (all devices, all
- * threads).  Memsets are not counted. */
+ * threads), the output-zeroing kernel included. */
 uint64_t kvcs_launch_count(void);
 
 /* ABI version: (major << 16) | minor.  Minor 2 added kvcs_write_kv and

@@ -6,7 +6,7 @@
 // layout family; the direct-load kernel for KV caches it cannot stage; the
 // state-row kernel for such state caches; the row-sum epilogue; or the write
 // kernels) and enqueues them, plus, when CTAs or launches share positions,
-// one cudaMemsetAsync of the output, on the caller's stream.
+// one kernel that zeroes the output first, on the caller's stream.
 
 #include <cuda_runtime.h>
 
@@ -405,6 +405,31 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
   return pl;
 }
 
+// Launch a checksum kernel.  Right after the zeroing kernel it is launched
+// with programmatic stream serialization: it may start while the zeroing runs
+// (every kernel waits for it before writing an output word; the zeroing
+// kernel itself waited for all earlier work before letting it start).  Any
+// other launch waits for the stream's earlier work as usual, so a kernel
+// before it that lets its dependents start early can never have them read
+// its inputs.
+cudaError_t launch(void (*kernel)(Params), dim3 grid, int threads, size_t smem, cudaStream_t st,
+                   bool after_zero, const Params &p) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (after_zero) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 // Shared body of kvcs_block_checksums and kvcs_group_checksums.
 int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block_size,
                   const kvcs_requests *reqs, int64_t total_positions,
@@ -428,11 +453,27 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
                             accumulate);
 
   if (pl.memset) {
-    if (cudaMemsetAsync(outs->values, 0,
-                        static_cast<size_t>(total_positions) * ncols * sizeof(uint64_t),
-                        st) != cudaSuccess)
+    // zero the output with a kernel that lets the first checksum launch start
+    // at once (that launch waits for it before writing any output word)
+    const long long words = total_positions * static_cast<long long>(ncols);
+    const long long blocks = std::max<long long>(
+        1, std::min<long long>((words + 1023) / 1024, static_cast<long long>(sms)));
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kvcs_zero_kernel, reinterpret_cast<u64 *>(outs->values),
+                           words) != cudaSuccess)
       return KVCS_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
   }
+  bool after_zero = pl.memset;
 
   long long min_nb = caches_in[0].num_blocks;
   for (int32_t i = 1; i < num_caches; ++i) min_nb = std::min<long long>(min_nb, caches_in[i].num_blocks);
@@ -485,22 +526,29 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
       const size_t smem = bulk_smem_bytes(p.stages, p.stage_bytes);
       const dim3 gd(static_cast<unsigned>(grid));
+      cudaError_t e;
       switch (l.family) {
-        case kFamHnd: kvcs_bulk_kernel<kFamHnd><<<gd, kBulkThreads, smem, st>>>(p); break;
-        case kFamXSplit: kvcs_bulk_kernel<kFamXSplit><<<gd, kBulkThreads, smem, st>>>(p); break;
-        case kFamState: kvcs_bulk_kernel<kFamState><<<gd, kBulkThreads, smem, st>>>(p); break;
-        case kFamHndSub: kvcs_bulk_kernel<kFamHndSub><<<gd, kBulkThreads, smem, st>>>(p); break;
-        default: kvcs_bulk_kernel<kFamRows><<<gd, kBulkThreads, smem, st>>>(p); break;
+        case kFamHnd: e = launch(kvcs_bulk_kernel<kFamHnd>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamXSplit: e = launch(kvcs_bulk_kernel<kFamXSplit>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamState: e = launch(kvcs_bulk_kernel<kFamState>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamHndSub: e = launch(kvcs_bulk_kernel<kFamHndSub>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        default: e = launch(kvcs_bulk_kernel<kFamRows>, gd, kBulkThreads, smem, st, after_zero, p); break;
       }
+      if (e != cudaSuccess) return KVCS_ECUDA;
     } else if (l.kernel == kKernelDirect) {
       p.split = 0;
-      kvcs_direct_kernel<<<static_cast<unsigned>(pl.generic_grid), kDirectThreads, 0, st>>>(p);
+      if (launch(kvcs_direct_kernel, dim3(static_cast<unsigned>(pl.generic_grid)), kDirectThreads,
+                 0, st, after_zero, p) != cudaSuccess)
+        return KVCS_ECUDA;
     } else {
       p.split = 0;
-      kvcs_state_kernel<<<static_cast<unsigned>(pl.generic_grid), kGenericThreads, 0, st>>>(p);
+      if (launch(kvcs_state_kernel, dim3(static_cast<unsigned>(pl.generic_grid)), kGenericThreads,
+                 0, st, after_zero, p) != cudaSuccess)
+        return KVCS_ECUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    after_zero = false;
   }
 
   if (outs->row_sums || outs->expected) {

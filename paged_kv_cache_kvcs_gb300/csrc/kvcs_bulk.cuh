@@ -348,6 +348,7 @@ __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
                                               int slot, long long dst, int mode) {
   __threadfence_block();
   const u64 total = atomicAdd(&hdr->ring_acc[slot], 0ull);
+  ptx::grid_dep_wait();   // the output is zeroed by the kernel before this one
   if (mode == kFlushStore) p.out[dst] = total;
   else atomicAdd(p.out + dst, total);
 }
@@ -428,8 +429,22 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
   }
 
   if (tid < 32) {
-    if (tid != 0) return;
     // ------------------------------ producer ------------------------------
+    // The whole warp looks up the request of the range's first position (one
+    // round of loads for up to 31 requests), with that position's block ids
+    // loaded alongside; lane 0 then runs the producer alone.
+    ReqCursor rc;
+    rc.r = -1;
+    long long b_cur = 0, b_next = 0;
+    if (u_begin < u_end) {
+      const long long pos0 = u_begin / p.units_per_pos;
+      if (tid == 0) {
+        b_cur = p.block_ids[pos0];
+        b_next = pos0 + 1 < p.total_positions ? p.block_ids[pos0 + 1] : 0;
+      }
+      rc = req_find_warp(p, pos0, tid);
+    }
+    if (tid != 0) return;
     if (g == 0 && p.num_requests >= 0) {
       if (p.pos_offsets[0] != 0 || p.pos_offsets[p.num_requests] != p.total_positions)
         set_status(p, kStatusBadRequests);
@@ -460,11 +475,6 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           sub = kk - half * p.caches[ci].upp;
         }
       }
-      ReqCursor rc;
-      rc.r = -1;
-      req_seek(p, rc, pos);
-      long long b_cur = p.block_ids[pos];
-      long long b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
       PosInfo cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
       int mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
       int fit = stage_fit<kFam>(p, cur, SB);
@@ -628,6 +638,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             const u32 prev = atomicAdd(&hdr->ring_cnt[slot], delta);
             if (prev + delta == 0u) finalize_slot(p, hdr, slot, dst, mode);
           } else if (cur.whole && !p.all_atomic) {
+            ptx::grid_dep_wait();
             p.out[dst] = 0ull;
           }
           n_emit = 0;
@@ -644,6 +655,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         }
       }
     }
+    // Every copy of this CTA is issued: a following kernel launched with
+    // programmatic stream serialization may start (it waits for this grid
+    // before it touches anything this grid writes).
+    ptx::grid_dep_launch();
     if (!aborted) {
       // one end-of-stream marker per consumer group
       for (int k = 0; k < p.groups; ++k) {

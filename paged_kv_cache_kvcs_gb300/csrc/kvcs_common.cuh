@@ -193,6 +193,49 @@ struct ReqCursor {
   long long fp, nt;   // first_position[r], num_tokens[r]
 };
 
+// The request holding `pos`, found by the 32 lanes of a warp together
+// (every lane returns the same cursor): while more than 31 requests remain
+// the lanes probe 32 evenly spaced pos_offsets and keep the bucket holding
+// pos, then one round of loads reads the remaining offsets with the
+// candidates' first_position and num_tokens.  One round of loads when the
+// call has at most 31 requests.  Reads only pos_offsets[0 .. R] and
+// first_position / num_tokens [0, R), whatever the arrays hold; a position
+// no request holds gives r = -1.
+__device__ __forceinline__ ReqCursor req_find_warp(const Params &p, long long pos, int lane) {
+  constexpr unsigned kAll = 0xffffffffu;
+  long long lo = 0, hi = p.num_requests;   // r in [lo, hi)
+  while (hi - lo > 31) {
+    const long long idx = lo + (hi - lo) * lane / 32;
+    const unsigned below = __ballot_sync(kAll, p.pos_offsets[idx] <= pos);
+    const int k = below ? 31 - __clz(below) : 0;   // last probe at or below pos
+    const long long nlo = __shfl_sync(kAll, idx, k);
+    const long long nhi = k < 31 ? __shfl_sync(kAll, idx, k + 1) : hi;
+    lo = nlo;
+    hi = nhi < hi ? nhi : hi;
+    if (!below) hi = lo + 1;                      // pos below every offset: no request
+  }
+  const long long r = lo + lane;
+  const bool in = r < hi;
+  const long long a = in ? p.pos_offsets[r] : 0;
+  const long long b = in ? p.pos_offsets[r + 1] : 0;
+  const long long fp = in ? p.first_position[r] : 0;
+  const long long nt = in ? p.num_tokens[r] : 0;
+  const unsigned hit = __ballot_sync(kAll, in && a <= pos && pos < b);
+  ReqCursor c;
+  if (!hit) {
+    c.r = -1;
+    c.po0 = c.po1 = c.fp = c.nt = 0;
+    return c;
+  }
+  const int k = __ffs(hit) - 1;
+  c.r = __shfl_sync(kAll, r, k);
+  c.po0 = __shfl_sync(kAll, a, k);
+  c.po1 = __shfl_sync(kAll, b, k);
+  c.fp = __shfl_sync(kAll, fp, k);
+  c.nt = __shfl_sync(kAll, nt, k);
+  return c;
+}
+
 __device__ __forceinline__ void req_load(const Params &p, ReqCursor &c, long long r) {
   c.r = r;
   if (r < 0) {

@@ -225,9 +225,10 @@ struct DirectWalk {
 };
 
 __device__ __forceinline__ void walk_seek(const Params &p, DirectWalk &w, long long pos,
-                                          int lane) {
+                                          int lane, bool first) {
   ReqCursor rc = w.rc;
-  req_seek(p, rc, pos);
+  if (first) rc = req_find_warp(p, pos, lane);
+  else req_seek(p, rc, pos);
   const PosInfo pi = position_info_quiet(p, pos, rc, p.block_ids[pos], lane == 0);
   __syncwarp();
   if (lane == 0) {
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kDirectThreads, 4)
       wk.half = k;
     }
     __syncwarp();
-    walk_seek(p, wk, pos, lane);
+    walk_seek(p, wk, pos, lane, true);
   }
   u64 acc = 0;
   for (long long it = i0; it < i1; ++it) {
@@ -298,7 +299,10 @@ __global__ void __launch_bounds__(kDirectThreads, 4)
     const int col = C.column;
     if (pos_done || it + 1 == i1 || p.caches[nci].column != col) {
       const u64 v = warp_sum(acc);
-      if (lane == 0 && v != 0) atomicAdd(p.out + wk.pos * p.num_columns + col, v);
+      if (lane == 0 && v != 0) {
+        ptx::grid_dep_wait();   // the output is zeroed by the kernel before this one
+        atomicAdd(p.out + wk.pos * p.num_columns + col, v);
+      }
       acc = 0;
     }
     __syncwarp();
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(kDirectThreads, 4)
       wk.half = nhalf;
     }
     __syncwarp();
-    if (pos_done && it + 1 < i1) walk_seek(p, wk, wk.pos + 1, lane);
+    if (pos_done && it + 1 < i1) walk_seek(p, wk, wk.pos + 1, lane, false);
   }
 }
 

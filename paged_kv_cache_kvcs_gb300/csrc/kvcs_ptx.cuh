@@ -74,6 +74,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(u32 bar, u32 parity,
   return false;
 }
 
+// Programmatic dependent launch.  grid_dep_launch lets the next kernel of
+// the stream (launched with programmatic stream serialization) start before
+// this one ends; grid_dep_wait makes the calling thread wait until the grids
+// it depends on have finished and their writes are visible (at once when the
+// kernel was launched without such a dependency).
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // L2 policy for data read exactly once.
 __device__ __forceinline__ u64 policy_evict_first() {
   u64 pol;

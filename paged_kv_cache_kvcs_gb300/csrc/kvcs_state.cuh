@@ -128,7 +128,10 @@ __global__ void __launch_bounds__(kGenericThreads)
     if (tid == 0) {
       u64 total = 0;
       for (int w = 0; w < kGenericThreads / 32; ++w) total += red[w];
-      if (total) atomicAdd(p.out + pos * p.num_columns + C.column, total);
+      if (total) {
+        ptx::grid_dep_wait();   // the output is zeroed by the kernel before this one
+        atomicAdd(p.out + pos * p.num_columns + C.column, total);
+      }
     }
     __syncthreads();
   }
