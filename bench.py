@@ -254,8 +254,8 @@ def measured_peak():
 # launches it, the shared device code and the kernel's own file.
 KERNEL_SOURCES = {
     "kvcs_bulk_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_bulk.cuh"],
-    "kvcs_write_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_write.cuh"],
-    "kvcs_direct_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_direct.cuh"],
+    "kvcs_write_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_write.cuh"],
+    "kvcs_direct_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_direct.cuh"],
 }
 
 
@@ -582,6 +582,12 @@ def run_write(args, ws, rank, local):
     launches = (kvcs.launch_count() - launches0) // (args.steps + max(3, args.warmup))
     t_plain = timed(plain, args.steps)
     t_unfused = timed(unfused, args.steps)
+    # the same fused call replayed from a CUDA graph, as a serving engine
+    # replays its captured step: no host work per call
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fused_w(raw)
+    t_graph = timed(graph.replay, args.steps)
     moved = 2 * n * layers * 2 * heads * hb          # bytes read + written
     if rank != 0:
         return
@@ -609,6 +615,8 @@ def run_write(args, ws, rank, local):
                              "llama3_8b_write", n, kernel="kvcs_write_kernel"),
                          "kernel": "kvcs_write_kernel", "launch_ms": round(t_fused * 1e3, 4)},
             "clocks": clocks,
+            "graph_ms_per_step": round(t_graph * 1e3, 4),
+            "graph_gbs": round(moved / t_graph / 1e9, 2),
             "write_only_ms": round(t_plain * 1e3, 4),
             "write_then_checksum_ms": round(t_unfused * 1e3, 4),
             "fused_vs_write_only": round(t_plain / t_fused, 4),

@@ -32,11 +32,37 @@ struct WriteParams {
 constexpr int kWriteThreads = 256;
 constexpr int kWriteBatch = 8;  // chunks per lane in flight
 
+// Loads of one batch of a token's row chunks for one cache: chunk idx = base
+// + 32 k (K chunks first, then V chunks), up to eight per lane; chunks past
+// the row are left untouched.
+__device__ __forceinline__ void load_row_batch(const DevCache &C, const unsigned char *srck,
+                                               const unsigned char *srcv, int base, int ch,
+                                               uint4 (&v)[kWriteBatch]) {
+  const int nh = (C.heads * C.hb) / ch;  // chunks per half
+  const int n = nh * C.halves;
+#pragma unroll
+  for (int k = 0; k < kWriteBatch; ++k) {
+    const int idx = base + 32 * k;
+    if (idx < n) {
+      const bool hv = idx >= nh;
+      const unsigned char *src = (hv ? srcv : srck) + (idx - (hv ? nh : 0)) * ch;
+      if (ch == 16) {
+        v[k] = *reinterpret_cast<const uint4 *>(src);
+      } else {
+        const u64 x = *reinterpret_cast<const u64 *>(src);
+        v[k] = make_uint4(static_cast<u32>(x), static_cast<u32>(x >> 32), 0u, 0u);
+      }
+    }
+  }
+}
+
 // One cache's K and V rows of one token: moved into the page slot `o` of
 // block `b` by the calling warp, up to eight chunks per lane in flight (the
 // K and V chunks of one batch together); returns the lane's share of the
-// token's checksum term for this cache.  Byte `off` of a row (head
-// h = off / hb, byte e = off mod hb) goes to, per layout:
+// token's checksum term for this cache.  When `first` is set, the batch at
+// base = lane was already loaded into v (its source does not depend on the
+// slot, so it was issued together with the slot's load).  Byte `off` of a
+// row (head h = off / hb, byte e = off mod hb) goes to, per layout:
 //   NHD, latent  o*row + off
 //   HND          ((o/kbs*heads + h)*kbs + o mod kbs)*hb + e
 // (x-split pages have their own kernel below.)
@@ -44,7 +70,7 @@ template <int kLayout>
 __device__ __forceinline__ u64 write_token_rows(const DevCache &C, const unsigned char *srck,
                                                 const unsigned char *srcv, long long bs,
                                                 long long b, long long o, u64 t, int ch,
-                                                int lane) {
+                                                int lane, uint4 (&v)[kWriteBatch], bool first) {
   const int row = C.heads * C.hb;
   const int nh = row / ch;          // chunks per half
   const int n = nh * C.halves;      // chunks of the token
@@ -61,21 +87,7 @@ __device__ __forceinline__ u64 write_token_rows(const DevCache &C, const unsigne
   const u64 tP = t * static_cast<u64>(C.P);
   u64 acc = 0;
   for (int base = lane; base < n; base += kWriteBatch * 32) {
-    uint4 v[kWriteBatch];
-#pragma unroll
-    for (int k = 0; k < kWriteBatch; ++k) {
-      const int idx = base + 32 * k;
-      if (idx < n) {
-        const bool hv = idx >= nh;
-        const unsigned char *src = (hv ? srcv : srck) + (idx - (hv ? nh : 0)) * ch;
-        if (ch == 16) {
-          v[k] = *reinterpret_cast<const uint4 *>(src);
-        } else {
-          const u64 x = *reinterpret_cast<const u64 *>(src);
-          v[k] = make_uint4(static_cast<u32>(x), static_cast<u32>(x >> 32), 0u, 0u);
-        }
-      }
-    }
+    if (!(first && base == lane)) load_row_batch(C, srck, srcv, base, ch, v);
 #pragma unroll
     for (int k = 0; k < kWriteBatch; ++k) {
       const int idx = base + 32 * k;
@@ -126,9 +138,16 @@ __global__ void __launch_bounds__(kWriteThreads, 2)
     const long long i = it - static_cast<long long>(chunk) * w.num_tokens;
     const int c_lo = chunk * cpi;
     const int c_hi = min(w.num_caches, c_lo + cpi);
-    // both table loads in flight together
+    // the table loads and the first cache's first batch of chunks in flight
+    // together
     const long long slot = w.slots[i];
     const long long t = w.positions[i];
+    uint4 v[kWriteBatch];
+    {
+      const DevCache &C0 = w.c[c_lo];
+      const long long row0 = static_cast<long long>(C0.heads) * C0.hb;
+      load_row_batch(C0, w.key[c_lo] + i * row0, w.value[c_lo] + i * row0, lane, ch, v);
+    }
     if (slot < 0) continue;  // padding token
     const long long b = slot / bs;
     const long long o = slot - b * bs;
@@ -142,7 +161,7 @@ __global__ void __launch_bounds__(kWriteThreads, 2)
       const DevCache &C = w.c[ci];
       const long long row = static_cast<long long>(C.heads) * C.hb;
       acc += write_token_rows<kLayout>(C, w.key[ci] + i * row, w.value[ci] + i * row, bs, b, o,
-                                       static_cast<u64>(t), ch, lane);
+                                       static_cast<u64>(t), ch, lane, v, ci == c_lo);
     }
     if (w.block_sums != nullptr && t >= 0) {
       acc = warp_sum(acc);
