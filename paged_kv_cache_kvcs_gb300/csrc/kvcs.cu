@@ -61,7 +61,8 @@ cudaError_t device_setup(int *sms) {
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamXSplit>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamState>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndSub>)})
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndSub>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRowsMis>)})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
@@ -84,11 +85,23 @@ long long page_bytes_of(const kvcs_cache &c, int block_size) {
   return static_cast<long long>(block_size) * c.num_heads * c.head_bytes;
 }
 
+// NHD or latent rows of pages that may start 8 bytes past a 16-byte boundary
+// (the base or a stride is 8 mod 16), rows whole 16-byte columns of one head:
+// the bulk kernel's misaligned-rows instance stages them.
+bool rows_misaligned(const kvcs_cache &c) {
+  if (c.layout != KVCS_LAYOUT_NHD && c.layout != KVCS_LAYOUT_LATENT) return false;
+  return reinterpret_cast<uintptr_t>(c.base) % 16 || c.half_stride % 16 || c.block_stride % 16;
+}
+
 // The bulk kernel stages whole rows (NHD, latent, state) or whole heads
-// (HND, x-split) with 16-byte-aligned bulk copies and reads 16-byte columns.
+// (HND, x-split) with 16-byte-aligned bulk copies and reads 16-byte columns;
+// NHD and latent pages 8 bytes off a 16-byte boundary too, their edge words
+// by 8-byte asynchronous copies.
 bool bulk_eligible(const kvcs_cache &c, int block_size) {
-  if (reinterpret_cast<uintptr_t>(c.base) % 16) return false;
-  if (c.head_bytes % 16 || c.half_stride % 16 || c.block_stride % 16) return false;
+  if (c.head_bytes % 16) return false;
+  if (!rows_misaligned(c) &&
+      (reinterpret_cast<uintptr_t>(c.base) % 16 || c.half_stride % 16 || c.block_stride % 16))
+    return false;
   const long long hb = c.head_bytes;
   switch (c.layout) {
     case KVCS_LAYOUT_NHD: return hb * c.num_heads <= kMaxUnitBytes;
@@ -221,11 +234,11 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
   return d;
 }
 
-// Largest unit of one cache, in bytes.
-long long unit_bytes(const DevCache &d, int block_size) {
+// Largest unit of one cache, in bytes of stage.
+long long unit_bytes(const kvcs_cache &c, const DevCache &d, int block_size) {
   if (d.layout == KVCS_LAYOUT_HND || d.layout == KVCS_LAYOUT_XSPLIT)
     return static_cast<long long>(d.rpu) * block_size * d.hb;
-  return static_cast<long long>(d.rpu) * d.rowb;
+  return static_cast<long long>(d.rpu) * d.rowb + (rows_misaligned(c) ? kMisPad : 0);
 }
 
 // Shape of one bulk launch over caches [lo, hi): units per position,
@@ -248,7 +261,7 @@ LaunchShape launch_shape(const kvcs_cache *caches, int lo, int hi, int block_siz
     const DevCache d = make_dev_cache(caches[i], block_size);
     ls.units_per_pos += static_cast<long long>(d.halves) * d.upp;
     ls.pages_per_pos += d.halves;
-    biggest = std::max(biggest, unit_bytes(d, block_size));
+    biggest = std::max(biggest, unit_bytes(caches[i], d, block_size));
     uniform = uniform && d.upp == 1 && caches[i].layout == caches[lo].layout &&
               caches[i].column == caches[lo].column && d.kbs == d0.kbs &&
               caches[i].num_heads == caches[lo].num_heads &&
@@ -260,12 +273,15 @@ LaunchShape launch_shape(const kvcs_cache *caches, int lo, int hi, int block_siz
     // and the producer packs consecutive pages of a position (e.g. a layer's
     // K and V) into one stage as far as their valid bytes fit.  The stage
     // holds as many whole pages as fit in the unit target.
+    // (pages are counted against the target without the misaligned-rows
+    // padding, so a stage packs as many pages as in an aligned pool)
     const long long page = static_cast<long long>(d0.page_bytes);
-    const long long ppu = std::max<long long>(
+    long long ppu = std::max<long long>(
         1, std::min<long long>(ls.pages_per_pos, kUnitTargetBytes / page));
+    if (rows_misaligned(caches[lo])) ppu = std::min<long long>(ppu, kMisMaxPages);
     ls.pack = 1;
     ls.full_pages = static_cast<int>(ppu);
-    biggest = std::max(biggest, ppu * page);
+    biggest = std::max(biggest, ppu * (page + (rows_misaligned(caches[lo]) ? kMisPad : 0)));
   }
   ls.stage_bytes = static_cast<int>((biggest + 127) / 128 * 128);
   ls.stages = std::min(kMaxStages, (kSmemLimit - kHeaderBytes) / ls.stage_bytes);
@@ -288,7 +304,7 @@ int family_of(const kvcs_cache &c, int block_size) {
                                                                           : kFamHnd;
     case KVCS_LAYOUT_XSPLIT: return kFamXSplit;
     case KVCS_LAYOUT_STATE: return kFamState;
-    default: return kFamRows;
+    default: return rows_misaligned(c) ? kFamRowsMis : kFamRows;
   }
 }
 
@@ -414,8 +430,7 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
 // its inputs.
 cudaError_t launch(void (*kernel)(Params), dim3 grid, int threads, size_t smem, cudaStream_t st,
                    bool after_zero, const Params &p) {
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = smem;
@@ -458,8 +473,7 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
     const long long words = total_positions * static_cast<long long>(ncols);
     const long long blocks = std::max<long long>(
         1, std::min<long long>((words + 1023) / 1024, static_cast<long long>(sms)));
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(256);
     cfg.stream = st;
@@ -532,6 +546,7 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
         case kFamXSplit: e = launch(kvcs_bulk_kernel<kFamXSplit>, gd, kBulkThreads, smem, st, after_zero, p); break;
         case kFamState: e = launch(kvcs_bulk_kernel<kFamState>, gd, kBulkThreads, smem, st, after_zero, p); break;
         case kFamHndSub: e = launch(kvcs_bulk_kernel<kFamHndSub>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamRowsMis: e = launch(kvcs_bulk_kernel<kFamRowsMis>, gd, kBulkThreads, smem, st, after_zero, p); break;
         default: e = launch(kvcs_bulk_kernel<kFamRows>, gd, kBulkThreads, smem, st, after_zero, p); break;
       }
       if (e != cudaSuccess) return KVCS_ECUDA;

@@ -175,6 +175,20 @@ __device__ __forceinline__ void accum_slots_sub(const unsigned char *p0, int hb,
   }
 }
 
+// One 16-byte column of a staged row: a 16-byte shared load, or, for
+// misaligned-rows pages (whose rows may start 8 bytes past a 16-byte
+// boundary in the stage), two 8-byte loads.
+template <int kFam>
+__device__ __forceinline__ uint4 stage_col(const unsigned char *p) {
+  if constexpr (kFam == kFamRowsMis) {
+    const uint2 a = *reinterpret_cast<const uint2 *>(p);
+    const uint2 b = *reinterpret_cast<const uint2 *>(p + 8);
+    return make_uint4(a.x, a.y, b.x, b.y);
+  } else {
+    return *reinterpret_cast<const uint4 *>(p);
+  }
+}
+
 // This thread's share of one staged unit's contribution to the block
 // checksum (see the reformulation at the top of this file).
 template <int kFam>
@@ -239,7 +253,7 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
       const u64 mrow = C.m0 + 2ull * static_cast<u64>(r0 + static_cast<u32>(r));
       acc += mrow * (SA + 2ull * per * SCA + 2ull * SB);
     }
-  } else if constexpr (kFam == kFamRows) {
+  } else if constexpr (kFam == kFamRows || kFam == kFamRowsMis) {
     const int nrows = m.count;
     const u32 r0 = static_cast<u32>(m.first);
     for (int col = t.col0; col < t.cols; col += t.cstep) {
@@ -260,7 +274,7 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
       for (; r + 7 * t.rstep < nrows; r += 8 * t.rstep, sp += 8 * step) {
         uint4 v[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const uint4 *>(sp + k * step);
+        for (int k = 0; k < 8; ++k) v[k] = stage_col<kFam>(sp + k * step);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
@@ -272,7 +286,7 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
         }
       }
       for (; r < nrows; r += t.rstep, sp += step) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(sp);
+        const uint4 v = stage_col<kFam>(sp);
         const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
         const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
         const u64 X = x0 + x1;
@@ -332,10 +346,12 @@ template <int kFam>
 __device__ __forceinline__ int stage_fit(const Params &p, const PosInfo &cur, int stage_bytes) {
   if (!p.pack) return 1;
   if (cur.skip) return 1 << 30;
-  if (cur.nv == p.block_size || (kFam != kFamRows && kFam != kFamHnd)) return p.full_pages;
+  if (cur.nv == p.block_size || (kFam != kFamRows && kFam != kFamHnd && kFam != kFamRowsMis))
+    return p.full_pages;
   const DevCache &C = p.caches[0];
-  const u32 bytes = kFam == kFamRows
-                        ? static_cast<u32>(cur.nv) * static_cast<u32>(C.rowb)
+  const u32 bytes = kFam == kFamRows ? static_cast<u32>(cur.nv) * static_cast<u32>(C.rowb)
+                    : kFam == kFamRowsMis
+                        ? static_cast<u32>(cur.nv) * static_cast<u32>(C.rowb) + kMisPad
                         : static_cast<u32>(C.heads) * static_cast<u32>(cur.nv) *
                               static_cast<u32>(C.hb);
   return max(1, static_cast<int>(static_cast<u32>(stage_bytes) / bytes));
@@ -485,7 +501,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         const DevCache &C = p.caches[ci];
         // One accumulator slot per (position, column); the caches arrive
         // sorted by column, so a column's units are consecutive.
-        const long long dst = pos * p.num_columns + col;
+        const long long dst_word = pos * p.num_columns + col;
         const int first = sub * C.rpu;
         int count = 0;
         u32 pbytes = 0;   // bytes copied per page of the unit
@@ -513,6 +529,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             count = max(0, min(C.rpu, C.heads - first));
             pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
             pstride = pbytes;
+          } else if constexpr (kFam == kFamRowsMis) {
+            // the rows, in a 16-byte-aligned region with room for the shift;
+            // pbytes counts the bytes the bulk copies bring (the two edge
+            // words of a misaligned page come by cp.async)
+            count = max(0, min(C.rpu, cur.nv - first));
+            pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
+            pstride = pbytes + kMisPad;
           } else {
             count = max(0, min(C.rpu, cur.nv - first));
             pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
@@ -531,6 +554,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           int left = p.pages_per_pos - (ci * C.halves + half);
           if (u_end - u < left) left = static_cast<int>(u_end - u);
           npg = max(1, min(left, fit));
+          if constexpr (kFam == kFamRowsMis) npg = min(npg, kMisMaxPages);
         }
         if (pbytes > 0) {
           if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
@@ -545,9 +569,44 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             hdr->ring_acc[slot] = 0ull;
             hdr->ring_cnt[slot] = 0u;
           }
-          store_meta(&hdr->meta[s], dst, cur.q, ci, half, first, count, cur.nv,
-                     mode, slot, npg);
           const u32 fb = ptx::smem_addr(&hdr->full[s]);
+          if constexpr (kFam == kFamRowsMis) {
+            // Per page: the 16-byte-aligned interior of its rows by bulk copy,
+            // and when the page starts 8 bytes past a boundary its first and
+            // last words by 8-byte cp.async, tracked on the same barrier.
+            u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
+            u32 tx = 0, dmask = 0;
+            int pci = ci, phalf = half;
+            for (int k2 = 0; k2 < npg; ++k2) {
+              const DevCache &D = p.caches[pci];
+              const unsigned char *src = D.base + static_cast<long long>(phalf) * D.half_stride +
+                                         cur.block * D.block_stride +
+                                         static_cast<u64>(first) * D.rowb;
+              if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+                ptx::bulk_g2s(dst, src, pbytes, fb, policy);
+                tx += pbytes;
+              } else {
+                dmask |= 1u << k2;
+                if (pbytes > 16) {
+                  ptx::bulk_g2s(dst + 16, src + 8, pbytes - 16, fb, policy);
+                  tx += pbytes - 16;
+                }
+                ptx::cp_async8(dst + 8, src);
+                ptx::cp_async8(dst + pbytes, src + pbytes - 8);
+              }
+              dst += pstride;
+              if (++phalf == D.halves) {
+                phalf = 0;
+                ++pci;
+              }
+            }
+            store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
+                       mode | static_cast<int>(dmask << 1), slot, npg);
+            if (dmask) ptx::cp_async_mbar_arrive(fb);
+            ptx::mbar_arrive_expect_tx(fb, tx);
+          } else {
+          store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
+                     mode, slot, npg);
           ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
           u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
           int pci = ci, phalf = half;
@@ -600,6 +659,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               ++pci;
             }
           }
+          }
           ++it;
           ++n_emit;
           if (++s == NS) {
@@ -636,10 +696,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           if (n_emit > 0) {
             const u32 delta = 0u - static_cast<u32>(p.group_warps) * n_emit;
             const u32 prev = atomicAdd(&hdr->ring_cnt[slot], delta);
-            if (prev + delta == 0u) finalize_slot(p, hdr, slot, dst, mode);
+            if (prev + delta == 0u) finalize_slot(p, hdr, slot, dst_word, mode);
           } else if (cur.whole && !p.all_atomic) {
             ptx::grid_dep_wait();
-            p.out[dst] = 0ull;
+            p.out[dst_word] = 0ull;
           }
           n_emit = 0;
         }
@@ -719,11 +779,18 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     for (int k = 0; k < m.npages; ++k) {
       const DevCache &C = p.caches[ci];
       if (C.rowb != map.rowb) make_map(map, C.rowb, gtid, gw * 32);
-      v += unit_sum<kFam>(C, m, half, sp, map, bsz);
-      sp += kFam == kFamHnd ? static_cast<size_t>(m.count) * static_cast<size_t>(m.nv) * C.hb
-            : head_family(kFam)
-                ? static_cast<size_t>(m.count) * static_cast<size_t>(bsz) * C.hb
-                : static_cast<size_t>(m.count) * C.rowb;
+      if constexpr (kFam == kFamRowsMis) {
+        // the page's first byte sits 8 bytes into its region when the page
+        // starts 8 bytes past a boundary
+        v += unit_sum<kFam>(C, m, half, sp + ((m.mode >> (1 + k)) & 1) * 8, map, bsz);
+        sp += static_cast<size_t>(m.count) * C.rowb + kMisPad;
+      } else {
+        v += unit_sum<kFam>(C, m, half, sp, map, bsz);
+        sp += kFam == kFamHnd ? static_cast<size_t>(m.count) * static_cast<size_t>(m.nv) * C.hb
+              : head_family(kFam)
+                  ? static_cast<size_t>(m.count) * static_cast<size_t>(bsz) * C.hb
+                  : static_cast<size_t>(m.count) * C.rowb;
+      }
       if (++half == C.halves) {
         half = 0;
         ++ci;
@@ -734,7 +801,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       atomicAdd(&hdr->ring_acc[m.slot], v);
       __threadfence_block();
       const u32 prev = atomicAdd(&hdr->ring_cnt[m.slot], 1u);
-      if (prev + 1u == 0u) finalize_slot(p, hdr, m.slot, m.dst, m.mode);
+      if (prev + 1u == 0u) finalize_slot(p, hdr, m.slot, m.dst, m.mode & 1);
       ptx::mbar_arrive(ptx::smem_addr(&hdr->empty[s]));
     }
     s += p.groups;

@@ -62,7 +62,16 @@ constexpr int kFamHnd = 1;     // HND: heads of a page
 constexpr int kFamXSplit = 2;  // x-split: heads of 16-byte chunks
 constexpr int kFamState = 3;   // Mamba states: rows of a state
 constexpr int kFamHndSub = 4;  // HND in kernel sub-blocks: heads of each sub-block
-constexpr int kNumFamilies = 5;
+constexpr int kFamRowsMis = 5; // NHD and latent rows of pages 8 bytes past a 16-byte
+                               // boundary (some or all)
+constexpr int kNumFamilies = 6;
+
+// Misaligned-rows units: at most this many pages (one flag bit each in the
+// unit's metadata).
+constexpr int kMisMaxPages = 30;
+// Bytes a misaligned-rows page takes in a stage beyond its rows: its region
+// starts 16-byte aligned and its first byte sits 8 bytes in when misaligned.
+constexpr int kMisPad = 16;
 
 // Families whose units are runs of whole heads, all block_size slots of them.
 __host__ __device__ constexpr bool head_family(int fam) {
@@ -140,7 +149,8 @@ struct __align__(16) UnitMeta {
   int first;       // NHD/latent: first slot of the unit; HND: first head
   int count;       // NHD/latent: slots in the unit; HND: heads in the unit
   int nv;          // valid slots of the block
-  int mode;        // kFlushStore or kFlushAtomic
+  int mode;        // bit 0: kFlushStore or kFlushAtomic; misaligned-rows units:
+                   // bit 1 + k set when page k starts 8 bytes past a boundary
   int slot;        // accumulator slot of the position
   int npages;      // consecutive pages in the unit (each packed after the
                    // previous one's valid bytes)

@@ -74,6 +74,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(u32 bar, u32 parity,
   return false;
 }
 
+// 8-byte asynchronous copy from global to shared memory (both addresses
+// 8-byte aligned); it completes in the background like a bulk copy.
+__device__ __forceinline__ void cp_async8(u32 dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued before has
+// completed (the barrier's pending count is raised first, so the current
+// phase waits for that arrival too).
+__device__ __forceinline__ void cp_async_mbar_arrive(u32 bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Programmatic dependent launch.  grid_dep_launch lets the next kernel of
 // the stream (launched with programmatic stream serialization) start before
 // this one ends; grid_dep_wait makes the calling thread wait until the grids

@@ -120,9 +120,14 @@ def test_validation_codes():
     assert code_of([FakeCache(layer=0, layout=4, head_bytes=8, piece_bytes=4),
                     FakeCache(layer=1)]) == K.KVCS_EINVAL
     assert code_of([FakeCache(piece_bytes=2)]) == K.KVCS_EINVAL
-    # strides that are 8- but not 16-byte multiples fall back to the generic kernel
-    assert plan([FakeCache(block_stride=page + 8)])["kernel"] == 1
+    # strides that are 8- but not 16-byte multiples: NHD rows stay on the bulk
+    # kernel (its misaligned-rows instance), HND heads go to the direct kernel
+    assert plan([FakeCache(block_stride=page + 8)])["kernel"] == 0
     assert plan([FakeCache(block_stride=page + 16)])["kernel"] == 0
+    assert plan([FakeCache(layout=1, block_stride=page + 8)])["kernel"] == 1
+    assert plan([FakeCache(layout=1, block_stride=page + 16)])["kernel"] == 0
+    # NHD heads of 8 mod 16 bytes (a 16-byte column would straddle two heads)
+    assert plan([FakeCache(head_bytes=24)])["kernel"] == 1
 
 
 def test_block_checksums_rejects_before_any_cuda_call():
@@ -149,9 +154,9 @@ def test_plan_shapes():
     assert p["units"] == 9220 * 32 * 2 and p["stage_bytes"] == 32768
     assert p["stages"] == 7 and p["smem_bytes"] <= 232448
     assert p["kv_bytes_max"] == 9220 * 32 * 2 * 32768
-    # 70B-shaped fp8: 16 KiB pages, three consecutive pages packed per unit
+    # 70B-shaped fp8: 16 KiB pages, a unit each, three packed per 48 KiB stage
     p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=16384)
-    assert p["units"] == 16384 * 54 and p["stage_bytes"] == 49152 and p["stages"] == 4
+    assert p["units"] == 16384 * 160 and p["stage_bytes"] == 49152 and p["stages"] == 4
     # one 70B-shaped request: too few positions for whole-position CTAs
     p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=128)
     assert p["split"] == 1 and p["memsets"] == 1 and p["grid"] == 152
@@ -163,11 +168,11 @@ def test_plan_shapes():
     # HND with 16 KiB per head (block_size 64): three heads per unit
     p = plan([FakeCache(layout=1, layer=i) for i in range(4)], bs=64, positions=500)
     assert p["units"] == 500 * 4 * 2 * 3 and p["stage_bytes"] == 49152
-    # tiny pages (4 KiB): all four pages of a position in one unit; few small
-    # positions are read one per CTA, with no memset
+    # tiny pages (4 KiB): all four pages of a position packed in one stage;
+    # few small positions are read one per CTA, with no zeroing
     p = plan([FakeCache(layer=i, num_heads=2, head_bytes=128) for i in range(2)],
              positions=7)
-    assert p["units"] == 7 and p["stage_bytes"] == 16384 and p["split"] == 0
+    assert p["units"] == 7 * 4 and p["stage_bytes"] == 16384 and p["split"] == 0
     assert p["grid"] == 7 and p["memsets"] == 0
     # ... but positions over 128 KiB, fewer than the SMs, are split at units
     p = plan([FakeCache(layer=i, num_heads=2, head_bytes=128) for i in range(20)],

@@ -1,9 +1,11 @@
-"""The direct-load kernel (KV pages the bulk-copy kernel cannot stage)
-against the oracle, through the C ABI: every layout, pools 0 or 8 bytes past
-a 16-byte boundary, rows that are 8 mod 16 bytes (chunks pair up over two
-rows), rows and head runs past a stage, pages whose alignment alternates
-with the block (strides 8 mod 16), ragged and empty positions, first
-positions past 2^57 (t P wraps 2^64).  Bit-exact uint64 equality."""
+"""Pages that are not all 16-byte aligned, against the oracle through the C
+ABI: the direct-load kernel (every layout, pools 0 or 8 bytes past a 16-byte
+boundary, rows that are 8 mod 16 bytes, where chunks pair up over two rows,
+rows and head runs past a stage, pages whose alignment alternates with the
+block) and the bulk kernel's misaligned-rows instance (NHD and latent rows
+of whole 16-byte columns: interiors by bulk copy, edge words by 8-byte
+asynchronous copies).  Ragged and empty positions, first positions past
+2^57 (t P wraps 2^64).  Bit-exact uint64 equality."""
 
 import dataclasses
 
@@ -38,10 +40,21 @@ def _shifted(wl, shift, block_pad=0):
                       wl.num_tokens, wl.block_ids, wl.info), keep
 
 
-def _check(wl):
+def _rows_bulk(c):
+    """NHD or latent rows of whole 16-byte columns of one head: the bulk
+    kernel stages them even 8 bytes off a boundary."""
+    if c.layout not in (W.LAYOUT_NHD, W.LAYOUT_LATENT) or c.head_bytes % 16:
+        return False
+    row = c.num_heads * c.head_bytes if c.layout == W.LAYOUT_NHD else c.head_bytes
+    return row <= 65536
+
+
+def _check(wl, kernel=None):
     from gpu_helpers import full_oracle, gpu_checksums
     plan = K.plan_for(wl.caches, wl.block_size, wl.num_positions)
-    assert plan["kernel"] == 1, plan
+    if kernel is None:
+        kernel = 0 if all(_rows_bulk(c) for c in wl.caches) else 1
+    assert plan["kernel"] == kernel, plan
     got, st = gpu_checksums(wl)
     exp, est = full_oracle(wl)
     assert st == est == 0
@@ -106,10 +119,10 @@ def test_many_positions_and_caches_misaligned():
     ranges start and end inside positions and inside a position's caches."""
     g = torch.Generator().manual_seed(5)
     lengths = torch.randint(1, 400, (96,), generator=g).tolist()
-    wl = W.random_case(23, DEV, layout=W.LAYOUT_NHD, layers=16, heads=2, head_bytes=64,
+    wl = W.random_case(23, DEV, layout=W.LAYOUT_NHD, layers=16, heads=2, head_bytes=24,
                        block_size=16, lengths=lengths)
     wl, keep = _shifted(wl, 8)
-    _check(wl)
+    _check(wl, kernel=1)
 
 
 def test_position_past_2_pow_57_misaligned():
@@ -152,3 +165,70 @@ def test_bad_block_id_and_columns_misaligned():
                       wl.num_tokens, wl.block_ids, 2, values=vals, accumulate=True)
     torch.cuda.synchronize()
     assert np.array_equal(vals.cpu().numpy().view(np.uint64), v * np.uint64(2))
+
+
+MIS_ROWS = [
+    # (layout, heads, head_bytes, block_size, lengths, first_positions)
+    (W.LAYOUT_NHD, 8, 256, 16, (70, 33, 5, 16), (1, 0, 0, 0)),     # 2 KiB rows
+    (W.LAYOUT_NHD, 2, 32, 16, (100, 1, 17), (0, 0, 1)),            # 64-byte rows
+    (W.LAYOUT_NHD, 8, 128, 16, (60, 37), (0, 0)),                  # fp8-shaped 16 KiB pages, packed
+    (W.LAYOUT_LATENT, 1, 1152, 64, (200, 64, 1), (0, 0, 0)),       # the MLA row
+    (W.LAYOUT_LATENT, 1, 16, 4, (9, 1, 5), (0, 0, 1)),             # 16-byte rows: edges only at nv 1
+    (W.LAYOUT_NHD, 64, 1024, 1, (7, 3), (0, 0)),                   # 64 KiB rows, a unit each
+    (W.LAYOUT_NHD, 2, 64, 16, [16 * k + 1 for k in range(40)], list(range(40))),  # one-token blocks
+]
+
+
+@pytest.mark.parametrize("place", ["base8", "stride8", "v_only"])
+@pytest.mark.parametrize("case", MIS_ROWS, ids=lambda c: f"l{c[0]}h{c[1]}b{c[2]}bs{c[3]}")
+def test_misaligned_rows_bulk_instance(case, place):
+    """NHD and latent rows 8 bytes off a 16-byte boundary: every page
+    (base8), every other block (stride8), or only the V pages (v_only: the
+    half stride is 8 mod 16) go to the bulk kernel's misaligned-rows
+    instance and give the oracle's checksums."""
+    layout, heads, hb, bs, lengths, fps = case
+    if layout == W.LAYOUT_LATENT and place == "v_only":
+        pytest.skip("a latent cache has no V pages")
+    wl = W.random_case(31, DEV, layout=layout, layers=3, heads=heads, head_bytes=hb,
+                       block_size=bs, lengths=lengths, first_positions=fps)
+    if place == "base8":
+        wl, keep = _shifted(wl, 8)
+    elif place == "stride8":
+        wl, keep = _shifted(wl, 0, block_pad=8)
+    else:
+        caches, keep = [], []
+        for c in wl.caches:
+            page = bs * c.num_heads * c.head_bytes
+            raw = torch.zeros(2 * c.num_blocks * page + 8, dtype=torch.uint8, device=DEV)
+            v = c.pool.view(2, c.num_blocks * page)
+            raw[:c.num_blocks * page] = v[0]
+            raw[c.num_blocks * page + 8:] = v[1]
+            keep.append(raw)
+            caches.append(dataclasses.replace(c, pool=raw, half_stride=c.num_blocks * page + 8))
+        wl = W.Workload(wl.name, bs, caches, wl.pos_offsets, wl.first_position,
+                        wl.num_tokens, wl.block_ids, wl.info)
+    _check(wl, kernel=0)
+
+
+def test_misaligned_rows_whole_positions_and_bad_ids():
+    """304 positions (whole-position mode, plain stores) of 8-byte-shifted
+    NHD pools, with a bad block id: 0 there and the status bit."""
+    from gpu_helpers import full_oracle
+    wl = W.random_case(32, DEV, layout=W.LAYOUT_NHD, layers=4, heads=4, head_bytes=64,
+                       block_size=16, lengths=[64] * 76)
+    wl, keep = _shifted(wl, 8)
+    assert wl.num_positions == 304
+    plan = K.plan_for(wl.caches, wl.block_size, wl.num_positions)
+    assert plan["kernel"] == 0
+    exp, _ = full_oracle(wl)
+    ids = wl.block_ids.clone()
+    ids[100] = -3
+    bad = W.Workload(wl.name, wl.block_size, wl.caches, wl.pos_offsets, wl.first_position,
+                     wl.num_tokens, ids, wl.info)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = K.workload_checksums(bad, status=status)
+    torch.cuda.synchronize()
+    want = exp.copy()
+    want[100] = 0
+    assert int(status.item()) & K.KVCS_STATUS_BAD_BLOCK_ID
+    assert np.array_equal(out.cpu().numpy().view(np.uint64), want)

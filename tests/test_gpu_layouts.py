@@ -42,7 +42,7 @@ def page_bytes(wl, c):
 
 
 @pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND])
-@pytest.mark.parametrize("hb", [64, 24])      # bulk kernel, generic kernel
+@pytest.mark.parametrize("hb", [64, 24])      # bulk kernel, direct kernel
 def test_kv_interleaved_per_block(layout, hb):
     """[num_blocks, 2, page]: half_stride = page, block_stride = 2 page."""
     wl, exp = canonical(1, layout, hb=hb)
@@ -76,7 +76,7 @@ def test_separate_k_and_v_tensors(v_first):
 
 
 @pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND, W.LAYOUT_LATENT])
-@pytest.mark.parametrize("pad", [256, 8])     # bulk kernel, generic kernel
+@pytest.mark.parametrize("pad", [256, 8])     # 16-byte and 8-byte block strides
 def test_padded_blocks(layout, pad):
     hb = 1152 if layout == W.LAYOUT_LATENT else 64
     heads = 1 if layout == W.LAYOUT_LATENT else 4
@@ -91,7 +91,9 @@ def test_padded_blocks(layout, pad):
         caches.append(dataclasses.replace(c, pool=buf, block_stride=stride,
                                           half_stride=c.num_blocks * stride))
     plan = K.plan_for(caches, wl.block_size, wl.num_positions)
-    assert plan["kernel"] == (0 if pad % 16 == 0 else 1)
+    # blocks 8 mod 16 apart: NHD and latent rows stay on the bulk kernel (its
+    # misaligned-rows instance), HND heads go to the direct kernel
+    assert plan["kernel"] == (0 if pad % 16 == 0 or layout != W.LAYOUT_HND else 1)
     got, st = run(with_caches(wl, caches))
     assert st == 0 and np.array_equal(got, exp)
 
@@ -122,7 +124,7 @@ def test_nhd_kernel_block_size_is_the_same_memory():
 
 
 @pytest.mark.parametrize("hb,bs", [(64, 16), (256, 16), (32, 5), (16, 1)])
-@pytest.mark.parametrize("pad", [0, 8])       # bulk kernel, generic kernel
+@pytest.mark.parametrize("pad", [0, 8])       # bulk kernel, direct kernel
 def test_xsplit_layout(hb, bs, pad):
     """[2, num_blocks, heads, head_bytes / 16, block_size, 16]: the x-split
     layout (16-byte x chunks) for K and V pages."""
@@ -169,8 +171,8 @@ def _relaid(c, bs, kind):
 @pytest.mark.parametrize("kind", ["nhd", "hnd", "hnd_sub4", "xsplit", "latent"])
 @pytest.mark.parametrize("heads,hb", [(8, 256), (2, 32)])   # >= and < 256 word columns
 def test_misaligned_pools_every_layout(kind, heads, hb):
-    """Pools starting 8 bytes past a 16-byte boundary go to the generic
-    kernel in every layout and give the canonical checksums."""
+    """Pools starting 8 bytes past a 16-byte boundary give the canonical
+    checksums in every layout."""
     bs = 16
     if kind == "latent":
         heads, hb = 1, hb * 4 + 8
@@ -184,7 +186,10 @@ def test_misaligned_pools_every_layout(kind, heads, hb):
         keep.append(raw)
         caches.append(dataclasses.replace(c, pool=raw[8:], **extra))
     wl2 = with_caches(wl, caches)
-    assert K.plan_for(wl2.caches, bs, wl2.num_positions)["kernel"] == 1
+    # NHD rows of whole 16-byte columns go to the bulk kernel's misaligned-rows
+    # instance; the other layouts (and 8-mod-16 latent rows) to the direct kernel
+    expect = 0 if kind == "nhd" else 1
+    assert K.plan_for(wl2.caches, bs, wl2.num_positions)["kernel"] == expect
     got, st = run(wl2)
     assert st == 0 and np.array_equal(got, exp)
 

@@ -142,14 +142,17 @@ def test_generic_kernel_matches_oracle(case):
     assert_equal(got, exp)
 
 
-def test_misaligned_base_uses_generic_kernel():
-    wl = W.random_case(4, DEV, layers=2, heads=2, head_bytes=32, block_size=4,
+@pytest.mark.parametrize("layout,kernel", [(W.LAYOUT_NHD, 0), (W.LAYOUT_HND, 1)])
+def test_misaligned_base(layout, kernel):
+    """Pools 8 bytes past a 16-byte boundary: NHD rows go to the bulk
+    kernel's misaligned-rows instance, HND heads to the direct kernel."""
+    wl = W.random_case(4, DEV, layout=layout, layers=2, heads=2, head_bytes=32, block_size=4,
                        lengths=(13,))
     for c in wl.caches:
         raw = torch.zeros(c.pool.numel() + 8, dtype=torch.uint8, device=DEV)
         raw[8:] = c.pool
         c.pool = raw[8:]
-    assert K.plan_for(wl.caches, wl.block_size, wl.num_positions)["kernel"] == 1
+    assert K.plan_for(wl.caches, wl.block_size, wl.num_positions)["kernel"] == kernel
     got, st = gpu(wl)
     exp, _ = oracle(wl)
     assert st == 0
