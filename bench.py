@@ -168,7 +168,22 @@ def arm_config(wl, args, ws) -> dict:
     same keys in both arms)."""
     return {**describe(wl, args.config), "parallelism": f"replicas{ws}",
             "memory_layout": args.layout, "columns": max(1, args.columns),
-            "verify": bool(args.verify)}
+            "verify": bool(args.verify),
+            "work_share": work_share(wl, args)}
+
+
+def work_share(wl, args) -> str:
+    """How the bulk kernel's units are shared out among its CTAs (planned
+    for this GPU, or for a GB300's 152 SMs where no GPU is visible: the
+    reference arm describes the same run on the host)."""
+    if args.static:
+        return "fixed"
+    import paged_kv_cache_kvcs_gb300 as kvcs
+    sms = (torch.cuda.get_device_properties(0).multi_processor_count
+           if torch.cuda.is_available() else 152)
+    plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions, num_sms=sms)
+    return ("dynamic (workspace)" if plan["dynamic"]
+            else "fixed (workspace given; call below the dynamic threshold)")
 
 
 # ---------------------------------------------------------------------------
@@ -651,6 +666,10 @@ def time_checksums(wl, args, dev, stream, ws, rank, steps, warmup, clocks=True) 
     raw_stream = stream.cuda_stream
     ncols = max(1, args.columns)
     values = None
+    # a workspace lets the bulk kernel balance its work dynamically (the
+    # default); --static keeps every CTA's share fixed
+    wspace = None if args.static else torch.zeros(kvcs.KVCS_WORKSPACE_WORDS,
+                                                   dtype=torch.int64, device=dev)
     if args.columns > 1 or args.verify:
         # the replica-key path: one column per key, plus (--verify) the
         # tagged row sums compared with stored values in the same call
@@ -674,10 +693,10 @@ def time_checksums(wl, args, dev, stream, ws, rank, steps, warmup, clocks=True) 
             kvcs.group_checksums(wl.caches, wl.block_size, wl.pos_offsets,
                                  wl.first_position, wl.num_tokens, wl.block_ids, ncols,
                                  values=values, status=status, stream=raw_stream,
-                                 total_positions=n_pos, **extras)
+                                 total_positions=n_pos, workspace=wspace, **extras)
         ck = None
     else:
-        ck = kvcs.workload_checksummer(wl)
+        ck = kvcs.workload_checksummer(wl, workspace=wspace)
 
         def step():
             ck(out, status, raw_stream)
@@ -716,13 +735,13 @@ def time_checksums(wl, args, dev, stream, ws, rank, steps, warmup, clocks=True) 
         result = values.cpu().numpy().view(np.uint64).sum(axis=1, dtype=np.uint64)
     else:
         result = out.cpu().numpy()
-    return {"state": bool(wl.caches) and wl.caches[0].layout == 4,
+    return {"state": bool(wl.caches) and wl.caches[0].layout == 4, "ws": wspace,
             "total_s": total_s, "launch_s": statistics.mean(per), "launches": int(launches),
             "clocks": clk, "plan": plan, "nbytes": kv_bytes(wl), "ck": ck, "out": out,
             "status": status, "result": result}
 
 
-def request_sweep(wl, stream, out, status) -> list:
+def request_sweep(wl, stream, out, status, ws=None) -> list:
     """The first 1, 2, 4, ... requests of the workload alone: GB/s per call
     timed back to back, and the same call replayed from a CUDA graph."""
     import paged_kv_cache_kvcs_gb300 as kvcs
@@ -733,7 +752,7 @@ def request_sweep(wl, stream, out, status) -> list:
         sub = type(wl)(wl.name, wl.block_size, wl.caches, wl.pos_offsets[:n + 1],
                        wl.first_position[:n], wl.num_tokens[:n],
                        wl.block_ids[:int(wl.pos_offsets[n])], wl.info)
-        sck = kvcs.workload_checksummer(sub)
+        sck = kvcs.workload_checksummer(sub, workspace=ws)
         sb = kv_bytes(sub)
         k = max(10, min(500, int(2e10 / max(sb, 1))))
         with torch.cuda.stream(stream):
@@ -827,7 +846,7 @@ def other_configs(args, dev, stream) -> dict:
                                                     "grid", "stage_bytes", "units")},
                  "roofline": roofline_of(r, name), "clocks": r["clocks"]}
         if name == "llama3_70b":
-            entry["sweep"] = request_sweep(wl, stream, r["out"], r["status"])
+            entry["sweep"] = request_sweep(wl, stream, r["out"], r["status"], r["ws"])
         if not args.no_cpu_baseline:
             entry["cpu_baseline"], entry["parity"] = cpu_leg(wl, r, args.other_cpu_seconds,
                                                              args.seed)
@@ -856,12 +875,12 @@ def run_ours(args, ws, rank, local):
     job_blocks = all_sum(wl.num_positions * args.steps, ws)
     value = job_bytes / total_s / 1e9
 
-    sweep = request_sweep(wl, stream, r["out"], r["status"]) if args.sweep else None
+    sweep = request_sweep(wl, stream, r["out"], r["status"], r["ws"]) if args.sweep else None
 
     # ---- end to end: host buffers through the public API ----
     e2e = None
     if not args.no_e2e and r["ck"] is not None:
-        e2e = run_e2e(args, wl, dev, stream, ws, r["ck"])
+        e2e = run_e2e(args, wl, dev, stream, ws, r["ck"], r["ws"])
 
     if rank != 0:
         return
@@ -903,7 +922,7 @@ def run_ours(args, ws, rank, local):
         raise SystemExit(f"GPU output differs from the oracle on: {', '.join(bad)}")
 
 
-def run_e2e(args, wl, dev, stream, ws, ck):
+def run_e2e(args, wl, dev, stream, ws, ck, workspace=None):
     """Each step: pinned host -> device copies of every KV pool and of the
     request tables, the checksum, and a device -> host read of the checksums
     and the status word.  The layers arrive in ``--e2e-groups`` groups, as a
@@ -929,7 +948,7 @@ def run_e2e(args, wl, dev, stream, ws, ck):
     groups = [list(range(bounds[g], bounds[g + 1])) for g in range(ngroups)]
     group_ck = [kvcs.Checksummer([wl.caches[i] for i in grp], wl.block_size, wl.pos_offsets,
                                  wl.first_position, wl.num_tokens, wl.block_ids,
-                                 wl.num_positions) for grp in groups]
+                                 wl.num_positions, workspace=workspace) for grp in groups]
     copy_stream = torch.cuda.Stream(dev)
     raw = stream.cuda_stream
 
@@ -1000,6 +1019,8 @@ def main():
                     help="replica-key columns (caches assigned round-robin)")
     ap.add_argument("--verify", action="store_true",
                     help="time the tagged row sums and their comparison too")
+    ap.add_argument("--static", action="store_true",
+                    help="no workspace: every CTA's share of the work is fixed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--other-cpu-seconds", type=float, default=4.0,

@@ -231,9 +231,28 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
  */
 #define KVCS_OUT_ACCUMULATE 1
 
+/*
+ * KVCS_OUT_WORKSPACE in flags: `workspace` (below) points to at least
+ * KVCS_WORKSPACE_WORDS uint64 words of DEVICE memory the call may use as
+ * scratch while it runs.  With it the bulk-copy kernel balances its work
+ * dynamically: each CTA reads a fixed share of the positions and then takes
+ * the rest in small chunks from a counter in the workspace, so CTAs on
+ * slower or busier SMs take less (without it every CTA's share is fixed and
+ * the call ends with its slowest SM).  Only calls of at least 1024 work
+ * units (KV pages, kvcs_plan's `units`) per SM use it; smaller calls keep
+ * the fixed shares, which suit them better, and leave the workspace alone.
+ * One counter is used per bulk-copy launch, for the first
+ * KVCS_WORKSPACE_WORDS launches.  The call zeroes the words it uses itself;
+ * their contents afterwards are unspecified.  Calls that may run at the
+ * same time on the GPU (other streams) must use different workspaces.
+ */
+#define KVCS_OUT_WORKSPACE 2
+#define KVCS_WORKSPACE_WORDS 16
+
 typedef struct kvcs_outputs {
   int32_t num_columns;       /* >= 1 and <= 64 */
-  int32_t flags;             /* 0 or KVCS_OUT_ACCUMULATE; other bits invalid */
+  int32_t flags;             /* KVCS_OUT_ACCUMULATE and/or KVCS_OUT_WORKSPACE;
+                                other bits invalid */
   uint64_t *values;          /* required: [total_positions][num_columns] */
   uint64_t *row_sums;        /* or NULL: [total_positions], sum of the row's
                                 values XOR tags[i] (when tags is given) */
@@ -244,6 +263,9 @@ typedef struct kvcs_outputs {
                                 1 where the tagged row sum != expected, else 0 */
   uint32_t *mismatch_count;  /* or NULL (needs expected): mismatching
                                 positions are added to this word */
+  uint64_t *workspace;       /* read only with KVCS_OUT_WORKSPACE in flags:
+                                DEVICE, KVCS_WORKSPACE_WORDS words, 8-byte
+                                aligned, used by this call alone */
 } kvcs_outputs;
 
 /*
@@ -343,7 +365,10 @@ typedef struct kvcs_plan_info {
   int32_t smem_bytes;    /* dynamic shared memory per CTA */
   int32_t stage_bytes;   /* bytes per pipeline stage (bulk kernel) */
   int32_t stages;        /* pipeline stages per CTA (bulk kernel) */
-  int32_t reserved;
+  int32_t dynamic;       /* 1 if the same call given a workspace
+                            (KVCS_OUT_WORKSPACE) would share the bulk
+                            kernel's last units out dynamically (one more
+                            small zeroing launch per call); 0 otherwise */
   int64_t units;         /* work units (page pieces) per launch */
   int64_t kv_bytes_max;  /* KV bytes if every position held block_size tokens */
 } kvcs_plan_info;
@@ -378,7 +403,9 @@ const char *kvcs_strerror(int code);
 uint64_t kvcs_launch_count(void);
 
 /* ABI version: (major << 16) | minor.  Minor 2 added kvcs_write_kv and
- * kvcs_outputs.flags (KVCS_OUT_ACCUMULATE; the field was reserved, 0). */
+ * kvcs_outputs.flags (KVCS_OUT_ACCUMULATE; the field was reserved, 0).
+ * Minor 3 added kvcs_outputs.workspace, read only when flags has
+ * KVCS_OUT_WORKSPACE (callers built against minor 2 never set it). */
 int32_t kvcs_version(void);
 
 #ifdef __cplusplus

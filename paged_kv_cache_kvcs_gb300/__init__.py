@@ -11,7 +11,7 @@ synthetic workloads (``workloads``).
 from ._binding import (  # noqa: F401
     KVCS_BLOCK_CHECKSUM_BYTES, KVCS_ECUDA, KVCS_EINVAL, KVCS_EUNSUPPORTED,
     KVCS_LAYOUT_HND, KVCS_LAYOUT_LATENT, KVCS_LAYOUT_NHD, KVCS_LAYOUT_XSPLIT,
-    KVCS_LAYOUT_STATE, KVCS_OUT_ACCUMULATE,
+    KVCS_LAYOUT_STATE, KVCS_OUT_ACCUMULATE, KVCS_OUT_WORKSPACE, KVCS_WORKSPACE_WORDS,
     KVCS_MAX_KV_HEADS_PER_LAYER, KVCS_OK, KVCS_STATUS_BAD_BLOCK_ID,
     KVCS_STATUS_BAD_REQUESTS, KVCS_STATUS_TIMEOUT, KvcsError, block_checksums,
     cache_array, kvcs_block_checksums, kvcs_cache, kvcs_plan, kvcs_plan_info,

@@ -30,6 +30,8 @@ KVCS_STATUS_BAD_REQUESTS = 2
 KVCS_STATUS_TIMEOUT = 4
 
 KVCS_OUT_ACCUMULATE = 1
+KVCS_OUT_WORKSPACE = 2
+KVCS_WORKSPACE_WORDS = 16
 
 
 class kvcs_cache(ctypes.Structure):
@@ -45,7 +47,8 @@ class kvcs_outputs(ctypes.Structure):
     _fields_ = [("num_columns", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("values", ctypes.c_void_p), ("row_sums", ctypes.c_void_p),
                 ("tags", ctypes.c_void_p), ("expected", ctypes.c_void_p),
-                ("mismatch", ctypes.c_void_p), ("mismatch_count", ctypes.c_void_p)]
+                ("mismatch", ctypes.c_void_p), ("mismatch_count", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p)]
 
 
 class kvcs_requests(ctypes.Structure):
@@ -61,7 +64,7 @@ class kvcs_plan_info(ctypes.Structure):
                 ("launches", ctypes.c_int32), ("memsets", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
-                ("stages", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("dynamic", ctypes.c_int32),
                 ("units", ctypes.c_int64), ("kv_bytes_max", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
@@ -317,19 +320,26 @@ def block_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
 class Checksummer:
     """A checksum call prepared once for a fixed set of caches and request
     arrays: the descriptors are checked and marshalled here, so each call
-    is a single ctypes call into ``kvcs_block_checksums``.
+    is a single ctypes call into ``kvcs_block_checksums`` (or, with a
+    ``workspace`` of ``KVCS_WORKSPACE_WORDS`` 64-bit CUDA words, into
+    ``kvcs_group_checksums``, which then balances its work dynamically).
 
     The request tensors may be refilled in place between calls (for
     example by host-to-device copies); their addresses must not change.
     """
 
     def __init__(self, caches: Sequence, block_size: int, pos_offsets,
-                 first_position, num_tokens, block_ids, total_positions: int):
+                 first_position, num_tokens, block_ids, total_positions: int,
+                 workspace=None):
         for c in caches:
             _check_pool(c, block_size)
         self.device = _check_requests(pos_offsets, first_position, num_tokens, block_ids,
                                       total_positions)
-        self._keep = (list(caches), pos_offsets, first_position, num_tokens, block_ids)
+        if workspace is not None:
+            _check_tensor("workspace", workspace, _words(), KVCS_WORKSPACE_WORDS, self.device)
+        self.workspace = workspace
+        self._keep = (list(caches), pos_offsets, first_position, num_tokens, block_ids,
+                      workspace)
         self.num_caches = len(caches)
         self.block_size = block_size
         self.total_positions = total_positions
@@ -353,9 +363,12 @@ class Checksummer:
         import torch
         if torch.cuda.current_device() != self.device.index:
             raise ValueError(f"the call was prepared on {self.device}; make it current")
-        if accumulate:
-            outs = kvcs_outputs(1, KVCS_OUT_ACCUMULATE,
-                                out.data_ptr() if self.total_positions > 0 else None)
+        if accumulate or self.workspace is not None:
+            flags = (KVCS_OUT_ACCUMULATE if accumulate else 0) | \
+                (KVCS_OUT_WORKSPACE if self.workspace is not None else 0)
+            outs = kvcs_outputs(1, flags, out.data_ptr() if self.total_positions > 0 else None,
+                                None, None, None, None, None,
+                                _ptr(self.workspace))
             rc = self._group_fn(self.caches, self.num_caches, self.block_size, self._reqs_ref,
                                 self.total_positions, ctypes.byref(outs),
                                 status.data_ptr() if status is not None else None,
@@ -381,10 +394,11 @@ def workload_checksums(wl, out=None, status=None, stream=None):
                            total_positions=wl.num_positions)
 
 
-def workload_checksummer(wl) -> Checksummer:
-    """A prepared call over a ``workloads.Workload``."""
+def workload_checksummer(wl, workspace=None) -> Checksummer:
+    """A prepared call over a ``workloads.Workload`` (with a workspace: the
+    dynamically balanced form)."""
     return Checksummer(wl.caches, wl.block_size, wl.pos_offsets, wl.first_position,
-                       wl.num_tokens, wl.block_ids, wl.num_positions)
+                       wl.num_tokens, wl.block_ids, wl.num_positions, workspace=workspace)
 
 
 def plan_for(caches: Sequence, block_size: int, total_positions: int,
@@ -411,13 +425,16 @@ def group_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
                     num_tokens, block_ids, num_columns: int, values=None,
                     row_sums=None, tags=None, expected=None, mismatch=None,
                     mismatch_count=None, status=None, stream=None,
-                    total_positions: int | None = None, accumulate: bool = False):
+                    total_positions: int | None = None, accumulate: bool = False,
+                    workspace=None):
     """Torch front end of ``kvcs_group_checksums``.  Each cache names its
     replica-key ``column``; returns ``values`` (int64 CUDA tensor
     ``[total_positions, num_columns]`` holding uint64 bits).  ``row_sums``,
     ``tags``, ``expected`` are int64 CUDA tensors of ``total_positions``;
     ``mismatch`` a uint8 one; ``mismatch_count`` an int32 one-element one.
-    ``accumulate`` adds the partials into the given ``values``."""
+    ``accumulate`` adds the partials into the given ``values``.  ``workspace``
+    (``KVCS_WORKSPACE_WORDS`` 64-bit CUDA words, used by this call alone)
+    lets the bulk kernel balance its work dynamically."""
     import torch
     for c in caches:
         _check_pool(c, block_size)
@@ -443,10 +460,14 @@ def group_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
     if mismatch_count is not None:
         _check_tensor("mismatch_count", mismatch_count, (torch.int32, torch.uint32), 1, dev)
     _check_status(status, dev)
-    outs = kvcs_outputs(num_columns, KVCS_OUT_ACCUMULATE if accumulate else 0,
+    if workspace is not None:
+        _check_tensor("workspace", workspace, _words(), KVCS_WORKSPACE_WORDS, dev)
+    flags = (KVCS_OUT_ACCUMULATE if accumulate else 0) | \
+        (KVCS_OUT_WORKSPACE if workspace is not None else 0)
+    outs = kvcs_outputs(num_columns, flags,
                         values.data_ptr() if total_positions > 0 else None,
                         _ptr(row_sums), _ptr(tags), _ptr(expected), _ptr(mismatch),
-                        _ptr(mismatch_count))
+                        _ptr(mismatch_count), _ptr(workspace))
     reqs = kvcs_requests(pos_offsets.numel() - 1, pos_offsets.data_ptr(),
                          first_position.data_ptr(), num_tokens.data_ptr(),
                          block_ids.data_ptr())

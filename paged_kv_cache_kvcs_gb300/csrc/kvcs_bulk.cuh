@@ -433,10 +433,15 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
   }
   __syncthreads();
 
-  // This CTA's unit range.
+  // This CTA's unit range: its fixed share.  With a work counter the units
+  // past pool_start are not shared out here: CTAs take them in chunks from
+  // the counter once their share is done.
   long long u_begin, u_end;
   const long long G = gridDim.x, g = blockIdx.x;
-  if (p.split) {
+  if (p.work) {
+    u_begin = p.pool_start * g / G;
+    u_end = p.pool_start * (g + 1) / G;
+  } else if (p.split) {
     u_begin = p.total_units * g / G;
     u_end = p.total_units * (g + 1) / G;
   } else {
@@ -473,126 +478,201 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     u32 it = 0;         // units emitted
     u32 seq = 0;        // positions that got an accumulator slot
     bool aborted = false;
-    if (u_begin < u_end) {
-      long long pos = u_begin / U;
-      int ci = 0, half = 0, sub = 0;
-      {
-        int kk = static_cast<int>(u_begin - pos * U);
-        if (p.pack) {
-          // every cache has the same halves, one unit per page
-          ci = kk / p.caches[0].halves;
-          half = kk - ci * p.caches[0].halves;
-        } else {
-          while (kk >= p.caches[ci].halves * p.caches[ci].upp) {
-            kk -= p.caches[ci].halves * p.caches[ci].upp;
-            ++ci;
-          }
-          half = kk / p.caches[ci].upp;
-          sub = kk - half * p.caches[ci].upp;
+    // Ranges of units: this CTA's fixed share, then, with a work counter,
+    // chunks taken from it until the pool is used up.  After the first
+    // chunk the next one is claimed a range ahead, so the atomic's latency
+    // overlaps the work.
+    long long ra = u_begin, rb = u_end;
+    unsigned long long next_chunk = 0ull;
+    bool first_range = true, claimed = false;
+    while (true) {
+      if (ra < rb) {
+        if (!first_range) {
+          // a chunk starts anywhere in the pool: find its request and
+          // block ids afresh (positions still only grow)
+          const long long pos0 = ra / p.units_per_pos;
+          req_seek(p, rc, pos0);
+          b_cur = p.block_ids[pos0];
+          b_next = pos0 + 1 < p.total_positions ? p.block_ids[pos0 + 1] : 0;
         }
-      }
-      PosInfo cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
-      int mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
-      int fit = stage_fit<kFam>(p, cur, SB);
-      int slot = 0;
-      u32 n_emit = 0;
-      int col = p.caches[ci].column;
-      for (long long u = u_begin; u < u_end;) {
-        const DevCache &C = p.caches[ci];
-        // One accumulator slot per (position, column); the caches arrive
-        // sorted by column, so a column's units are consecutive.
-        const long long dst_word = pos * p.num_columns + col;
-        const int first = sub * C.rpu;
-        int count = 0;
-        u32 pbytes = 0;   // bytes copied per page of the unit
-        u32 pstride = 0;  // bytes a page of the unit occupies in the stage
-        if (!cur.skip) {
-          if constexpr (head_family(kFam)) {
-            count = max(0, min(C.rpu, C.heads - first));
-            if constexpr (kFam == kFamHnd) {
-              // each head's first nv slots (its valid ones), heads packed
-              // one after another in the stage
-              pstride = static_cast<u32>(count) * static_cast<u32>(cur.nv) *
-                        static_cast<u32>(C.hb);
-              pbytes = pstride;
-            } else {
-              // the unit's heads with all their slots, staged as in memory
-              pstride = static_cast<u32>(count) * static_cast<u32>(bs) * static_cast<u32>(C.hb);
-              pbytes = pstride;
-              if constexpr (kFam == kFamHndSub) {
-                const int nsb = (cur.nv + C.kbs - 1) / C.kbs;  // sub-blocks with valid slots
-                pbytes = static_cast<u32>(count) * static_cast<u32>(nsb * C.kbs) *
-                         static_cast<u32>(C.hb);
-              }
-            }
-          } else if constexpr (kFam == kFamState) {
-            count = max(0, min(C.rpu, C.heads - first));
-            pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
-            pstride = pbytes;
-          } else if constexpr (kFam == kFamRowsMis) {
-            // the rows, in a 16-byte-aligned region with room for the shift;
-            // pbytes counts the bytes the bulk copies bring (the two edge
-            // words of a misaligned page come by cp.async)
-            count = max(0, min(C.rpu, cur.nv - first));
-            pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
-            pstride = pbytes + kMisPad;
+        long long pos = ra / U;
+        int ci = 0, half = 0, sub = 0;
+        {
+          int kk = static_cast<int>(ra - pos * U);
+          if (p.pack) {
+            // every cache has the same halves, one unit per page
+            ci = kk / p.caches[0].halves;
+            half = kk - ci * p.caches[0].halves;
           } else {
-            count = max(0, min(C.rpu, cur.nv - first));
-            pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
-            pstride = pbytes;
+            while (kk >= p.caches[ci].halves * p.caches[ci].upp) {
+              kk -= p.caches[ci].halves * p.caches[ci].upp;
+              ++ci;
+            }
+            half = kk / p.caches[ci].upp;
+            sub = kk - half * p.caches[ci].upp;
           }
         }
-        // Pages per unit: one, or, when the launch's pages all look alike and
-        // each is a unit, as many consecutive pages of the position (in this
-        // CTA's range) as the stage holds -- many more when blocks are
-        // partial.  A skipped position is passed over in one step.
-        int npg = 1;
-        // (the two forms of the test and of the cursor step below measured
-        // fastest for their families: rows a packed step per unit, heads the
-        // one-page step whenever a unit holds one page)
-        if (kFam == kFamRows ? p.pack != 0 : fit > 1) {
-          int left = p.pages_per_pos - (ci * C.halves + half);
-          if (u_end - u < left) left = static_cast<int>(u_end - u);
-          npg = max(1, min(left, fit));
-          if constexpr (kFam == kFamRowsMis) npg = min(npg, kMisMaxPages);
-        }
-        if (pbytes > 0) {
-          if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
-                                      p.timeout_ns)) {
-            set_status(p, kStatusTimeout);
-            aborted = true;
-            break;
+        PosInfo cur = position_info(p, pos, rc, b_cur, ra, rb);
+        int mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
+        int fit = stage_fit<kFam>(p, cur, SB);
+        int slot = 0;
+        u32 n_emit = 0;
+        int col = p.caches[ci].column;
+        for (long long u = ra; u < rb;) {
+          const DevCache &C = p.caches[ci];
+          // One accumulator slot per (position, column); the caches arrive
+          // sorted by column, so a column's units are consecutive.
+          const long long dst_word = pos * p.num_columns + col;
+          const int first = sub * C.rpu;
+          int count = 0;
+          u32 pbytes = 0;   // bytes copied per page of the unit
+          u32 pstride = 0;  // bytes a page of the unit occupies in the stage
+          if (!cur.skip) {
+            if constexpr (head_family(kFam)) {
+              count = max(0, min(C.rpu, C.heads - first));
+              if constexpr (kFam == kFamHnd) {
+                // each head's first nv slots (its valid ones), heads packed
+                // one after another in the stage
+                pstride = static_cast<u32>(count) * static_cast<u32>(cur.nv) *
+                          static_cast<u32>(C.hb);
+                pbytes = pstride;
+              } else {
+                // the unit's heads with all their slots, staged as in memory
+                pstride = static_cast<u32>(count) * static_cast<u32>(bs) * static_cast<u32>(C.hb);
+                pbytes = pstride;
+                if constexpr (kFam == kFamHndSub) {
+                  const int nsb = (cur.nv + C.kbs - 1) / C.kbs;  // sub-blocks with valid slots
+                  pbytes = static_cast<u32>(count) * static_cast<u32>(nsb * C.kbs) *
+                           static_cast<u32>(C.hb);
+                }
+              }
+            } else if constexpr (kFam == kFamState) {
+              count = max(0, min(C.rpu, C.heads - first));
+              pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
+              pstride = pbytes;
+            } else if constexpr (kFam == kFamRowsMis) {
+              // the rows, in a 16-byte-aligned region with room for the shift;
+              // pbytes counts the bytes the bulk copies bring (the two edge
+              // words of a misaligned page come by cp.async)
+              count = max(0, min(C.rpu, cur.nv - first));
+              pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
+              pstride = pbytes + kMisPad;
+            } else {
+              count = max(0, min(C.rpu, cur.nv - first));
+              pbytes = static_cast<u32>(count) * static_cast<u32>(C.rowb);
+              pstride = pbytes;
+            }
           }
-          if (n_emit == 0) {
-            slot = static_cast<int>(seq % kRingSlots);
-            ++seq;
-            hdr->ring_acc[slot] = 0ull;
-            hdr->ring_cnt[slot] = 0u;
+          // Pages per unit: one, or, when the launch's pages all look alike and
+          // each is a unit, as many consecutive pages of the position (in this
+          // CTA's range) as the stage holds -- many more when blocks are
+          // partial.  A skipped position is passed over in one step.
+          int npg = 1;
+          // (the two forms of the test and of the cursor step below measured
+          // fastest for their families: rows a packed step per unit, heads the
+          // one-page step whenever a unit holds one page)
+          if (kFam == kFamRows ? p.pack != 0 : fit > 1) {
+            int left = p.pages_per_pos - (ci * C.halves + half);
+            if (rb - u < left) left = static_cast<int>(rb - u);
+            npg = max(1, min(left, fit));
+            if constexpr (kFam == kFamRowsMis) npg = min(npg, kMisMaxPages);
           }
-          const u32 fb = ptx::smem_addr(&hdr->full[s]);
-          if constexpr (kFam == kFamRowsMis) {
-            // Per page: the 16-byte-aligned interior of its rows by bulk copy,
-            // and when the page starts 8 bytes past a boundary its first and
-            // last words by 8-byte cp.async, tracked on the same barrier.
+          if (pbytes > 0) {
+            if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
+                                        p.timeout_ns)) {
+              set_status(p, kStatusTimeout);
+              aborted = true;
+              break;
+            }
+            if (n_emit == 0) {
+              slot = static_cast<int>(seq % kRingSlots);
+              ++seq;
+              hdr->ring_acc[slot] = 0ull;
+              hdr->ring_cnt[slot] = 0u;
+            }
+            const u32 fb = ptx::smem_addr(&hdr->full[s]);
+            if constexpr (kFam == kFamRowsMis) {
+              // Per page: the 16-byte-aligned interior of its rows by bulk copy,
+              // and when the page starts 8 bytes past a boundary its first and
+              // last words by 8-byte cp.async, tracked on the same barrier.
+              u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
+              u32 tx = 0, dmask = 0;
+              int pci = ci, phalf = half;
+              for (int k2 = 0; k2 < npg; ++k2) {
+                const DevCache &D = p.caches[pci];
+                const unsigned char *src = D.base + static_cast<long long>(phalf) * D.half_stride +
+                                           cur.block * D.block_stride +
+                                           static_cast<u64>(first) * D.rowb;
+                if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+                  ptx::bulk_g2s(dst, src, pbytes, fb, policy);
+                  tx += pbytes;
+                } else {
+                  dmask |= 1u << k2;
+                  if (pbytes > 16) {
+                    ptx::bulk_g2s(dst + 16, src + 8, pbytes - 16, fb, policy);
+                    tx += pbytes - 16;
+                  }
+                  ptx::cp_async8(dst + 8, src);
+                  ptx::cp_async8(dst + pbytes, src + pbytes - 8);
+                }
+                dst += pstride;
+                if (++phalf == D.halves) {
+                  phalf = 0;
+                  ++pci;
+                }
+              }
+              store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
+                         mode | static_cast<int>(dmask << 1), slot, npg);
+              if (dmask) ptx::cp_async_mbar_arrive(fb);
+              ptx::mbar_arrive_expect_tx(fb, tx);
+            } else {
+            store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
+                       mode, slot, npg);
+            ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
             u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
-            u32 tx = 0, dmask = 0;
             int pci = ci, phalf = half;
             for (int k2 = 0; k2 < npg; ++k2) {
               const DevCache &D = p.caches[pci];
-              const unsigned char *src = D.base + static_cast<long long>(phalf) * D.half_stride +
-                                         cur.block * D.block_stride +
-                                         static_cast<u64>(first) * D.rowb;
-              if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-                ptx::bulk_g2s(dst, src, pbytes, fb, policy);
-                tx += pbytes;
-              } else {
-                dmask |= 1u << k2;
-                if (pbytes > 16) {
-                  ptx::bulk_g2s(dst + 16, src + 8, pbytes - 16, fb, policy);
-                  tx += pbytes - 16;
+              const unsigned char *page = D.base +
+                  static_cast<long long>(phalf) * D.half_stride +
+                  cur.block * D.block_stride;
+              if constexpr (kFam == kFamHndSub) {
+                // [sub-block][heads][kbs][hb]: in each sub-block that holds
+                // valid slots the unit's heads are one contiguous run; when
+                // the unit has every head those runs are one range
+                const u64 sub_page = static_cast<u64>(D.heads) * D.kbs * D.hb;
+                const u32 run = static_cast<u32>(count) * static_cast<u32>(D.kbs * D.hb);
+                if (count == D.heads) {
+                  ptx::bulk_g2s(dst, page, pbytes, fb, policy);
+                } else {
+                  for (int sb = 0; sb * D.kbs < cur.nv; ++sb)
+                    ptx::bulk_g2s(dst + static_cast<u32>(sb) * run,
+                                  page + static_cast<u64>(sb) * sub_page +
+                                      static_cast<u64>(first) * D.kbs * D.hb,
+                                  run, fb, policy);
                 }
-                ptx::cp_async8(dst + 8, src);
-                ptx::cp_async8(dst + pbytes, src + pbytes - 8);
+              } else if constexpr (kFam == kFamHnd) {
+                // [heads][block_size][hb]: a full block's heads are one
+                // contiguous run; a partial block's valid slots are one run of
+                // nv slots per head, copied one after another
+                const unsigned char *src = page + static_cast<u64>(first) * bs * D.hb;
+                if (cur.nv == bs) {
+                  ptx::bulk_g2s(dst, src, pstride, fb, policy);
+                } else {
+                  const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(D.hb);
+                  const u64 hstep = static_cast<u64>(bs) * static_cast<u64>(D.hb);
+                  for (int h = 0; h < count; ++h)
+                    ptx::bulk_g2s(dst + static_cast<u32>(h) * run, src + h * hstep, run, fb,
+                                  policy);
+                }
+              } else if constexpr (head_family(kFam)) {
+                // [heads][chunks][block_size][16]: the unit's heads are one
+                // contiguous run of whole slots
+                ptx::bulk_g2s(dst, page + static_cast<u64>(first) * bs * D.hb, pstride,
+                              fb, policy);
+              } else {
+                ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes,
+                              fb, policy);
               }
               dst += pstride;
               if (++phalf == D.halves) {
@@ -600,120 +680,76 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                 ++pci;
               }
             }
-            store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
-                       mode | static_cast<int>(dmask << 1), slot, npg);
-            if (dmask) ptx::cp_async_mbar_arrive(fb);
-            ptx::mbar_arrive_expect_tx(fb, tx);
-          } else {
-          store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
-                     mode, slot, npg);
-          ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
-          u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
-          int pci = ci, phalf = half;
-          for (int k2 = 0; k2 < npg; ++k2) {
-            const DevCache &D = p.caches[pci];
-            const unsigned char *page = D.base +
-                static_cast<long long>(phalf) * D.half_stride +
-                cur.block * D.block_stride;
-            if constexpr (kFam == kFamHndSub) {
-              // [sub-block][heads][kbs][hb]: in each sub-block that holds
-              // valid slots the unit's heads are one contiguous run; when
-              // the unit has every head those runs are one range
-              const u64 sub_page = static_cast<u64>(D.heads) * D.kbs * D.hb;
-              const u32 run = static_cast<u32>(count) * static_cast<u32>(D.kbs * D.hb);
-              if (count == D.heads) {
-                ptx::bulk_g2s(dst, page, pbytes, fb, policy);
-              } else {
-                for (int sb = 0; sb * D.kbs < cur.nv; ++sb)
-                  ptx::bulk_g2s(dst + static_cast<u32>(sb) * run,
-                                page + static_cast<u64>(sb) * sub_page +
-                                    static_cast<u64>(first) * D.kbs * D.hb,
-                                run, fb, policy);
-              }
-            } else if constexpr (kFam == kFamHnd) {
-              // [heads][block_size][hb]: a full block's heads are one
-              // contiguous run; a partial block's valid slots are one run of
-              // nv slots per head, copied one after another
-              const unsigned char *src = page + static_cast<u64>(first) * bs * D.hb;
-              if (cur.nv == bs) {
-                ptx::bulk_g2s(dst, src, pstride, fb, policy);
-              } else {
-                const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(D.hb);
-                const u64 hstep = static_cast<u64>(bs) * static_cast<u64>(D.hb);
-                for (int h = 0; h < count; ++h)
-                  ptx::bulk_g2s(dst + static_cast<u32>(h) * run, src + h * hstep, run, fb,
-                                policy);
-              }
-            } else if constexpr (head_family(kFam)) {
-              // [heads][chunks][block_size][16]: the unit's heads are one
-              // contiguous run of whole slots
-              ptx::bulk_g2s(dst, page + static_cast<u64>(first) * bs * D.hb, pstride,
-                            fb, policy);
-            } else {
-              ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes,
-                            fb, policy);
             }
-            dst += pstride;
-            if (++phalf == D.halves) {
-              phalf = 0;
-              ++pci;
+            ++it;
+            ++n_emit;
+            if (++s == NS) {
+              s = 0;
+              ++f;
             }
           }
+          // advance the cursor past this unit's npg host units
+          u += npg;
+          bool pos_done = false;
+          if (kFam == kFamRows && p.pack) {
+            // packed pages: every cache has C.halves halves
+            const int flat = ci * C.halves + half + npg;
+            ci = flat / C.halves;
+            half = flat - ci * C.halves;
+            pos_done = ci >= p.num_caches;
+          } else if (npg > 1) {
+            half += npg;
+            while (half >= C.halves) {
+              half -= C.halves;
+              ++ci;
+            }
+            pos_done = ci >= p.num_caches;
+          } else if (++sub == C.upp) {
+            sub = 0;
+            if (++half == C.halves) {
+              half = 0;
+              pos_done = ++ci == p.num_caches;
+            }
           }
-          ++it;
-          ++n_emit;
-          if (++s == NS) {
-            s = 0;
-            ++f;
+          if (pos_done) ci = 0;
+          if (pos_done || u == rb || p.caches[ci].column != col) {
+            // close the (position, column): this thread's share of the count
+            if (n_emit > 0) {
+              const u32 delta = 0u - static_cast<u32>(p.group_warps) * n_emit;
+              const u32 prev = atomicAdd(&hdr->ring_cnt[slot], delta);
+              if (prev + delta == 0u) finalize_slot(p, hdr, slot, dst_word, mode);
+            } else if (cur.whole && !p.all_atomic) {
+              ptx::grid_dep_wait();
+              p.out[dst_word] = 0ull;
+            }
+            n_emit = 0;
+          }
+          col = p.caches[ci].column;
+          if (pos_done && u < rb) {
+            ++pos;
+            b_cur = b_next;
+            b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
+            req_seek(p, rc, pos);
+            cur = position_info(p, pos, rc, b_cur, ra, rb);
+            mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
+            fit = stage_fit<kFam>(p, cur, SB);
           }
         }
-        // advance the cursor past this unit's npg host units
-        u += npg;
-        bool pos_done = false;
-        if (kFam == kFamRows && p.pack) {
-          // packed pages: every cache has C.halves halves
-          const int flat = ci * C.halves + half + npg;
-          ci = flat / C.halves;
-          half = flat - ci * C.halves;
-          pos_done = ci >= p.num_caches;
-        } else if (npg > 1) {
-          half += npg;
-          while (half >= C.halves) {
-            half -= C.halves;
-            ++ci;
-          }
-          pos_done = ci >= p.num_caches;
-        } else if (++sub == C.upp) {
-          sub = 0;
-          if (++half == C.halves) {
-            half = 0;
-            pos_done = ++ci == p.num_caches;
-          }
-        }
-        if (pos_done) ci = 0;
-        if (pos_done || u == u_end || p.caches[ci].column != col) {
-          // close the (position, column): this thread's share of the count
-          if (n_emit > 0) {
-            const u32 delta = 0u - static_cast<u32>(p.group_warps) * n_emit;
-            const u32 prev = atomicAdd(&hdr->ring_cnt[slot], delta);
-            if (prev + delta == 0u) finalize_slot(p, hdr, slot, dst_word, mode);
-          } else if (cur.whole && !p.all_atomic) {
-            ptx::grid_dep_wait();
-            p.out[dst_word] = 0ull;
-          }
-          n_emit = 0;
-        }
-        col = p.caches[ci].column;
-        if (pos_done && u < u_end) {
-          ++pos;
-          b_cur = b_next;
-          b_next = pos + 1 < p.total_positions ? p.block_ids[pos + 1] : 0;
-          req_seek(p, rc, pos);
-          cur = position_info(p, pos, rc, b_cur, u_begin, u_end);
-          mode = (cur.whole && !p.all_atomic) ? kFlushStore : kFlushAtomic;
-          fit = stage_fit<kFam>(p, cur, SB);
-        }
+        if (aborted) break;
       }
+      if (!p.work) break;
+      if (!claimed) {
+        // the counter is zeroed by the kernel launched before this one
+        ptx::grid_dep_wait();
+        next_chunk = atomicAdd(p.work, 1ull);
+        claimed = true;
+      }
+      const long long ca = p.pool_start + static_cast<long long>(next_chunk) * p.chunk_units;
+      if (ca >= p.total_units) break;
+      ra = ca;
+      rb = min(p.total_units, ca + p.chunk_units);
+      next_chunk = atomicAdd(p.work, 1ull);
+      first_range = false;
     }
     // Every copy of this CTA is issued: a following kernel launched with
     // programmatic stream serialization may start (it waits for this grid

@@ -129,6 +129,10 @@ struct Params {
   int stage_bytes;           // bytes per stage (multiple of 128)
   int group_warps;           // consumer warps per group: 1, 2, 4 or 8
   int groups;                // kConsumerWarps / group_warps, <= stages
+  unsigned long long *work;  // work counter (zeroed before the launch), or null:
+                             // no dynamic share-out
+  long long pool_start;      // with `work`: units [pool_start, total_units) are
+  long long chunk_units;     // handed out in chunks of chunk_units
   int pack;                  // 1: every cache has the same geometry and each
                              // page is a unit; consecutive pages of a position
                              // are packed into one stage as far as it holds

@@ -45,19 +45,21 @@ __global__ void __launch_bounds__(256) kvcs_rows_kernel(const RowParams rp) {
   }
 }
 
-// Zeroes the n output words that the checksum kernels then add into.  It is
+// Zeroes the n output words that the checksum kernels then add into, and the
+// n_work work counters they take chunks from.  It is
 // launched so that it may start while the stream's previous kernel ends, and
 // first waits for all earlier work to finish.  Then it lets the next kernel
 // of the stream start at once: that kernel reads its inputs meanwhile (all
 // written by work that has finished) and waits for this grid before it
 // writes an output word.
-__global__ void __launch_bounds__(256) kvcs_zero_kernel(u64 *out, long long n) {
+__global__ void __launch_bounds__(256)
+    kvcs_zero_kernel(u64 *out, long long n, u64 *work, int n_work) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += step)
-    out[i] = 0ull;
+  const long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  for (long long i = t0; i < n; i += step) out[i] = 0ull;
+  if (t0 < n_work) work[t0] = 0ull;   // the work counters of the launches
 }
 
 // tags[i] = (first eight bytes of hash i, little-endian) XOR fingerprint.

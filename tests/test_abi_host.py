@@ -154,12 +154,24 @@ def test_plan_shapes():
     assert p["units"] == 9220 * 32 * 2 and p["stage_bytes"] == 32768
     assert p["stages"] == 7 and p["smem_bytes"] <= 232448
     assert p["kv_bytes_max"] == 9220 * 32 * 2 * 32768
+    # with a workspace this call would share its last units out (>= 1024
+    # units per SM) ...
+    assert p["dynamic"] == 1
     # 70B-shaped fp8: 16 KiB pages, a unit each, three packed per 48 KiB stage
     p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=16384)
     assert p["units"] == 16384 * 160 and p["stage_bytes"] == 49152 and p["stages"] == 4
     # one 70B-shaped request: too few positions for whole-position CTAs
     p = plan([FakeCache(layer=i, head_bytes=128) for i in range(80)], positions=128)
     assert p["split"] == 1 and p["memsets"] == 1 and p["grid"] == 152
+    # ... this one (134 units per SM) keeps the fixed split; the threshold
+    # is 1024 units per SM of the planned GPU
+    assert p["dynamic"] == 0
+    assert plan([FakeCache(layer=i, head_bytes=128) for i in range(80)],
+                positions=973)["dynamic"] == 1
+    assert plan([FakeCache(layer=i, head_bytes=128) for i in range(80)],
+                positions=972)["dynamic"] == 0
+    assert plan([FakeCache(layer=i, head_bytes=128) for i in range(80)],
+                positions=972, sms=100)["dynamic"] == 1
     # latent rows of 1152 B: two units of 32 rows per 64-slot page
     p = plan([FakeCache(layout=2, num_heads=1, head_bytes=1152, layer=i)
               for i in range(61)], bs=64, positions=4096)

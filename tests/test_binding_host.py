@@ -192,3 +192,28 @@ def test_group_outputs_checked(on_cuda0, bad):
         cols = 0 if bad == "columns_zero" else 65
     with pytest.raises(ValueError):
         K.group_checksums([_Cache()], 16, po, fp, nt, ids, cols, total_positions=n, **kw)
+
+
+def test_workspace_checked(on_cuda0):
+    po, fp, nt, ids = _fake_tables()
+    for ws in (FakeTensor(K.KVCS_WORKSPACE_WORDS - 1, torch.int64),
+               FakeTensor(K.KVCS_WORKSPACE_WORDS, torch.int32),
+               FakeTensor(K.KVCS_WORKSPACE_WORDS, torch.int64, dev=1)):
+        with pytest.raises(ValueError):
+            K.group_checksums([_Cache()], 16, po, fp, nt, ids, 1, total_positions=10,
+                              values=FakeTensor(10, torch.int64), workspace=ws)
+        with pytest.raises(ValueError):
+            K.Checksummer([_Cache()], 16, po, fp, nt, ids, 10, workspace=ws)
+
+
+def test_output_flags_validated():
+    """Unknown flag bits, and a workspace flag without a workspace, are
+    refused before any CUDA call (no GPU here)."""
+    lib = K.load_library()
+    arr = K.cache_array([_Cache()])
+    reqs = B.kvcs_requests(1, 16, 32, 48, 64)
+    for flags, ws in ((4, None), (K.KVCS_OUT_WORKSPACE, None), (K.KVCS_OUT_WORKSPACE, 4100)):
+        outs = B.kvcs_outputs(1, flags, 4096, None, None, None, None, None, ws)
+        rc = lib.kvcs_group_checksums(arr, 1, 16, ctypes.byref(reqs), 4, ctypes.byref(outs),
+                                      None, None)
+        assert rc == K.KVCS_EINVAL, (flags, ws)
