@@ -162,7 +162,8 @@ def test_dynamic_in_a_cuda_graph():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         ck(out, None, s.cuda_stream)
-    gen = torch.Generator(device=DEV).manual_seed(9)
+    gen = torch.Generator(device=DEV).manual_seed(977)  # not the fill's own seed
+    prev = K.workload_checksums(wl)
     for _ in range(2):
         for c in wl.caches:
             c.pool.copy_(torch.randint(0, 256, c.pool.shape, dtype=torch.uint8, device=DEV,
@@ -171,7 +172,8 @@ def test_dynamic_in_a_cuda_graph():
         torch.cuda.synchronize()
         ref = K.workload_checksums(wl)
         torch.cuda.synchronize()
-        assert torch.equal(out, ref)
+        assert torch.equal(out, ref) and not torch.equal(ref, prev)
+        prev = ref
 
 
 def test_dynamic_full_size_llama3_8b():
