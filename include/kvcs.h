@@ -24,7 +24,9 @@
  * (module docstring, paragraph on TP ranks and PP stages).
  *
  * Memory: the caller owns every buffer.  The library allocates nothing and
- * enqueues all work on the caller's stream; calls are asynchronous.
+ * enqueues all work on the caller's stream; calls are asynchronous.  (Its
+ * one piece of device memory of its own is the 128-byte scratch array of
+ * kvcs_block_checksums_noalloc, part of the loaded module.)
  * Stream order: a call's kernels start only after the stream's earlier work
  * has finished.  The checksum kernels let a following kernel that was
  * launched with programmatic stream serialization start before they end;
@@ -32,7 +34,8 @@
  * them (griddepcontrol.wait, cudaGridDependencySynchronize) before it reads
  * what they write.
  * Thread safety: calls may be issued concurrently from several host threads
- * and streams; they share no mutable state apart from a launch counter.
+ * and streams; they share no mutable state apart from a launch counter
+ * (and, for kvcs_block_checksums_noalloc, its scratch array: see there).
  */
 #ifndef KVCS_H_
 #define KVCS_H_
@@ -160,6 +163,10 @@ typedef struct kvcs_requests {
                                  1 GiB or more (kvcs_write_kv) */
 #define KVCS_ECUDA (-3)       /* a CUDA call failed (launch, attribute query);
                                  work may have been partly enqueued */
+#define KVCS_ETOOLARGE (-4)   /* the call is beyond a fixed limit of
+                                 kvcs_block_checksums_noalloc (more than
+                                 KVCS_NOALLOC_MAX_CACHES caches); nothing is
+                                 enqueued */
 
 /* Bits set in the caller's device status word by the kernels (OR-ed in; the
  * caller zeroes the word when it wants a fresh reading).  None of them traps
@@ -282,6 +289,44 @@ int kvcs_group_checksums(const kvcs_cache *caches, int32_t num_caches,
                          int32_t block_size, const kvcs_requests *reqs,
                          int64_t total_positions, const kvcs_outputs *outs,
                          uint32_t *status, void *stream);
+
+/*
+ * kvcs_block_checksums_noalloc -- kvcs_block_checksums for callers that
+ * cannot allocate device memory, with the dynamic share-out of a workspace
+ * call (KVCS_OUT_WORKSPACE) but no workspace to pass.
+ *
+ * The paged-KV checksum has no counterpart of this entry point: it exists
+ * for the library's users.  Some callers cannot call cudaMalloc or any
+ * allocator: code that runs where the process's allocator must not be
+ * entered (inside a caching allocator's own hooks, a memory-pool callback,
+ * or a real-time serving loop that forbids allocation after start-up), and
+ * code that owns no device buffer of its own to lend (a plug-in given only
+ * the KV pools and an output array).  This entry point asks for nothing
+ * beyond the inputs and the output: its scratch, the bulk kernel's work
+ * counters, is a module-scope device array of KVCS_WORKSPACE_WORDS words
+ * (128 bytes) that every GPU which loads the library holds until the
+ * process exits.  The call itself allocates nothing: no cudaMalloc or
+ * cudaFree and no allocating library routine.
+ *
+ * Arguments, results, status bits and errors as kvcs_block_checksums, plus:
+ *   - num_caches above KVCS_NOALLOC_MAX_CACHES returns KVCS_ETOOLARGE before
+ *     any CUDA call (within it, every bulk-copy launch of the call has a
+ *     counter of the array to itself);
+ *   - the first call on a device looks up the array's device address there
+ *     (cudaGetSymbolAddress, with that device current) and keeps it, so
+ *     make that first call before any stream capture on the device;
+ *   - every call on a device shares the one array, which keeps the last
+ *     call's counters: each call zeroes the counters it uses (a small kernel
+ *     ahead of its checksum launches, in stream order).  Calls that can
+ *     overlap on the GPU (other streams, other threads) race on the
+ *     counters and may then return wrong checksums: issue them in one
+ *     stream order, or use kvcs_group_checksums with a workspace per stream.
+ */
+#define KVCS_NOALLOC_MAX_CACHES 1024
+int kvcs_block_checksums_noalloc(const kvcs_cache *caches, int32_t num_caches,
+                                 int32_t block_size, const kvcs_requests *reqs,
+                                 int64_t total_positions, uint64_t *out,
+                                 uint32_t *status, void *stream);
 
 /*
  * kvcs_block_checksum_tags -- the 64-bit tag of each block (the checksum

@@ -18,4 +18,6 @@ from ._binding import (  # noqa: F401
     kvcs_requests, launch_count, load_library, plan_for, selftest_wait_timeout,
     strerror, version,
     workload_checksums, Checksummer, workload_checksummer, kvcs_outputs,
-    group_checksums, block_checksum_tags, write_kv, KVWriter)
+    group_checksums, block_checksum_tags, write_kv, KVWriter,
+    KVCS_ETOOLARGE, KVCS_NOALLOC_MAX_CACHES, block_checksums_noalloc,
+    kvcs_block_checksums_noalloc)

@@ -24,6 +24,7 @@ KVCS_OK = 0
 KVCS_EINVAL = -1
 KVCS_EUNSUPPORTED = -2
 KVCS_ECUDA = -3
+KVCS_ETOOLARGE = -4
 
 KVCS_STATUS_BAD_BLOCK_ID = 1
 KVCS_STATUS_BAD_REQUESTS = 2
@@ -32,6 +33,7 @@ KVCS_STATUS_TIMEOUT = 4
 KVCS_OUT_ACCUMULATE = 1
 KVCS_OUT_WORKSPACE = 2
 KVCS_WORKSPACE_WORDS = 16
+KVCS_NOALLOC_MAX_CACHES = 1024
 
 
 class kvcs_cache(ctypes.Structure):
@@ -74,6 +76,10 @@ class kvcs_plan_info(ctypes.Structure):
 # Every symbol kvcs.h declares, with its ctypes signature.
 SIGNATURES = {
     "kvcs_block_checksums": (ctypes.c_int, [
+        ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
+        ctypes.POINTER(kvcs_requests), ctypes.c_int64, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p]),
+    "kvcs_block_checksums_noalloc": (ctypes.c_int, [
         ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
         ctypes.POINTER(kvcs_requests), ctypes.c_int64, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_void_p]),
@@ -172,6 +178,19 @@ def kvcs_block_checksums(caches: ctypes.Array, num_caches: int, block_size: int,
         out, status or None, stream or None)
     if rc != KVCS_OK:
         raise KvcsError(rc, "kvcs_block_checksums")
+    return rc
+
+
+def kvcs_block_checksums_noalloc(caches: ctypes.Array, num_caches: int, block_size: int,
+                                 reqs: kvcs_requests, total_positions: int, out: int,
+                                 status: int | None, stream: int | None) -> int:
+    """The C entry point, one-to-one; raises ``KvcsError`` on a negative
+    return."""
+    rc = load_library().kvcs_block_checksums_noalloc(
+        caches, num_caches, block_size, ctypes.byref(reqs), total_positions,
+        out, status or None, stream or None)
+    if rc != KVCS_OK:
+        raise KvcsError(rc, "kvcs_block_checksums_noalloc")
     return rc
 
 
@@ -314,6 +333,34 @@ def block_checksums(caches: Sequence, block_size: int, pos_offsets, first_positi
     kvcs_block_checksums(arr, len(caches), block_size, reqs, total_positions,
                          out.data_ptr() if total_positions > 0 else None,
                          status.data_ptr() if status is not None else None, stream)
+    return out
+
+
+def block_checksums_noalloc(caches: Sequence, block_size: int, pos_offsets, first_position,
+                            num_tokens, block_ids, out, total_positions: int, status=None,
+                            stream=None):
+    """Torch front end of ``kvcs_block_checksums_noalloc``: arguments as
+    ``block_checksums``, except that ``out`` and ``total_positions`` are
+    required, so that nothing on this path allocates device memory or
+    synchronises.  Calls on one device share the library's scratch and must
+    not overlap on the GPU (one stream order)."""
+    import torch
+    for c in caches:
+        _check_pool(c, block_size)
+    dev = _check_requests(pos_offsets, first_position, num_tokens, block_ids, total_positions)
+    _check_tensor("out", out, _words(), total_positions, dev)
+    _check_status(status, dev)
+    reqs = kvcs_requests(pos_offsets.numel() - 1, pos_offsets.data_ptr(),
+                         first_position.data_ptr(), num_tokens.data_ptr(),
+                         block_ids.data_ptr())
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    arr = cache_array(caches)
+    kvcs_block_checksums_noalloc(arr, len(caches), block_size, reqs, total_positions,
+                                 out.data_ptr() if total_positions > 0 else None,
+                                 status.data_ptr() if status is not None else None, stream)
     return out
 
 

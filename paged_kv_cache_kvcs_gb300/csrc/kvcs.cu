@@ -37,6 +37,7 @@ struct DeviceState {
   std::mutex mu;
   std::atomic<bool> done{false};  // set only once the setup succeeded
   int sms = 0;
+  std::atomic<u64 *> noalloc_scratch{nullptr};  // this device's g_noalloc_scratch
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -633,6 +634,41 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
   return KVCS_OK;
 }
 
+// Scratch of kvcs_block_checksums_noalloc: the bulk kernel's work counters
+// for callers that cannot lend a workspace.  A module-scope device array,
+// so every GPU that loads the library holds its 128 bytes until the process
+// exits; on the host its name only stands for the symbol (its device
+// address comes from cudaGetSymbolAddress).
+static __device__ __align__(256) u64 g_noalloc_scratch[KVCS_WORKSPACE_WORDS];
+
+// Within KVCS_NOALLOC_MAX_CACHES caches a call never has more bulk-copy
+// launches (per layout family, groups of kMaxCachesPerLaunch) than counters.
+static_assert(KVCS_NOALLOC_MAX_CACHES / kMaxCachesPerLaunch + kNumFamilies <=
+                  KVCS_WORKSPACE_WORDS,
+              "the no-alloc scratch must hold a counter per bulk launch");
+
+// Device address of g_noalloc_scratch on the current device: looked up once
+// per device, with that device current, and kept.
+cudaError_t noalloc_scratch(u64 **ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  DeviceState &d = g_dev[dev];
+  u64 *p = d.noalloc_scratch.load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(d.mu);
+    p = d.noalloc_scratch.load(std::memory_order_relaxed);
+    if (!p) {
+      e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_noalloc_scratch);
+      if (e != cudaSuccess || !p) return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+      d.noalloc_scratch.store(p, std::memory_order_release);
+    }
+  }
+  *ptr = p;
+  return cudaSuccess;
+}
+
 int columns_of(const kvcs_cache *caches, int32_t num_caches) {
   int m = 0;
   for (int32_t i = 0; caches && i < num_caches; ++i) m = std::max(m, caches[i].column + 1);
@@ -693,6 +729,31 @@ int kvcs_group_checksums(const kvcs_cache *caches, int32_t num_caches,
                          int64_t total_positions, const kvcs_outputs *outs,
                          uint32_t *status, void *stream) {
   return run_checksums(caches, num_caches, block_size, reqs, total_positions, outs,
+                       status, static_cast<cudaStream_t>(stream));
+}
+
+int kvcs_block_checksums_noalloc(const kvcs_cache *caches, int32_t num_caches,
+                                 int32_t block_size, const kvcs_requests *reqs,
+                                 int64_t total_positions, uint64_t *out,
+                                 uint32_t *status, void *stream) {
+  // arguments first, with no CUDA call, as in kvcs_block_checksums
+  if (num_caches > KVCS_NOALLOC_MAX_CACHES) return KVCS_ETOOLARGE;
+  int rc = validate_caches(caches, num_caches, block_size, 1);
+  if (rc != KVCS_OK) return rc;
+  if (!reqs || total_positions < 0 || reqs->num_requests < 0) return KVCS_EINVAL;
+  if (total_positions == 0) return KVCS_OK;
+  if (!out || reinterpret_cast<uintptr_t>(out) % 8 || !reqs->pos_offsets ||
+      !reqs->first_position || !reqs->num_tokens || !reqs->block_ids)
+    return KVCS_EINVAL;
+  u64 *scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return KVCS_ECUDA;
+  kvcs_outputs o;
+  std::memset(&o, 0, sizeof(o));
+  o.num_columns = 1;
+  o.flags = KVCS_OUT_WORKSPACE;
+  o.values = out;
+  o.workspace = reinterpret_cast<uint64_t *>(scratch);
+  return run_checksums(caches, num_caches, block_size, reqs, total_positions, &o,
                        status, static_cast<cudaStream_t>(stream));
 }
 
@@ -829,6 +890,9 @@ const char *kvcs_strerror(int code) {
       return "unsupported geometry (global heads past 65536 per layer, or a token row of 1 GiB "
              "or more in a write)";
     case KVCS_ECUDA: return "CUDA error";
+    case KVCS_ETOOLARGE:
+      return "beyond the fixed limit of kvcs_block_checksums_noalloc (more than "
+             "KVCS_NOALLOC_MAX_CACHES = 1024 caches)";
     default: return "unknown error";
   }
 }

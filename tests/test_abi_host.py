@@ -145,6 +145,28 @@ def test_block_checksums_rejects_before_any_cuda_call():
     assert rc == K.KVCS_OK              # nothing to do, nothing enqueued
 
 
+def test_noalloc_rejects_before_any_cuda_call():
+    """kvcs_block_checksums_noalloc: bad arguments and more than
+    KVCS_NOALLOC_MAX_CACHES caches are refused on the host (no GPU here, so
+    any CUDA call would have returned KVCS_ECUDA instead)."""
+    fn = K.load_library().kvcs_block_checksums_noalloc
+    reqs = B.kvcs_requests(1, 16, 32, 48, 64)
+    arr = K.cache_array([FakeCache(head_bytes=12)])
+    assert fn(arr, 1, 16, ctypes.byref(reqs), 4, 128, None, None) == K.KVCS_EINVAL
+    arr = K.cache_array([FakeCache()])
+    assert fn(arr, 1, 16, ctypes.byref(reqs), 4, None, None, None) == K.KVCS_EINVAL
+    assert fn(arr, 1, 16, ctypes.byref(reqs), 4, 132, None, None) == K.KVCS_EINVAL
+    assert fn(arr, 1, 16, None, 4, 128, None, None) == K.KVCS_EINVAL
+    assert fn(arr, 1, 16, ctypes.byref(reqs), 0, None, None, None) == K.KVCS_OK
+    n = K.KVCS_NOALLOC_MAX_CACHES
+    many = K.cache_array([FakeCache(layer=i, num_heads=1, head_bytes=16) for i in range(n + 1)])
+    assert fn(many, n + 1, 16, ctypes.byref(reqs), 4, 128, None, None) == K.KVCS_ETOOLARGE
+    assert "1024" in K.strerror(K.KVCS_ETOOLARGE)
+    # within the limit the arguments pass the host checks and the call goes
+    # on to its first CUDA call, which fails here without a GPU
+    assert fn(many, n, 16, ctypes.byref(reqs), 4, 128, None, None) == K.KVCS_ECUDA
+
+
 def test_plan_shapes():
     llama8b = [FakeCache(layer=i, num_blocks=9300) for i in range(32)]
     p = plan(llama8b, positions=9220)
