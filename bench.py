@@ -55,6 +55,9 @@ def make_workload(name: str, seed: int, device):
         return W.llama3_8b(seed, device)
     if name == "llama3_8b_small":      # 2.5 GB, 8 x 152 positions: ncu captures
         return W.llama3_8b(seed, device, num_requests=19, min_len=1024, max_len=1024)
+    if name == "llama3_8b_mid":        # 5.1 GB, 16 x 152 positions, 1024 units a SM: the
+        # smallest 8B-shaped call with the dynamic share-out (ncu captures)
+        return W.llama3_8b(seed, device, num_requests=38, min_len=1024, max_len=1024)
     if name == "mla":
         return W.mla(seed, device)
     if name == "mla_small":            # 608 positions = 4 x 152, 2.7 GB: ncu captures
@@ -100,6 +103,13 @@ def relayout(wl, layout: str):
         bs, H, hb, nb = wl.block_size, c.num_heads, c.head_bytes, c.num_blocks
         page = bs * H * hb
         v = c.pool.view(2, nb, bs, H, hb)
+        if layout == "misaligned_hnd":   # HND pools starting 8 bytes past a boundary
+            buf = torch.empty(c.pool.numel() + 8, dtype=torch.uint8, device=c.pool.device)
+            pool = buf[8:]
+            pool.copy_(v.permute(0, 1, 3, 2, 4).reshape(-1))
+            caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_HND))
+            c.pool = None
+            continue
         if layout == "hnd":
             pool = v.permute(0, 1, 3, 2, 4).contiguous().view(-1)
             caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_HND))
@@ -636,6 +646,8 @@ def run_write(args, ws, rank, local):
             "write_then_checksum_ms": round(t_unfused * 1e3, 4),
             "fused_vs_write_only": round(t_plain / t_fused, 4),
             "fused_vs_write_then_checksum": round(t_unfused / t_fused, 4)}
+    if one_layer:
+        line["per_layer_calls"] = per_layer_calls(args, dev, stream, lay, rank, scrub, scrub_out)
     if ws == 1 and not args.no_cpu_baseline:
         # the oracle computing the same block words from the written pages
         cores = host_cores()
@@ -653,6 +665,55 @@ def run_write(args, ws, rank, local):
         words = sums[bids.long()].cpu().numpy()
         line["parity"] = parity_check(words, ot["positions"], ot["values"])
     print(json.dumps(line), flush=True)
+
+
+def per_layer_calls(args, dev, stream, lay, rank, scrub, scrub_out) -> dict:
+    """A decode forward pass writes its layers one call at a time.  Here 32
+    one-layer calls (each its own pool and new rows) run back to back after
+    one L2 flush, timed per call; beside them the isolated event pattern of
+    the one-layer line with a one-element fill kernel in place of the call,
+    the floor that pattern puts under any kernel."""
+    import paged_kv_cache_kvcs_gb300 as kvcs
+    from paged_kv_cache_kvcs_gb300 import workloads as W
+    wb = W.llama3_8b_write(args.seed + rank + 1, dev, kind="decode", layout=lay[0],
+                           kernel_block_size=lay[1], layers=32)
+    sums = torch.zeros(wb.num_blocks, dtype=torch.int64, device=dev)
+    writers = [kvcs.KVWriter([c], wb.block_size, [k], [v], wb.slot_mapping, wb.positions,
+                             block_sums=sums)
+               for c, k, v in zip(wb.caches, wb.keys, wb.values)]
+    raw = stream.cuda_stream
+    tiny = torch.zeros(1, dtype=torch.int64, device=dev)
+    k = max(5, args.steps)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            for w in writers:
+                w(raw)
+            tiny.fill_(1)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(k)]
+        for a, b in ev:
+            torch.sum(scrub, dim=0, out=scrub_out)
+            a.record(stream)
+            for w in writers:
+                w(raw)
+            b.record(stream)
+        fl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(k)]
+        for a, b in fl:
+            torch.sum(scrub, dim=0, out=scrub_out)
+            a.record(stream)
+            tiny.fill_(1)
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    t_pass = sum(a.elapsed_time(b) for a, b in ev) / k / 1e3
+    t_floor = sum(a.elapsed_time(b) for a, b in fl) / k / 1e3
+    moved = 2 * wb.slot_mapping.numel() * 2 * wb.info["heads"] * wb.info["head_bytes"]
+    return {"calls": len(writers), "us_per_call": round(t_pass / len(writers) * 1e6, 3),
+            "gbs_per_call": round(moved / (t_pass / len(writers)) / 1e9, 2),
+            "pass_us": round(t_pass * 1e6, 2),
+            "isolated_event_floor_us": round(t_floor * 1e6, 3),
+            "what": "32 one-layer calls back to back after one L2 flush; floor: the one-layer "
+                    "line's event pattern around a one-element fill kernel"}
 
 
 def time_checksums(wl, args, dev, stream, ws, rank, steps, warmup, clocks=True) -> dict:
@@ -1013,7 +1074,7 @@ def main():
                     help="also time the first 1, 2, 4, ... requests alone")
     ap.add_argument("--layout", default="nhd",
                     choices=("nhd", "hnd", "hnd_sub4", "interleaved", "separate_kv", "xsplit",
-                             "misaligned"),
+                             "misaligned", "misaligned_hnd"),
                     help="re-lay-out the (NHD) workload's pools before timing")
     ap.add_argument("--columns", type=int, default=1,
                     help="replica-key columns (caches assigned round-robin)")

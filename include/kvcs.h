@@ -27,9 +27,11 @@
  * enqueues all work on the caller's stream; calls are asynchronous.  (Its
  * one piece of device memory of its own is the 128-byte scratch array of
  * kvcs_block_checksums_noalloc, part of the loaded module.)
- * Stream order: a call's kernels start only after the stream's earlier work
- * has finished.  The checksum kernels let a following kernel that was
- * launched with programmatic stream serialization start before they end;
+ * Stream order: a call's kernels touch memory only after the stream's
+ * earlier work has finished (kvcs_write_kv's kernel may be scheduled while
+ * the previous kernel ends, and waits for it before any access).  The
+ * checksum and write kernels let a following kernel that was launched with
+ * programmatic stream serialization start before they end;
  * as with any programmatic dependent launch, such a kernel must wait for
  * them (griddepcontrol.wait, cudaGridDependencySynchronize) before it reads
  * what they write.

@@ -469,6 +469,25 @@ cudaError_t launch(void (*kernel)(Params), dim3 grid, int threads, size_t smem, 
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// A write kernel, launched with programmatic stream serialization: it may be
+// scheduled while the stream's previous kernel ends, and waits
+// (griddepcontrol.wait) for all earlier work before it touches memory.  A
+// run of one-layer calls, as a forward pass issues them, then pays the
+// launch latency of each once, overlapped with the previous call.
+cudaError_t launch_write(void (*kernel)(WriteParams), unsigned grid, cudaStream_t st,
+                         const WriteParams &w) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(static_cast<unsigned>(kWriteThreads));
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, w);
+}
+
 // Shared body of kvcs_block_checksums and kvcs_group_checksums.
 int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block_size,
                   const kvcs_requests *reqs, int64_t total_positions,
@@ -860,13 +879,14 @@ int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_si
       const unsigned xgrid = static_cast<unsigned>(std::max<long long>(
           1, std::min<long long>((xbase * w.head_chunks + warps_per_cta - 1) / warps_per_cta,
                                  32LL * sms)));
+      cudaError_t e;
       if (fam == KVCS_LAYOUT_HND)
-        kvcs_write_kernel<kLayoutHND><<<grid, kWriteThreads, 0, st>>>(w);
+        e = launch_write(kvcs_write_kernel<kLayoutHND>, grid, st, w);
       else if (fam == KVCS_LAYOUT_XSPLIT)
-        kvcs_write_xsplit_kernel<<<xgrid, kWriteThreads, 0, st>>>(w);
+        e = launch_write(kvcs_write_xsplit_kernel, xgrid, st, w);
       else
-        kvcs_write_kernel<kLayoutNHD><<<grid, kWriteThreads, 0, st>>>(w);
-      if (cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
+        e = launch_write(kvcs_write_kernel<kLayoutNHD>, grid, st, w);
+      if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return KVCS_ECUDA;
       g_launches.fetch_add(1, std::memory_order_relaxed);
     }
   }

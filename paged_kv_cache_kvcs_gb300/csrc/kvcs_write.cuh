@@ -125,6 +125,10 @@ __device__ __forceinline__ u64 write_token_rows(const DevCache &C, const unsigne
 template <int kLayout>
 __global__ void __launch_bounds__(kWriteThreads, 2)
     kvcs_write_kernel(const __grid_constant__ WriteParams w) {
+  // launched with programmatic stream serialization: wait for the stream's
+  // earlier work before any access, then let the next kernel be scheduled
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (kWriteThreads / 32);
   const long long bs = w.block_size;
@@ -185,6 +189,8 @@ constexpr int kXTile = 16;  // pieces per tile row
 
 __global__ void __launch_bounds__(kWriteThreads, 2)
     kvcs_write_xsplit_kernel(const __grid_constant__ WriteParams w) {
+  ptx::grid_dep_wait();   // as kvcs_write_kernel
+  ptx::grid_dep_launch();
   // per warp: 32 tokens x (kXTile + 1) pieces; the pad spreads a column's
   // reads over the banks
   __shared__ uint4 tile[kWriteThreads / 32][32 * (kXTile + 1)];
