@@ -192,6 +192,8 @@ def work_share(wl, args) -> str:
     sms = (torch.cuda.get_device_properties(0).multi_processor_count
            if torch.cuda.is_available() else 152)
     plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions, num_sms=sms)
+    if plan["kernel"] == 1:
+        return "fixed (no bulk-copy launch: the direct-load kernel's warps own fixed ranges)"
     return ("dynamic (workspace)" if plan["dynamic"]
             else "fixed (workspace given; call below the dynamic threshold)")
 
@@ -911,6 +913,8 @@ def other_configs(args, dev, stream) -> dict:
         if not args.no_cpu_baseline:
             entry["cpu_baseline"], entry["parity"] = cpu_leg(wl, r, args.other_cpu_seconds,
                                                              args.seed)
+            entry["cpu_baseline"]["one_thread"] = oracle_one_thread(
+                wl, args.other_cpu_seconds / 2, args.seed)
         res[name] = entry
         del wl, r
     torch.cuda.empty_cache()
