@@ -58,12 +58,14 @@ cudaError_t device_setup(int *sms) {
   if (!d.done.load(std::memory_order_relaxed)) {
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    for (const void *fn : {reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamXSplit>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamState>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndSub>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRowsMis>)})
+    for (const void *fn : {reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows, false>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd, false>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamXSplit, false>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamState, false>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndSub, false>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRowsMis, false>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows, true>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd, true>)})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
@@ -609,14 +611,27 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
       const size_t smem = bulk_smem_bytes(p.stages, p.stage_bytes);
       const dim3 gd(static_cast<unsigned>(grid));
+      // Calls whose blocks are mostly partial (at most one block of a
+      // request is partial, so at most about two positions per request)
+      // pack many pages into a unit; they take the instances whose whole
+      // producer warp issues the copies and whose consumers reduce packed
+      // units at once.
+      const bool wide = p.pack && total_positions <= 2 * reqs->num_requests &&
+                        (l.family == kFamRows || l.family == kFamHnd);
       cudaError_t e;
       switch (l.family) {
-        case kFamHnd: e = launch(kvcs_bulk_kernel<kFamHnd>, gd, kBulkThreads, smem, st, after_zero, p); break;
-        case kFamXSplit: e = launch(kvcs_bulk_kernel<kFamXSplit>, gd, kBulkThreads, smem, st, after_zero, p); break;
-        case kFamState: e = launch(kvcs_bulk_kernel<kFamState>, gd, kBulkThreads, smem, st, after_zero, p); break;
-        case kFamHndSub: e = launch(kvcs_bulk_kernel<kFamHndSub>, gd, kBulkThreads, smem, st, after_zero, p); break;
-        case kFamRowsMis: e = launch(kvcs_bulk_kernel<kFamRowsMis>, gd, kBulkThreads, smem, st, after_zero, p); break;
-        default: e = launch(kvcs_bulk_kernel<kFamRows>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamHnd:
+          e = wide ? launch(kvcs_bulk_kernel<kFamHnd, true>, gd, kBulkThreads, smem, st, after_zero, p)
+                   : launch(kvcs_bulk_kernel<kFamHnd, false>, gd, kBulkThreads, smem, st, after_zero, p);
+          break;
+        case kFamXSplit: e = launch(kvcs_bulk_kernel<kFamXSplit, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamState: e = launch(kvcs_bulk_kernel<kFamState, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamHndSub: e = launch(kvcs_bulk_kernel<kFamHndSub, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamRowsMis: e = launch(kvcs_bulk_kernel<kFamRowsMis, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        default:
+          e = wide ? launch(kvcs_bulk_kernel<kFamRows, true>, gd, kBulkThreads, smem, st, after_zero, p)
+                   : launch(kvcs_bulk_kernel<kFamRows, false>, gd, kBulkThreads, smem, st, after_zero, p);
+          break;
       }
       if (e != cudaSuccess) return KVCS_ECUDA;
     } else if (l.kernel == kKernelDirect) {

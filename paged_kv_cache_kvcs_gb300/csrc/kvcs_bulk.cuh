@@ -338,6 +338,111 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
   return acc;
 }
 
+// This thread's share of a packed unit of several pages (launches whose
+// pages all look alike: same layout, heads and head bytes, one page per
+// (cache, half) from the unit's first on), for the rows and HND families.
+// What the pages share is worked out once: the thread's 16-byte columns
+// (rows family) or (head, column) groups (HND), their head and piece, and
+// the piece weight B of each half.  Per page only the cache's m0 and the
+// half change, so a page costs the running sums of its few valid rows and
+// one fold, m (B S + 2P T + 2U).  The sum is the one unit_sum gives page by
+// page, in another order.
+template <int kFam>
+__device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m,
+                                          const unsigned char *stage, int gtid, int nt,
+                                          u64 bsz) {
+  const DevCache &C0 = p.caches[m.cache];
+  const u64 P = static_cast<u64>(C0.P);
+  const u64 twoP = 2ull * P;
+  const u64 t0P = static_cast<u64>(m.q) * bsz * P;
+  const u64 hstep = 2ull * static_cast<u64>(C0.hb >> 3);  // B of the V half - B of the K half
+  const int H = C0.halves;
+  const int npg = m.npages;
+  u64 acc = 0;
+  if constexpr (kFam == kFamRows) {
+    const int rowb = C0.rowb;
+    const int cols = rowb >> 4;
+    const int nrows = m.count;
+    const u32 r0 = static_cast<u32>(m.first);
+    const size_t pstride = static_cast<size_t>(nrows) * rowb;
+    int col0, cstep, rl, rstep;
+    if (cols <= nt) {
+      rstep = nt / cols;
+      rl = gtid / cols;
+      col0 = gtid - rl * cols;
+      cstep = cols;
+      if (rl >= rstep) col0 = cols;
+    } else {
+      rstep = 1;
+      rl = 0;
+      col0 = gtid;
+      cstep = nt;
+    }
+    const size_t step = static_cast<size_t>(rstep) * rowb;
+    for (int col = col0; col < cols; col += cstep) {
+      int h_col, p_col;
+      if (C0.layout == kLayoutNHD) {
+        const int cb = col << 4;
+        h_col = C0.hb_shift >= 0 ? (cb >> C0.hb_shift) : cb / C0.hb;
+        p_col = (cb - h_col * C0.hb) >> 3;
+      } else {
+        h_col = 0;
+        p_col = col << 1;
+      }
+      const u64 mh_off = 2ull * static_cast<u64>(h_col);
+      const u64 B0 = 2ull * (t0P + static_cast<u64>(p_col)) + 1ull;
+      const unsigned char *sp0 = stage + static_cast<size_t>(rl) * rowb + (col << 4);
+      int ci = m.cache, half = m.half;
+      for (int k = 0; k < npg; ++k) {
+        u64 S = 0, T = 0, U = 0;
+        const unsigned char *sp = sp0 + static_cast<size_t>(k) * pstride;
+        for (int r = rl; r < nrows; r += rstep, sp += step) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(sp);
+          const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
+          const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
+          const u64 X = x0 + x1;
+          S += X;
+          U += x1;
+          T += static_cast<u64>(r0 + static_cast<u32>(r)) * X;
+        }
+        const u64 B = half ? B0 + hstep : B0;
+        acc += (p.caches[ci].m0 + mh_off) * (B * S + twoP * T + 2ull * U);
+        if (++half == H) {
+          half = 0;
+          ++ci;
+        }
+      }
+    }
+  } else {
+    // HND: each page staged as its heads one after another, nv slots each
+    const int nv = m.nv;
+    const int hb = C0.hb;
+    const int cpr = hb >> 4;
+    const int groups = m.count * cpr;
+    const size_t pstride = static_cast<size_t>(m.count) * nv * hb;
+    for (int g = gtid; g < groups; g += nt) {
+      const int hl = g / cpr;
+      const int col = g - hl * cpr;
+      const u64 mh_off = 2ull * static_cast<u64>(m.first + hl);
+      const u64 B0 = 2ull * (t0P + static_cast<u64>(col << 1)) + 1ull;
+      const unsigned char *gp0 = stage + static_cast<size_t>(hl) * nv * hb + (col << 4);
+      int ci = m.cache, half = m.half;
+      for (int k = 0; k < npg; ++k) {
+        u64 S = 0, T = 0, U = 0;
+        accum_slots(gp0 + static_cast<size_t>(k) * pstride, static_cast<size_t>(hb), 0, nv, 0,
+                    S, T, U);
+        const u64 B = half ? B0 + hstep : B0;
+        acc += (p.caches[ci].m0 + mh_off) * (B * S + twoP * T + 2ull * U);
+        if (++half == H) {
+          half = 0;
+          ++ci;
+        }
+      }
+    }
+  }
+  return acc;
+}
+
 // Pages of one position a stage holds in packed launches (every page alike,
 // each a unit): the host's count for full pages; for a partial block of the
 // row and HND families, as many pages as their valid bytes allow; a skipped
@@ -413,8 +518,13 @@ __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
 // Every wait is bounded; a wait that runs out sets KVCS_STATUS_TIMEOUT and
 // the kernel returns without hanging.
 //
-// kFam is the layout family of every cache in the launch.
-template <int kFam>
+// kFam is the layout family of every cache in the launch.  kWide (rows and
+// HND families, for calls whose blocks are mostly partial, such as the
+// newest block of each request) keeps the whole producer warp in the loop:
+// every lane computes the same cursor, lane 0 alone waits, writes metadata
+// and counters, and the lanes share out the copies of a unit's pages; the
+// consumers then reduce packed units of several pages with packed_sum.
+template <int kFam, bool kWide>
 __global__ void __launch_bounds__(kBulkThreads, 1)
     kvcs_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -453,20 +563,22 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     // ------------------------------ producer ------------------------------
     // The whole warp looks up the request of the range's first position (one
     // round of loads for up to 31 requests), with that position's block ids
-    // loaded alongside; lane 0 then runs the producer alone.
+    // loaded alongside; lane 0 then runs the producer alone (kWide: the
+    // warp runs it, lane 0 leading).
     ReqCursor rc;
     rc.r = -1;
     long long b_cur = 0, b_next = 0;
     if (u_begin < u_end) {
       const long long pos0 = u_begin / p.units_per_pos;
-      if (tid == 0) {
+      if (kWide || tid == 0) {
         b_cur = p.block_ids[pos0];
         b_next = pos0 + 1 < p.total_positions ? p.block_ids[pos0 + 1] : 0;
       }
       rc = req_find_warp(p, pos0, tid);
     }
-    if (tid != 0) return;
-    if (g == 0 && p.num_requests >= 0) {
+    if (!kWide && tid != 0) return;
+    const bool lead = !kWide || tid == 0;
+    if (lead && g == 0 && p.num_requests >= 0) {
       if (p.pos_offsets[0] != 0 || p.pos_offsets[p.num_requests] != p.total_positions)
         set_status(p, kStatusBadRequests);
     }
@@ -578,20 +690,27 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             if constexpr (kFam == kFamRowsMis) npg = min(npg, kMisMaxPages);
           }
           if (pbytes > 0) {
-            if (!ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]), (f & 1u) ^ 1u,
-                                        p.timeout_ns)) {
-              set_status(p, kStatusTimeout);
+            bool free_stage = true;
+            if (lead)
+              free_stage = ptx::mbar_wait_bounded(ptx::smem_addr(&hdr->empty[s]),
+                                                  (f & 1u) ^ 1u, p.timeout_ns);
+            if constexpr (kWide) free_stage = __shfl_sync(0xffffffffu, free_stage, 0);
+            if (!free_stage) {
+              if (lead) set_status(p, kStatusTimeout);
               aborted = true;
               break;
             }
             if (n_emit == 0) {
               slot = static_cast<int>(seq % kRingSlots);
               ++seq;
-              hdr->ring_acc[slot] = 0ull;
-              hdr->ring_cnt[slot] = 0u;
+              if (lead) {
+                hdr->ring_acc[slot] = 0ull;
+                hdr->ring_cnt[slot] = 0u;
+              }
             }
             const u32 fb = ptx::smem_addr(&hdr->full[s]);
             if constexpr (kFam == kFamRowsMis) {
+              static_assert(!kWide, "the misaligned-rows instance has one producer lane");
               // Per page: the 16-byte-aligned interior of its rows by bulk copy,
               // and when the page starts 8 bytes past a boundary its first and
               // last words by 8-byte cp.async, tracked on the same barrier.
@@ -626,9 +745,48 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               if (dmask) ptx::cp_async_mbar_arrive(fb);
               ptx::mbar_arrive_expect_tx(fb, tx);
             } else {
-            store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
-                       mode, slot, npg);
-            ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
+            if (lead) {
+              store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
+                         mode, slot, npg);
+              ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
+            }
+            if constexpr (kWide) {
+              // the lanes share the unit's copies: copy idx is page k2 (or,
+              // for a partial HND block, head h of page k2), issued by lane
+              // idx mod 32 once lane 0 has set the stage's byte count
+              __syncwarp();
+              const u32 dst0 = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
+              const int H0 = C.halves;
+              const int cpp = (kFam == kFamHnd && cur.nv != bs) ? count : 1;
+              for (int idx = tid; idx < npg * cpp; idx += 32) {
+                const int k2 = cpp == 1 ? idx : idx / cpp;
+                const int h = idx - k2 * cpp;
+                int pci = ci, phalf = half;
+                if (k2 > 0) {  // packed pages: every cache has H0 halves
+                  const int flat = ci * H0 + half + k2;
+                  pci = H0 == 1 ? flat : flat >> 1;
+                  phalf = flat - pci * H0;
+                }
+                const DevCache &D = p.caches[pci];
+                const unsigned char *page = D.base +
+                    static_cast<long long>(phalf) * D.half_stride + cur.block * D.block_stride;
+                const u32 dst = dst0 + static_cast<u32>(k2) * pstride;
+                if constexpr (kFam == kFamHnd) {
+                  const unsigned char *src = page + static_cast<u64>(first) * bs * D.hb;
+                  if (cur.nv == bs) {
+                    ptx::bulk_g2s(dst, src, pstride, fb, policy);
+                  } else {
+                    const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(D.hb);
+                    ptx::bulk_g2s(dst + static_cast<u32>(h) * run,
+                                  src + static_cast<u64>(h) * bs * D.hb, run, fb, policy);
+                  }
+                } else {
+                  static_assert(!kWide || kFam == kFamRows, "wide producer: rows or HND");
+                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes, fb,
+                                policy);
+                }
+              }
+            } else {
             u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
             int pci = ci, phalf = half;
             for (int k2 = 0; k2 < npg; ++k2) {
@@ -681,6 +839,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               }
             }
             }
+            }
             ++it;
             ++n_emit;
             if (++s == NS) {
@@ -715,12 +874,16 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
           if (pos_done || u == rb || p.caches[ci].column != col) {
             // close the (position, column): this thread's share of the count
             if (n_emit > 0) {
-              const u32 delta = 0u - static_cast<u32>(p.group_warps) * n_emit;
-              const u32 prev = atomicAdd(&hdr->ring_cnt[slot], delta);
-              if (prev + delta == 0u) finalize_slot(p, hdr, slot, dst_word, mode);
+              if (lead) {
+                const u32 delta = 0u - static_cast<u32>(p.group_warps) * n_emit;
+                const u32 prev = atomicAdd(&hdr->ring_cnt[slot], delta);
+                if (prev + delta == 0u) finalize_slot(p, hdr, slot, dst_word, mode);
+              }
             } else if (cur.whole && !p.all_atomic) {
-              ptx::grid_dep_wait();
-              p.out[dst_word] = 0ull;
+              if (lead) {
+                ptx::grid_dep_wait();
+                p.out[dst_word] = 0ull;
+              }
             }
             n_emit = 0;
           }
@@ -741,20 +904,23 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       if (!claimed) {
         // the counter is zeroed by the kernel launched before this one
         ptx::grid_dep_wait();
-        next_chunk = atomicAdd(p.work, 1ull);
+        if (lead) next_chunk = atomicAdd(p.work, 1ull);
+        if constexpr (kWide) next_chunk = __shfl_sync(0xffffffffu, next_chunk, 0);
         claimed = true;
       }
       const long long ca = p.pool_start + static_cast<long long>(next_chunk) * p.chunk_units;
       if (ca >= p.total_units) break;
       ra = ca;
       rb = min(p.total_units, ca + p.chunk_units);
-      next_chunk = atomicAdd(p.work, 1ull);
+      if (lead) next_chunk = atomicAdd(p.work, 1ull);
+      if constexpr (kWide) next_chunk = __shfl_sync(0xffffffffu, next_chunk, 0);
       first_range = false;
     }
     // Every copy of this CTA is issued: a following kernel launched with
     // programmatic stream serialization may start (it waits for this grid
     // before it touches anything this grid writes).
     ptx::grid_dep_launch();
+    if (!lead) return;
     if (!aborted) {
       // one end-of-stream marker per consumer group
       for (int k = 0; k < p.groups; ++k) {
@@ -812,7 +978,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     const unsigned char *sp = stages + static_cast<size_t>(s) * SB;
     int ci = m.cache, half = m.half;
     u64 v = 0;
-    for (int k = 0; k < m.npages; ++k) {
+    bool packed = false;
+    if constexpr (kWide) {
+      if (m.npages > 1) {
+        v = packed_sum<kFam>(p, m, sp, gtid, gw * 32, bsz);
+        packed = true;
+      }
+    }
+    for (int k = 0; !packed && k < m.npages; ++k) {
       const DevCache &C = p.caches[ci];
       if (C.rowb != map.rowb) make_map(map, C.rowb, gtid, gw * 32);
       if constexpr (kFam == kFamRowsMis) {

@@ -15,11 +15,20 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _check_all(wl):
+def _check_all(wl, workspace=False):
     """Library output of one call over ``wl`` equals the oracle at every
-    position; returns the output."""
+    position; returns the output.  With ``workspace`` the call passes one
+    (the benchmark's launch configuration: the dynamic share-out)."""
     from gpu_helpers import gpu_checksums, oracle_every_position
-    got, st = gpu_checksums(wl)
+    if workspace:
+        ws = torch.zeros(K.KVCS_WORKSPACE_WORDS, dtype=torch.int64, device=DEV)
+        out = torch.empty(wl.num_positions, dtype=torch.int64, device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        K.workload_checksummer(wl, workspace=ws)(out, status)
+        torch.cuda.synchronize()
+        got, st = out.cpu().numpy().view(np.uint64), int(status.item())
+    else:
+        got, st = gpu_checksums(wl)
     assert st == 0
     exp, est = oracle_every_position(wl)
     assert est == 0
@@ -39,6 +48,29 @@ def test_llama3_8b_full():
     assert plan["kernel"] == 0 and plan["launches"] == 1
     got = _check_all(wl)
     assert np.count_nonzero(got) == got.size
+    del wl
+    _free()
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_llama3_8b_full_other_seeds(seed):
+    """The 8B-shaped workload's other two seeds (other lengths, block ids and
+    values), in the benchmark's launch configuration."""
+    wl = W.llama3_8b(seed, DEV)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert K.plan_for(wl.caches, wl.block_size, wl.num_positions, num_sms=sms)["dynamic"] == 1
+    got = _check_all(wl, workspace=True)
+    assert np.count_nonzero(got) == got.size
+    del wl
+    _free()
+
+
+@pytest.mark.parametrize("name", ["mla", "llama3_70b"])
+def test_dynamic_share_out_full(name):
+    """MLA and 70B at full size as the benchmark times them (with a
+    workspace: the dynamic share-out), every position against the oracle."""
+    wl = W.mla(0, DEV) if name == "mla" else W.llama3_70b(0, DEV)
+    _check_all(wl, workspace=True)
     del wl
     _free()
 
