@@ -604,20 +604,24 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
           kMinChunkUnits, pool / (static_cast<long long>(pl.bulk_grid) * kChunksPerCta));
     }
     if (l.kernel == kKernelBulk) {
+      // Calls whose blocks are mostly partial (at most one block of a
+      // request is partial, so at most about two positions per request)
+      // pack many pages into a unit; they take the instances whose whole
+      // producer warp issues the copies and whose consumers reduce packed
+      // units at once.  Their page-address table takes shared memory from
+      // the ring (one stage less where the ring fills it).
+      const bool wide = p.pack && total_positions <= 2 * reqs->num_requests &&
+                        (l.family == kFamRows || l.family == kFamHnd);
+      if (wide)
+        p.stages = std::min(p.stages,
+                            (kSmemLimit - kHeaderBytes - kWideTableBytes) / p.stage_bytes);
       p.split = pl.split;
       p.group_warps = group_warps_for(p.stages);
       p.groups = kConsumerWarps / p.group_warps;
       long long grid = pl.bulk_grid;
       if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
-      const size_t smem = bulk_smem_bytes(p.stages, p.stage_bytes);
+      const size_t smem = bulk_smem_bytes(p.stages, p.stage_bytes) + (wide ? kWideTableBytes : 0);
       const dim3 gd(static_cast<unsigned>(grid));
-      // Calls whose blocks are mostly partial (at most one block of a
-      // request is partial, so at most about two positions per request)
-      // pack many pages into a unit; they take the instances whose whole
-      // producer warp issues the copies and whose consumers reduce packed
-      // units at once.
-      const bool wide = p.pack && total_positions <= 2 * reqs->num_requests &&
-                        (l.family == kFamRows || l.family == kFamHnd);
       cudaError_t e;
       switch (l.family) {
         case kFamHnd:

@@ -529,7 +529,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     kvcs_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   SmemHeader *hdr = reinterpret_cast<SmemHeader *>(smem);
-  unsigned char *stages = smem + kHeaderBytes;
+  unsigned char *stages = smem + kHeaderBytes + (kWide ? kWideTableBytes : 0);
+  PageAddr *tab = reinterpret_cast<PageAddr *>(smem + kHeaderBytes);
   const int NS = p.stages;
   const int SB = p.stage_bytes;
 
@@ -540,6 +541,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       ptx::mbar_init(ptx::smem_addr(&hdr->empty[s]), p.group_warps);
     }
     ptx::fence_barrier_init();
+  }
+  if constexpr (kWide) {
+    for (int i = tid; i < p.num_caches; i += kBulkThreads)
+      tab[i] = PageAddr{p.caches[i].base, p.caches[i].half_stride, p.caches[i].block_stride};
   }
   __syncthreads();
 
@@ -767,22 +772,24 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                   pci = H0 == 1 ? flat : flat >> 1;
                   phalf = flat - pci * H0;
                 }
-                const DevCache &D = p.caches[pci];
+                // (packed pages share their geometry: C's hb and rowb hold for
+                // every page; only the addressing differs)
+                const PageAddr D = tab[pci];
                 const unsigned char *page = D.base +
                     static_cast<long long>(phalf) * D.half_stride + cur.block * D.block_stride;
                 const u32 dst = dst0 + static_cast<u32>(k2) * pstride;
                 if constexpr (kFam == kFamHnd) {
-                  const unsigned char *src = page + static_cast<u64>(first) * bs * D.hb;
+                  const unsigned char *src = page + static_cast<u64>(first) * bs * C.hb;
                   if (cur.nv == bs) {
                     ptx::bulk_g2s(dst, src, pstride, fb, policy);
                   } else {
-                    const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(D.hb);
+                    const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(C.hb);
                     ptx::bulk_g2s(dst + static_cast<u32>(h) * run,
-                                  src + static_cast<u64>(h) * bs * D.hb, run, fb, policy);
+                                  src + static_cast<u64>(h) * bs * C.hb, run, fb, policy);
                   }
                 } else {
                   static_assert(!kWide || kFam == kFamRows, "wide producer: rows or HND");
-                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * D.rowb, pbytes, fb,
+                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * C.rowb, pbytes, fb,
                                 policy);
                 }
               }

@@ -170,6 +170,19 @@ struct SmemHeader {
 };
 constexpr int kHeaderBytes = (static_cast<int>(sizeof(SmemHeader)) + 127) / 128 * 128;
 
+// The page addressing of a launch's caches, copied into shared memory by the
+// wide bulk instances (after the header, before the stages): their producer
+// lanes each address a different cache's page, and shared memory serves
+// such reads at once where the parameter space would take them one address
+// at a time.
+struct PageAddr {
+  const unsigned char *base;
+  long long half_stride;
+  long long block_stride;
+};
+constexpr int kWideTableBytes =
+    (kMaxCachesPerLaunch * static_cast<int>(sizeof(PageAddr)) + 127) / 128 * 128;
+
 __device__ __forceinline__ void set_status(const Params &p, u32 bit) {
   if (p.status) atomicOr(p.status, bit);
 }
