@@ -348,7 +348,7 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
 // one fold, m (B S + 2P T + 2U).  The sum is the one unit_sum gives page by
 // page, in another order.
 template <int kFam>
-__device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m,
+__device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m, int first,
                                           const unsigned char *stage, int gtid, int nt,
                                           u64 bsz) {
   const DevCache &C0 = p.caches[m.cache];
@@ -363,7 +363,7 @@ __device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m,
     const int rowb = C0.rowb;
     const int cols = rowb >> 4;
     const int nrows = m.count;
-    const u32 r0 = static_cast<u32>(m.first);
+    const u32 r0 = static_cast<u32>(first);
     const size_t pstride = static_cast<size_t>(nrows) * rowb;
     int col0, cstep, rl, rstep;
     if (cols <= nt) {
@@ -423,7 +423,7 @@ __device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m,
     for (int g = gtid; g < groups; g += nt) {
       const int hl = g / cpr;
       const int col = g - hl * cpr;
-      const u64 mh_off = 2ull * static_cast<u64>(m.first + hl);
+      const u64 mh_off = 2ull * static_cast<u64>(first + hl);
       const u64 B0 = 2ull * (t0P + static_cast<u64>(col << 1)) + 1ull;
       const unsigned char *gp0 = stage + static_cast<size_t>(hl) * nv * hb + (col << 4);
       int ci = m.cache, half = m.half;
@@ -441,6 +441,56 @@ __device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m,
     }
   }
   return acc;
+}
+
+// The consumer group's fetch of a unit whose pages it reads itself (the wide
+// HND instance, partial blocks of several heads): each page's valid rows
+// (rows family; not used at present) or each head's nv valid slots (HND)
+// by 16-byte cp.async, into the same compact layout the producer's bulk
+// copies give, the group's threads taking consecutive 16-byte chunks.  `block` is the position's physical block;
+// pages are (cache, half) from the unit's first on.
+template <int kFam>
+__device__ __forceinline__ void gather_unit(const Params &p, const UnitMeta &m,
+                                            const PageAddr *tab, u32 stage, int gtid, int nt,
+                                            long long bs) {
+  const DevCache &C0 = p.caches[m.cache];
+  const long long block = static_cast<long long>(static_cast<u32>(m.first));
+  const int H = C0.halves;
+  int ci = m.cache, half = m.half;
+  u32 dst = stage;
+  if constexpr (kFam == kFamRows) {
+    const u32 cpg = static_cast<u32>(m.count) * static_cast<u32>(C0.rowb) >> 4;
+    for (int k = 0; k < m.npages; ++k) {
+      const PageAddr a = tab[ci];
+      const unsigned char *src = a.base + static_cast<long long>(half) * a.half_stride +
+                                 block * a.block_stride;
+      for (u32 j = static_cast<u32>(gtid); j < cpg; j += static_cast<u32>(nt))
+        ptx::cp_async16(dst + (j << 4), src + (static_cast<size_t>(j) << 4));
+      dst += cpg << 4;
+      if (++half == H) {
+        half = 0;
+        ++ci;
+      }
+    }
+  } else {
+    const u32 cph = static_cast<u32>(m.nv) * static_cast<u32>(C0.hb) >> 4;  // chunks a head
+    const u32 cpg = static_cast<u32>(m.count) * cph;
+    const size_t hstride = static_cast<size_t>(bs) * C0.hb;                  // a head's slots
+    for (int k = 0; k < m.npages; ++k) {
+      const PageAddr a = tab[ci];
+      const unsigned char *src = a.base + static_cast<long long>(half) * a.half_stride +
+                                 block * a.block_stride;
+      for (u32 j = static_cast<u32>(gtid); j < cpg; j += static_cast<u32>(nt)) {
+        const u32 h = j / cph;
+        ptx::cp_async16(dst + (j << 4), src + h * hstride + (static_cast<size_t>(j - h * cph) << 4));
+      }
+      dst += cpg << 4;
+      if (++half == H) {
+        half = 0;
+        ++ci;
+      }
+    }
+  }
 }
 
 // Pages of one position a stage holds in packed launches (every page alike,
@@ -530,7 +580,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   SmemHeader *hdr = reinterpret_cast<SmemHeader *>(smem);
   unsigned char *stages = smem + kHeaderBytes + (kWide ? kWideTableBytes : 0);
-  PageAddr *tab = reinterpret_cast<PageAddr *>(smem + kHeaderBytes);
+  WideTable *wt = reinterpret_cast<WideTable *>(smem + kHeaderBytes);
   const int NS = p.stages;
   const int SB = p.stage_bytes;
 
@@ -544,7 +594,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
   }
   if constexpr (kWide) {
     for (int i = tid; i < p.num_caches; i += kBulkThreads)
-      tab[i] = PageAddr{p.caches[i].base, p.caches[i].half_stride, p.caches[i].block_stride};
+      wt->page[i] = PageAddr{p.caches[i].base, p.caches[i].half_stride,
+                             p.caches[i].block_stride};
+    if (kFam == kFamHnd && tid == 0) {
+      for (int s = 0; s < NS; ++s)
+        ptx::mbar_init(ptx::smem_addr(&wt->landed[s]), p.group_warps * 32);
+      ptx::fence_barrier_init();
+    }
   }
   __syncthreads();
 
@@ -595,6 +651,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     u32 it = 0;         // units emitted
     u32 seq = 0;        // positions that got an accumulator slot
     bool aborted = false;
+    u32 gpar = 0;       // wide: parity of each stage's next landed phase
     // Ranges of units: this CTA's fixed share, then, with a work counter,
     // chunks taken from it until the pool is used up.  After the first
     // chunk the next one is claimed a range ahead, so the atomic's latency
@@ -750,12 +807,28 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               if (dmask) ptx::cp_async_mbar_arrive(fb);
               ptx::mbar_arrive_expect_tx(fb, tx);
             } else {
+            // wide HND instance: a unit of partial pages of several heads is
+            // fetched by its consumer group, since each head's run of valid
+            // slots would cost a bulk copy of its own (measured: 915 -> 1840
+            // GB/s on one-token blocks; for rows, one contiguous run a page,
+            // the bulk copies are faster: 3265 against 2530)
+            const bool gather = kWide && kFam == kFamHnd && cur.nv != bs && C.heads > 1;
             if (lead) {
-              store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
-                         mode, slot, npg);
-              ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
+              if (gather) {
+                const int par = static_cast<int>((gpar >> s) & 1u);
+                store_meta(&hdr->meta[s], dst_word, cur.q, ci, half,
+                           static_cast<int>(cur.block), count, cur.nv,
+                           mode | kModeGather | (par ? kModeLandedParity : 0), slot, npg);
+                ptx::mbar_arrive(fb);
+              } else {
+                store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
+                           mode, slot, npg);
+                ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
+              }
             }
-            if constexpr (kWide) {
+            if (gather) {
+              gpar ^= 1u << s;
+            } else if constexpr (kWide) {
               // the lanes share the unit's copies: copy idx is page k2 (or,
               // for a partial HND block, head h of page k2), issued by lane
               // idx mod 32 once lane 0 has set the stage's byte count
@@ -774,7 +847,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                 }
                 // (packed pages share their geometry: C's hb and rowb hold for
                 // every page; only the addressing differs)
-                const PageAddr D = tab[pci];
+                const PageAddr D = wt->page[pci];
                 const unsigned char *page = D.base +
                     static_cast<long long>(phalf) * D.half_stride + cur.block * D.block_stride;
                 const u32 dst = dst0 + static_cast<u32>(k2) * pstride;
@@ -986,9 +1059,30 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     int ci = m.cache, half = m.half;
     u64 v = 0;
     bool packed = false;
-    if constexpr (kWide) {
+    if constexpr (kWide && kFam == kFamHnd) {
+      if (m.mode & kModeGather) {
+        // fetch the unit's valid bytes, then wait (bounded) until every
+        // thread's copies of the group have landed
+        const u32 lb = ptx::smem_addr(&wt->landed[s]);
+        gather_unit<kFam>(p, m, wt->page, ptx::smem_addr(sp), gtid, gw * 32,
+                          static_cast<long long>(bsz));
+        ptx::cp_async_mbar_arrive_noinc(lb);
+        const bool landed =
+            ptx::mbar_wait_bounded(lb, (m.mode & kModeLandedParity) ? 1u : 0u, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, landed)) {
+          ptx::cp_async_wait_all();
+          if (lane == 0) set_status(p, kStatusTimeout);
+          return;
+        }
+        v = packed_sum<kFam>(p, m, 0, sp, gtid, gw * 32, bsz);
+        packed = true;
+      } else if (m.npages > 1) {
+        v = packed_sum<kFam>(p, m, m.first, sp, gtid, gw * 32, bsz);
+        packed = true;
+      }
+    } else if constexpr (kWide) {
       if (m.npages > 1) {
-        v = packed_sum<kFam>(p, m, sp, gtid, gw * 32, bsz);
+        v = packed_sum<kFam>(p, m, m.first, sp, gtid, gw * 32, bsz);
         packed = true;
       }
     }

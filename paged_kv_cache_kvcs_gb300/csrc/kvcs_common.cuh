@@ -174,14 +174,25 @@ constexpr int kHeaderBytes = (static_cast<int>(sizeof(SmemHeader)) + 127) / 128 
 // wide bulk instances (after the header, before the stages): their producer
 // lanes each address a different cache's page, and shared memory serves
 // such reads at once where the parameter space would take them one address
-// at a time.
+// at a time.  After it, one "landed" mbarrier per stage for the units the
+// consumers fetch themselves.
 struct PageAddr {
   const unsigned char *base;
   long long half_stride;
   long long block_stride;
 };
-constexpr int kWideTableBytes =
-    (kMaxCachesPerLaunch * static_cast<int>(sizeof(PageAddr)) + 127) / 128 * 128;
+struct WideTable {
+  PageAddr page[kMaxCachesPerLaunch];
+  u64 landed[kMaxStages];
+};
+constexpr int kWideTableBytes = (static_cast<int>(sizeof(WideTable)) + 127) / 128 * 128;
+
+// UnitMeta.mode in the wide instances: bit 1 marks a unit whose pages the
+// consumer group fetches itself (its `first` field then holds the block id,
+// the unit's pages starting at row or head 0), bit 2 the parity of that
+// fill's phase of the stage's landed barrier.
+constexpr int kModeGather = 2;
+constexpr int kModeLandedParity = 4;
 
 __device__ __forceinline__ void set_status(const Params &p, u32 bit) {
   if (p.status) atomicOr(p.status, bit);
