@@ -393,6 +393,8 @@ __device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m, in
       const u64 B0 = 2ull * (t0P + static_cast<u64>(p_col)) + 1ull;
       const unsigned char *sp0 = stage + static_cast<size_t>(rl) * rowb + (col << 4);
       int ci = m.cache, half = m.half;
+      // pages are independent: let the compiler overlap several
+#pragma unroll 4
       for (int k = 0; k < npg; ++k) {
         u64 S = 0, T = 0, U = 0;
         const unsigned char *sp = sp0 + static_cast<size_t>(k) * pstride;
@@ -427,6 +429,8 @@ __device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m, in
       const u64 B0 = 2ull * (t0P + static_cast<u64>(col << 1)) + 1ull;
       const unsigned char *gp0 = stage + static_cast<size_t>(hl) * nv * hb + (col << 4);
       int ci = m.cache, half = m.half;
+      // pages are independent: let the compiler overlap several
+#pragma unroll 4
       for (int k = 0; k < npg; ++k) {
         u64 S = 0, T = 0, U = 0;
         accum_slots(gp0 + static_cast<size_t>(k) * pstride, static_cast<size_t>(hb), 0, nv, 0,
@@ -476,13 +480,23 @@ __device__ __forceinline__ void gather_unit(const Params &p, const UnitMeta &m,
     const u32 cph = static_cast<u32>(m.nv) * static_cast<u32>(C0.hb) >> 4;  // chunks a head
     const u32 cpg = static_cast<u32>(m.count) * cph;
     const size_t hstride = static_cast<size_t>(bs) * C0.hb;                  // a head's slots
+    // this thread's chunks j = gtid + i nt of a page, as (head, chunk in the
+    // head's run), stepped without a division per chunk
+    const u32 h0 = static_cast<u32>(gtid) / cph, c0 = static_cast<u32>(gtid) - h0 * cph;
+    const u32 dh = static_cast<u32>(nt) / cph, dc = static_cast<u32>(nt) - dh * cph;
     for (int k = 0; k < m.npages; ++k) {
       const PageAddr a = tab[ci];
       const unsigned char *src = a.base + static_cast<long long>(half) * a.half_stride +
                                  block * a.block_stride;
+      u32 h = h0, c = c0;
       for (u32 j = static_cast<u32>(gtid); j < cpg; j += static_cast<u32>(nt)) {
-        const u32 h = j / cph;
-        ptx::cp_async16(dst + (j << 4), src + h * hstride + (static_cast<size_t>(j - h * cph) << 4));
+        ptx::cp_async16(dst + (j << 4), src + h * hstride + (static_cast<size_t>(c) << 4));
+        h += dh;
+        c += dc;
+        if (c >= cph) {
+          c -= cph;
+          ++h;
+        }
       }
       dst += cpg << 4;
       if (++half == H) {
