@@ -64,6 +64,7 @@ cudaError_t device_setup(int *sms) {
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamState, false>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndSub, false>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRowsMis, false>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndMis, false>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows, true>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd, true>)})
       if (e == cudaSuccess)
@@ -96,13 +97,27 @@ bool rows_misaligned(const kvcs_cache &c) {
   return reinterpret_cast<uintptr_t>(c.base) % 16 || c.half_stride % 16 || c.block_stride % 16;
 }
 
+// HND caches without kernel sub-blocks whose pages may start 8 bytes past a
+// 16-byte boundary: a unit's heads, all slots of them, are one contiguous
+// run, staged as misaligned rows are.
+bool hnd_misaligned(const kvcs_cache &c, int block_size) {
+  if (c.layout != KVCS_LAYOUT_HND) return false;
+  if (c.kernel_block_size > 0 && c.kernel_block_size != block_size) return false;
+  return reinterpret_cast<uintptr_t>(c.base) % 16 || c.half_stride % 16 || c.block_stride % 16;
+}
+
+// Pages of the cache staged with the misaligned split (rows or HND heads).
+bool staged_misaligned(const kvcs_cache &c, int block_size) {
+  return rows_misaligned(c) || hnd_misaligned(c, block_size);
+}
+
 // The bulk kernel stages whole rows (NHD, latent, state) or whole heads
 // (HND, x-split) with 16-byte-aligned bulk copies and reads 16-byte columns;
 // NHD and latent pages 8 bytes off a 16-byte boundary too, their edge words
 // by 8-byte asynchronous copies.
 bool bulk_eligible(const kvcs_cache &c, int block_size) {
   if (c.head_bytes % 16) return false;
-  if (!rows_misaligned(c) &&
+  if (!staged_misaligned(c, block_size) &&
       (reinterpret_cast<uintptr_t>(c.base) % 16 || c.half_stride % 16 || c.block_stride % 16))
     return false;
   const long long hb = c.head_bytes;
@@ -240,7 +255,8 @@ DevCache make_dev_cache(const kvcs_cache &c, int block_size) {
 // Largest unit of one cache, in bytes of stage.
 long long unit_bytes(const kvcs_cache &c, const DevCache &d, int block_size) {
   if (d.layout == KVCS_LAYOUT_HND || d.layout == KVCS_LAYOUT_XSPLIT)
-    return static_cast<long long>(d.rpu) * block_size * d.hb;
+    return static_cast<long long>(d.rpu) * block_size * d.hb +
+           (hnd_misaligned(c, block_size) ? kMisPad : 0);
   return static_cast<long long>(d.rpu) * d.rowb + (rows_misaligned(c) ? kMisPad : 0);
 }
 
@@ -281,10 +297,11 @@ LaunchShape launch_shape(const kvcs_cache *caches, int lo, int hi, int block_siz
     const long long page = static_cast<long long>(d0.page_bytes);
     long long ppu = std::max<long long>(
         1, std::min<long long>(ls.pages_per_pos, kUnitTargetBytes / page));
-    if (rows_misaligned(caches[lo])) ppu = std::min<long long>(ppu, kMisMaxPages);
+    const bool mis = staged_misaligned(caches[lo], block_size);
+    if (mis) ppu = std::min<long long>(ppu, kMisMaxPages);
     ls.pack = 1;
     ls.full_pages = static_cast<int>(ppu);
-    biggest = std::max(biggest, ppu * (page + (rows_misaligned(caches[lo]) ? kMisPad : 0)));
+    biggest = std::max(biggest, ppu * (page + (mis ? kMisPad : 0)));
   }
   ls.stage_bytes = static_cast<int>((biggest + 127) / 128 * 128);
   ls.stages = std::min(kMaxStages, (kSmemLimit - kHeaderBytes) / ls.stage_bytes);
@@ -304,7 +321,8 @@ int family_of(const kvcs_cache &c, int block_size) {
   switch (c.layout) {
     case KVCS_LAYOUT_HND:
       return c.kernel_block_size > 0 && c.kernel_block_size != block_size ? kFamHndSub
-                                                                          : kFamHnd;
+             : hnd_misaligned(c, block_size)                               ? kFamHndMis
+                                                                           : kFamHnd;
     case KVCS_LAYOUT_XSPLIT: return kFamXSplit;
     case KVCS_LAYOUT_STATE: return kFamState;
     default: return rows_misaligned(c) ? kFamRowsMis : kFamRows;
@@ -632,6 +650,7 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
         case kFamState: e = launch(kvcs_bulk_kernel<kFamState, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
         case kFamHndSub: e = launch(kvcs_bulk_kernel<kFamHndSub, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
         case kFamRowsMis: e = launch(kvcs_bulk_kernel<kFamRowsMis, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamHndMis: e = launch(kvcs_bulk_kernel<kFamHndMis, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
         default:
           e = wide ? launch(kvcs_bulk_kernel<kFamRows, true>, gd, kBulkThreads, smem, st, after_zero, p)
                    : launch(kvcs_bulk_kernel<kFamRows, false>, gd, kBulkThreads, smem, st, after_zero, p);

@@ -47,6 +47,20 @@ __device__ __forceinline__ void make_map(ThreadMap &t, int rowb, int gtid,
 // Running sums S, T, U over slots [s_lo, s_hi) of one (head, 16-byte column)
 // group whose slot s is staged at p0 + (s - s_off) * stride (s >= s_off);
 // eight independent shared loads per iteration.
+// (kHalves: each 16-byte column read as two 8-byte loads, for stages whose
+// columns sit 8 bytes past a 16-byte boundary)
+template <bool kHalves = false>
+__device__ __forceinline__ uint4 col16(const unsigned char *p) {
+  if constexpr (kHalves) {
+    const uint2 a = *reinterpret_cast<const uint2 *>(p);
+    const uint2 b = *reinterpret_cast<const uint2 *>(p + 8);
+    return make_uint4(a.x, a.y, b.x, b.y);
+  } else {
+    return *reinterpret_cast<const uint4 *>(p);
+  }
+}
+
+template <bool kHalves = false>
 __device__ __forceinline__ void accum_slots(const unsigned char *p0, size_t stride,
                                             int s_lo, int s_hi, int s_off, u64 &S,
                                             u64 &T, u64 &U) {
@@ -55,7 +69,7 @@ __device__ __forceinline__ void accum_slots(const unsigned char *p0, size_t stri
     uint4 v[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      v[k] = *reinterpret_cast<const uint4 *>(p0 + static_cast<size_t>(s + k - s_off) * stride);
+      v[k] = col16<kHalves>(p0 + static_cast<size_t>(s + k - s_off) * stride);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
@@ -67,8 +81,7 @@ __device__ __forceinline__ void accum_slots(const unsigned char *p0, size_t stri
     }
   }
   for (; s < s_hi; ++s) {
-    const uint4 v =
-        *reinterpret_cast<const uint4 *>(p0 + static_cast<size_t>(s - s_off) * stride);
+    const uint4 v = col16<kHalves>(p0 + static_cast<size_t>(s - s_off) * stride);
     const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
     const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
     const u64 X = x0 + x1;
@@ -325,6 +338,11 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
         // heads staged one after another, nv slots each
         accum_slots(stage + static_cast<size_t>(hl) * nv * C.hb + (col << 4),
                     static_cast<size_t>(C.hb), 0, nv, 0, S, T, U);
+      } else if constexpr (kFam == kFamHndMis) {
+        // heads staged as they lie in the page (all block_size slots), the
+        // stage's copy possibly 8 bytes past a 16-byte boundary
+        accum_slots<true>(stage + static_cast<size_t>(hl) * bsi * C.hb + (col << 4),
+                          static_cast<size_t>(C.hb), 0, nv, 0, S, T, U);
       } else {
         // sub-block sb holds slots [sb*kbs, (sb+1)*kbs) of every head
         accum_slots_sub(stage + static_cast<size_t>(hl) * C.kbs * C.hb + (col << 4), C.hb,
@@ -728,6 +746,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                 // the unit's heads with all their slots, staged as in memory
                 pstride = static_cast<u32>(count) * static_cast<u32>(bs) * static_cast<u32>(C.hb);
                 pbytes = pstride;
+                // (misaligned: in a 16-byte-aligned region with room for the shift)
+                if constexpr (kFam == kFamHndMis) pstride = pbytes + kMisPad;
                 if constexpr (kFam == kFamHndSub) {
                   const int nsb = (cur.nv + C.kbs - 1) / C.kbs;  // sub-blocks with valid slots
                   pbytes = static_cast<u32>(count) * static_cast<u32>(nsb * C.kbs) *
@@ -763,7 +783,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             int left = p.pages_per_pos - (ci * C.halves + half);
             if (rb - u < left) left = static_cast<int>(rb - u);
             npg = max(1, min(left, fit));
-            if constexpr (kFam == kFamRowsMis) npg = min(npg, kMisMaxPages);
+            if constexpr (mis_family(kFam)) npg = min(npg, kMisMaxPages);
           }
           if (pbytes > 0) {
             bool free_stage = true;
@@ -785,19 +805,22 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
               }
             }
             const u32 fb = ptx::smem_addr(&hdr->full[s]);
-            if constexpr (kFam == kFamRowsMis) {
-              static_assert(!kWide, "the misaligned-rows instance has one producer lane");
-              // Per page: the 16-byte-aligned interior of its rows by bulk copy,
-              // and when the page starts 8 bytes past a boundary its first and
-              // last words by 8-byte cp.async, tracked on the same barrier.
+            if constexpr (mis_family(kFam)) {
+              static_assert(!kWide, "the misaligned instances have one producer lane");
+              // Per page: the 16-byte-aligned interior of its unit's bytes (rows,
+              // or heads with all their slots) by bulk copy, and when they start
+              // 8 bytes past a boundary their first and last words by 8-byte
+              // cp.async, tracked on the same barrier.
               u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
               u32 tx = 0, dmask = 0;
               int pci = ci, phalf = half;
               for (int k2 = 0; k2 < npg; ++k2) {
                 const DevCache &D = p.caches[pci];
-                const unsigned char *src = D.base + static_cast<long long>(phalf) * D.half_stride +
-                                           cur.block * D.block_stride +
-                                           static_cast<u64>(first) * D.rowb;
+                const unsigned char *src =
+                    D.base + static_cast<long long>(phalf) * D.half_stride +
+                    cur.block * D.block_stride +
+                    (kFam == kFamHndMis ? static_cast<u64>(first) * bs * D.hb
+                                        : static_cast<u64>(first) * D.rowb);
                 if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
                   ptx::bulk_g2s(dst, src, pbytes, fb, policy);
                   tx += pbytes;
@@ -1103,11 +1126,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     for (int k = 0; !packed && k < m.npages; ++k) {
       const DevCache &C = p.caches[ci];
       if (C.rowb != map.rowb) make_map(map, C.rowb, gtid, gw * 32);
-      if constexpr (kFam == kFamRowsMis) {
+      if constexpr (mis_family(kFam)) {
         // the page's first byte sits 8 bytes into its region when the page
         // starts 8 bytes past a boundary
         v += unit_sum<kFam>(C, m, half, sp + ((m.mode >> (1 + k)) & 1) * 8, map, bsz);
-        sp += static_cast<size_t>(m.count) * C.rowb + kMisPad;
+        sp += (kFam == kFamHndMis ? static_cast<size_t>(m.count) * bsz * C.hb
+                                  : static_cast<size_t>(m.count) * C.rowb) + kMisPad;
       } else {
         v += unit_sum<kFam>(C, m, half, sp, map, bsz);
         sp += kFam == kFamHnd ? static_cast<size_t>(m.count) * static_cast<size_t>(m.nv) * C.hb

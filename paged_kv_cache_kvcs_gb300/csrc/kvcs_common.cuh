@@ -64,18 +64,26 @@ constexpr int kFamState = 3;   // Mamba states: rows of a state
 constexpr int kFamHndSub = 4;  // HND in kernel sub-blocks: heads of each sub-block
 constexpr int kFamRowsMis = 5; // NHD and latent rows of pages 8 bytes past a 16-byte
                                // boundary (some or all)
-constexpr int kNumFamilies = 6;
+constexpr int kFamHndMis = 6;  // HND (no kernel sub-blocks) heads of pages 8 bytes past
+                               // a 16-byte boundary (some or all)
+constexpr int kNumFamilies = 7;
 
-// Misaligned-rows units: at most this many pages (one flag bit each in the
-// unit's metadata).
+// Misaligned units (rows or heads): at most this many pages (one flag bit
+// each in the unit's metadata).
 constexpr int kMisMaxPages = 30;
-// Bytes a misaligned-rows page takes in a stage beyond its rows: its region
+// Bytes a misaligned page takes in a stage beyond its bytes: its region
 // starts 16-byte aligned and its first byte sits 8 bytes in when misaligned.
 constexpr int kMisPad = 16;
 
 // Families whose units are runs of whole heads, all block_size slots of them.
 __host__ __device__ constexpr bool head_family(int fam) {
-  return fam == kFamHnd || fam == kFamHndSub || fam == kFamXSplit;
+  return fam == kFamHnd || fam == kFamHndSub || fam == kFamXSplit || fam == kFamHndMis;
+}
+
+// Families staged with the misaligned pages' split: the 16-byte-aligned
+// interior by bulk copy, the edge words by 8-byte cp.async.
+__host__ __device__ constexpr bool mis_family(int fam) {
+  return fam == kFamRowsMis || fam == kFamHndMis;
 }
 
 constexpr u32 kStatusBadBlockId = 1u;

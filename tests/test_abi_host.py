@@ -120,12 +120,15 @@ def test_validation_codes():
     assert code_of([FakeCache(layer=0, layout=4, head_bytes=8, piece_bytes=4),
                     FakeCache(layer=1)]) == K.KVCS_EINVAL
     assert code_of([FakeCache(piece_bytes=2)]) == K.KVCS_EINVAL
-    # strides that are 8- but not 16-byte multiples: NHD rows stay on the bulk
-    # kernel (its misaligned-rows instance), HND heads go to the direct kernel
+    # strides that are 8- but not 16-byte multiples: NHD rows and HND heads
+    # stay on the bulk kernel (its misaligned instances); HND in kernel
+    # sub-blocks goes to the direct kernel
     assert plan([FakeCache(block_stride=page + 8)])["kernel"] == 0
     assert plan([FakeCache(block_stride=page + 16)])["kernel"] == 0
-    assert plan([FakeCache(layout=1, block_stride=page + 8)])["kernel"] == 1
+    assert plan([FakeCache(layout=1, block_stride=page + 8)])["kernel"] == 0
     assert plan([FakeCache(layout=1, block_stride=page + 16)])["kernel"] == 0
+    assert plan([FakeCache(layout=1, block_stride=page + 8, kernel_block_size=4)])["kernel"] == 1
+    assert plan([FakeCache(layout=1, block_stride=page + 8, kernel_block_size=16)])["kernel"] == 0
     # NHD heads of 8 mod 16 bytes (a 16-byte column would straddle two heads)
     assert plan([FakeCache(head_bytes=24)])["kernel"] == 1
 

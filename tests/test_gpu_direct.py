@@ -2,10 +2,11 @@
 ABI: the direct-load kernel (every layout, pools 0 or 8 bytes past a 16-byte
 boundary, rows that are 8 mod 16 bytes, where chunks pair up over two rows,
 rows and head runs past a stage, pages whose alignment alternates with the
-block) and the bulk kernel's misaligned-rows instance (NHD and latent rows
-of whole 16-byte columns: interiors by bulk copy, edge words by 8-byte
-asynchronous copies).  Ragged and empty positions, first positions past
-2^57 (t P wraps 2^64).  Bit-exact uint64 equality."""
+block) and the bulk kernel's misaligned instances (NHD and latent rows of
+whole 16-byte columns, and HND heads without kernel sub-blocks: interiors by
+bulk copy, edge words by 8-byte asynchronous copies).  Ragged and empty
+positions, first positions past 2^57 (t P wraps 2^64).  Bit-exact uint64
+equality."""
 
 import dataclasses
 
@@ -40,10 +41,16 @@ def _shifted(wl, shift, block_pad=0):
                       wl.num_tokens, wl.block_ids, wl.info), keep
 
 
-def _rows_bulk(c):
-    """NHD or latent rows of whole 16-byte columns of one head: the bulk
-    kernel stages them even 8 bytes off a boundary."""
-    if c.layout not in (W.LAYOUT_NHD, W.LAYOUT_LATENT) or c.head_bytes % 16:
+def _rows_bulk(c, bs):
+    """NHD or latent rows of whole 16-byte columns of one head, and HND heads
+    of whole 16-byte columns without kernel sub-blocks: the bulk kernel
+    stages them even 8 bytes off a boundary."""
+    if c.head_bytes % 16:
+        return False
+    if c.layout == W.LAYOUT_HND:
+        subs = getattr(c, "kernel_block_size", 0) not in (0, bs)
+        return not subs and c.head_bytes * bs <= 65536
+    if c.layout not in (W.LAYOUT_NHD, W.LAYOUT_LATENT):
         return False
     row = c.num_heads * c.head_bytes if c.layout == W.LAYOUT_NHD else c.head_bytes
     return row <= 65536
@@ -53,7 +60,7 @@ def _check(wl, kernel=None):
     from gpu_helpers import full_oracle, gpu_checksums
     plan = K.plan_for(wl.caches, wl.block_size, wl.num_positions)
     if kernel is None:
-        kernel = 0 if all(_rows_bulk(c) for c in wl.caches) else 1
+        kernel = 0 if all(_rows_bulk(c, wl.block_size) for c in wl.caches) else 1
     assert plan["kernel"] == kernel, plan
     got, st = gpu_checksums(wl)
     exp, est = full_oracle(wl)
@@ -190,6 +197,46 @@ def test_misaligned_rows_bulk_instance(case, place):
     if layout == W.LAYOUT_LATENT and place == "v_only":
         pytest.skip("a latent cache has no V pages")
     wl = W.random_case(31, DEV, layout=layout, layers=3, heads=heads, head_bytes=hb,
+                       block_size=bs, lengths=lengths, first_positions=fps)
+    if place == "base8":
+        wl, keep = _shifted(wl, 8)
+    elif place == "stride8":
+        wl, keep = _shifted(wl, 0, block_pad=8)
+    else:
+        caches, keep = [], []
+        for c in wl.caches:
+            page = bs * c.num_heads * c.head_bytes
+            raw = torch.zeros(2 * c.num_blocks * page + 8, dtype=torch.uint8, device=DEV)
+            v = c.pool.view(2, c.num_blocks * page)
+            raw[:c.num_blocks * page] = v[0]
+            raw[c.num_blocks * page + 8:] = v[1]
+            keep.append(raw)
+            caches.append(dataclasses.replace(c, pool=raw, half_stride=c.num_blocks * page + 8))
+        wl = W.Workload(wl.name, bs, caches, wl.pos_offsets, wl.first_position,
+                        wl.num_tokens, wl.block_ids, wl.info)
+    _check(wl, kernel=0)
+
+
+MIS_HND = [
+    # (heads, head_bytes, block_size, lengths, first_positions)
+    (8, 256, 16, (70, 33, 5, 16), (1, 0, 0, 0)),       # 32 KiB pages, a unit each
+    (8, 128, 16, (60, 37), (0, 0)),                     # fp8-shaped 16 KiB pages, packed
+    (2, 32, 16, (100, 1, 17), (0, 0, 1)),               # 1 KiB pages, many to a stage
+    (4, 256, 64, (150, 64, 9), (0, 0, 0)),              # 16 KiB heads: two units a page
+    (8, 64, 16, [16 * k + 1 for k in range(40)], list(range(40))),  # one-token blocks
+]
+
+
+@pytest.mark.parametrize("place", ["base8", "stride8", "v_only"])
+@pytest.mark.parametrize("case", MIS_HND, ids=lambda c: f"h{c[0]}b{c[1]}bs{c[2]}")
+def test_misaligned_hnd_bulk_instance(case, place):
+    """HND heads 8 bytes off a 16-byte boundary: every page (base8), every
+    other block (stride8), or only the V pages (v_only) go to the bulk
+    kernel's misaligned-heads instance (a unit's heads, all their slots, as
+    one run: interior by bulk copy, edge words by 8-byte copies) and give
+    the oracle's checksums."""
+    heads, hb, bs, lengths, fps = case
+    wl = W.random_case(33, DEV, layout=W.LAYOUT_HND, layers=3, heads=heads, head_bytes=hb,
                        block_size=bs, lengths=lengths, first_positions=fps)
     if place == "base8":
         wl, keep = _shifted(wl, 8)

@@ -91,9 +91,9 @@ def test_padded_blocks(layout, pad):
         caches.append(dataclasses.replace(c, pool=buf, block_stride=stride,
                                           half_stride=c.num_blocks * stride))
     plan = K.plan_for(caches, wl.block_size, wl.num_positions)
-    # blocks 8 mod 16 apart: NHD and latent rows stay on the bulk kernel (its
-    # misaligned-rows instance), HND heads go to the direct kernel
-    assert plan["kernel"] == (0 if pad % 16 == 0 or layout != W.LAYOUT_HND else 1)
+    # blocks 8 mod 16 apart: NHD and latent rows and HND heads stay on the
+    # bulk kernel (its misaligned instances)
+    assert plan["kernel"] == 0
     got, st = run(with_caches(wl, caches))
     assert st == 0 and np.array_equal(got, exp)
 
@@ -186,9 +186,10 @@ def test_misaligned_pools_every_layout(kind, heads, hb):
         keep.append(raw)
         caches.append(dataclasses.replace(c, pool=raw[8:], **extra))
     wl2 = with_caches(wl, caches)
-    # NHD rows of whole 16-byte columns go to the bulk kernel's misaligned-rows
-    # instance; the other layouts (and 8-mod-16 latent rows) to the direct kernel
-    expect = 0 if kind == "nhd" else 1
+    # NHD rows of whole 16-byte columns and HND heads (no sub-blocks) go to the
+    # bulk kernel's misaligned instances; the other layouts (and 8-mod-16
+    # latent rows) to the direct kernel
+    expect = 0 if kind in ("nhd", "hnd") else 1
     assert K.plan_for(wl2.caches, bs, wl2.num_positions)["kernel"] == expect
     got, st = run(wl2)
     assert st == 0 and np.array_equal(got, exp)

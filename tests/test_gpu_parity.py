@@ -142,10 +142,10 @@ def test_generic_kernel_matches_oracle(case):
     assert_equal(got, exp)
 
 
-@pytest.mark.parametrize("layout,kernel", [(W.LAYOUT_NHD, 0), (W.LAYOUT_HND, 1)])
+@pytest.mark.parametrize("layout,kernel", [(W.LAYOUT_NHD, 0), (W.LAYOUT_HND, 0)])
 def test_misaligned_base(layout, kernel):
-    """Pools 8 bytes past a 16-byte boundary: NHD rows go to the bulk
-    kernel's misaligned-rows instance, HND heads to the direct kernel."""
+    """Pools 8 bytes past a 16-byte boundary: NHD rows and HND heads go to
+    the bulk kernel's misaligned instances."""
     wl = W.random_case(4, DEV, layout=layout, layers=2, heads=2, head_bytes=32, block_size=4,
                        lengths=(13,))
     for c in wl.caches:
