@@ -65,6 +65,7 @@ cudaError_t device_setup(int *sms) {
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndSub, false>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRowsMis, false>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndMis, false>),
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamXSplitMis, false>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows, true>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd, true>)})
       if (e == cudaSuccess)
@@ -97,12 +98,15 @@ bool rows_misaligned(const kvcs_cache &c) {
   return reinterpret_cast<uintptr_t>(c.base) % 16 || c.half_stride % 16 || c.block_stride % 16;
 }
 
-// HND caches without kernel sub-blocks whose pages may start 8 bytes past a
-// 16-byte boundary: a unit's heads, all slots of them, are one contiguous
-// run, staged as misaligned rows are.
+// HND caches without kernel sub-blocks, and x-split caches, whose pages may
+// start 8 bytes past a 16-byte boundary: a unit's heads, all slots of them,
+// are one contiguous run, staged as misaligned rows are.
 bool hnd_misaligned(const kvcs_cache &c, int block_size) {
-  if (c.layout != KVCS_LAYOUT_HND) return false;
-  if (c.kernel_block_size > 0 && c.kernel_block_size != block_size) return false;
+  if (c.layout == KVCS_LAYOUT_HND) {
+    if (c.kernel_block_size > 0 && c.kernel_block_size != block_size) return false;
+  } else if (c.layout != KVCS_LAYOUT_XSPLIT) {
+    return false;
+  }
   return reinterpret_cast<uintptr_t>(c.base) % 16 || c.half_stride % 16 || c.block_stride % 16;
 }
 
@@ -323,7 +327,7 @@ int family_of(const kvcs_cache &c, int block_size) {
       return c.kernel_block_size > 0 && c.kernel_block_size != block_size ? kFamHndSub
              : hnd_misaligned(c, block_size)                               ? kFamHndMis
                                                                            : kFamHnd;
-    case KVCS_LAYOUT_XSPLIT: return kFamXSplit;
+    case KVCS_LAYOUT_XSPLIT: return hnd_misaligned(c, block_size) ? kFamXSplitMis : kFamXSplit;
     case KVCS_LAYOUT_STATE: return kFamState;
     default: return rows_misaligned(c) ? kFamRowsMis : kFamRows;
   }
@@ -651,6 +655,7 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
         case kFamHndSub: e = launch(kvcs_bulk_kernel<kFamHndSub, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
         case kFamRowsMis: e = launch(kvcs_bulk_kernel<kFamRowsMis, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
         case kFamHndMis: e = launch(kvcs_bulk_kernel<kFamHndMis, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
+        case kFamXSplitMis: e = launch(kvcs_bulk_kernel<kFamXSplitMis, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
         default:
           e = wide ? launch(kvcs_bulk_kernel<kFamRows, true>, gd, kBulkThreads, smem, st, after_zero, p)
                    : launch(kvcs_bulk_kernel<kFamRows, false>, gd, kBulkThreads, smem, st, after_zero, p);

@@ -95,6 +95,7 @@ __device__ __forceinline__ void accum_slots(const unsigned char *p0, size_t stri
 // 16-byte rows at gp), starting at slot s0 and wrapping: groups start at
 // different slots so a warp's reads spread over the shared-memory banks;
 // four independent loads per iteration.
+template <bool kHalves = false>
 __device__ __forceinline__ void accum_slots_rotated(const unsigned char *gp, int s0,
                                                     int nv, u64 &S, u64 &T, u64 &U) {
   int k = 0;
@@ -105,7 +106,7 @@ __device__ __forceinline__ void accum_slots_rotated(const unsigned char *gp, int
     for (int i = 0; i < 4; ++i) {
       sl[i] = s0 + k + i;
       if (sl[i] >= nv) sl[i] -= nv;
-      v[i] = *reinterpret_cast<const uint4 *>(gp + static_cast<size_t>(sl[i]) * 16);
+      v[i] = col16<kHalves>(gp + static_cast<size_t>(sl[i]) * 16);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -120,7 +121,7 @@ __device__ __forceinline__ void accum_slots_rotated(const unsigned char *gp, int
   for (; k < nv; ++k) {
     int sl = s0 + k;
     if (sl >= nv) sl -= nv;
-    const uint4 v = *reinterpret_cast<const uint4 *>(gp + static_cast<size_t>(sl) * 16);
+    const uint4 v = col16<kHalves>(gp + static_cast<size_t>(sl) * 16);
     const u64 x0 = (static_cast<u64>(v.y) << 32) | v.x;
     const u64 x1 = (static_cast<u64>(v.w) << 32) | v.z;
     const u64 X = x0 + x1;
@@ -329,11 +330,13 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
       const int hl = g / cpr;
       const int col = g - hl * cpr;
       u64 S = 0, T = 0, U = 0;
-      if constexpr (kFam == kFamXSplit) {
+      if constexpr (kFam == kFamXSplit || kFam == kFamXSplitMis) {
         // the group's slots are one contiguous run of 16-byte rows; start
         // at a group-dependent slot so a warp's reads spread over the banks
+        // (misaligned pages: the stage's copy may sit 8 bytes past a
+        // 16-byte boundary, read as 8-byte halves)
         const unsigned char *gp = stage + static_cast<size_t>(g) * bsi * 16;
-        accum_slots_rotated(gp, g % nv, nv, S, T, U);
+        accum_slots_rotated<kFam == kFamXSplitMis>(gp, g % nv, nv, S, T, U);
       } else if constexpr (kFam == kFamHnd) {
         // heads staged one after another, nv slots each
         accum_slots(stage + static_cast<size_t>(hl) * nv * C.hb + (col << 4),
@@ -747,7 +750,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                 pstride = static_cast<u32>(count) * static_cast<u32>(bs) * static_cast<u32>(C.hb);
                 pbytes = pstride;
                 // (misaligned: in a 16-byte-aligned region with room for the shift)
-                if constexpr (kFam == kFamHndMis) pstride = pbytes + kMisPad;
+                if constexpr (mis_family(kFam)) pstride = pbytes + kMisPad;
                 if constexpr (kFam == kFamHndSub) {
                   const int nsb = (cur.nv + C.kbs - 1) / C.kbs;  // sub-blocks with valid slots
                   pbytes = static_cast<u32>(count) * static_cast<u32>(nsb * C.kbs) *
@@ -819,8 +822,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                 const unsigned char *src =
                     D.base + static_cast<long long>(phalf) * D.half_stride +
                     cur.block * D.block_stride +
-                    (kFam == kFamHndMis ? static_cast<u64>(first) * bs * D.hb
-                                        : static_cast<u64>(first) * D.rowb);
+                    (head_family(kFam) ? static_cast<u64>(first) * bs * D.hb
+                                       : static_cast<u64>(first) * D.rowb);
                 if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
                   ptx::bulk_g2s(dst, src, pbytes, fb, policy);
                   tx += pbytes;
@@ -1130,8 +1133,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         // the page's first byte sits 8 bytes into its region when the page
         // starts 8 bytes past a boundary
         v += unit_sum<kFam>(C, m, half, sp + ((m.mode >> (1 + k)) & 1) * 8, map, bsz);
-        sp += (kFam == kFamHndMis ? static_cast<size_t>(m.count) * bsz * C.hb
-                                  : static_cast<size_t>(m.count) * C.rowb) + kMisPad;
+        sp += (head_family(kFam) ? static_cast<size_t>(m.count) * bsz * C.hb
+                                 : static_cast<size_t>(m.count) * C.rowb) + kMisPad;
       } else {
         v += unit_sum<kFam>(C, m, half, sp, map, bsz);
         sp += kFam == kFamHnd ? static_cast<size_t>(m.count) * static_cast<size_t>(m.nv) * C.hb

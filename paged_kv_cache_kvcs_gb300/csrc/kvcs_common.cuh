@@ -66,7 +66,9 @@ constexpr int kFamRowsMis = 5; // NHD and latent rows of pages 8 bytes past a 16
                                // boundary (some or all)
 constexpr int kFamHndMis = 6;  // HND (no kernel sub-blocks) heads of pages 8 bytes past
                                // a 16-byte boundary (some or all)
-constexpr int kNumFamilies = 7;
+constexpr int kFamXSplitMis = 7;  // x-split heads of pages 8 bytes past a 16-byte
+                                  // boundary (some or all)
+constexpr int kNumFamilies = 8;
 
 // Misaligned units (rows or heads): at most this many pages (one flag bit
 // each in the unit's metadata).
@@ -77,13 +79,14 @@ constexpr int kMisPad = 16;
 
 // Families whose units are runs of whole heads, all block_size slots of them.
 __host__ __device__ constexpr bool head_family(int fam) {
-  return fam == kFamHnd || fam == kFamHndSub || fam == kFamXSplit || fam == kFamHndMis;
+  return fam == kFamHnd || fam == kFamHndSub || fam == kFamXSplit || fam == kFamHndMis ||
+         fam == kFamXSplitMis;
 }
 
 // Families staged with the misaligned pages' split: the 16-byte-aligned
 // interior by bulk copy, the edge words by 8-byte cp.async.
 __host__ __device__ constexpr bool mis_family(int fam) {
-  return fam == kFamRowsMis || fam == kFamHndMis;
+  return fam == kFamRowsMis || fam == kFamHndMis || fam == kFamXSplitMis;
 }
 
 constexpr u32 kStatusBadBlockId = 1u;

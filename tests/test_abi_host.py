@@ -129,6 +129,7 @@ def test_validation_codes():
     assert plan([FakeCache(layout=1, block_stride=page + 16)])["kernel"] == 0
     assert plan([FakeCache(layout=1, block_stride=page + 8, kernel_block_size=4)])["kernel"] == 1
     assert plan([FakeCache(layout=1, block_stride=page + 8, kernel_block_size=16)])["kernel"] == 0
+    assert plan([FakeCache(layout=3, block_stride=page + 8)])["kernel"] == 0   # x-split
     # NHD heads of 8 mod 16 bytes (a 16-byte column would straddle two heads)
     assert plan([FakeCache(head_bytes=24)])["kernel"] == 1
 

@@ -47,9 +47,9 @@ def _rows_bulk(c, bs):
     stages them even 8 bytes off a boundary."""
     if c.head_bytes % 16:
         return False
-    if c.layout == W.LAYOUT_HND:
+    if c.layout in (W.LAYOUT_HND, W.LAYOUT_XSPLIT):
         subs = getattr(c, "kernel_block_size", 0) not in (0, bs)
-        return not subs and c.head_bytes * bs <= 65536
+        return not (subs and c.layout == W.LAYOUT_HND) and c.head_bytes * bs <= 65536
     if c.layout not in (W.LAYOUT_NHD, W.LAYOUT_LATENT):
         return False
     row = c.num_heads * c.head_bytes if c.layout == W.LAYOUT_NHD else c.head_bytes
@@ -227,16 +227,17 @@ MIS_HND = [
 ]
 
 
+@pytest.mark.parametrize("layout", [W.LAYOUT_HND, W.LAYOUT_XSPLIT])
 @pytest.mark.parametrize("place", ["base8", "stride8", "v_only"])
 @pytest.mark.parametrize("case", MIS_HND, ids=lambda c: f"h{c[0]}b{c[1]}bs{c[2]}")
-def test_misaligned_hnd_bulk_instance(case, place):
-    """HND heads 8 bytes off a 16-byte boundary: every page (base8), every
-    other block (stride8), or only the V pages (v_only) go to the bulk
-    kernel's misaligned-heads instance (a unit's heads, all their slots, as
-    one run: interior by bulk copy, edge words by 8-byte copies) and give
-    the oracle's checksums."""
+def test_misaligned_heads_bulk_instances(case, place, layout):
+    """HND and x-split heads 8 bytes off a 16-byte boundary: every page
+    (base8), every other block (stride8), or only the V pages (v_only) go
+    to the bulk kernel's misaligned-heads instances (a unit's heads, all
+    their slots, as one run: interior by bulk copy, edge words by 8-byte
+    copies) and give the oracle's checksums."""
     heads, hb, bs, lengths, fps = case
-    wl = W.random_case(33, DEV, layout=W.LAYOUT_HND, layers=3, heads=heads, head_bytes=hb,
+    wl = W.random_case(33, DEV, layout=layout, layers=3, heads=heads, head_bytes=hb,
                        block_size=bs, lengths=lengths, first_positions=fps)
     if place == "base8":
         wl, keep = _shifted(wl, 8)

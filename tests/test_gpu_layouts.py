@@ -124,7 +124,7 @@ def test_nhd_kernel_block_size_is_the_same_memory():
 
 
 @pytest.mark.parametrize("hb,bs", [(64, 16), (256, 16), (32, 5), (16, 1)])
-@pytest.mark.parametrize("pad", [0, 8])       # bulk kernel, direct kernel
+@pytest.mark.parametrize("pad", [0, 8])       # bulk kernel, its misaligned-heads instance
 def test_xsplit_layout(hb, bs, pad):
     """[2, num_blocks, heads, head_bytes / 16, block_size, 16]: the x-split
     layout (16-byte x chunks) for K and V pages."""
@@ -147,7 +147,7 @@ def test_xsplit_layout(hb, bs, pad):
             spec = dataclasses.replace(c, pool=x.view(-1), layout=W.LAYOUT_XSPLIT)
         caches.append(spec)
     plan = K.plan_for(caches, wl.block_size, wl.num_positions)
-    assert plan["kernel"] == (1 if pad else 0)
+    assert plan["kernel"] == 0
     got, st = run(with_caches(wl, caches))
     assert st == 0 and np.array_equal(got, exp)
 
@@ -186,10 +186,10 @@ def test_misaligned_pools_every_layout(kind, heads, hb):
         keep.append(raw)
         caches.append(dataclasses.replace(c, pool=raw[8:], **extra))
     wl2 = with_caches(wl, caches)
-    # NHD rows of whole 16-byte columns and HND heads (no sub-blocks) go to the
-    # bulk kernel's misaligned instances; the other layouts (and 8-mod-16
-    # latent rows) to the direct kernel
-    expect = 0 if kind in ("nhd", "hnd") else 1
+    # NHD rows of whole 16-byte columns, HND heads (no sub-blocks) and x-split
+    # heads go to the bulk kernel's misaligned instances; HND sub-blocks (and
+    # 8-mod-16 latent rows) to the direct kernel
+    expect = 0 if kind in ("nhd", "hnd", "xsplit") else 1
     assert K.plan_for(wl2.caches, bs, wl2.num_positions)["kernel"] == expect
     got, st = run(wl2)
     assert st == 0 and np.array_equal(got, exp)
