@@ -103,13 +103,18 @@ def relayout(wl, layout: str):
         bs, H, hb, nb = wl.block_size, c.num_heads, c.head_bytes, c.num_blocks
         page = bs * H * hb
         v = c.pool.view(2, nb, bs, H, hb)
-        if layout in ("misaligned_hnd", "misaligned_xsplit"):
-            # HND or x-split pools starting 8 bytes past a 16-byte boundary
+        if layout in ("misaligned_hnd", "misaligned_hnd_sub4", "misaligned_xsplit"):
+            # HND (plain or in 4-slot kernel sub-blocks) or x-split pools
+            # starting 8 bytes past a 16-byte boundary
             buf = torch.empty(c.pool.numel() + 8, dtype=torch.uint8, device=c.pool.device)
             pool = buf[8:]
             if layout == "misaligned_hnd":
                 pool.copy_(v.permute(0, 1, 3, 2, 4).reshape(-1))
                 caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_HND))
+            elif layout == "misaligned_hnd_sub4":
+                pool.copy_(v.view(2, nb, bs // 4, 4, H, hb).permute(0, 1, 2, 4, 3, 5).reshape(-1))
+                caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_HND,
+                                                  kernel_block_size=4))
             else:
                 pool.copy_(v.view(2, nb, bs, H, hb // 16, 16).permute(0, 1, 3, 4, 2, 5).reshape(-1))
                 caches.append(dataclasses.replace(c, pool=pool, layout=W.LAYOUT_XSPLIT))
@@ -1083,7 +1088,8 @@ def main():
                     help="also time the first 1, 2, 4, ... requests alone")
     ap.add_argument("--layout", default="nhd",
                     choices=("nhd", "hnd", "hnd_sub4", "interleaved", "separate_kv", "xsplit",
-                             "misaligned", "misaligned_hnd", "misaligned_xsplit"),
+                             "misaligned", "misaligned_hnd", "misaligned_hnd_sub4",
+                             "misaligned_xsplit"),
                     help="re-lay-out the (NHD) workload's pools before timing")
     ap.add_argument("--columns", type=int, default=1,
                     help="replica-key columns (caches assigned round-robin)")
