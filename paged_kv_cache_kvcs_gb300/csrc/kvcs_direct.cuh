@@ -164,6 +164,119 @@ __device__ __forceinline__ u64 run_sum(const unsigned char *base, int nrows, con
   return acc;
 }
 
+// A lane's part in every run of one shape (rows of rowb <= 512 bytes, nrows
+// rows, starting d = 0 or 8 bytes past a 16-byte boundary), worked out once
+// for the runs of a page that share it: HND heads (or sub-blocks of heads)
+// and x-split chunks.  It is run_sum's mapping with everything that depends
+// only on the shape taken out of the run: the lane's chunk column, its
+// super-rows, the edge words, and for its two words the row within a
+// super-row, the word within the row and the super-row shift.
+struct RunPlan {
+  int rowb, nrows, d;   // the shape (rowb = -1: none yet)
+  int active;           // the lane holds a column
+  int pr;               // rows per super-row
+  int s0, s_full;       // the lane's batched super-rows: s0, s0 + rstep, ... < s_full
+  int rstep;
+  int lstep;            // bytes between the lane's chunks
+  int first_off;        // its first batched chunk, from the aligned base
+  int head_word;        // 1: its chunk's second word is the run's first word (read alone)
+  int tail;             // 1: one more chunk past s_full whose first word is in the run
+  int tail_off, tail_s; // that chunk's offset from the aligned base, and its super-row
+  int rin0, rin1;       // row within the super-row of word 0 and word 1
+  int w0, w1;           // word within the row
+  int srd0, srd1;       // word j belongs to the previous super-row
+};
+
+__device__ __forceinline__ void plan_runs(RunPlan &pl, int rowb, int nrows, int d, int lane) {
+  pl.rowb = rowb;
+  pl.nrows = nrows;
+  pl.d = d;
+  pl.pr = (rowb & 15) ? 2 : 1;
+  const int srb = pl.pr * rowb;
+  const int cps = srb >> 4;                       // <= 32 here
+  const int len = nrows * rowb;
+  const int nsr = (nrows + pl.pr - 1) / pl.pr + (d ? 1 : 0);
+  pl.rstep = 32 / cps;
+  const int sr0 = lane / cps;
+  const int c = lane - sr0 * cps;
+  pl.active = sr0 < pl.rstep && nrows > 0;
+  pl.lstep = pl.rstep * srb;
+  const int room = len + d - 8 - 16 * c;
+  int s_full = room > 0 ? (room + srb - 1) / srb : 0;
+  if (s_full > nsr) s_full = nsr;
+  pl.s_full = s_full;
+  int s = sr0;
+  pl.head_word = d && c == 0 && s == 0;
+  if (pl.head_word) s += pl.rstep;
+  pl.s0 = s;
+  pl.first_off = (s * cps + c) * 16;
+  const int ot = s_full * srb + 16 * c - d;
+  pl.tail = s_full < nsr && ot >= 0 && ot < len && s_full >= sr0 && (s_full - sr0) % pl.rstep == 0;
+  pl.tail_off = s_full * srb + 16 * c;
+  pl.tail_s = s_full;
+  int rin[2], w[2], srd[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    int u = 16 * c - d + 8 * j;
+    srd[j] = 0;
+    if (u < 0) {
+      u += srb;
+      srd[j] = 1;
+    }
+    rin[j] = u / rowb;
+    w[j] = (u - rin[j] * rowb) >> 3;
+  }
+  pl.rin0 = rin[0];
+  pl.rin1 = rin[1];
+  pl.w0 = w[0];
+  pl.w1 = w[1];
+  pl.srd0 = srd[0];
+  pl.srd1 = srd[1];
+}
+
+// This lane's share of one run of the planned shape whose words are pieces
+// piece0 + (word in the row) of one head, weighted m = m0 + 2 head, the
+// run's row r holding the token in slot slot0 + r: run_sum's result.
+__device__ __forceinline__ u64 run_sum_planned(const unsigned char *base, const RunPlan &pl,
+                                               u64 m, u64 t0, u64 P, int slot0, int piece0) {
+  if (!pl.active) return 0;
+  const unsigned char *A = base - pl.d;
+  u64 xh = 0, xt = 0;
+  if (pl.head_word) xh = ld_stream8(base);
+  if (pl.tail) xt = ld_stream8(A + pl.tail_off);
+  u64 S0 = 0, T0 = 0, S1 = 0, T1 = 0;
+  const unsigned char *cp = A + pl.first_off;
+  for (int s = pl.s0; s < pl.s_full; s += kDirectBatch * pl.rstep) {
+    uint4 v[kDirectBatch];
+#pragma unroll
+    for (int k = 0; k < kDirectBatch; ++k) {
+      v[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (s + k * pl.rstep < pl.s_full) v[k] = ld_stream16(cp + k * pl.lstep);
+    }
+    cp += kDirectBatch * pl.lstep;
+#pragma unroll
+    for (int k = 0; k < kDirectBatch; ++k) {
+      const u64 sk = static_cast<u64>(static_cast<u32>(s + k * pl.rstep));
+      const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
+      const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
+      S0 += x0;
+      T0 += sk * x0;
+      S1 += x1;
+      T1 += sk * x1;
+    }
+  }
+  S1 += xh;
+  S0 += xt;
+  T0 += static_cast<u64>(static_cast<u32>(pl.tail_s)) * xt;
+  T0 -= static_cast<u64>(pl.srd0) * S0;
+  T1 -= static_cast<u64>(pl.srd1) * S1;
+  // B_j = 2 ((t0 + slot0 + rin_j) P + piece0 + w_j) + 1 = K + 2 (rin_j P + w_j)
+  const u64 K = 2ull * ((t0 + static_cast<u64>(slot0)) * P + static_cast<u64>(piece0)) + 1ull;
+  const u64 B0 = K + 2ull * (static_cast<u64>(pl.rin0) * P + static_cast<u64>(pl.w0));
+  const u64 B1 = K + 2ull * (static_cast<u64>(pl.rin1) * P + static_cast<u64>(pl.w1));
+  return m * (B0 * S0 + B1 * S1 + 2ull * P * static_cast<u64>(pl.pr) * (T0 + T1));
+}
+
 // This lane's share of one page (one half of one cache at one position) in
 // the page's layout, cut into runs of whole rows:
 //   NHD, latent   one run of nv rows of heads * hb (latent: one row) bytes
@@ -171,7 +284,7 @@ __device__ __forceinline__ u64 run_sum(const unsigned char *base, int nrows, con
 //                 sub-blocks, per (sub-block, head) one run of its valid slots
 //   x-split       per (head, 16-byte chunk) one run of nv 16-byte slots
 __device__ __forceinline__ u64 page_sum(const DevCache &C, const unsigned char *page, int half,
-                                        int nv, u64 t0, long long bs, int lane) {
+                                        int nv, u64 t0, long long bs, int lane, RunPlan &pl) {
   const u64 P = static_cast<u64>(C.P);
   const int hw = C.hb >> 3;
   RunShape R;
@@ -186,6 +299,8 @@ __device__ __forceinline__ u64 page_sum(const DevCache &C, const unsigned char *
   } else if (C.layout == kLayoutHND) {
     R.rowb = C.hb;
     const int kbs = C.kbs;
+    // runs of one shape (rows of at most 512 bytes) share a plan
+    const bool planned = (C.hb & 15) == 0 ? C.hb <= 512 : 2 * C.hb <= 512;
     for (int sb = 0; sb * kbs < nv; ++sb) {
       R.slot0 = sb * kbs;
       const int rows = min(kbs, nv - sb * kbs);
@@ -193,7 +308,14 @@ __device__ __forceinline__ u64 page_sum(const DevCache &C, const unsigned char *
         R.head = h;
         const unsigned char *run =
             page + (static_cast<long long>(sb) * C.heads + h) * kbs * C.hb;
-        acc += run_sum(run, rows, R, C.m0, t0, P, lane);
+        if (planned) {
+          const int d = static_cast<int>(reinterpret_cast<uintptr_t>(run) & 15u);
+          if (pl.nrows != rows || pl.d != d || pl.rowb != C.hb) plan_runs(pl, C.hb, rows, d, lane);
+          acc += run_sum_planned(run, pl, C.m0 + 2ull * static_cast<u64>(h), t0, P, R.slot0,
+                                 R.piece0);
+        } else {
+          acc += run_sum(run, rows, R, C.m0, t0, P, lane);
+        }
       }
     }
   } else {  // x-split
@@ -204,7 +326,10 @@ __device__ __forceinline__ u64 page_sum(const DevCache &C, const unsigned char *
       for (int c = 0; c < chunks; ++c) {
         R.piece0 = half * hw + 2 * c;
         const unsigned char *run = page + (static_cast<long long>(h) * chunks + c) * bs * 16;
-        acc += run_sum(run, nv, R, C.m0, t0, P, lane);
+        const int d = static_cast<int>(reinterpret_cast<uintptr_t>(run) & 15u);
+        if (pl.rowb != 16 || pl.d != d || pl.nrows != nv) plan_runs(pl, 16, nv, d, lane);
+        acc += run_sum_planned(run, pl, C.m0 + 2ull * static_cast<u64>(h), t0, P, 0,
+                               R.piece0);
       }
     }
   }
@@ -250,6 +375,11 @@ __device__ __forceinline__ void walk_seek(const Params &p, DirectWalk &w, long l
 __global__ void __launch_bounds__(kDirectThreads, 4)
     kvcs_direct_kernel(const __grid_constant__ Params p) {
   __shared__ DirectWalk walks[kDirectThreads / 32];
+  // each lane's run plan, kept in shared memory (the registers go to the
+  // loads in flight) and reused while the run shape stays the same
+  __shared__ RunPlan plans[kDirectThreads];
+  RunPlan &pl = plans[threadIdx.x];
+  pl.rowb = -1;
   const int lane = threadIdx.x & 31;
   const long long wpc = kDirectThreads / 32;
   const long long warp = static_cast<long long>(blockIdx.x) * wpc + (threadIdx.x >> 5);
@@ -287,7 +417,7 @@ __global__ void __launch_bounds__(kDirectThreads, 4)
       const unsigned char *page = C.base + static_cast<long long>(half) * C.half_stride +
                                   wk.block * C.block_stride;
       acc += page_sum(C, page, half, wk.nv, static_cast<u64>(wk.q) * static_cast<u64>(bs), bs,
-                      lane);
+                      lane, pl);
     }
     int nci = ci, nhalf = half + 1;
     bool pos_done = false;
