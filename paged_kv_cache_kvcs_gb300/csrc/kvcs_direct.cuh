@@ -237,6 +237,7 @@ __device__ __forceinline__ void plan_runs(RunPlan &pl, int rowb, int nrows, int 
 // This lane's share of one run of the planned shape whose words are pieces
 // piece0 + (word in the row) of one head, weighted m = m0 + 2 head, the
 // run's row r holding the token in slot slot0 + r: run_sum's result.
+template <int kB = kDirectBatch>
 __device__ __forceinline__ u64 run_sum_planned(const unsigned char *base, const RunPlan &pl,
                                                u64 m, u64 t0, u64 P, int slot0, int piece0) {
   if (!pl.active) return 0;
@@ -246,16 +247,16 @@ __device__ __forceinline__ u64 run_sum_planned(const unsigned char *base, const 
   if (pl.tail) xt = ld_stream8(A + pl.tail_off);
   u64 S0 = 0, T0 = 0, S1 = 0, T1 = 0;
   const unsigned char *cp = A + pl.first_off;
-  for (int s = pl.s0; s < pl.s_full; s += kDirectBatch * pl.rstep) {
-    uint4 v[kDirectBatch];
+  for (int s = pl.s0; s < pl.s_full; s += kB * pl.rstep) {
+    uint4 v[kB];
 #pragma unroll
-    for (int k = 0; k < kDirectBatch; ++k) {
+    for (int k = 0; k < kB; ++k) {
       v[k] = make_uint4(0u, 0u, 0u, 0u);
       if (s + k * pl.rstep < pl.s_full) v[k] = ld_stream16(cp + k * pl.lstep);
     }
-    cp += kDirectBatch * pl.lstep;
+    cp += kB * pl.lstep;
 #pragma unroll
-    for (int k = 0; k < kDirectBatch; ++k) {
+    for (int k = 0; k < kB; ++k) {
       const u64 sk = static_cast<u64>(static_cast<u32>(s + k * pl.rstep));
       const u64 x0 = (static_cast<u64>(v[k].y) << 32) | v[k].x;
       const u64 x1 = (static_cast<u64>(v[k].w) << 32) | v[k].z;
@@ -304,6 +305,28 @@ __device__ __forceinline__ u64 page_sum(const DevCache &C, const unsigned char *
     for (int sb = 0; sb * kbs < nv; ++sb) {
       R.slot0 = sb * kbs;
       const int rows = min(kbs, nv - sb * kbs);
+      const long long hstride = static_cast<long long>(kbs) * C.hb;
+      const unsigned char *sbp = page + static_cast<long long>(sb) * C.heads * hstride;
+      if (planned && (hstride & 15) == 0) {
+        // every head run of the sub-block has one shape: two runs at a time,
+        // four loads each, in flight together
+        const int d = static_cast<int>(reinterpret_cast<uintptr_t>(sbp) & 15u);
+        if (pl.nrows != rows || pl.d != d || pl.rowb != C.hb) plan_runs(pl, C.hb, rows, d, lane);
+        int h = 0;
+        for (; h + 1 < C.heads; h += 2) {
+          const u64 a0 = run_sum_planned<4>(sbp + h * hstride, pl,
+                                            C.m0 + 2ull * static_cast<u64>(h), t0, P, R.slot0,
+                                            R.piece0);
+          const u64 a1 = run_sum_planned<4>(sbp + (h + 1) * hstride, pl,
+                                            C.m0 + 2ull * static_cast<u64>(h + 1), t0, P,
+                                            R.slot0, R.piece0);
+          acc += a0 + a1;
+        }
+        if (h < C.heads)
+          acc += run_sum_planned<4>(sbp + h * hstride, pl, C.m0 + 2ull * static_cast<u64>(h),
+                                    t0, P, R.slot0, R.piece0);
+        continue;
+      }
       for (int h = 0; h < C.heads; ++h) {
         R.head = h;
         const unsigned char *run =
