@@ -308,21 +308,21 @@ __device__ __forceinline__ u64 page_sum(const DevCache &C, const unsigned char *
       const long long hstride = static_cast<long long>(kbs) * C.hb;
       const unsigned char *sbp = page + static_cast<long long>(sb) * C.heads * hstride;
       if (planned && (hstride & 15) == 0) {
-        // every head run of the sub-block has one shape: two runs at a time,
-        // four loads each, in flight together
+        // every head run of the sub-block has one shape: four runs at a time,
+        // two loads each, in flight together
         const int d = static_cast<int>(reinterpret_cast<uintptr_t>(sbp) & 15u);
         if (pl.nrows != rows || pl.d != d || pl.rowb != C.hb) plan_runs(pl, C.hb, rows, d, lane);
         int h = 0;
-        for (; h + 1 < C.heads; h += 2) {
-          const u64 a0 = run_sum_planned<4>(sbp + h * hstride, pl,
-                                            C.m0 + 2ull * static_cast<u64>(h), t0, P, R.slot0,
-                                            R.piece0);
-          const u64 a1 = run_sum_planned<4>(sbp + (h + 1) * hstride, pl,
-                                            C.m0 + 2ull * static_cast<u64>(h + 1), t0, P,
-                                            R.slot0, R.piece0);
-          acc += a0 + a1;
+        for (; h + 3 < C.heads; h += 4) {
+          u64 a[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            a[i] = run_sum_planned<2>(sbp + (h + i) * hstride, pl,
+                                      C.m0 + 2ull * static_cast<u64>(h + i), t0, P, R.slot0,
+                                      R.piece0);
+          acc += (a[0] + a[1]) + (a[2] + a[3]);
         }
-        if (h < C.heads)
+        for (; h < C.heads; ++h)
           acc += run_sum_planned<4>(sbp + h * hstride, pl, C.m0 + 2ull * static_cast<u64>(h),
                                     t0, P, R.slot0, R.piece0);
         continue;
