@@ -407,7 +407,10 @@ typedef struct kvcs_plan_info {
   int32_t memsets;       /* output-zeroing launches per call (0 or 1): one
                             small kernel before the checksum launches, which
                             overlap it (programmatic dependent launch) */
-  int32_t grid;          /* CTAs per kernel launch */
+  int32_t grid;          /* CTAs per kernel launch (a call with at most two
+                            positions per request, mostly partial blocks,
+                            launches twice this many CTAs for its NHD, latent
+                            and HND caches) */
   int32_t threads;       /* threads per CTA */
   int32_t smem_bytes;    /* dynamic shared memory per CTA */
   int32_t stage_bytes;   /* bytes per pipeline stage (bulk kernel) */

@@ -630,17 +630,18 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       // request is partial, so at most about two positions per request)
       // pack many pages into a unit; they take the instances whose whole
       // producer warp issues the copies and whose consumers reduce packed
-      // units at once.  Their page-address table takes shared memory from
-      // the ring (one stage less where the ring fills it).
+      // units at once.  Their producers, not DRAM, set the pace, so they
+      // run two CTAs a SM (two producers), each with half the shared
+      // memory: its page-address table and a ring of fewer stages.
       const bool wide = p.pack && total_positions <= 2 * reqs->num_requests &&
                         (l.family == kFamRows || l.family == kFamHnd);
       if (wide)
-        p.stages = std::min(p.stages,
-                            (kSmemLimit - kHeaderBytes - kWideTableBytes) / p.stage_bytes);
+        p.stages = std::max(1, std::min(p.stages, (kSmemLimit / 2 - 1024 - kHeaderBytes -
+                                                    kWideTableBytes) / p.stage_bytes));
       p.split = pl.split;
       p.group_warps = group_warps_for(p.stages);
       p.groups = kConsumerWarps / p.group_warps;
-      long long grid = pl.bulk_grid;
+      long long grid = pl.bulk_grid * (wide ? 2 : 1);
       if (p.split) grid = std::max<long long>(1, std::min<long long>(grid, p.total_units));
       const size_t smem = bulk_smem_bytes(p.stages, p.stage_bytes) + (wide ? kWideTableBytes : 0);
       const dim3 gd(static_cast<unsigned>(grid));

@@ -609,8 +609,9 @@ __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
 // every lane computes the same cursor, lane 0 alone waits, writes metadata
 // and counters, and the lanes share out the copies of a unit's pages; the
 // consumers then reduce packed units of several pages with packed_sum.
+// The wide instances run two CTAs a SM (each with half the shared memory).
 template <int kFam, bool kWide>
-__global__ void __launch_bounds__(kBulkThreads, 1)
+__global__ void __launch_bounds__(kBulkThreads, kWide ? 2 : 1)
     kvcs_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   SmemHeader *hdr = reinterpret_cast<SmemHeader *>(smem);
