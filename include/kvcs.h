@@ -94,8 +94,14 @@ typedef enum kvcs_layout {
  * the layout's order (STATE: num_heads * head_bytes); the page of
  * (half, block) starts at base + half * half_stride + block * block_stride. */
 typedef struct kvcs_cache {
-  const void *base;    /* DEVICE pointer to the pool; 8-byte aligned
-                          (16-byte alignment enables the bulk-copy kernel) */
+  const void *base;    /* DEVICE pointer to the pool; 8-byte aligned.  Pools
+                          and strides that are 16-byte multiples are read
+                          with plain bulk copies, those only 8-byte aligned
+                          (NHD, latent, HND without sub-blocks, x-split)
+                          with bulk copies of the aligned interiors and
+                          8-byte copies of the edge words; the rest, and
+                          heads of 8 mod 16 bytes, with direct loads.
+                          Results are the same either way. */
   int64_t num_blocks;  /* pages in the pool; valid block ids are [0, num_blocks) */
   int32_t layout;      /* a kvcs_layout */
   int32_t layer;       /* layer number taken from the layer's name, >= 0 */
