@@ -109,6 +109,30 @@ def test_repeated_calls_on_the_same_workload():
     assert torch.equal(o1, ref2) and not torch.equal(ref2, ref)
 
 
+def test_two_decode_shaped_calls_in_a_row():
+    """The newest block of each of 4096 requests (one valid token each), NHD
+    then HND: calls of mostly partial blocks, which take the wide instances,
+    back to back through the shared counters."""
+    calls = [W.llama3_8b_decode(s, DEV, num_requests=4096, layout=lay)
+             for s, lay in ((3, W.LAYOUT_NHD), (4, W.LAYOUT_HND))]
+    for wl in calls:
+        assert wl.num_positions == wl.num_requests and _uses_counters(wl)
+    s = torch.cuda.Stream()
+    outs = [torch.empty(wl.num_positions, dtype=torch.int64, device=DEV) for wl in calls]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    for wl, out in zip(calls, outs):
+        assert _noalloc(wl, out, st, s.cuda_stream) == K.KVCS_OK
+    with torch.cuda.stream(s):
+        refs = [_existing(wl, s.cuda_stream) for wl in calls]
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for out, ref in zip(outs, refs):
+        assert torch.equal(out, ref)
+    del calls
+    torch.cuda.empty_cache()
+
+
 def test_small_call_and_limits():
     """A call too small for the counters (fixed split) still equals the
     existing entry; more than KVCS_NOALLOC_MAX_CACHES caches is refused
