@@ -469,12 +469,12 @@ __device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m, in
 }
 
 // The consumer group's fetch of a unit whose pages it reads itself (the wide
-// HND instance, partial blocks of several heads): each page's valid rows
-// (rows family; not used at present) or each head's nv valid slots (HND)
+// HND instance, partial blocks of several heads): each head's nv valid slots
 // by 16-byte cp.async, into the same compact layout the producer's bulk
-// copies give, the group's threads taking consecutive 16-byte chunks.  `block` is the position's physical block;
-// pages are (cache, half) from the unit's first on.
-template <int kFam>
+// copies give ([head][nv][head_bytes] per page), the group's threads taking
+// consecutive 16-byte chunks.  The unit's `first` field holds the
+// position's physical block; its pages are (cache, half) from the unit's
+// first on.
 __device__ __forceinline__ void gather_unit(const Params &p, const UnitMeta &m,
                                             const PageAddr *tab, u32 stage, int gtid, int nt,
                                             long long bs) {
@@ -483,47 +483,31 @@ __device__ __forceinline__ void gather_unit(const Params &p, const UnitMeta &m,
   const int H = C0.halves;
   int ci = m.cache, half = m.half;
   u32 dst = stage;
-  if constexpr (kFam == kFamRows) {
-    const u32 cpg = static_cast<u32>(m.count) * static_cast<u32>(C0.rowb) >> 4;
-    for (int k = 0; k < m.npages; ++k) {
-      const PageAddr a = tab[ci];
-      const unsigned char *src = a.base + static_cast<long long>(half) * a.half_stride +
-                                 block * a.block_stride;
-      for (u32 j = static_cast<u32>(gtid); j < cpg; j += static_cast<u32>(nt))
-        ptx::cp_async16(dst + (j << 4), src + (static_cast<size_t>(j) << 4));
-      dst += cpg << 4;
-      if (++half == H) {
-        half = 0;
-        ++ci;
+  const u32 cph = static_cast<u32>(m.nv) * static_cast<u32>(C0.hb) >> 4;  // chunks a head
+  const u32 cpg = static_cast<u32>(m.count) * cph;
+  const size_t hstride = static_cast<size_t>(bs) * C0.hb;                  // a head's slots
+  // this thread's chunks j = gtid + i nt of a page, as (head, chunk in the
+  // head's run), stepped without a division per chunk
+  const u32 h0 = static_cast<u32>(gtid) / cph, c0 = static_cast<u32>(gtid) - h0 * cph;
+  const u32 dh = static_cast<u32>(nt) / cph, dc = static_cast<u32>(nt) - dh * cph;
+  for (int k = 0; k < m.npages; ++k) {
+    const PageAddr a = tab[ci];
+    const unsigned char *src = a.base + static_cast<long long>(half) * a.half_stride +
+                               block * a.block_stride;
+    u32 h = h0, c = c0;
+    for (u32 j = static_cast<u32>(gtid); j < cpg; j += static_cast<u32>(nt)) {
+      ptx::cp_async16(dst + (j << 4), src + h * hstride + (static_cast<size_t>(c) << 4));
+      h += dh;
+      c += dc;
+      if (c >= cph) {
+        c -= cph;
+        ++h;
       }
     }
-  } else {
-    const u32 cph = static_cast<u32>(m.nv) * static_cast<u32>(C0.hb) >> 4;  // chunks a head
-    const u32 cpg = static_cast<u32>(m.count) * cph;
-    const size_t hstride = static_cast<size_t>(bs) * C0.hb;                  // a head's slots
-    // this thread's chunks j = gtid + i nt of a page, as (head, chunk in the
-    // head's run), stepped without a division per chunk
-    const u32 h0 = static_cast<u32>(gtid) / cph, c0 = static_cast<u32>(gtid) - h0 * cph;
-    const u32 dh = static_cast<u32>(nt) / cph, dc = static_cast<u32>(nt) - dh * cph;
-    for (int k = 0; k < m.npages; ++k) {
-      const PageAddr a = tab[ci];
-      const unsigned char *src = a.base + static_cast<long long>(half) * a.half_stride +
-                                 block * a.block_stride;
-      u32 h = h0, c = c0;
-      for (u32 j = static_cast<u32>(gtid); j < cpg; j += static_cast<u32>(nt)) {
-        ptx::cp_async16(dst + (j << 4), src + h * hstride + (static_cast<size_t>(c) << 4));
-        h += dh;
-        c += dc;
-        if (c >= cph) {
-          c -= cph;
-          ++h;
-        }
-      }
-      dst += cpg << 4;
-      if (++half == H) {
-        half = 0;
-        ++ci;
-      }
+    dst += cpg << 4;
+    if (++half == H) {
+      half = 0;
+      ++ci;
     }
   }
 }
@@ -1105,7 +1089,7 @@ __global__ void __launch_bounds__(kBulkThreads, kWide ? 2 : 1)
         // fetch the unit's valid bytes, then wait (bounded) until every
         // thread's copies of the group have landed
         const u32 lb = ptx::smem_addr(&wt->landed[s]);
-        gather_unit<kFam>(p, m, wt->page, ptx::smem_addr(sp), gtid, gw * 32,
+        gather_unit(p, m, wt->page, ptx::smem_addr(sp), gtid, gw * 32,
                           static_cast<long long>(bsz));
         ptx::cp_async_mbar_arrive_noinc(lb);
         const bool landed =
