@@ -113,3 +113,24 @@ def test_decode_with_workspace(layout):
     _check(wl, workspace=True)
     del wl
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND])
+def test_accumulating_calls(layout):
+    """An accumulating call (every result added into the caller's words)
+    through the wide instances, twice onto the same words: twice the
+    oracle's checksums, mod 2^64."""
+    from gpu_helpers import full_oracle
+    lengths, first = _newest_blocks(31, 200, 16)
+    wl = W.random_case(12, DEV, layout=layout, layers=4, heads=8, head_bytes=256, block_size=16,
+                       lengths=lengths, first_positions=first)
+    exp, st = full_oracle(wl)
+    assert st == 0
+    vals = torch.zeros((wl.num_positions, 1), dtype=torch.int64, device=DEV)
+    for _ in range(2):
+        K.group_checksums(wl.caches, wl.block_size, wl.pos_offsets, wl.first_position,
+                          wl.num_tokens, wl.block_ids, 1, values=vals, accumulate=True,
+                          total_positions=wl.num_positions)
+    torch.cuda.synchronize()
+    got = vals.cpu().numpy().view(np.uint64).reshape(-1)
+    assert np.array_equal(got, exp.reshape(-1) * np.uint64(2))
