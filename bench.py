@@ -201,7 +201,8 @@ def work_share(wl, args) -> str:
     import paged_kv_cache_kvcs_gb300 as kvcs
     sms = (torch.cuda.get_device_properties(0).multi_processor_count
            if torch.cuda.is_available() else 152)
-    plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions, num_sms=sms)
+    plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions, num_sms=sms,
+                         num_requests=wl.num_requests)
     if plan["kernel"] == 1:
         return "fixed (no bulk-copy launch: the direct-load kernel's warps own fixed ranges)"
     return ("dynamic (workspace)" if plan["dynamic"]
@@ -293,6 +294,8 @@ KERNEL_SOURCES = {
     "kvcs_bulk_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_bulk.cuh"],
     "kvcs_write_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_write.cuh"],
     "kvcs_direct_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_direct.cuh"],
+    "kvcs_slots_kernel": ["kvcs.cu", "kvcs_common.cuh", "kvcs_ptx.cuh", "kvcs_direct.cuh",
+                          "kvcs_slots.cuh"],
 }
 
 
@@ -735,7 +738,8 @@ def time_checksums(wl, args, dev, stream, ws, rank, steps, warmup, clocks=True) 
     import paged_kv_cache_kvcs_gb300 as kvcs
     out = torch.empty(wl.num_positions, dtype=torch.int64, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions)
+    plan = kvcs.plan_for(wl.caches, wl.block_size, wl.num_positions,
+                         num_requests=wl.num_requests)
     raw_stream = stream.cuda_stream
     ncols = max(1, args.columns)
     values = None
@@ -874,7 +878,8 @@ def roofline_of(r, workload: str) -> dict:
     peak, peak_kind = measured_peak()
     achieved = r["nbytes"] / r["launch_s"] / 1e9
     plan = r["plan"]
-    kernel = direct_kernel_name(r) if plan["kernel"] == 1 else "kvcs_bulk_kernel"
+    kernel = (direct_kernel_name(r) if plan["kernel"] == 1 else
+              "kvcs_slots_kernel" if plan["kernel"] == 3 else "kvcs_bulk_kernel")
     traffic = (profiled_traffic(workload, plan["units"], kernel=kernel)
                if kernel in KERNEL_SOURCES else None)
     return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,

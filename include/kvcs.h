@@ -256,8 +256,13 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
  * the call ends with its slowest SM).  Only calls of at least 1024 work
  * units (KV pages, kvcs_plan's `units`) per SM use it; smaller calls keep
  * the fixed shares, which suit them better, and leave the workspace alone.
- * One counter is used per bulk-copy launch, for the first
- * KVCS_WORKSPACE_WORDS launches.  The call zeroes the words it uses itself;
+ * The valid-slot kernel (calls of at most two positions per request: their
+ * latent and HND caches) uses it the same way from 64 pages per warp on:
+ * each warp reads a fixed quarter share of the pages, then ranges of the
+ * rest that shrink as they run out (the positions' valid slots, and so
+ * their bytes, differ).  One counter is used per bulk-copy or valid-slot
+ * launch, for the first KVCS_WORKSPACE_WORDS launches.  The call zeroes the
+ * words it uses itself;
  * their contents afterwards are unspecified.  Calls that may run at the
  * same time on the GPU (other streams) must use different workspaces.
  */
@@ -401,11 +406,14 @@ int kvcs_write_kv(const kvcs_cache *caches, int32_t num_caches, int32_t block_si
                   void *stream);
 
 /* Which kernel and launch shape kvcs_block_checksums would use.  Filled by
- * kvcs_plan; no CUDA work is enqueued. */
+ * kvcs_plan and kvcs_plan_requests; no CUDA work is enqueued. */
 typedef struct kvcs_plan_info {
   int32_t kernel;        /* 0 = bulk-copy pipeline, 1 = generic direct
                             loads, 2 = both (caches the bulk kernel cannot
-                            stage go to the generic one) */
+                            stage go to the generic one), 3 = the valid-slot
+                            kernel for every launch (a call with at most two
+                            positions per request over latent or HND
+                            caches; the fields below then describe it) */
   int32_t split;         /* 1 if the bulk kernel splits positions across CTAs
                             (output zeroed first, partial sums added with
                             64-bit atomics; the generic kernel always adds) */
@@ -415,17 +423,21 @@ typedef struct kvcs_plan_info {
                             overlap it (programmatic dependent launch) */
   int32_t grid;          /* CTAs per kernel launch (a call with at most two
                             positions per request, mostly partial blocks,
-                            launches twice this many CTAs for its NHD, latent
-                            and HND caches) */
+                            launches twice this many CTAs for its NHD
+                            caches) */
   int32_t threads;       /* threads per CTA */
   int32_t smem_bytes;    /* dynamic shared memory per CTA */
   int32_t stage_bytes;   /* bytes per pipeline stage (bulk kernel) */
   int32_t stages;        /* pipeline stages per CTA (bulk kernel) */
   int32_t dynamic;       /* 1 if the same call given a workspace
                             (KVCS_OUT_WORKSPACE) would share the bulk
-                            kernel's last units out dynamically (one more
-                            small zeroing launch per call); 0 otherwise */
-  int64_t units;         /* work units (page pieces) per launch */
+                            kernel's (or the valid-slot kernel's) last units
+                            out dynamically (one more small zeroing launch
+                            per call); 0 otherwise */
+  int32_t slot_launches; /* launches on the valid-slot kernel (0 from
+                            kvcs_plan, which does not know the requests) */
+  int64_t units;         /* work units (page pieces; for the valid-slot
+                            kernel, pages) per launch */
   int64_t kv_bytes_max;  /* KV bytes if every position held block_size tokens */
 } kvcs_plan_info;
 
@@ -436,6 +448,18 @@ typedef struct kvcs_plan_info {
  */
 int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
               int64_t total_positions, int32_t num_sms, kvcs_plan_info *info);
+
+/*
+ * kvcs_plan_requests -- as kvcs_plan, for a call of num_requests requests
+ * (reqs->num_requests of the checksum call): a call of at most two
+ * positions per request (total_positions <= 2 num_requests) sends its
+ * latent and HND caches (no kernel sub-blocks, 16-byte aligned, all of one
+ * geometry) to the valid-slot kernel, which kvcs_plan cannot tell.
+ * num_requests < 0 plans as kvcs_plan does.
+ */
+int kvcs_plan_requests(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+                       int64_t total_positions, int64_t num_requests, int32_t num_sms,
+                       kvcs_plan_info *info);
 
 /*
  * kvcs_selftest_wait_timeout -- check, on the caller's GPU, that a pipeline
@@ -461,7 +485,9 @@ uint64_t kvcs_launch_count(void);
 /* ABI version: (major << 16) | minor.  Minor 2 added kvcs_write_kv and
  * kvcs_outputs.flags (KVCS_OUT_ACCUMULATE; the field was reserved, 0).
  * Minor 3 added kvcs_outputs.workspace, read only when flags has
- * KVCS_OUT_WORKSPACE (callers built against minor 2 never set it). */
+ * KVCS_OUT_WORKSPACE (callers built against minor 2 never set it).
+ * Minor 4 added kvcs_plan_requests and kvcs_plan_info.slot_launches (the
+ * struct grew: callers pass the minor-4 layout). */
 int32_t kvcs_version(void);
 
 #ifdef __cplusplus

@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     KVCS_MAX_KV_HEADS_PER_LAYER, KVCS_OK, KVCS_STATUS_BAD_BLOCK_ID,
     KVCS_STATUS_BAD_REQUESTS, KVCS_STATUS_TIMEOUT, KvcsError, block_checksums,
     cache_array, kvcs_block_checksums, kvcs_cache, kvcs_plan, kvcs_plan_info,
+    kvcs_plan_requests,
     kvcs_requests, launch_count, load_library, plan_for, selftest_wait_timeout,
     strerror, version,
     workload_checksums, Checksummer, workload_checksummer, kvcs_outputs,

@@ -67,6 +67,7 @@ class kvcs_plan_info(ctypes.Structure):
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("dynamic", ctypes.c_int32),
+                ("slot_launches", ctypes.c_int32),
                 ("units", ctypes.c_int64), ("kv_bytes_max", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
@@ -97,6 +98,9 @@ SIGNATURES = {
     "kvcs_plan": (ctypes.c_int, [
         ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(kvcs_plan_info)]),
+    "kvcs_plan_requests": (ctypes.c_int, [
+        ctypes.POINTER(kvcs_cache), ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(kvcs_plan_info)]),
     "kvcs_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64,
                                                    ctypes.c_void_p]),
     "kvcs_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -201,6 +205,16 @@ def kvcs_plan(caches: ctypes.Array, num_caches: int, block_size: int,
                                   total_positions, num_sms, ctypes.byref(info))
     if rc != KVCS_OK:
         raise KvcsError(rc, "kvcs_plan")
+    return info.as_dict()
+
+
+def kvcs_plan_requests(caches: ctypes.Array, num_caches: int, block_size: int,
+                       total_positions: int, num_requests: int, num_sms: int = 0) -> dict:
+    info = kvcs_plan_info()
+    rc = load_library().kvcs_plan_requests(caches, num_caches, block_size, total_positions,
+                                           num_requests, num_sms, ctypes.byref(info))
+    if rc != KVCS_OK:
+        raise KvcsError(rc, "kvcs_plan_requests")
     return info.as_dict()
 
 
@@ -449,9 +463,14 @@ def workload_checksummer(wl, workspace=None) -> Checksummer:
 
 
 def plan_for(caches: Sequence, block_size: int, total_positions: int,
-             num_sms: int = 0) -> dict:
-    return kvcs_plan(cache_array(caches), len(caches), block_size,
-                     total_positions, num_sms)
+             num_sms: int = 0, num_requests: int | None = None) -> dict:
+    """The plan of a call (``kvcs_plan``, or ``kvcs_plan_requests`` when
+    ``num_requests`` is given)."""
+    if num_requests is None:
+        return kvcs_plan(cache_array(caches), len(caches), block_size,
+                         total_positions, num_sms)
+    return kvcs_plan_requests(cache_array(caches), len(caches), block_size,
+                              total_positions, num_requests, num_sms)
 
 
 def selftest_wait_timeout(status, limit_ns: int, stream=None) -> None:

@@ -21,6 +21,7 @@
 #include "kvcs.h"
 #include "kvcs_bulk.cuh"
 #include "kvcs_direct.cuh"
+#include "kvcs_slots.cuh"
 #include "kvcs_epilogue.cuh"
 #include "kvcs_state.cuh"
 #include "kvcs_write.cuh"
@@ -66,8 +67,7 @@ cudaError_t device_setup(int *sms) {
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRowsMis, false>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHndMis, false>),
                            reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamXSplitMis, false>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows, true>),
-                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamHnd, true>)})
+                           reinterpret_cast<const void *>(kvcs_bulk_kernel<kFamRows, true>)})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
@@ -339,6 +339,7 @@ int family_of(const kvcs_cache &c, int block_size) {
 constexpr int kKernelBulk = 0;
 constexpr int kKernelDirect = 1;
 constexpr int kKernelState = 2;
+constexpr int kKernelSlots = 3;
 
 struct Launch {
   int kernel;
@@ -349,9 +350,11 @@ struct Launch {
 // How a call runs: caches the bulk kernel can stage go to its instance for
 // their layout family (up to kMaxCachesPerLaunch per launch), the other KV
 // caches to the direct-load kernel and the other state caches to the
-// state-row kernel.  With more than one launch, or a direct-load or
-// state-row launch, every result is added atomically into an output zeroed
-// first.
+// state-row kernel.  In a call whose blocks are mostly partial (at most two
+// positions per request), a launch of alike NHD, latent or HND pages goes
+// to the valid-slot kernel instead.  With more than one launch, or a
+// direct-load, state-row or valid-slot launch, every result is added
+// atomically into an output zeroed first.
 struct Plan {
   std::vector<Launch> launches;
   int kernel = 0;         // 0 bulk only, 1 direct loads only, 2 both
@@ -381,9 +384,43 @@ constexpr long long kPoolShare = 16;
 constexpr long long kChunksPerCta = 8;
 constexpr long long kMinChunkUnits = 16;
 
+// Caches of one launch the valid-slot kernel reads: latent or HND (no kernel
+// sub-blocks) pages the bulk kernel stages without the misaligned split, all
+// of one geometry, each page under 2 GiB (its byte offsets fit 32 bits).
+// NHD pages of such calls stay with the bulk kernel: a partial NHD page's
+// valid slots are one contiguous run, which its bulk copies fetch with more
+// bytes in flight than registers hold (measured on the newest blocks of
+// 256 to 16384 requests of 1 to 15 tokens: the bulk copies 5 to 17% faster;
+// with one token a block the register loads were 41% faster).
+bool slots_eligible(int family, const kvcs_cache *c, size_t n, int32_t block_size) {
+  if (family != kFamHnd && !(family == kFamRows && c[0].layout == KVCS_LAYOUT_LATENT))
+    return false;
+  for (size_t i = 0; i < n; ++i) {
+    if (c[i].layout != c[0].layout || c[i].num_heads != c[0].num_heads ||
+        c[i].head_bytes != c[0].head_bytes)
+      return false;
+  }
+  return page_bytes_of(c[0], block_size) < (1LL << 31);
+}
+
+// CTAs of a valid-slot launch over `pages` pages: kSlotsCtasPerSm a SM,
+// fewer when there are few pages (a warp at least kSlotsPages of them).
+long long slots_grid(long long pages, int sms) {
+  const long long per_cta = static_cast<long long>(kSlotsWarps) * kSlotsPages;
+  return std::max<long long>(1, std::min<long long>(static_cast<long long>(kSlotsCtasPerSm) * sms,
+                                                    (pages + per_cta - 1) / per_cta));
+}
+
+// Whether a valid-slot launch with a work counter hands its last pages out
+// from it: at least kSlotsDynamicPages pages a warp.
+bool slots_dynamic(long long pages, long long grid) {
+  return pages >= kSlotsDynamicPages * kSlotsWarps * grid;
+}
+
+// num_requests < 0: not known (kvcs_plan), planned as a call of whole blocks.
 Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
                int64_t total_positions, int sms, bool accumulate = false,
-               bool workspace = false) {
+               bool workspace = false, long long num_requests = -1) {
   Plan pl;
   std::vector<kvcs_cache> fam[kNumFamilies], gen;
   std::vector<kvcs_cache> bulk;
@@ -398,22 +435,29 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
         (c.layout == KVCS_LAYOUT_LATENT || c.layout == KVCS_LAYOUT_STATE) ? 1 : 2;
     pl.kv_bytes_max += halves * page_bytes_of(c, block_size) * total_positions;
   }
+  const bool partial = num_requests >= 0 && total_positions <= 2 * num_requests;
+  bool has_bulk = false, has_slots = false;
   for (int f = 0; f <= kNumFamilies; ++f) {
     const std::vector<kvcs_cache> &set = f < kNumFamilies ? fam[f] : gen;
     for (size_t lo = 0; lo < set.size(); lo += kMaxCachesPerLaunch) {
       const size_t hi = std::min(set.size(), lo + kMaxCachesPerLaunch);
-      const int kernel = f < kNumFamilies ? kKernelBulk
-                         : set[lo].layout == KVCS_LAYOUT_STATE ? kKernelState
-                                                                : kKernelDirect;
+      int kernel = f < kNumFamilies ? kKernelBulk
+                   : set[lo].layout == KVCS_LAYOUT_STATE ? kKernelState
+                                                          : kKernelDirect;
+      if (kernel == kKernelBulk && partial &&
+          slots_eligible(f, set.data() + lo, hi - lo, block_size))
+        kernel = kKernelSlots;
+      has_bulk = has_bulk || kernel == kKernelBulk;
+      has_slots = has_slots || kernel == kKernelSlots;
       pl.launches.push_back({kernel, f < kNumFamilies ? f : 0,
                              std::vector<kvcs_cache>(set.begin() + lo, set.begin() + hi)});
     }
   }
   pl.kernel = gen.empty() ? 0 : (bulk.empty() ? 1 : 2);
   // accumulating calls add every result into the caller's values
-  pl.all_atomic = accumulate || pl.launches.size() > 1 || !gen.empty();
+  pl.all_atomic = accumulate || pl.launches.size() > 1 || !gen.empty() || has_slots;
   if (sms < 1) sms = 1;
-  if (!bulk.empty()) {
+  if (has_bulk) {
     bool first = true;
     for (const Launch &l : pl.launches) {
       if (l.kernel != kKernelBulk) continue;
@@ -465,7 +509,7 @@ Plan make_plan(const std::vector<kvcs_cache> &sorted, int32_t block_size,
   }
   if (pl.dynamic) pl.all_atomic = true;
   pl.memset = !accumulate && total_positions > 0 &&
-              (pl.all_atomic || (!bulk.empty() && pl.split));
+              (pl.all_atomic || (has_bulk && pl.split));
   return pl;
 }
 
@@ -539,12 +583,15 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
   int sms = 0;
   if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
   const Plan pl = make_plan(by_column(caches_in, num_caches), block_size, total_positions, sms,
-                            accumulate, workspace != nullptr);
+                            accumulate, workspace != nullptr, reqs->num_requests);
   // one work counter per dynamic bulk launch, at most KVCS_WORKSPACE_WORDS
+  // (and one per valid-slot launch, whose items are then handed out one at
+  // a time)
   int n_work = 0;
-  if (pl.dynamic)
-    for (const Launch &l : pl.launches)
-      if (l.kernel == kKernelBulk && n_work < KVCS_WORKSPACE_WORDS) ++n_work;
+  for (const Launch &l : pl.launches)
+    if (((l.kernel == kKernelBulk && pl.dynamic) || (l.kernel == kKernelSlots && workspace)) &&
+        n_work < KVCS_WORKSPACE_WORDS)
+      ++n_work;
 
   if (pl.memset || n_work > 0) {
     // zero the output with a kernel that lets the first checksum launch start
@@ -598,6 +645,9 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       p.caches[i] = make_dev_cache(l.caches[i], block_size);
       U += static_cast<long long>(p.caches[i].halves) * p.caches[i].upp;
     }
+    for (int i = n - 1; i >= 0; --i)
+      p.caches[i].run_end = i + 1 < n && p.caches[i + 1].column == p.caches[i].column
+                                ? p.caches[i + 1].run_end : i + 1;
     p.pack = 0;
     p.full_pages = 1;
     p.pages_per_pos = 0;
@@ -628,13 +678,14 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
     if (l.kernel == kKernelBulk) {
       // Calls whose blocks are mostly partial (at most one block of a
       // request is partial, so at most about two positions per request)
-      // pack many pages into a unit; they take the instances whose whole
-      // producer warp issues the copies and whose consumers reduce packed
-      // units at once.  Their producers, not DRAM, set the pace, so they
-      // run two CTAs a SM (two producers), each with half the shared
-      // memory: its page-address table and a ring of fewer stages.
+      // pack many pages into a unit; their NHD pages take the instance
+      // whose whole producer warp issues the copies and whose consumers
+      // reduce packed units at once.  Its producers, not DRAM, set the
+      // pace, so it runs two CTAs a SM (two producers), each with half the
+      // shared memory: its page-address table and a ring of fewer stages.
+      // (Such calls' latent and HND pages go to the valid-slot kernel.)
       const bool wide = p.pack && total_positions <= 2 * reqs->num_requests &&
-                        (l.family == kFamRows || l.family == kFamHnd);
+                        l.family == kFamRows;
       if (wide)
         p.stages = std::max(1, std::min(p.stages, (kSmemLimit / 2 - 1024 - kHeaderBytes -
                                                     kWideTableBytes) / p.stage_bytes));
@@ -648,8 +699,7 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       cudaError_t e;
       switch (l.family) {
         case kFamHnd:
-          e = wide ? launch(kvcs_bulk_kernel<kFamHnd, true>, gd, kBulkThreads, smem, st, after_zero, p)
-                   : launch(kvcs_bulk_kernel<kFamHnd, false>, gd, kBulkThreads, smem, st, after_zero, p);
+          e = launch(kvcs_bulk_kernel<kFamHnd, false>, gd, kBulkThreads, smem, st, after_zero, p);
           break;
         case kFamXSplit: e = launch(kvcs_bulk_kernel<kFamXSplit, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
         case kFamState: e = launch(kvcs_bulk_kernel<kFamState, false>, gd, kBulkThreads, smem, st, after_zero, p); break;
@@ -662,6 +712,22 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
                    : launch(kvcs_bulk_kernel<kFamRows, false>, gd, kBulkThreads, smem, st, after_zero, p);
           break;
       }
+      if (e != cudaSuccess) return KVCS_ECUDA;
+    } else if (l.kernel == kKernelSlots) {
+      p.split = 0;
+      const long long pages = total_positions * p.pages_per_pos;
+      const long long grid = slots_grid(pages, sms);
+      // with a work counter, on enough pages: the last pages handed out from it
+      p.pool_start = pages;
+      if (workspace && work_used < n_work) {
+        p.work = workspace + work_used++;
+        if (slots_dynamic(pages, grid)) p.pool_start = pages / kSlotsFixedShare;
+      }
+      const dim3 gd(static_cast<unsigned>(grid));
+      const cudaError_t e =
+          l.family == kFamHnd
+              ? launch(kvcs_slots_kernel<true>, gd, kSlotsThreads, 0, st, after_zero, p)
+              : launch(kvcs_slots_kernel<false>, gd, kSlotsThreads, 0, st, after_zero, p);
       if (e != cudaSuccess) return KVCS_ECUDA;
     } else if (l.kernel == kKernelDirect) {
       p.split = 0;
@@ -745,8 +811,9 @@ using namespace kvcs;
 
 extern "C" {
 
-int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
-              int64_t total_positions, int32_t num_sms, kvcs_plan_info *info) {
+int kvcs_plan_requests(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+                       int64_t total_positions, int64_t num_requests, int32_t num_sms,
+                       kvcs_plan_info *info) {
   if (!info || total_positions < 0) return KVCS_EINVAL;
   int rc = validate_caches(caches, num_caches, block_size, columns_of(caches, num_caches));
   if (rc != KVCS_OK) return rc;
@@ -754,12 +821,37 @@ int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
   if (sms <= 0) {
     if (device_setup(&sms) != cudaSuccess) return KVCS_ECUDA;
   }
-  const Plan pl = make_plan(by_column(caches, num_caches), block_size, total_positions, sms);
+  const std::vector<kvcs_cache> sorted = by_column(caches, num_caches);
+  const Plan pl = make_plan(sorted, block_size, total_positions, sms, false, false,
+                            num_requests);
   std::memset(info, 0, sizeof(*info));
-  info->kernel = pl.kernel;
-  info->split = pl.kernel != 1 ? pl.split : 0;
+  int n_slots = 0, n_other = 0, max_ipp = 0;
+  for (const Launch &l : pl.launches) {
+    if (l.kernel != kKernelSlots) {
+      ++n_other;
+      continue;
+    }
+    ++n_slots;
+    int ipp = 0;
+    for (const kvcs_cache &c : l.caches) ipp += c.layout == KVCS_LAYOUT_LATENT ? 1 : 2;
+    max_ipp = std::max(max_ipp, ipp);
+  }
+  info->slot_launches = total_positions > 0 ? n_slots : 0;
   info->launches = total_positions > 0 ? static_cast<int32_t>(pl.launches.size()) : 0;
   info->memsets = pl.memset ? 1 : 0;
+  info->kv_bytes_max = pl.kv_bytes_max;
+  if (n_slots > 0 && n_other == 0) {
+    // every launch on the valid-slot kernel
+    const long long pages = total_positions * max_ipp;
+    info->kernel = 3;
+    info->grid = static_cast<int32_t>(slots_grid(pages, sms));
+    info->threads = kSlotsThreads;
+    info->units = pages;
+    info->dynamic = total_positions > 0 && slots_dynamic(pages, info->grid) ? 1 : 0;
+    return KVCS_OK;
+  }
+  info->kernel = pl.kernel;
+  info->split = pl.kernel != 1 ? pl.split : 0;
   info->grid = pl.kernel == 1 ? pl.generic_grid : pl.bulk_grid;
   info->threads = pl.kernel != 1 ? kBulkThreads
                   : caches[0].layout == KVCS_LAYOUT_STATE ? kGenericThreads
@@ -768,11 +860,15 @@ int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
   info->stage_bytes = pl.kernel != 1 ? pl.stage_bytes : 0;
   info->stages = pl.kernel != 1 ? pl.stages : 0;
   info->units = pl.kernel == 1 ? total_positions : pl.units;
-  info->kv_bytes_max = pl.kv_bytes_max;
   info->dynamic = total_positions > 0 &&
-                  make_plan(by_column(caches, num_caches), block_size, total_positions, sms,
-                            false, true).dynamic ? 1 : 0;
+                  make_plan(sorted, block_size, total_positions, sms, false, true,
+                            num_requests).dynamic ? 1 : 0;
   return KVCS_OK;
+}
+
+int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
+              int64_t total_positions, int32_t num_sms, kvcs_plan_info *info) {
+  return kvcs_plan_requests(caches, num_caches, block_size, total_positions, -1, num_sms, info);
 }
 
 int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
@@ -963,6 +1059,6 @@ const char *kvcs_strerror(int code) {
 
 uint64_t kvcs_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int32_t kvcs_version(void) { return (1 << 16) | 3; }
+int32_t kvcs_version(void) { return (1 << 16) | 4; }
 
 }  // extern "C"

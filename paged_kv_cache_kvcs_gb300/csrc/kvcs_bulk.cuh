@@ -361,10 +361,9 @@ __device__ __forceinline__ u64 unit_sum(const DevCache &C, const UnitMeta &m,
 
 // This thread's share of a packed unit of several pages (launches whose
 // pages all look alike: same layout, heads and head bytes, one page per
-// (cache, half) from the unit's first on), for the rows and HND families.
-// What the pages share is worked out once: the thread's 16-byte columns
-// (rows family) or (head, column) groups (HND), their head and piece, and
-// the piece weight B of each half.  Per page only the cache's m0 and the
+// (cache, half) from the unit's first on), for the rows family.  What the
+// pages share is worked out once: the thread's 16-byte columns, their head
+// and piece, and the piece weight B of each half.  Per page only the cache's m0 and the
 // half change, so a page costs the running sums of its few valid rows and
 // one fold, m (B S + 2P T + 2U).  The sum is the one unit_sum gives page by
 // page, in another order.
@@ -380,7 +379,8 @@ __device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m, in
   const int H = C0.halves;
   const int npg = m.npages;
   u64 acc = 0;
-  if constexpr (kFam == kFamRows) {
+  static_assert(kFam == kFamRows, "packed units of several pages: rows");
+  {
     const int rowb = C0.rowb;
     const int cols = rowb >> 4;
     const int nrows = m.count;
@@ -436,80 +436,8 @@ __device__ __forceinline__ u64 packed_sum(const Params &p, const UnitMeta &m, in
         }
       }
     }
-  } else {
-    // HND: each page staged as its heads one after another, nv slots each
-    const int nv = m.nv;
-    const int hb = C0.hb;
-    const int cpr = hb >> 4;
-    const int groups = m.count * cpr;
-    const size_t pstride = static_cast<size_t>(m.count) * nv * hb;
-    for (int g = gtid; g < groups; g += nt) {
-      const int hl = g / cpr;
-      const int col = g - hl * cpr;
-      const u64 mh_off = 2ull * static_cast<u64>(first + hl);
-      const u64 B0 = 2ull * (t0P + static_cast<u64>(col << 1)) + 1ull;
-      const unsigned char *gp0 = stage + static_cast<size_t>(hl) * nv * hb + (col << 4);
-      int ci = m.cache, half = m.half;
-      // pages are independent: let the compiler overlap several
-#pragma unroll 4
-      for (int k = 0; k < npg; ++k) {
-        u64 S = 0, T = 0, U = 0;
-        accum_slots(gp0 + static_cast<size_t>(k) * pstride, static_cast<size_t>(hb), 0, nv, 0,
-                    S, T, U);
-        const u64 B = half ? B0 + hstep : B0;
-        acc += (p.caches[ci].m0 + mh_off) * (B * S + twoP * T + 2ull * U);
-        if (++half == H) {
-          half = 0;
-          ++ci;
-        }
-      }
-    }
   }
   return acc;
-}
-
-// The consumer group's fetch of a unit whose pages it reads itself (the wide
-// HND instance, partial blocks of several heads): each head's nv valid slots
-// by 16-byte cp.async, into the same compact layout the producer's bulk
-// copies give ([head][nv][head_bytes] per page), the group's threads taking
-// consecutive 16-byte chunks.  The unit's `first` field holds the
-// position's physical block; its pages are (cache, half) from the unit's
-// first on.
-__device__ __forceinline__ void gather_unit(const Params &p, const UnitMeta &m,
-                                            const PageAddr *tab, u32 stage, int gtid, int nt,
-                                            long long bs) {
-  const DevCache &C0 = p.caches[m.cache];
-  const long long block = static_cast<long long>(static_cast<u32>(m.first));
-  const int H = C0.halves;
-  int ci = m.cache, half = m.half;
-  u32 dst = stage;
-  const u32 cph = static_cast<u32>(m.nv) * static_cast<u32>(C0.hb) >> 4;  // chunks a head
-  const u32 cpg = static_cast<u32>(m.count) * cph;
-  const size_t hstride = static_cast<size_t>(bs) * C0.hb;                  // a head's slots
-  // this thread's chunks j = gtid + i nt of a page, as (head, chunk in the
-  // head's run), stepped without a division per chunk
-  const u32 h0 = static_cast<u32>(gtid) / cph, c0 = static_cast<u32>(gtid) - h0 * cph;
-  const u32 dh = static_cast<u32>(nt) / cph, dc = static_cast<u32>(nt) - dh * cph;
-  for (int k = 0; k < m.npages; ++k) {
-    const PageAddr a = tab[ci];
-    const unsigned char *src = a.base + static_cast<long long>(half) * a.half_stride +
-                               block * a.block_stride;
-    u32 h = h0, c = c0;
-    for (u32 j = static_cast<u32>(gtid); j < cpg; j += static_cast<u32>(nt)) {
-      ptx::cp_async16(dst + (j << 4), src + h * hstride + (static_cast<size_t>(c) << 4));
-      h += dh;
-      c += dc;
-      if (c >= cph) {
-        c -= cph;
-        ++h;
-      }
-    }
-    dst += cpg << 4;
-    if (++half == H) {
-      half = 0;
-      ++ci;
-    }
-  }
 }
 
 // Pages of one position a stage holds in packed launches (every page alike,
@@ -587,13 +515,13 @@ __device__ __forceinline__ void finalize_slot(const Params &p, SmemHeader *hdr,
 // Every wait is bounded; a wait that runs out sets KVCS_STATUS_TIMEOUT and
 // the kernel returns without hanging.
 //
-// kFam is the layout family of every cache in the launch.  kWide (rows and
-// HND families, for calls whose blocks are mostly partial, such as the
-// newest block of each request) keeps the whole producer warp in the loop:
+// kFam is the layout family of every cache in the launch.  kWide (rows
+// family, for calls whose blocks are mostly partial, such as the newest
+// block of each request) keeps the whole producer warp in the loop:
 // every lane computes the same cursor, lane 0 alone waits, writes metadata
 // and counters, and the lanes share out the copies of a unit's pages; the
 // consumers then reduce packed units of several pages with packed_sum.
-// The wide instances run two CTAs a SM (each with half the shared memory).
+// The wide instance runs two CTAs a SM (each with half the shared memory).
 template <int kFam, bool kWide>
 __global__ void __launch_bounds__(kBulkThreads, kWide ? 2 : 1)
     kvcs_bulk_kernel(const __grid_constant__ Params p) {
@@ -616,11 +544,6 @@ __global__ void __launch_bounds__(kBulkThreads, kWide ? 2 : 1)
     for (int i = tid; i < p.num_caches; i += kBulkThreads)
       wt->page[i] = PageAddr{p.caches[i].base, p.caches[i].half_stride,
                              p.caches[i].block_stride};
-    if (kFam == kFamHnd && tid == 0) {
-      for (int s = 0; s < NS; ++s)
-        ptx::mbar_init(ptx::smem_addr(&wt->landed[s]), p.group_warps * 32);
-      ptx::fence_barrier_init();
-    }
   }
   __syncthreads();
 
@@ -671,7 +594,6 @@ __global__ void __launch_bounds__(kBulkThreads, kWide ? 2 : 1)
     u32 it = 0;         // units emitted
     u32 seq = 0;        // positions that got an accumulator slot
     bool aborted = false;
-    u32 gpar = 0;       // wide: parity of each stage's next landed phase
     // Ranges of units: this CTA's fixed share, then, with a work counter,
     // chunks taken from it until the pool is used up.  After the first
     // chunk the next one is claimed a range ahead, so the atomic's latency
@@ -832,64 +754,32 @@ __global__ void __launch_bounds__(kBulkThreads, kWide ? 2 : 1)
               if (dmask) ptx::cp_async_mbar_arrive(fb);
               ptx::mbar_arrive_expect_tx(fb, tx);
             } else {
-            // wide HND instance: a unit of partial pages of several heads is
-            // fetched by its consumer group, since each head's run of valid
-            // slots would cost a bulk copy of its own (measured: 915 -> 1840
-            // GB/s on one-token blocks; for rows, one contiguous run a page,
-            // the bulk copies are faster: 3265 against 2530)
-            const bool gather = kWide && kFam == kFamHnd && cur.nv != bs && C.heads > 1;
             if (lead) {
-              if (gather) {
-                const int par = static_cast<int>((gpar >> s) & 1u);
-                store_meta(&hdr->meta[s], dst_word, cur.q, ci, half,
-                           static_cast<int>(cur.block), count, cur.nv,
-                           mode | kModeGather | (par ? kModeLandedParity : 0), slot, npg);
-                ptx::mbar_arrive(fb);
-              } else {
-                store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
-                           mode, slot, npg);
-                ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
-              }
+              store_meta(&hdr->meta[s], dst_word, cur.q, ci, half, first, count, cur.nv,
+                         mode, slot, npg);
+              ptx::mbar_arrive_expect_tx(fb, pbytes * static_cast<u32>(npg));
             }
-            if (gather) {
-              gpar ^= 1u << s;
-            } else if constexpr (kWide) {
-              // the lanes share the unit's copies: copy idx is page k2 (or,
-              // for a partial HND block, head h of page k2), issued by lane
-              // idx mod 32 once lane 0 has set the stage's byte count
+            if constexpr (kWide) {
+              static_assert(kFam == kFamRows, "the wide producer stages rows");
+              // the lanes share the unit's copies: page k2 by lane k2 mod 32,
+              // once lane 0 has set the stage's byte count
               __syncwarp();
               const u32 dst0 = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
               const int H0 = C.halves;
-              const int cpp = (kFam == kFamHnd && cur.nv != bs) ? count : 1;
-              for (int idx = tid; idx < npg * cpp; idx += 32) {
-                const int k2 = cpp == 1 ? idx : idx / cpp;
-                const int h = idx - k2 * cpp;
+              for (int k2 = tid; k2 < npg; k2 += 32) {
                 int pci = ci, phalf = half;
                 if (k2 > 0) {  // packed pages: every cache has H0 halves
                   const int flat = ci * H0 + half + k2;
                   pci = H0 == 1 ? flat : flat >> 1;
                   phalf = flat - pci * H0;
                 }
-                // (packed pages share their geometry: C's hb and rowb hold for
-                // every page; only the addressing differs)
+                // (packed pages share their geometry: C's rowb holds for every
+                // page; only the addressing differs)
                 const PageAddr D = wt->page[pci];
                 const unsigned char *page = D.base +
                     static_cast<long long>(phalf) * D.half_stride + cur.block * D.block_stride;
-                const u32 dst = dst0 + static_cast<u32>(k2) * pstride;
-                if constexpr (kFam == kFamHnd) {
-                  const unsigned char *src = page + static_cast<u64>(first) * bs * C.hb;
-                  if (cur.nv == bs) {
-                    ptx::bulk_g2s(dst, src, pstride, fb, policy);
-                  } else {
-                    const u32 run = static_cast<u32>(cur.nv) * static_cast<u32>(C.hb);
-                    ptx::bulk_g2s(dst + static_cast<u32>(h) * run,
-                                  src + static_cast<u64>(h) * bs * C.hb, run, fb, policy);
-                  }
-                } else {
-                  static_assert(!kWide || kFam == kFamRows, "wide producer: rows or HND");
-                  ptx::bulk_g2s(dst, page + static_cast<u64>(first) * C.rowb, pbytes, fb,
-                                policy);
-                }
+                ptx::bulk_g2s(dst0 + static_cast<u32>(k2) * pstride,
+                              page + static_cast<u64>(first) * C.rowb, pbytes, fb, policy);
               }
             } else {
             u32 dst = ptx::smem_addr(stages + static_cast<size_t>(s) * SB);
@@ -1084,28 +974,7 @@ __global__ void __launch_bounds__(kBulkThreads, kWide ? 2 : 1)
     int ci = m.cache, half = m.half;
     u64 v = 0;
     bool packed = false;
-    if constexpr (kWide && kFam == kFamHnd) {
-      if (m.mode & kModeGather) {
-        // fetch the unit's valid bytes, then wait (bounded) until every
-        // thread's copies of the group have landed
-        const u32 lb = ptx::smem_addr(&wt->landed[s]);
-        gather_unit(p, m, wt->page, ptx::smem_addr(sp), gtid, gw * 32,
-                          static_cast<long long>(bsz));
-        ptx::cp_async_mbar_arrive_noinc(lb);
-        const bool landed =
-            ptx::mbar_wait_bounded(lb, (m.mode & kModeLandedParity) ? 1u : 0u, p.timeout_ns);
-        if (!__all_sync(0xffffffffu, landed)) {
-          ptx::cp_async_wait_all();
-          if (lane == 0) set_status(p, kStatusTimeout);
-          return;
-        }
-        v = packed_sum<kFam>(p, m, 0, sp, gtid, gw * 32, bsz);
-        packed = true;
-      } else if (m.npages > 1) {
-        v = packed_sum<kFam>(p, m, m.first, sp, gtid, gw * 32, bsz);
-        packed = true;
-      }
-    } else if constexpr (kWide) {
+    if constexpr (kWide) {
       if (m.npages > 1) {
         v = packed_sum<kFam>(p, m, m.first, sp, gtid, gw * 32, bsz);
         packed = true;

@@ -116,7 +116,8 @@ struct DevCache {
   int kbs;          // HND: slots per kernel sub-block (block_size if none)
   int chunks;       // HND: 1; x-split: 16-byte chunks per head (hb / 16)
   int pbytes;       // piece bytes: 8, or a state's element bytes (2 or 4)
-  int pad;
+  int run_end;      // the first cache of the launch after this one with
+                    // another column (the caches are sorted by column)
 };
 
 struct Params {
@@ -182,11 +183,10 @@ struct SmemHeader {
 constexpr int kHeaderBytes = (static_cast<int>(sizeof(SmemHeader)) + 127) / 128 * 128;
 
 // The page addressing of a launch's caches, copied into shared memory by the
-// wide bulk instances (after the header, before the stages): their producer
+// wide bulk instance (after the header, before the stages): its producer
 // lanes each address a different cache's page, and shared memory serves
 // such reads at once where the parameter space would take them one address
-// at a time.  After it, one "landed" mbarrier per stage for the units the
-// consumers fetch themselves.
+// at a time.
 struct PageAddr {
   const unsigned char *base;
   long long half_stride;
@@ -194,16 +194,8 @@ struct PageAddr {
 };
 struct WideTable {
   PageAddr page[kMaxCachesPerLaunch];
-  u64 landed[kMaxStages];
 };
 constexpr int kWideTableBytes = (static_cast<int>(sizeof(WideTable)) + 127) / 128 * 128;
-
-// UnitMeta.mode in the wide instances: bit 1 marks a unit whose pages the
-// consumer group fetches itself (its `first` field then holds the block id,
-// the unit's pages starting at row or head 0), bit 2 the parity of that
-// fill's phase of the stage's landed barrier.
-constexpr int kModeGather = 2;
-constexpr int kModeLandedParity = 4;
 
 __device__ __forceinline__ void set_status(const Params &p, u32 bit) {
   if (p.status) atomicOr(p.status, bit);

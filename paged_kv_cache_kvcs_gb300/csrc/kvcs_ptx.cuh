@@ -87,22 +87,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive(u32 bar) {
   asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 16 bytes from global to shared memory, not kept in L1.
-__device__ __forceinline__ void cp_async16(u32 dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-// As cp_async_mbar_arrive, but the arrival is one of the barrier's expected
-// arrivals (its pending count is not raised).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(u32 bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Wait until every cp.async this thread issued has completed.
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // Programmatic dependent launch.  grid_dep_launch lets the next kernel of
 // the stream (launched with programmatic stream serialization) start before
 // this one ends; grid_dep_wait makes the calling thread wait until the grids

@@ -1,9 +1,10 @@
 """Calls whose blocks are mostly partial (at most two positions per request,
-such as the newest block of each request): the bulk kernel's instances in
-which the whole producer warp issues a unit's copies and the consumers
-reduce a packed unit of many pages at once.  Each case compares every
-position with the oracle (one exact value per block position: module
-docstring item 2 of the checksum page)."""
+such as the newest block of each request): NHD caches on the bulk kernel's
+instance in which the whole producer warp issues a unit's copies and the
+consumers reduce a packed unit of many pages at once; latent and HND caches
+on the valid-slot kernel.  Each case compares every position with the oracle
+(one exact value per block position: module docstring item 2 of the checksum
+page)."""
 
 import numpy as np
 import pytest

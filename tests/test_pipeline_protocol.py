@@ -385,174 +385,3 @@ def test_model_catches_lanes_leaving_one_by_one():
     with pytest.raises(ExitedLanesInCollective):
         for trial, NS, gw, units, _, fw, fu in _timeout_trials(uniform=False):
             simulate_timeout(trial, NS, gw, units, NS + 2, fw, fu, uniform=False)
-
-
-# ---------------------------------------------------------------------------
-# Units the consumer group fetches itself (the wide HND instance)
-# ---------------------------------------------------------------------------
-
-def simulate_gather(seed, stages, group_warps, units, ring_slots, gather_share,
-                    fill_parity=False):
-    """As ``simulate``, where some units are fetched by their consumer group:
-    the producer writes the metadata and arrives on ``full`` with no copy,
-    recording in the metadata the parity of that stage's next phase of its
-    "landed" barrier (a bit per stage it flips at each such fill).  Each
-    warp of the group issues its copy, whose landing arrives on ``landed``
-    (expected arrivals: the group's warps), and waits on ``landed`` with
-    the recorded parity before it reads.  ``fill_parity`` waits with the
-    fill's parity instead (wrong when a stage mixes both kinds of fill).
-    Returns {position: sum}."""
-    rnd = random.Random(seed)
-    NS, G = stages, group_warps
-    groups = 8 // G
-    full = [Bar(1) for _ in range(NS)]
-    empty = [Bar(G) for _ in range(NS)]
-    landed = [Bar(G) for _ in range(NS)]
-    stage, meta = [None] * NS, [None] * NS
-    gdata = [[None] * G for _ in range(NS)]   # each warp's fetched share
-    inflight = []
-    acc, cnt = [0] * ring_slots, [0] * ring_slots
-    done = {}
-    gpar = 0
-    kinds = [rnd.random() < gather_share for _ in units]
-
-    def finalize(slot, pos):
-        assert pos not in done, f"position {pos} finalised twice"
-        done[pos] = acc[slot]
-
-    prod = dict(i=0, it=0, seq=0, pos=None, n=0, slot=None, dones=0, state="emit")
-    warps = [dict(it=w // G, phase="release", live=True, m=None) for w in range(8)]
-
-    def close_position():
-        if prod["n"]:
-            sl = prod["slot"]
-            cnt[sl] -= G * prod["n"]
-            if cnt[sl] == 0:
-                finalize(sl, prod["pos"])
-        prod["n"] = 0
-
-    for _ in range(800000):
-        actors = ([] if prod["state"] == "end" else ["P"]) + \
-                 [w for w in range(8) if warps[w]["live"]] + (["L"] if inflight else [])
-        if not actors:
-            return done
-        a = rnd.choice(actors)
-        if a == "L":
-            item = inflight.pop(rnd.randrange(len(inflight)))
-            if item[0] == "bulk":
-                _, s, u = item
-                stage[s] = u
-                full[s].land(1)
-            else:                          # a warp's own copy lands
-                _, s, u, k = item
-                gdata[s][k] = u
-                landed[s].arrive()
-        elif a == "P":
-            s, f = prod["it"] % NS, prod["it"] // NS
-            if prod["state"] == "emit":
-                if prod["i"] == len(units):
-                    close_position()
-                    prod["state"] = "dones"
-                    continue
-                pos, _ = units[prod["i"]]
-                if prod["pos"] is not None and pos != prod["pos"]:
-                    close_position()
-                prod["pos"] = pos
-                if not empty[s].try_wait((f & 1) ^ 1):
-                    continue
-                if prod["n"] == 0:
-                    sl = prod["seq"] % ring_slots
-                    prod["seq"] += 1
-                    acc[sl], cnt[sl], prod["slot"] = 0, 0, sl
-                g = kinds[prod["i"]]
-                par = (gpar >> s) & 1
-                meta[s] = (prod["it"], pos, prod["slot"], units[prod["i"]][1], g, par)
-                stage[s] = None
-                if g:
-                    gpar ^= 1 << s
-                    full[s].arrive()
-                else:
-                    full[s].arrive(tx=1)
-                    inflight.append(("bulk", s, prod["it"]))
-                prod["it"] += 1
-                prod["n"] += 1
-                prod["i"] += 1
-            else:
-                if prod["dones"] == groups:
-                    prod["state"] = "end"
-                    continue
-                if not empty[s].try_wait((f & 1) ^ 1):
-                    continue
-                meta[s] = (prod["it"], -1, None, 0, False, 0)
-                full[s].arrive()
-                prod["it"] += 1
-                prod["dones"] += 1
-        else:
-            w = warps[a]
-            s, f = w["it"] % NS, w["it"] // NS
-            if w["phase"] == "release":
-                if f > 0 and not empty[s].try_wait((f - 1) & 1):
-                    continue
-                w["phase"] = "full"
-            elif w["phase"] == "full":
-                if not full[s].try_wait(f & 1):
-                    continue
-                m = meta[s]
-                if m[0] != w["it"]:
-                    raise WrongUnit(f"group expected unit {w['it']}, stage holds {m[0]}")
-                if m[1] < 0:
-                    w["live"] = False
-                    continue
-                w["m"] = m
-                if m[4]:
-                    inflight.append(("own", s, w["it"], a % G))
-                    w["phase"] = "landed"
-                else:
-                    if stage[s] != w["it"]:
-                        raise WrongUnit(f"unit {w['it']}: data not landed")
-                    w["phase"] = "work"
-            elif w["phase"] == "landed":
-                par = (f & 1) if fill_parity else w["m"][5]
-                if not landed[s].try_wait(par):
-                    continue
-                if any(x != w["it"] for x in gdata[s]):
-                    raise WrongUnit(f"unit {w['it']}: a warp's copy has not landed")
-                w["phase"] = "work"
-            else:
-                _, pos, sl, val, _, _ = w["m"]
-                if a % G == 0:
-                    acc[sl] += val
-                cnt[sl] += 1
-                if cnt[sl] == 0:
-                    finalize(sl, pos)
-                empty[s].arrive()
-                w["it"] += groups
-                w["phase"] = "release"
-    raise AssertionError("no progress")
-
-
-@pytest.mark.parametrize("share", [1.0, 0.5, 0.2])
-def test_gathered_units_delivered_once(share):
-    for trial in range(600):
-        rnd = random.Random(10_000 + trial)
-        NS = rnd.choice([1, 2, 3, 4, 6, 7, 8, 14])
-        units, expect = random_units(rnd)
-        got = simulate_gather(trial, NS, group_warps_for(NS), units, NS + 2, share)
-        assert got == expect, (trial, NS, share)
-
-
-def test_model_catches_fill_parity_for_landed():
-    """Waiting on the landed barrier with the fill's parity goes wrong once
-    a stage mixes fills the group fetches with bulk-copied ones."""
-    for trial in range(3000):
-        rnd = random.Random(20_000 + trial)
-        NS = rnd.choice([1, 2, 3, 4])
-        units, expect = random_units(rnd)
-        try:
-            got = simulate_gather(trial, NS, group_warps_for(NS), units, NS + 2, 0.5,
-                                  fill_parity=True)
-        except AssertionError:
-            return
-        if got != expect:
-            return
-    raise AssertionError("the model did not catch the wrong parity")
