@@ -32,7 +32,7 @@ def _newest_blocks(seed, n, block_size, full_share=0.0):
 
 def _check(wl, workspace=False):
     from gpu_helpers import full_oracle
-    assert wl.num_positions <= 2 * wl.num_requests      # the wide instances apply
+    assert wl.num_positions <= 2 * wl.num_requests      # the mostly-partial path applies
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     out = torch.empty(wl.num_positions, dtype=torch.int64, device=DEV)
     ws = (torch.zeros(K.KVCS_WORKSPACE_WORDS, dtype=torch.int64, device=DEV)
@@ -92,7 +92,7 @@ def test_two_positions_per_request():
 
 def test_few_positions_split():
     """Fewer positions than SMs (ranges cut at unit granularity, zeroed
-    output, atomics) in the wide instances."""
+    output, atomics) on the mostly-partial path."""
     lengths, first = _newest_blocks(21, 40, 16)
     for layout in (W.LAYOUT_NHD, W.LAYOUT_HND):
         wl = W.random_case(8, DEV, layout=layout, layers=16, heads=8, head_bytes=256,
@@ -119,7 +119,7 @@ def test_decode_with_workspace(layout):
 @pytest.mark.parametrize("layout", [W.LAYOUT_NHD, W.LAYOUT_HND])
 def test_accumulating_calls(layout):
     """An accumulating call (every result added into the caller's words)
-    through the wide instances, twice onto the same words: twice the
+    through the mostly-partial path, twice onto the same words: twice the
     oracle's checksums, mod 2^64."""
     from gpu_helpers import full_oracle
     lengths, first = _newest_blocks(31, 200, 16)

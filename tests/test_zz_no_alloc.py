@@ -111,8 +111,8 @@ def test_repeated_calls_on_the_same_workload():
 
 def test_two_decode_shaped_calls_in_a_row():
     """The newest block of each of 4096 requests (one valid token each), NHD
-    then HND: calls of mostly partial blocks, which take the wide instances,
-    back to back through the shared counters."""
+    then HND: calls of mostly partial blocks (the wide rows instance, then
+    the valid-slot kernel), back to back through the shared counters."""
     calls = [W.llama3_8b_decode(s, DEV, num_requests=4096, layout=lay)
              for s, lay in ((3, W.LAYOUT_NHD), (4, W.LAYOUT_HND))]
     for wl in calls:
