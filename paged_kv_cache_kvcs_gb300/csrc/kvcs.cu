@@ -411,6 +411,14 @@ long long slots_grid(long long pages, int sms) {
                                                     (pages + per_cta - 1) / per_cta));
 }
 
+// Window groups of a valid-slot launch of `grid` CTAs (slots_grid): a call
+// whose pages leave SMs idle runs up to four times the CTAs, groups of them
+// splitting each page's windows of valid chunks.
+long long slots_window_groups(long long grid, int sms) {
+  const long long full = static_cast<long long>(kSlotsCtasPerSm) * sms;
+  return grid < full ? std::max<long long>(1, std::min<long long>(4, full / grid)) : 1;
+}
+
 // Whether a valid-slot launch with a work counter hands its last pages out
 // from it: at least kSlotsDynamicPages pages a warp.
 bool slots_dynamic(long long pages, long long grid) {
@@ -716,12 +724,16 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
     } else if (l.kernel == kKernelSlots) {
       p.split = 0;
       const long long pages = total_positions * p.pages_per_pos;
-      const long long grid = slots_grid(pages, sms);
-      // with a work counter, on enough pages: the last pages handed out from it
+      const long long g0 = slots_grid(pages, sms);
+      const long long wg = slots_window_groups(g0, sms);
+      const long long grid = g0 * wg;
+      p.window_groups = static_cast<int>(wg);
+      // with a work counter, on enough pages: the last pages handed out from
+      // it (never with window groups: those calls have few pages)
       p.pool_start = pages;
       if (workspace && work_used < n_work) {
         p.work = workspace + work_used++;
-        if (slots_dynamic(pages, grid)) p.pool_start = pages / kSlotsFixedShare;
+        if (wg == 1 && slots_dynamic(pages, g0)) p.pool_start = pages / kSlotsFixedShare;
       }
       const dim3 gd(static_cast<unsigned>(grid));
       const cudaError_t e =
@@ -844,10 +856,12 @@ int kvcs_plan_requests(const kvcs_cache *caches, int32_t num_caches, int32_t blo
     // every launch on the valid-slot kernel
     const long long pages = total_positions * max_ipp;
     info->kernel = 3;
-    info->grid = static_cast<int32_t>(slots_grid(pages, sms));
+    const long long g0 = slots_grid(pages, sms);
+    const long long wg = slots_window_groups(g0, sms);
+    info->grid = static_cast<int32_t>(g0 * wg);
     info->threads = kSlotsThreads;
     info->units = pages;
-    info->dynamic = total_positions > 0 && slots_dynamic(pages, info->grid) ? 1 : 0;
+    info->dynamic = total_positions > 0 && wg == 1 && slots_dynamic(pages, g0) ? 1 : 0;
     return KVCS_OK;
   }
   info->kernel = pl.kernel;

@@ -152,6 +152,9 @@ struct Params {
   int pages_per_pos;         // sum of halves over the caches
   int num_columns;           // replica-key columns of the output
   int state_call;            // the caches hold Mamba states (block position 0)
+  int window_groups;         // valid-slot kernel: groups of warps that split
+                             // every page's windows of valid chunks (1, or
+                             // more for calls of few pages)
   DevCache caches[kMaxCachesPerLaunch];
 };
 

@@ -86,12 +86,12 @@ __device__ __forceinline__ void slot_map(SlotMap &sm, const DevCache &C, u32 nv,
 
 // Pages [i0, i1) of the (position, cache, half) order, walked by one warp:
 // for each position with valid slots and each run of its pages of one
-// column (the caches are sorted by column), every window of the valid
-// chunks over the run's pages, two pages' loads at a time, then one 64-bit
-// atomic of the warp's total into the output.
+// column (the caches are sorted by column), windows wg, wg + G, ... of the
+// valid chunks over the run's pages, two pages' loads at a time, then one
+// 64-bit atomic of the warp's total into the output.
 template <bool kHnd>
 __device__ __forceinline__ void slots_range(const Params &p, long long i0, long long i1,
-                                            SlotMap &sm, int lane) {
+                                            u32 wg, u32 G, SlotMap &sm, int lane) {
   const long long ipp = p.pages_per_pos;
   const DevCache &C0 = p.caches[0];
   const int H = C0.halves;
@@ -115,7 +115,7 @@ __device__ __forceinline__ void slots_range(const Params &p, long long i0, long 
         const int col = Ca.column;
         const int kb = min(kend, Ca.run_end * H);
         u64 acc = 0;
-        for (u32 cb = 0; cb < nch; cb += kSlotsWindow) {
+        for (u32 cb = wg * kSlotsWindow; cb < nch; cb += G * kSlotsWindow) {
           if (sm.nv != nv || sm.c0 != cb) slot_map<kHnd>(sm, C0, nv, bs, cb, lane);
           for (int kk = ka; kk < kb; kk += kSlotsPages) {
             uint4 v[kSlotsPages][kSlotsCols];
@@ -170,9 +170,12 @@ __device__ __forceinline__ void slots_range(const Params &p, long long i0, long 
 // positions differ, so fixed ranges alone can end far apart).  Each
 // (position, column) total is added into the pre-zeroed output (or the
 // caller's words, for accumulating calls) with one 64-bit atomic per warp.
-// Every page of the launch has the same geometry; kHnd selects the HND walk
-// (else NHD or latent).  No shared memory, no barrier: warps never wait for
-// each other.
+// A call of few pages (never shared out dynamically) runs window_groups
+// groups of warps, group g over all the pages but only windows g,
+// g + window_groups, ... of each, so a page with many valid slots is read
+// by several warps at once.  Every page of the launch has the same
+// geometry; kHnd selects the HND walk (else NHD or latent).  No shared
+// memory, no barrier: warps never wait for each other.
 template <bool kHnd>
 __global__ void __launch_bounds__(kSlotsThreads, kSlotsCtasPerSm)
     kvcs_slots_kernel(const __grid_constant__ Params p) {
@@ -185,12 +188,21 @@ __global__ void __launch_bounds__(kSlotsThreads, kSlotsCtasPerSm)
       set_status(p, kStatusBadRequests);
   }
   const long long items = p.total_positions * p.pages_per_pos;
-  const long long fixed = p.work ? p.pool_start : items;
   SlotMap sm;
   sm.nv = 0;
   sm.c0 = 0;
+  const long long G = p.window_groups > 1 ? p.window_groups : 1;
+  if (G > 1) {
+    // the grid is G groups of W / G warps (the host launches a multiple)
+    const long long W0 = W / G, g = warp / W0, w0 = warp - g * W0;
+    const long long i0 = items * w0 / W0, i1 = items * (w0 + 1) / W0;
+    if (g < G && i0 < i1)
+      slots_range<kHnd>(p, i0, i1, static_cast<u32>(g), static_cast<u32>(G), sm, lane);
+    return;
+  }
+  const long long fixed = p.work ? p.pool_start : items;
   const long long i0 = fixed * warp / W, i1 = fixed * (warp + 1) / W;
-  if (i0 < i1) slots_range<kHnd>(p, i0, i1, sm, lane);
+  if (i0 < i1) slots_range<kHnd>(p, i0, i1, 0u, 1u, sm, lane);
   if (!p.work) return;
   // a range is taken only once the warp is free for it: taking one ahead
   // would hand out the pool before the warps' speeds are known
@@ -203,7 +215,7 @@ __global__ void __launch_bounds__(kSlotsThreads, kSlotsCtasPerSm)
     if (lo >= items) break;
     const long long hi = min(lo + n, items);
     left = items - hi;
-    slots_range<kHnd>(p, lo, hi, sm, lane);
+    slots_range<kHnd>(p, lo, hi, 0u, 1u, sm, lane);
   }
 }
 
