@@ -244,6 +244,44 @@ def test_plan_shapes():
     assert p["launches"] == 3 and p["memsets"] == 1
 
 
+def test_plan_requests_routes_mostly_partial_calls():
+    """kvcs_plan_requests: with at most two positions per request, latent and
+    HND caches (alike, aligned, no sub-blocks) go to the valid-slot kernel
+    (kernel 3), NHD caches stay on the bulk kernel, and a mixed call reports
+    its valid-slot launches among the others; more positions per request,
+    or an unknown request count, plan as kvcs_plan does."""
+    def pr(caches, positions, requests, bs=16):
+        return K.plan_for(caches, bs, positions, num_sms=152, num_requests=requests)
+
+    hnd = [FakeCache(layout=1, layer=i) for i in range(32)]
+    nhd = [FakeCache(layout=0, layer=i) for i in range(32)]
+    lat = [FakeCache(layout=2, layer=i, num_heads=1, head_bytes=1152) for i in range(61)]
+    for caches, bs in ((hnd, 16), (lat, 64)):
+        p = pr(caches, 4096, 4096, bs)
+        halves = 1 if caches is lat else 2
+        assert p["kernel"] == 3 and p["slot_launches"] == 1 and p["launches"] == 1
+        assert p["threads"] == 256 and p["smem_bytes"] == 0 and p["memsets"] == 1
+        assert p["units"] == 4096 * len(caches) * halves
+        assert p["grid"] == 304
+        assert pr(caches, 8193, 4096, bs)["slot_launches"] == 0     # > 2 a request
+        assert pr(caches, 4096, -1, bs) == plan(caches, bs, 4096)   # not known
+    p = pr(nhd, 4096, 4096)
+    assert p["kernel"] == 0 and p["slot_launches"] == 0
+    mixed = hnd[:4] + [FakeCache(layout=0, layer=10 + i) for i in range(4)]
+    p = pr(mixed, 100, 100)
+    assert p["kernel"] == 0 and p["slot_launches"] == 1 and p["launches"] == 2
+    # HND in kernel sub-blocks, or caches of two geometries, stay on the bulk kernel
+    assert pr([FakeCache(layout=1, kernel_block_size=4)], 100, 100)["slot_launches"] == 0
+    two = [FakeCache(layout=1, layer=0), FakeCache(layout=1, layer=1, head_bytes=128)]
+    assert pr(two, 100, 100)["slot_launches"] == 0
+    # few pages: a small grid, in window groups (up to 4 x the CTAs the pages fill)
+    small = pr(hnd[:2], 10, 10)                  # 40 pages: 3 CTAs, 4 window groups
+    assert small["grid"] == 12
+    # the dynamic share-out from 64 pages a warp (152 SMs: 304 CTAs)
+    assert pr(hnd, 2432, 2432)["dynamic"] == 1          # 155,648 pages
+    assert pr(hnd, 2431, 2431)["dynamic"] == 0
+
+
 def test_group_and_tags_reject_bad_arguments_without_cuda():
     lib = K.load_library()
     arr = K.cache_array([FakeCache(layer=0), FakeCache(layer=1, column=1)])
