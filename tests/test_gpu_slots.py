@@ -214,3 +214,74 @@ def test_far_positions_wrap():
     assert _plan(wl)["kernel"] == 3
     st, _ = _check(wl)
     assert st == 0
+
+
+def _random_call(seed):
+    """One random call of mostly partial blocks over latent or HND caches:
+    its workload (columns assigned), the number of columns, whether it
+    accumulates and whether it passes a workspace."""
+    g = torch.Generator().manual_seed(seed)
+
+    def pick(xs):
+        return xs[int(torch.randint(0, len(xs), (1,), generator=g))]
+
+    layout = pick([W.LAYOUT_HND, W.LAYOUT_LATENT])
+    bs = pick([1, 2, 4, 8, 16, 32, 64])
+    if layout == W.LAYOUT_LATENT:
+        heads, hb = 1, pick([16, 48, 80, 576, 1152])
+    else:
+        heads, hb = pick([1, 2, 3, 4, 8]), pick([16, 32, 48, 128, 256])
+    layers = pick([1, 2, 5, 8])
+    n = pick([1, 2, 7, 40, 150, 600])
+    shape = pick(["one_token", "random", "some_full", "two_positions"])
+    lengths, first, extra = [], [], []
+    for _ in range(n):
+        k = int(torch.randint(0, 100, (1,), generator=g))
+        if shape == "one_token" or bs == 1:
+            nv = 1
+        elif shape == "some_full" and float(torch.rand(1, generator=g)) < 0.3:
+            nv = bs
+        else:
+            nv = int(torch.randint(1, bs, (1,), generator=g))
+        lengths.append(k * bs + nv)
+        if shape == "two_positions" and k > 0:
+            first.append(k - 1)                 # the last full block and the newest
+        else:
+            first.append(k)
+        extra.append(1 if shape == "two_positions" and k == 0 else 0)
+    wl = W.random_case(2000 + seed, DEV, layout=layout, layers=layers, heads=heads,
+                       head_bytes=hb, block_size=bs, lengths=lengths, first_positions=first,
+                       extra_positions=extra)
+    cols = pick([1, 1, 2, 3]) if layers >= 3 else 1
+    caches = [dataclasses.replace(c, column=i % cols) for i, c in enumerate(wl.caches)]
+    wl = dataclasses.replace(wl, caches=caches)
+    return wl, cols, pick([False, True]), pick([False, True])
+
+
+@pytest.mark.parametrize("block", range(6))
+def test_random_calls_match_oracle(block):
+    from gpu_helpers import full_oracle
+    for seed in range(block * 20, (block + 1) * 20):
+        wl, cols, accumulate, workspace = _random_call(seed)
+        assert wl.num_positions <= 2 * wl.num_requests
+        assert _plan(wl)["slot_launches"] >= 1, seed
+        ws = (torch.full((K.KVCS_WORKSPACE_WORDS,), -1, dtype=torch.int64, device=DEV)
+              if workspace else None)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        vals = torch.zeros((wl.num_positions, cols), dtype=torch.int64, device=DEV)
+        calls = 2 if accumulate else 1
+        for _ in range(calls):
+            K.group_checksums(wl.caches, wl.block_size, wl.pos_offsets, wl.first_position,
+                              wl.num_tokens, wl.block_ids, cols, values=vals,
+                              accumulate=accumulate, total_positions=wl.num_positions,
+                              workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, seed
+        got = vals.cpu().numpy().view(np.uint64)
+        for c in range(cols):
+            sub = dataclasses.replace(wl, caches=[x for x in wl.caches if x.column == c])
+            exp, est = full_oracle(sub)
+            assert est == 0
+            want = np.asarray(exp).reshape(-1) * np.uint64(calls)
+            bad = np.flatnonzero(got[:, c] != want)
+            assert bad.size == 0, (seed, c, bad.size, bad[:6].tolist())
