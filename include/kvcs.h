@@ -257,7 +257,8 @@ int kvcs_block_checksums(const kvcs_cache *caches, int32_t num_caches,
  * units (KV pages, kvcs_plan's `units`) per SM use it; smaller calls keep
  * the fixed shares, which suit them better, and leave the workspace alone.
  * The valid-slot kernel (calls of at most two positions per request: their
- * latent and HND caches) uses it the same way from 64 pages per warp on:
+ * latent and HND caches, and NHD caches of pages of at most 8 KiB) uses it
+ * the same way from 64 pages per warp on:
  * each warp reads a fixed quarter share of the pages, then ranges of the
  * rest that shrink as they run out (the positions' valid slots, and so
  * their bytes, differ).  One counter is used per bulk-copy or valid-slot
@@ -413,7 +414,8 @@ typedef struct kvcs_plan_info {
                             stage go to the generic one), 3 = the valid-slot
                             kernel for every launch (a call with at most two
                             positions per request over latent or HND
-                            caches; the fields below then describe it) */
+                            caches, or NHD caches of pages of at most 8 KiB;
+                            the fields below then describe it) */
   int32_t split;         /* 1 if the bulk kernel splits positions across CTAs
                             (output zeroed first, partial sums added with
                             64-bit atomics; the generic kernel always adds) */
@@ -424,7 +426,7 @@ typedef struct kvcs_plan_info {
   int32_t grid;          /* CTAs per kernel launch (a call with at most two
                             positions per request, mostly partial blocks,
                             launches twice this many CTAs for its NHD
-                            caches) */
+                            caches of pages over 8 KiB) */
   int32_t threads;       /* threads per CTA */
   int32_t smem_bytes;    /* dynamic shared memory per CTA */
   int32_t stage_bytes;   /* bytes per pipeline stage (bulk kernel) */
@@ -453,8 +455,9 @@ int kvcs_plan(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,
  * kvcs_plan_requests -- as kvcs_plan, for a call of num_requests requests
  * (reqs->num_requests of the checksum call): a call of at most two
  * positions per request (total_positions <= 2 num_requests) sends its
- * latent and HND caches (no kernel sub-blocks, 16-byte aligned, all of one
- * geometry) to the valid-slot kernel, which kvcs_plan cannot tell.
+ * latent and HND caches (no kernel sub-blocks), and NHD caches of pages of
+ * at most 8 KiB (block_size x heads x head_bytes), 16-byte aligned and all
+ * of one geometry, to the valid-slot kernel, which kvcs_plan cannot tell.
  * num_requests < 0 plans as kvcs_plan does.
  */
 int kvcs_plan_requests(const kvcs_cache *caches, int32_t num_caches, int32_t block_size,

@@ -351,8 +351,9 @@ struct Launch {
 // their layout family (up to kMaxCachesPerLaunch per launch), the other KV
 // caches to the direct-load kernel and the other state caches to the
 // state-row kernel.  In a call whose blocks are mostly partial (at most two
-// positions per request), a launch of alike NHD, latent or HND pages goes
-// to the valid-slot kernel instead.  With more than one launch, or a
+// positions per request), a launch of alike latent or HND pages, or of NHD
+// pages of at most kSlotsNhdPageBytes, goes to the valid-slot kernel
+// instead.  With more than one launch, or a
 // direct-load, state-row or valid-slot launch, every result is added
 // atomically into an output zeroed first.
 struct Plan {
@@ -385,16 +386,23 @@ constexpr long long kChunksPerCta = 8;
 constexpr long long kMinChunkUnits = 16;
 
 // Caches of one launch the valid-slot kernel reads: latent or HND (no kernel
-// sub-blocks) pages the bulk kernel stages without the misaligned split, all
-// of one geometry, each page under 2 GiB (its byte offsets fit 32 bits).
-// NHD pages of such calls stay with the bulk kernel: a partial NHD page's
-// valid slots are one contiguous run, which its bulk copies fetch with more
-// bytes in flight than registers hold (measured on the newest blocks of
-// 256 to 16384 requests of 1 to 15 tokens: the bulk copies 5 to 17% faster;
-// with one token a block the register loads were 41% faster).
+// sub-blocks) pages, and NHD pages of at most kSlotsNhdPageBytes, that the
+// bulk kernel stages without the misaligned split, all of one geometry, each
+// page under 2 GiB (its byte offsets fit 32 bits).  Larger NHD pages of such
+// calls stay with the bulk kernel: a partial NHD page's valid slots are one
+// contiguous run, which its bulk copies fetch with more bytes in flight than
+// registers hold.  Measured on the newest blocks of 8192 requests of 1 to
+// block_size - 1 tokens, 32 layers: pages of 4 and 8 KiB 6-38% faster on this
+// kernel, pages of 16 and 32 KiB 2-7% faster on the bulk kernel (with one
+// token a block this kernel was 41-97% faster at every page size).
+constexpr long long kSlotsNhdPageBytes = 8192;
 bool slots_eligible(int family, const kvcs_cache *c, size_t n, int32_t block_size) {
-  if (family != kFamHnd && !(family == kFamRows && c[0].layout == KVCS_LAYOUT_LATENT))
+  if (family == kFamRows) {
+    if (c[0].layout != KVCS_LAYOUT_LATENT && page_bytes_of(c[0], block_size) > kSlotsNhdPageBytes)
+      return false;
+  } else if (family != kFamHnd) {
     return false;
+  }
   for (size_t i = 0; i < n; ++i) {
     if (c[i].layout != c[0].layout || c[i].num_heads != c[0].num_heads ||
         c[i].head_bytes != c[0].head_bytes)
@@ -691,7 +699,8 @@ int run_checksums(const kvcs_cache *caches_in, int32_t num_caches, int32_t block
       // reduce packed units at once.  Its producers, not DRAM, set the
       // pace, so it runs two CTAs a SM (two producers), each with half the
       // shared memory: its page-address table and a ring of fewer stages.
-      // (Such calls' latent and HND pages go to the valid-slot kernel.)
+      // (Such calls' latent and HND pages, and NHD pages of at most
+      // kSlotsNhdPageBytes, go to the valid-slot kernel.)
       const bool wide = p.pack && total_positions <= 2 * reqs->num_requests &&
                         l.family == kFamRows;
       if (wide)

@@ -1,8 +1,8 @@
 // kvcs_slots.cuh -- the valid-slot kernel: calls whose blocks are mostly
 // partial (at most about two positions a request, such as the newest block
-// of each request) over latent or HND pages that are 16-byte aligned and
-// alike (the planner keeps such calls' NHD pages on the bulk kernel; the
-// rows walk here serves latent rows).  A page then holds a few valid slots
+// of each request) over latent or HND pages, or NHD pages of at most 8 KiB,
+// that are 16-byte aligned and alike (the planner keeps larger NHD pages of
+// such calls on the bulk kernel).  A page then holds a few valid slots
 // (nv of block_size), a few hundred bytes to a few KiB in one or a few runs,
 // and staging it through shared memory costs more instructions than reading
 // it: each warp reads its pages' valid bytes straight into registers with

@@ -246,8 +246,9 @@ def test_plan_shapes():
 
 def test_plan_requests_routes_mostly_partial_calls():
     """kvcs_plan_requests: with at most two positions per request, latent and
-    HND caches (alike, aligned, no sub-blocks) go to the valid-slot kernel
-    (kernel 3), NHD caches stay on the bulk kernel, and a mixed call reports
+    HND caches (alike, aligned, no sub-blocks) and NHD caches of pages up to
+    8 KiB go to the valid-slot kernel (kernel 3), larger NHD pages stay on
+    the bulk kernel, and a mixed call reports
     its valid-slot launches among the others; more positions per request,
     or an unknown request count, plan as kvcs_plan does."""
     def pr(caches, positions, requests, bs=16):
@@ -265,8 +266,11 @@ def test_plan_requests_routes_mostly_partial_calls():
         assert p["grid"] == 304
         assert pr(caches, 8193, 4096, bs)["slot_launches"] == 0     # > 2 a request
         assert pr(caches, 4096, -1, bs) == plan(caches, bs, 4096)   # not known
-    p = pr(nhd, 4096, 4096)
+    p = pr(nhd, 4096, 4096)                      # 32 KiB NHD pages: the bulk kernel
     assert p["kernel"] == 0 and p["slot_launches"] == 0
+    small = [FakeCache(layout=0, layer=i, num_heads=8, head_bytes=128) for i in range(4)]
+    assert pr(small, 100, 100, bs=8)["kernel"] == 3      # 8 KiB pages
+    assert pr(small, 100, 100, bs=16)["kernel"] == 0     # 16 KiB pages
     mixed = hnd[:4] + [FakeCache(layout=0, layer=10 + i) for i in range(4)]
     p = pr(mixed, 100, 100)
     assert p["kernel"] == 0 and p["slot_launches"] == 1 and p["launches"] == 2

@@ -1,5 +1,6 @@
 """The valid-slot kernel (calls of at most two positions per request over
-latent or HND caches: the newest block of each request, and the like):
+latent or HND caches, or NHD caches of pages up to 8 KiB: the newest block
+of each request, and the like):
 every position against the oracle (one exact value per block position:
 module docstring item 2 of the checksum page), in its fixed and dynamic
 share-outs, with replica-key columns and accumulating calls, bad block ids,
@@ -64,6 +65,9 @@ CASES = {
     "latent_odd_row": (W.LAYOUT_LATENT, 9, 1, 80, 8, 333, False, 0.0),
     "hnd_block_1": (W.LAYOUT_HND, 3, 4, 64, 1, 200, False, 1.0),
     "few_positions": (W.LAYOUT_HND, 16, 8, 256, 16, 3, False, 0.0),
+    "nhd_8k_pages": (W.LAYOUT_NHD, 6, 8, 128, 8, 300, False, 0.1),
+    "nhd_8k_pages_one_token": (W.LAYOUT_NHD, 6, 8, 256, 4, 300, True, 0.0),
+    "nhd_4k_pages_3_heads": (W.LAYOUT_NHD, 5, 3, 80, 16, 200, False, 0.0),
 }
 
 
@@ -225,10 +229,14 @@ def _random_call(seed):
     def pick(xs):
         return xs[int(torch.randint(0, len(xs), (1,), generator=g))]
 
-    layout = pick([W.LAYOUT_HND, W.LAYOUT_LATENT])
+    layout = pick([W.LAYOUT_HND, W.LAYOUT_LATENT, W.LAYOUT_NHD])
     bs = pick([1, 2, 4, 8, 16, 32, 64])
     if layout == W.LAYOUT_LATENT:
         heads, hb = 1, pick([16, 48, 80, 576, 1152])
+    elif layout == W.LAYOUT_NHD:
+        # pages of at most 8 KiB (larger NHD pages stay on the bulk kernel)
+        heads, hb, bs = pick([(8, 128, 8), (2, 128, 16), (8, 256, 4), (1, 64, 64),
+                              (4, 32, 16), (3, 48, 8), (1, 16, 1)])
     else:
         heads, hb = pick([1, 2, 3, 4, 8]), pick([16, 32, 48, 128, 256])
     layers = pick([1, 2, 5, 8])
